@@ -1,0 +1,167 @@
+"""fp64 CPU oracle for the DSA forward path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product path (``sparse_attention_gemm_gb300``) never imports it and shares no
+code with it.  The arithmetic lives in ``dsa_oracle.c`` (plain C, fp64); this
+module compiles it with gcc and marshals numpy arrays to it.
+
+Sources are cited per function in ``dsa_oracle.c``: the NeMo AutoModel API
+reference pages (``glm_moe_dsa.kernels.cudnn_dsa``,
+``common.cudnn_sparse_attention``, ``qwen3_8_flash_next.cudnn_qsa``) and the
+cuDNN Frontend "DeepSeek Sparse Attention (DSA)" page.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile dsa_oracle.c into oracle/_build/liboracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)  # no OpenMP available
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # DSA_ORACLE_LIB lets the mutation tests load a deliberately broken copy.
+            lib = ctypes.CDLL(os.environ.get("DSA_ORACLE_LIB") or build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_int64
+            D = ctypes.c_double
+            lib.oracle_num_threads.restype = I
+            lib.oracle_thd_metadata.argtypes = [P, I, I, P, P]
+            lib.oracle_thd_metadata.restype = I
+            lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
+            lib.oracle_indexer_scores.restype = None
+            lib.oracle_topk.argtypes = [P, L, P, P, I, I, P, P]
+            lib.oracle_topk.restype = I
+            lib.oracle_compact_sort.argtypes = [P, I, I, L, P, P]
+            lib.oracle_compact_sort.restype = None
+            lib.oracle_pack_routes.argtypes = [P, I, I, I, P]
+            lib.oracle_pack_routes.restype = None
+            lib.oracle_sparse_attn.argtypes = [P, P, L, P, P, P, P, I, I, I, I, I, I, D, P, P, P, P]
+            lib.oracle_sparse_attn.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def thd_metadata(cu_seqlens, T: int):
+    """start[t], len[t] for every token (see dsa_oracle.c)."""
+    cu = _i32(cu_seqlens)
+    start = np.empty(T, np.int32)
+    length = np.empty(T, np.int32)
+    rc = _load().oracle_thd_metadata(_ptr(cu), cu.size - 1, T, _ptr(start), _ptr(length))
+    if rc != 0:
+        raise ValueError("cu_seqlens is not a valid prefix array over [0, T)")
+    return start, length
+
+
+def indexer_scores(qi_rows, ki, w_rows, start_rows, len_rows, s_max: int, want_abs: bool = False):
+    """scores [n, s_max] (fp64, -inf beyond len) and optionally abs_scale."""
+    qi_rows, ki, w_rows = _f64(qi_rows), _f64(ki), _f64(w_rows)
+    n, Hi, d = qi_rows.shape
+    start_rows, len_rows = _i32(start_rows), _i32(len_rows)
+    out = np.empty((n, s_max), np.float64)
+    mag = np.empty((n, s_max), np.float64) if want_abs else None
+    _load().oracle_indexer_scores(_ptr(qi_rows), _ptr(ki), _ptr(w_rows), _ptr(start_rows),
+                                  _ptr(len_rows), n, Hi, d, s_max, _ptr(out), _ptr(mag))
+    return (out, mag) if want_abs else out
+
+
+def topk(scores, len_rows, k: int, start_rows=None):
+    """(idx [n, k] int32 ascending with -1 suffix, topk_len [n])."""
+    scores = _f64(scores)
+    n, ld = scores.shape
+    len_rows = _i32(len_rows)
+    start_rows = None if start_rows is None else _i32(start_rows)
+    idx = np.empty((n, k), np.int32)
+    tl = np.empty(n, np.int32)
+    rc = _load().oracle_topk(_ptr(scores), ld, _ptr(len_rows), _ptr(start_rows), n, k, _ptr(idx), _ptr(tl))
+    if rc != 0:
+        raise MemoryError("oracle_topk: allocation failed")
+    return idx, tl
+
+
+def compact_sort(indices, key_count: int):
+    ind = _i32(indices)
+    T, K = ind.shape
+    out = np.empty_like(ind)
+    lengths = np.empty(T, np.int32)
+    _load().oracle_compact_sort(_ptr(ind), T, K, int(key_count), _ptr(out), _ptr(lengths))
+    return out, lengths
+
+
+def pack_routes(routes):
+    r = _i32(routes)
+    B, S, W = r.shape
+    Wp = (W + 3) // 4 * 4
+    out = np.empty((B * S, Wp), np.int32)
+    _load().oracle_pack_routes(_ptr(r), B, S, W, _ptr(out))
+    return out
+
+
+def sparse_attn(q_rows, kv, idx_rows, scale: float, topk_length=None, sink=None, v=None, dqk=None, dv=None):
+    """Returns dict(out [n,H,Dv], lse, lse_kv, max_logits) in fp64.
+
+    kv is [Tkv, kv_ld]; QK uses its first ``dqk`` columns (default: q's last
+    dim); V is ``v`` when given, else the first ``dv`` columns of kv.
+    """
+    q_rows, kv = _f64(q_rows), _f64(kv)
+    n, H, Dqk = q_rows.shape
+    if dqk is not None and dqk != Dqk:
+        raise ValueError("q's last dimension must equal dqk")
+    Tkv, kv_ld = kv.shape
+    vv = None if v is None else _f64(v)
+    Dv = dv if dv is not None else (vv.shape[1] if vv is not None else min(512, Dqk))
+    idx_rows = _i32(idx_rows)
+    K = idx_rows.shape[1]
+    tl = None if topk_length is None else _i32(topk_length)
+    sk = None if sink is None else _f64(sink)
+    out = np.empty((n, H, Dv), np.float64)
+    lse = np.empty((n, H), np.float64)
+    lse_kv = np.empty((n, H), np.float64)
+    ml = np.empty((n, H), np.float64)
+    _load().oracle_sparse_attn(_ptr(q_rows), _ptr(kv), kv_ld, _ptr(vv), _ptr(idx_rows), _ptr(tl), _ptr(sk),
+                               n, Tkv, H, Dqk, Dv, K, float(scale), _ptr(out), _ptr(lse), _ptr(lse_kv), _ptr(ml))
+    return {"out": out, "lse": lse, "lse_kv": lse_kv, "max_logits": ml}

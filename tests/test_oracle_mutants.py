@@ -1,0 +1,66 @@
+"""Mutation check for the oracle pins (CPU only).
+
+Each case copies oracle/dsa_oracle.c, plants one plausible mistake (a dropped
+term, a wrong sign or index, a transposed operand, a reversed tie-break),
+compiles the copy and runs tests/test_oracle_pins.py against it in a
+subprocess.  The pins must fail for every mutant; the unmodified source must
+pass.  Mistakes are planted only in the oracle copy, never in product code.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(ROOT, "oracle", "dsa_oracle.c")
+
+MUTANTS = {
+    "indexer_drop_relu": ("s += w[h] * (dot > 0.0 ? dot : 0.0);", "s += w[h] * dot;"),
+    "indexer_drop_weight": ("s += w[h] * (dot > 0.0 ? dot : 0.0);", "s += (dot > 0.0 ? dot : 0.0);"),
+    "indexer_ignore_doc_start": ("ki + (int64_t)(start_rows[r] + j) * d", "ki + (int64_t)(j) * d"),
+    "indexer_drop_diagonal": ("if (j >= len_rows[r]) {", "if (j + 1 >= len_rows[r]) {"),
+    "indexer_transposed_q": ("dot += qi[h * d + c] * k[c];", "dot += qi[c * Hi + h] * k[c];"),
+    "topk_tiebreak_reversed": ("return (x->j < y->j) ? -1 : (x->j > y->j);",
+                               "return (x->j > y->j) ? -1 : (x->j < y->j);"),
+    "topk_ascending_scores": ("if (x->score > y->score) return -1;\n  if (x->score < y->score) return 1;",
+                              "if (x->score < y->score) return -1;\n  if (x->score > y->score) return 1;"),
+    "topk_unsorted_ids": ("qsort(out, (size_t)n, sizeof(int32_t), cmp_i32_asc);", ""),
+    "attn_drop_sink": ("double z = zkv + exp(sk - ref);", "double z = zkv;"),
+    "attn_sign_in_exp": ("double p = exp(s[j] - ref);", "double p = exp(ref - s[j]);"),
+    "attn_drop_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
+    "attn_lse_kv_with_sink": ("if (lse_kv) lse_kv[rh] = ref + log(zkv);", "if (lse_kv) lse_kv[rh] = ref + log(z);"),
+    "compact_keeps_key_count": ("(int64_t)id < key_count", "(int64_t)id <= key_count"),
+    "pack_wrong_batch_stride": ("v = b * S + id;", "v = b * W + id;"),
+    "metadata_len_off_by_one": ("len[t] = t - cu[b] + 1;", "len[t] = t - cu[b];"),
+}
+
+
+def _build(tmp_path, text, name):
+    c = tmp_path / f"{name}.c"
+    c.write_text(text)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", "-o", str(so), str(c), "-lm"],
+                   check=True, capture_output=True)
+    return str(so)
+
+
+def _run_pins(lib):
+    env = dict(os.environ, DSA_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return r.returncode
+
+
+def test_unmodified_oracle_passes_pins(tmp_path):
+    assert _run_pins(_build(tmp_path, open(SRC).read(), "orig")) == 0
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert _run_pins(_build(tmp_path, src.replace(old, new), name)) != 0, f"pins missed mutant {name}"

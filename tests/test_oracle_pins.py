@@ -1,0 +1,388 @@
+"""Pins for the fp64 CPU oracle (runs without a GPU).
+
+Each test ties the oracle to something other than itself: hand-derived
+fixtures under tests/golden (each citing the passage it follows), brute force
+over all subsets on tiny inputs, closed forms, special cases that reduce to
+numpy/scipy routines, and invariants.  The cases are chosen so that a dropped
+term, a wrong sign, a wrong index or a transposed operand in the oracle fails
+at least one of them (tests/test_oracle_mutants.py plants such mistakes and
+checks that they are caught).
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- metadata
+def test_metadata_golden():
+    g = _gold("thd_metadata.json")
+    start, length = oracle.thd_metadata(np.array(g["cu_seqlens"]), g["T"])
+    assert start.tolist() == g["start"]
+    assert length.tolist() == g["len"]
+
+
+@pytest.mark.parametrize("cu,T", [([1, 4], 4), ([0, 3, 2], 3), ([0, 3], 4)])
+def test_metadata_rejects_invalid(cu, T):
+    with pytest.raises(ValueError):
+        oracle.thd_metadata(np.array(cu), T)
+
+
+# ----------------------------------------------------------------- indexer
+def _rand_bf16_like(rng, shape, lo=-4, hi=4):
+    return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
+
+
+def test_indexer_single_head_is_relu_matmul():
+    # Hi = 1, w = 1: score[t, j] = max(0, qi[t] . ki[start + j]) -- a plain matmul.
+    rng = np.random.default_rng(11)
+    T, d = 13, 7
+    qi = rng.standard_normal((T, 1, d))
+    ki = rng.standard_normal((T, d))
+    w = np.ones((T, 1))
+    start, length = oracle.thd_metadata(np.array([0, T]), T)
+    got = oracle.indexer_scores(qi, ki, w, start, length, T)
+    ref = np.maximum(qi[:, 0, :] @ ki.T, 0.0)
+    for t in range(T):
+        np.testing.assert_allclose(got[t, : t + 1], ref[t, : t + 1], rtol=1e-13, atol=1e-13)
+        assert np.all(np.isneginf(got[t, t + 1:]))
+
+
+def test_indexer_one_hot_weights_select_the_head():
+    # w = e_h picks head h alone; distinct data per head catches a head/dim mix-up.
+    rng = np.random.default_rng(12)
+    T, Hi, d = 9, 3, 5
+    qi = rng.standard_normal((T, Hi, d))
+    ki = rng.standard_normal((T, d))
+    start, length = oracle.thd_metadata(np.array([0, T]), T)
+    for h in range(Hi):
+        w = np.zeros((T, Hi))
+        w[:, h] = 2.5
+        got = oracle.indexer_scores(qi, ki, w, start, length, T)
+        ref = 2.5 * np.maximum(qi[:, h, :] @ ki.T, 0.0)
+        for t in range(T):
+            np.testing.assert_allclose(got[t, : t + 1], ref[t, : t + 1], rtol=1e-13, atol=1e-13)
+
+
+def test_indexer_linear_in_weights_and_sign():
+    rng = np.random.default_rng(13)
+    T, Hi, d = 8, 4, 6
+    qi = rng.standard_normal((T, Hi, d))
+    ki = rng.standard_normal((T, d))
+    start, length = oracle.thd_metadata(np.array([0, T]), T)
+    w1 = rng.random((T, Hi))
+    w2 = rng.random((T, Hi))
+    s1 = oracle.indexer_scores(qi, ki, w1, start, length, T)
+    s2 = oracle.indexer_scores(qi, ki, w2, start, length, T)
+    s12 = oracle.indexer_scores(qi, ki, w1 + w2, start, length, T)
+    sneg = oracle.indexer_scores(qi, ki, -w1, start, length, T)
+    for t in range(T):
+        np.testing.assert_allclose(s12[t, : t + 1], s1[t, : t + 1] + s2[t, : t + 1], rtol=1e-12)
+        np.testing.assert_allclose(sneg[t, : t + 1], -s1[t, : t + 1], rtol=1e-14)
+        assert np.all(s1[t, : t + 1] >= 0.0)
+
+
+def test_indexer_document_isolation_and_mask():
+    # THD: a token sees exactly the keys from its document start to itself.
+    rng = np.random.default_rng(14)
+    cu = np.array([0, 4, 5, 11])
+    T, Hi, d = 11, 2, 3
+    qi = _rand_bf16_like(rng, (T, Hi, d))
+    ki = _rand_bf16_like(rng, (T, d))
+    w = _rand_bf16_like(rng, (T, Hi), 1, 4)
+    start, length = oracle.thd_metadata(cu, T)
+    s_max = int(np.max(np.diff(cu)))
+    base = oracle.indexer_scores(qi, ki, w, start, length, s_max)
+    # finite exactly on j < len, -inf beyond
+    for t in range(T):
+        assert np.all(np.isfinite(base[t, : length[t]]))
+        assert np.all(np.isneginf(base[t, length[t]:]))
+    # scramble the keys of every other document: row t is unchanged
+    for b in range(len(cu) - 1):
+        ki2 = ki.copy()
+        others = [r for r in range(T) if not (cu[b] <= r < cu[b + 1])]
+        ki2[others] = _rand_bf16_like(rng, (len(others), d))
+        s2 = oracle.indexer_scores(qi, ki2, w, start, length, s_max)
+        rows = slice(cu[b], cu[b + 1])
+        np.testing.assert_array_equal(s2[rows], base[rows])
+    # the diagonal (key == query) is included: brute-force one entry by hand
+    t = 7
+    j = length[t] - 1
+    assert start[t] + j == t
+    hand = sum(w[t, h] * max(0.0, float(np.dot(qi[t, h], ki[t]))) for h in range(Hi))
+    assert base[t, j] == hand
+
+
+def test_indexer_integer_inputs_are_exact_and_bounded():
+    # The tiny workload's integer inputs give integer scores below 2^24 (exact in fp32).
+    rng = np.random.default_rng(15)
+    T, Hi, d = 32, 8, 64
+    qi = _rand_bf16_like(rng, (T, Hi, d))
+    ki = _rand_bf16_like(rng, (T, d))
+    w = _rand_bf16_like(rng, (T, Hi), 1, 4)
+    start, length = oracle.thd_metadata(np.array([0, T]), T)
+    s, a = oracle.indexer_scores(qi, ki, w, start, length, T, want_abs=True)
+    fin = np.isfinite(s)
+    assert np.all(s[fin] == np.round(s[fin]))
+    assert np.all(np.abs(s[fin]) <= a[fin])
+    assert np.max(a[fin]) < 2 ** 24
+
+
+# -------------------------------------------------------------------- top-k
+def test_topk_golden_ties():
+    g = _gold("topk_ties.json")
+    for c in g["k_cases"]:
+        idx, tl = oracle.topk(np.array([c["scores"]], float), np.array([c["len"]]), c["k"],
+                              start_rows=np.array([c["start"]]))
+        assert idx[0].tolist() == c["idx"]
+        assert tl[0] == c["topk_length"]
+
+
+def _brute_topk(scores, k):
+    """The unique subset whose every member beats every non-member under
+    (score descending, index ascending), found by enumerating all subsets."""
+    n = len(scores)
+    m = min(k, n)
+
+    def beats(a, b):
+        return scores[a] > scores[b] or (scores[a] == scores[b] and a < b)
+
+    found = []
+    for sub in itertools.combinations(range(n), m):
+        rest = [j for j in range(n) if j not in sub]
+        if all(beats(a, b) for a in sub for b in rest):
+            found.append(sorted(sub))
+    assert len(found) == 1
+    return found[0]
+
+
+def test_topk_brute_force_small_with_ties():
+    rng = np.random.default_rng(21)
+    for trial in range(300):
+        n = int(rng.integers(0, 10))
+        k = int(rng.integers(1, 6))
+        ld = 10
+        row = np.full(ld, -np.inf)
+        row[:n] = rng.integers(-2, 3, size=n)  # heavy ties
+        start = int(rng.integers(0, 100))
+        idx, tl = oracle.topk(row[None], np.array([n]), k, start_rows=np.array([start]))
+        want = [start + j for j in _brute_topk(list(row[:n]), k)] if n else []
+        assert idx[0, : len(want)].tolist() == want, (trial, row, k)
+        assert np.all(idx[0, len(want):] == -1)
+        assert tl[0] == len(want)
+
+
+def test_topk_distinct_scores_match_argsort():
+    rng = np.random.default_rng(22)
+    n, k = 500, 37
+    row = rng.permutation(n).astype(float) * 0.5 - 100
+    idx, tl = oracle.topk(row[None], np.array([n]), k)
+    want = np.sort(np.argsort(-row, kind="stable")[:k])
+    np.testing.assert_array_equal(idx[0], want)
+    assert tl[0] == k
+
+
+def test_topk_all_equal_takes_lowest_indices():
+    n, k = 50, 8
+    idx, _ = oracle.topk(np.zeros((1, n)), np.array([n]), k, start_rows=np.array([1000]))
+    assert idx[0].tolist() == list(range(1000, 1008))
+
+
+def test_topk_invariants_random():
+    rng = np.random.default_rng(23)
+    T, ld, k = 40, 300, 64
+    lens = rng.integers(0, ld + 1, size=T)
+    sc = rng.integers(0, 40, size=(T, ld)).astype(float)
+    starts = rng.integers(0, 5000, size=T)
+    idx, tl = oracle.topk(sc, lens, k, start_rows=starts)
+    for t in range(T):
+        n = min(k, lens[t])
+        assert tl[t] == n
+        sel = idx[t, :n] - starts[t]
+        assert np.all(np.diff(sel) > 0) and np.all(idx[t, n:] == -1)
+        assert np.all((sel >= 0) & (sel < lens[t]))
+        rest = np.setdiff1d(np.arange(lens[t]), sel)
+        if rest.size and n:
+            # every selected score >= every unselected one; at equality the
+            # selected index is the smaller one
+            minsel = sc[t, sel].min()
+            assert np.all(sc[t, rest] <= minsel)
+            tied = rest[sc[t, rest] == minsel]
+            assert np.all(tied > sel[sc[t, sel] == minsel].max())
+
+
+# ----------------------------------------------------------- compact / sort
+def test_compact_sort_golden():
+    g = _gold("compact_sort.json")
+    out, lengths = oracle.compact_sort(np.array(g["in"]), g["key_count"])
+    assert out.tolist() == g["out"]
+    assert lengths.tolist() == g["lengths"]
+
+
+def test_compact_sort_matches_numpy_sort():
+    rng = np.random.default_rng(31)
+    T, K, kc = 50, 33, 40
+    ind = rng.integers(-5, 50, size=(T, K)).astype(np.int32)
+    out, lengths = oracle.compact_sort(ind, kc)
+    for t in range(T):
+        v = np.sort(ind[t][(ind[t] >= 0) & (ind[t] < kc)])
+        assert lengths[t] == v.size
+        np.testing.assert_array_equal(out[t, : v.size], v)
+        assert np.all(out[t, v.size:] == -1)
+
+
+# ----------------------------------------------------------- route packing
+def test_pack_routes_golden():
+    g = _gold("pack_routes.json")
+    out = oracle.pack_routes(np.array(g["routes"]))
+    assert out.tolist() == g["packed"]
+
+
+def test_pack_routes_invariants():
+    rng = np.random.default_rng(41)
+    B, S, W = 3, 17, 10
+    r = rng.integers(-3, S + 3, size=(B, S, W)).astype(np.int32)
+    out = oracle.pack_routes(r)
+    assert out.shape == (B * S, 12)
+    assert np.all(out[:, W:] == -1)
+    valid = (r >= 0) & (r < S)
+    assert np.array_equal(out[:, :W] >= 0, valid.reshape(B * S, W))
+    b_of_row = np.repeat(np.arange(B), S)
+    ok = out[:, :W] >= 0
+    assert np.all((out[:, :W][ok] // S) == np.broadcast_to(b_of_row[:, None], (B * S, W))[ok])
+    assert np.all((out[:, :W][ok] % S) == r.reshape(B * S, W)[ok])
+
+
+# --------------------------------------------------------------- attention
+def test_attention_golden_hand_example():
+    g = _gold("attention_hand.json")
+    res = oracle.sparse_attn(np.array(g["q"]), np.array(g["kv"]), np.array(g["idx"]), math.log(3) / 2,
+                             sink=np.array(g["sink"]), dv=1)
+    np.testing.assert_allclose(res["out"], np.array(g["out"]), rtol=1e-14)
+    assert res["lse"][0, 0] == pytest.approx(math.log(g["lse_ln"]), rel=1e-14)
+    assert res["lse_kv"][0, 0] == pytest.approx(math.log(g["lse_kv_ln"]), rel=1e-14)
+    assert res["max_logits"][0, 0] == pytest.approx(math.log(g["max_logits_ln"]), rel=1e-14)
+
+
+def _dense_causal_with_sink(q, kv, sink, scale, dv, t):
+    """Dense causal attention for row t with the sink as an extra logit whose
+    value vector is zero, through scipy's softmax/logsumexp."""
+    logits = scale * q[t] @ kv[: t + 1].T                  # [H, t+1]
+    full = np.concatenate([logits, sink[:, None]], axis=1)  # sink as one more column
+    p = softmax(full, axis=1)
+    out = p[:, :-1] @ kv[: t + 1, :dv]
+    return out, logsumexp(full, axis=1), logsumexp(logits, axis=1), logits.max(axis=1), p
+
+
+@pytest.mark.parametrize("qscale", [1.0, 30.0])
+def test_attention_all_selected_equals_dense(qscale):
+    rng = np.random.default_rng(51)
+    T, H, Dqk, Dv = 12, 3, 10, 6
+    q = rng.standard_normal((T, H, Dqk)) * qscale
+    kv = rng.standard_normal((T, Dqk))
+    sink = rng.standard_normal(H) * 3
+    K = T
+    idx = np.full((T, K), -1, np.int32)
+    for t in range(T):
+        idx[t, : t + 1] = rng.permutation(t + 1)  # every causal key, in any slot order
+    res = oracle.sparse_attn(q, kv, idx, 0.37, sink=sink, dv=Dv)
+    for t in range(T):
+        out, lse, lse_kv, ml, p = _dense_causal_with_sink(q, kv, sink, 0.37, Dv, t)
+        np.testing.assert_allclose(res["out"][t], out, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(res["lse"][t], lse, rtol=1e-12)
+        np.testing.assert_allclose(res["lse_kv"][t], lse_kv, rtol=1e-12)
+        np.testing.assert_allclose(res["max_logits"][t], ml, rtol=1e-12)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=1e-12)
+
+
+def test_attention_single_key_no_sink():
+    rng = np.random.default_rng(52)
+    q = rng.standard_normal((1, 2, 8))
+    kv = rng.standard_normal((5, 8))
+    res = oracle.sparse_attn(q, kv, np.array([[3, -1, -1]]), 0.5, dv=4)
+    np.testing.assert_allclose(res["out"][0], np.broadcast_to(kv[3, :4], (2, 4)), rtol=1e-14)
+    np.testing.assert_allclose(res["lse"][0], 0.5 * q[0] @ kv[3], rtol=1e-13)
+
+
+def test_attention_identical_keys_closed_form():
+    # n copies of one key: out = V * n e^s / (n e^s + e^sink).
+    rng = np.random.default_rng(53)
+    q = rng.standard_normal((1, 4, 6))
+    kv = rng.standard_normal((3, 6))
+    sink = rng.standard_normal(4)
+    n = 5
+    res = oracle.sparse_attn(q, kv, np.array([[1] * n + [-1]]), 0.8, sink=sink, dv=6)
+    s = 0.8 * q[0] @ kv[1]
+    frac = n * np.exp(s) / (n * np.exp(s) + np.exp(sink))
+    np.testing.assert_allclose(res["out"][0], frac[:, None] * kv[1][None, :], rtol=1e-12)
+    np.testing.assert_allclose(res["lse"][0], np.log(n * np.exp(s) + np.exp(sink)), rtol=1e-12)
+
+
+def test_attention_slot_semantics():
+    rng = np.random.default_rng(54)
+    T, H, D, Tkv, K = 6, 2, 8, 20, 7
+    q = rng.standard_normal((T, H, D))
+    kv = rng.standard_normal((Tkv, D))
+    sink = rng.standard_normal(H)
+    idx = rng.integers(0, Tkv, size=(T, K)).astype(np.int32)
+    base = oracle.sparse_attn(q, kv, idx, 0.3, sink=sink, dv=5)
+    # slot order is irrelevant
+    perm = oracle.sparse_attn(q, kv, idx[:, rng.permutation(K)], 0.3, sink=sink, dv=5)
+    np.testing.assert_allclose(perm["out"], base["out"], rtol=1e-12)
+    # invalid and out-of-range slots are absent slots
+    bad = np.concatenate([idx, np.array([[-1, Tkv, Tkv + 5, -7]] * T, np.int32)], axis=1)
+    withbad = oracle.sparse_attn(q, kv, bad, 0.3, sink=sink, dv=5)
+    np.testing.assert_allclose(withbad["out"], base["out"], rtol=1e-13)
+    np.testing.assert_allclose(withbad["lse"], base["lse"], rtol=1e-13)
+    # topk_length truncation equals -1 padding; lengths clamp to [0, K]
+    lens = np.array([0, 3, 7, 9, -2, 5], np.int32)
+    trunc = oracle.sparse_attn(q, kv, idx, 0.3, sink=sink, dv=5, topk_length=lens)
+    pad = idx.copy()
+    for t in range(T):
+        pad[t, max(0, min(K, lens[t])):] = -1
+    padded = oracle.sparse_attn(q, kv, pad, 0.3, sink=sink, dv=5)
+    np.testing.assert_allclose(trunc["out"], padded["out"], rtol=1e-13)
+    np.testing.assert_allclose(trunc["lse"], padded["lse"], rtol=1e-13)
+    # lse (with sink) = logaddexp(lse_kv, sink) on non-empty rows
+    np.testing.assert_allclose(base["lse"], np.logaddexp(base["lse_kv"], sink[None, :]), rtol=1e-12)
+
+
+def test_attention_empty_rows():
+    q = np.ones((2, 3, 4))
+    kv = np.ones((4, 4))
+    sink = np.array([0.5, -1.0, 2.0])
+    res = oracle.sparse_attn(q, kv, np.full((2, 3), -1, np.int32), 1.0, sink=sink, dv=2)
+    assert np.all(res["out"] == 0.0)
+    assert np.all(np.isposinf(res["lse_kv"])) and np.all(np.isneginf(res["max_logits"]))
+    np.testing.assert_array_equal(res["lse"], np.broadcast_to(sink, (2, 3)))
+    nos = oracle.sparse_attn(q, kv, np.full((2, 3), -1, np.int32), 1.0, dv=2)
+    assert np.all(np.isneginf(nos["lse"]))
+
+
+def test_attention_separate_v_equals_latent_layout():
+    # With V separate: pad q with zeros in front of kv' = [v | k]; V' = first Dv columns.
+    rng = np.random.default_rng(55)
+    T, H, Dk, Dv, Tkv, K = 5, 3, 6, 4, 9, 5
+    q = rng.standard_normal((T, H, Dk))
+    k = rng.standard_normal((Tkv, Dk))
+    v = rng.standard_normal((Tkv, Dv))
+    idx = rng.integers(-1, Tkv, size=(T, K)).astype(np.int32)
+    a = oracle.sparse_attn(q, k, idx, 0.6, v=v)
+    q2 = np.concatenate([np.zeros((T, H, Dv)), q], axis=2)
+    kv2 = np.concatenate([v, k], axis=1)
+    b = oracle.sparse_attn(q2, kv2, idx, 0.6, dv=Dv)
+    np.testing.assert_allclose(a["out"], b["out"], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(a["lse"], b["lse"], rtol=1e-12)
