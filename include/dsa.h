@@ -1,0 +1,186 @@
+/*
+ * dsa.h -- C ABI of libdsa.so, the GB300 (sm_103a) DeepSeek Sparse Attention
+ * (DSA) forward hot path.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor argument is a caller-owned, contiguous, row-major DEVICE
+ *    pointer on the current CUDA device.  bf16 tensors are passed as void*
+ *    (IEEE bfloat16 bit patterns), fp32 as float*, ids as int32_t*.
+ *  - The library never allocates, frees or synchronises.  Work is enqueued
+ *    on `stream` and the call returns immediately; scratch space is passed in
+ *    by the caller and sized by a query function.
+ *  - All host-visible arguments are validated before anything is launched or
+ *    written.  On failure nothing is enqueued and an error code is returned;
+ *    dsa_last_error() then describes it.  There is no fallback path.
+ *  - Values inside device tensors (ids, cu_seqlens monotonicity, lengths) are
+ *    a caller contract: the kernels clamp or skip what is out of range but do
+ *    not report it.  Bounded device waits that give up, and candidate buffers
+ *    that overflow, set bits in the device status word (dsa_device_status).
+ *  - Layout names follow the pages: T = total (packed THD) query tokens,
+ *    H = attention heads, Hi = indexer heads, d = indexer head dim,
+ *    K = top-k / sparse width, Dqk = query/key dim, Dv = value dim.
+ *
+ * Sources, by page and section:
+ *  [cuDNN-DSA] cuDNN Frontend, "DeepSeek Sparse Attention (DSA)":
+ *      1 Sparse Attention Forward, 3 Indexer Forward, 4 Combined Indexer
+ *      Forward + Top-K, 5 Indexer Top-K, "Compact vs. non-compact sparse
+ *      indices".
+ *  [NeMo-GLM] NeMo AutoModel, nemo_automodel.components.models.glm_moe_dsa.
+ *      kernels.cudnn_dsa: prepare_cudnn_dsa_packed_metadata,
+ *      cudnn_indexer_topk, cudnn_sparse_attention, _compact_and_sort_indices,
+ *      _topk_wrapper_chunked and the module constants.
+ *  [NeMo-common] NeMo AutoModel, ...models.common.cudnn_sparse_attention.
+ *  [NeMo-QSA] NeMo AutoModel, ...models.qwen3_8_flash_next.cudnn_qsa:
+ *      _pack_indices, cudnn_sparse_gqa_attention.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes (the pages' ValueError / RuntimeError split, [NeMo-GLM]
+ * cudnn_indexer_topk and cudnn_sparse_attention "Raises"). */
+#define DSA_OK 0
+#define DSA_ERR_VALUE 1        /* bad shape, size, k, scale, pointer or alignment */
+#define DSA_ERR_UNSUPPORTED 2  /* no CUDA device, or the device is not sm_103 */
+#define DSA_ERR_CUDA 3         /* a CUDA runtime call or launch failed */
+#define DSA_ERR_WORKSPACE 4    /* workspace pointer/size too small or misaligned */
+
+/* Bits of the device status word (see dsa_device_status). */
+#define DSA_STATUS_WAIT_TIMEOUT 0x1u   /* a bounded device wait gave up */
+#define DSA_STATUS_CAND_OVERFLOW 0x2u  /* fused top-k candidate buffer overflowed */
+
+/* Limits ([NeMo-GLM] _MAX_TOPK = 2048, _INDEX_HEAD_DIM = 128,
+ * _ATTENTION_HEAD_DIM = 576, _VALUE_HEAD_DIM = 512; [cuDNN-DSA] 5: top_k <= 2048). */
+#define DSA_MAX_TOPK 2048
+#define DSA_MAX_COMPACT_WIDTH 16384
+
+/* Thread-local description of the last error returned on this thread
+ * (empty string after a successful call).  Never NULL. */
+const char* dsa_last_error(void);
+
+/* Reads (and when clear != 0, resets) the status word of the current
+ * device: an OR of DSA_STATUS_* bits set by kernels since the last clear.
+ * This call synchronises the device (it is a diagnostic, not part of the
+ * hot path).  Returns DSA_OK or DSA_ERR_CUDA / DSA_ERR_UNSUPPORTED. */
+int dsa_device_status(uint32_t* flags, int clear);
+
+/* THD metadata ([NeMo-GLM] prepare_cudnn_dsa_packed_metadata, "Returns":
+ * per-query storage starts and real causal lengths).
+ *   cu_seqlens int32 [n_docs + 1]: cumulative document lengths, cu[0] = 0,
+ *       cu[n_docs] = T, non-decreasing (device contract).
+ *   start int32 [T] (out): first row of the token's document.
+ *   len   int32 [T] (out): causal length t - start[t] + 1.
+ * Errors: DSA_ERR_VALUE for n_docs < 1, T < 0 or NULL pointers (T = 0 is a
+ * no-op). */
+int dsa_thd_metadata(const int32_t* cu_seqlens, int n_docs, int T, int32_t* start, int32_t* len,
+                     cudaStream_t stream);
+
+/* Lightning-indexer scores, dense ([cuDNN-DSA] 3 with ratio 1 and zero causal
+ * offsets; THD form of [NeMo-GLM] cudnn_indexer_topk):
+ *   scores[t, j] = sum_h w[t, h] * ReLU( sum_c qi[t, h, c] * ki[start[t] + j, c] )
+ * for 0 <= j < len[t] and -inf for len[t] <= j < s_max.  The head weights
+ * arrive already scaled; nothing is rescaled here.
+ *   qi bf16 [T, Hi, d], ki bf16 [T, d], w fp32 [T, Hi],
+ *   cu_seqlens int32 [n_docs + 1] (as in dsa_thd_metadata),
+ *   s_max: the longest document (host value; columns written per row),
+ *   scores fp32 [T, ld] (out), ld >= s_max, ld % 4 == 0.
+ * Accumulation is fp32 on the tensor cores (products of bf16 are exact).
+ * Shapes: d in {64, 128}, Hi in {8, 16, 32, 64}; qi, ki 16-byte aligned.
+ * Errors: DSA_ERR_VALUE on any violated shape/alignment rule. */
+int dsa_indexer_scores(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                       int n_docs, int T, int Hi, int d, int s_max, float* scores, int64_t ld,
+                       cudaStream_t stream);
+
+/* Per-row top-k ([cuDNN-DSA] 5 radix top-k with per-row lengths, top_k <=
+ * 2048; tie-break of [cuDNN-DSA] 4 deterministic=True; compact prefix of
+ * [NeMo-GLM] cudnn_sparse_attention topk_length):
+ * for row t the min(k, len[t]) largest of scores[t, 0:len[t]] are selected,
+ * equal scores going to the smaller column.  Their ids (row_start[t] + j, or
+ * j when row_start is NULL) are written in ASCENDING id order, then -1.
+ *   scores fp32 [T, ld], len int32 [T] (clamped to [0, ld]),
+ *   row_start int32 [T] or NULL, idx int32 [T, k] (out),
+ *   topk_length int32 [T] or NULL (out, = min(k, len[t])),
+ *   vals fp32 [T, k] or NULL (out: the score of each selected slot, -inf
+ *   on padding).
+ * Shapes: 1 <= k <= 2048, ld >= 1; NaN scores have no defined order.
+ * Errors: DSA_ERR_VALUE. */
+int dsa_topk(const float* scores, int64_t ld, const int32_t* len, const int32_t* row_start, int T,
+             int k, int32_t* idx, int32_t* topk_length, float* vals, cudaStream_t stream);
+
+/* Compact and sort ([NeMo-common] _compact_and_sort_indices; [cuDNN-DSA]
+ * "Compact vs. non-compact sparse indices"): per row, ids with
+ * 0 <= id < key_count are sorted ascending into a prefix (duplicates kept),
+ * the rest of the row is -1, lengths[t] = number of valid ids.  The id
+ * convention is preserved (local stays local).
+ *   in int32 [T, K], out int32 [T, K] (may alias in), lengths int32 [T].
+ * Shapes: 1 <= K <= DSA_MAX_COMPACT_WIDTH, key_count >= 0.
+ * Errors: DSA_ERR_VALUE. */
+int dsa_compact_sort_indices(const int32_t* in, int T, int K, int64_t key_count, int32_t* out,
+                             int32_t* lengths, cudaStream_t stream);
+
+/* Workspace bytes that dsa_indexer_topk needs for these shapes (0 on invalid
+ * shapes).  Depends on shapes only, never on data. */
+size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max);
+
+/* Fused indexer + top-k ([cuDNN-DSA] 4: one call, no dense [T, S] score
+ * matrix, caller-owned candidate buffer, -1 padding, deterministic
+ * tie-break; stage 2 is a separate selection as in [cuDNN-DSA] "Limitations").
+ * Result: identical (bit for bit) to dsa_indexer_scores followed by dsa_topk
+ * with global ids (row_start = start[t]).
+ *   inputs as dsa_indexer_scores; idx int32 [T, k] (out, ascending global
+ *   ids, -1 suffix); topk_length int32 [T] or NULL (out);
+ *   workspace: device buffer of ws_bytes >= dsa_indexer_topk_workspace_size,
+ *   256-byte aligned, contents ignored on entry.
+ * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE.  If a row's candidates exceed
+ * the workspace's per-row capacity the row is recomputed through a dense
+ * fallback inside the workspace; DSA_STATUS_CAND_OVERFLOW records that it
+ * happened. */
+int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                     int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
+                     int32_t* topk_length, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Sparse MQA attention forward ([cuDNN-DSA] 1; THD shapes of [NeMo-GLM]
+ * cudnn_sparse_attention).  For row t, head h and valid slot j (j <
+ * clamp(topk_length[t], 0, K) when lengths are given, and 0 <= idx[t,j] <
+ * Tkv):  s_j = scale * q[t,h,:] . kv[idx[t,j], 0:Dqk]; invalid or
+ * out-of-range slots count as absent, duplicates are separate slots.
+ *   Z = sum_j exp(s_j) + exp(sink[h]);  out[t,h,:] = sum_j exp(s_j) V_j / Z
+ * with V_j = v[idx_j, :] when v is given, else kv[idx_j, 0:Dv].
+ *   q bf16 [T, H, Dqk]; kv bf16 [Tkv, Dqk]; v bf16 [Tkv, Dv] or NULL;
+ *   idx int32 [T, K]; topk_length int32 [T] or NULL; sink fp32 [H] or NULL
+ *   (NULL = -inf, i.e. no sink);
+ *   out bf16 [T, H, Dv] (out);
+ *   lse fp32 [T, H] (out, required): log Z, the denominator out uses (sink
+ *       included; empty row: sink[h], or -inf without a sink);
+ *   lse_kv fp32 [T, H] or NULL (out): log sum_j exp(s_j), KV only (empty
+ *       row: +inf) -- the cuDNN "lse" statistic;
+ *   max_logits fp32 [T, H] or NULL (out): max_j s_j (empty row: -inf).
+ * Shapes: (Dqk, Dv) in {(576, 512), (512, 512)} with v == NULL, or
+ * (256, 256) with a separate v; 1 <= H <= 128; K >= 0; scale finite > 0;
+ * q, kv, v, out 16-byte aligned.
+ * Errors: DSA_ERR_VALUE. */
+int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int32_t* idx,
+                        const int32_t* topk_length, const float* sink, int T, int Tkv, int H,
+                        int Dqk, int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
+                        float* max_logits, cudaStream_t stream);
+
+/* Route packing ([NeMo-QSA] _pack_indices): routes int32 [B, S, W] hold
+ * batch-local ids; out int32 [B*S, Wp] with Wp = ceil(W/4)*4 receives
+ * b*S + id for 0 <= id < S and -1 otherwise (including slots W..Wp-1).
+ * Shapes: B, S >= 1, 1 <= W.  Errors: DSA_ERR_VALUE. */
+int dsa_pack_routes(const int32_t* routes, int B, int S, int W, int32_t* out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,589 @@
+// indexer.cu -- lightning-indexer scores on tcgen05 (dense and fused top-k).
+//
+// score[t, j] = sum_h w[t, h] * ReLU(qi[t, h, :] . ki[start[t] + j, :])
+// (cuDNN Frontend DSA page, section 3 Indexer Forward, ratio 1; THD shapes of
+// NeMo glm_moe_dsa cudnn_indexer_topk; head weights arrive pre-scaled).
+//
+// Tiling ("swap AB"): one tcgen05.mma computes D[key, (token, head)] for a
+// tile of 128 keys (M) against a block of QB tokens x Hi heads = 256 query
+// rows (N), contracting over d (K) in steps of 16.  The accumulator lives in
+// TMEM (2 x 256 fp32 columns, double-buffered) so that the epilogue of one key
+// tile overlaps the MMAs of the next.  Each epilogue thread owns one key (a
+// TMEM lane) and reduces over the heads of its tokens:
+//     score = fma(w[h], max(D, 0), score), h = 0 .. Hi-1 in order,
+// which is the same instruction sequence in both modes, so the fused mode
+// sees exactly the scores that the dense mode writes.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads (qi block once per block,
+// ki tiles through a multi-stage ring), warp 1 allocates TMEM and issues the
+// MMAs, warps 2..9 run the epilogue (two warps per TMEM lane quarter, each on
+// half of the 256 columns).  The kernel is persistent: CTA c handles query
+// blocks nblocks-1-c, nblocks-1-c-grid, ... (the longest causal rows first).
+//
+// Dense mode writes scores[t, j] for j < len[t] and -inf up to s_max.
+// Fused mode (cuDNN DSA section 4: no dense score matrix, caller-owned
+// candidate buffer) appends (key(score), j) to row t's candidate list when
+// key(score) >= tau[t], a running lower bound of the row's k-th largest key.
+// tau is the lower edge of the highest histogram bin at which the emitted
+// candidates so far number >= k; since the emitted keys are a subset of the
+// keys seen, that edge never exceeds the final k-th largest key, so every
+// member of the final top-k (ties included) is emitted.  Stage 2 then
+// selects exactly from the candidates (topk.cu).
+#include <climits>
+
+#include "common.cuh"
+#include "topk_select.cuh"
+
+namespace {
+
+constexpr int kKeyTile = 128;
+constexpr int kNRows = 256;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kHistWords = 8192;   // 16384 16-bit bin counters shared by the block's rows
+constexpr int kTauUpdateEvery = 256;
+
+struct IndexerParams {
+  const float* w;
+  const int32_t* cu;
+  int n_docs;
+  int T;
+  int Hi;
+  int d;
+  int qb;        // tokens per block = 256 / Hi
+  int nblocks;
+  int stages;
+  // dense
+  float* scores;
+  int64_t ld;
+  int s_max;
+  // fused
+  uint32_t* cand_key;
+  int32_t* cand_idx;
+  int32_t* cand_cnt;
+  int cap;
+  int k;
+  int hist_bits;  // log2(bins per row)
+  uint32_t* status;
+};
+
+struct SmemLayout {
+  uint32_t q_off, k_off, w_off, tok_off, hist_off, row_off, bar_off, misc_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int fused) {
+  SmemLayout L;
+  const uint32_t nch = d / 64;
+  uint32_t o = 0;
+  L.q_off = o;
+  o += nch * kNRows * 128;
+  L.k_off = o;
+  o += stages * nch * kKeyTile * 128;
+  L.w_off = o;
+  o += kNRows * 4;
+  L.tok_off = o;
+  o += 2 * 32 * 4;
+  L.hist_off = o;
+  if (fused) o += kHistWords * 4;
+  L.row_off = o;
+  o += 4 * 32 * 4;  // tau, cnt, since, spare per row
+  L.bar_off = o;
+  o += (2 * 8 + 6) * 8;
+  L.misc_off = o;
+  o += 16;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ int doc_start(const int32_t* __restrict__ cu, int n_docs, int t) {
+  int lo = 0, hi = n_docs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return __ldg(cu + lo);
+}
+
+struct BlockRange {
+  int t0, t1, kt0, kt1;
+};
+
+__device__ __forceinline__ BlockRange block_range(const IndexerParams& p, int blk) {
+  BlockRange r;
+  r.t0 = blk * p.qb;
+  r.t1 = min(r.t0 + p.qb, p.T);
+  r.kt0 = doc_start(p.cu, p.n_docs, r.t0) / kKeyTile;
+  r.kt1 = (r.t1 - 1) / kKeyTile;
+  return r;
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Raise tau of one row from its packed 16-bit histogram (one warp).
+__device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, int hist_bits, int k, uint32_t* tau) {
+  const int lane = threadIdx.x & 31;
+  const int per = words / 32;  // words per lane; lane 0 owns the highest bins
+  const int w_hi = words - lane * per;
+  int s = 0;
+  for (int i = w_hi - 1; i >= w_hi - per; --i) {
+    const uint32_t v = hist_row[i];
+    s += static_cast<int>((v & 0xFFFFu) + (v >> 16));
+  }
+  int incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int excl = incl - s;
+  if (excl < k && incl >= k) {
+    int acc = excl;
+    for (int i = w_hi - 1; i >= w_hi - per; --i) {
+      const uint32_t v = hist_row[i];
+      const int hi_c = static_cast<int>(v >> 16), lo_c = static_cast<int>(v & 0xFFFFu);
+      int bin = -1;
+      if (acc + hi_c >= k) bin = 2 * i + 1;
+      else if (acc + hi_c + lo_c >= k) bin = 2 * i;
+      if (bin >= 0) {
+        const uint32_t t = static_cast<uint32_t>(bin) << (32 - hist_bits);
+        if (t > *tau) *tau = t;
+        break;
+      }
+      acc += hi_c + lo_c;
+    }
+  }
+  __syncwarp();
+}
+
+template <int FUSED, int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const IndexerParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = dsa::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const SmemLayout L = smem_layout(p.d, p.stages, p.qb, FUSED);
+  uint8_t* qbuf = smem + L.q_off;
+  uint8_t* kbuf = smem + L.k_off;
+  float* w_s = reinterpret_cast<float*>(smem + L.w_off);
+  int32_t* tok_start = reinterpret_cast<int32_t*>(smem + L.tok_off);
+  int32_t* tok_len = tok_start + 32;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist_off);
+  uint32_t* row_tau = reinterpret_cast<uint32_t*>(smem + L.row_off);
+  int32_t* row_cnt = reinterpret_cast<int32_t*>(row_tau + 32);
+  int32_t* row_since = row_cnt + 32;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + 8;
+  uint64_t* qfull = bars + 16;
+  uint64_t* qempty = bars + 17;
+  uint64_t* tfull = bars + 18;   // [2]
+  uint64_t* tempty = bars + 20;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nch = p.d / 64;
+  const int S = p.stages;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      dsa::mbar_init(&full[s], 1);
+      dsa::mbar_init(&empty[s], 1);
+    }
+    dsa::mbar_init(qfull, 1);
+    dsa::mbar_init(qempty, 1);
+    for (int b = 0; b < 2; ++b) {
+      dsa::mbar_init(&tfull[b], 1);
+      dsa::mbar_init(&tempty[b], kEpiWarps);
+    }
+    *abort_flag = 0;
+    dsa::fence_barrier_init();
+  }
+  if (warp == 1) dsa::tmem_alloc(tmem_slot, kTmemCols);
+  dsa::tc_fence_before();
+  __syncthreads();
+  dsa::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      dsa::tma_prefetch_desc(&map_q);
+      dsa::tma_prefetch_desc(&map_k);
+      int stage = 0;
+      uint32_t phase = 0;
+      int iter = 0;
+      bool ok = true;
+      for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
+        const BlockRange br = block_range(p, blk);
+        if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
+        for (int c = 0; c < nch; ++c)
+          dsa::tma_load_2d(qbuf + c * kNRows * 128, &map_q, c * 64, br.t0 * p.Hi, qfull);
+        for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+          if (!dsa::mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          dsa::mbar_expect_tx(&full[stage], nch * kKeyTile * 128);
+          uint8_t* dst = kbuf + stage * nch * kKeyTile * 128;
+          for (int c = 0; c < nch; ++c)
+            dsa::tma_load_2d(dst + c * kKeyTile * 128, &map_k, c * 64, kt * kKeyTile, &full[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = dsa::idesc_bf16(kKeyTile, kNRows, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int iter = 0;
+      bool ok = true;
+      const uint32_t q_addr = dsa::smem_u32(qbuf), k_addr = dsa::smem_u32(kbuf);
+      for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
+        const BlockRange br = block_range(p, blk);
+        if (!dsa::mbar_wait(qfull, iter & 1, abort_flag, p.status)) break;
+        dsa::tc_fence_after();
+        for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+          if (!dsa::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!dsa::mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          dsa::tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kNRows;
+          const uint32_t a0 = k_addr + stage * nch * kKeyTile * 128;
+          for (int c = 0; c < nch; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = dsa::smem_desc(a0 + c * kKeyTile * 128 + kk * 32, 16, 1024, dsa::kSwizzle128B);
+              const uint64_t bd = dsa::smem_desc(q_addr + c * kNRows * 128 + kk * 32, 16, 1024, dsa::kSwizzle128B);
+              dsa::umma_bf16(d_tmem, ad, bd, idesc, (c | kk) != 0);
+            }
+          }
+          dsa::umma_commit(&empty[stage]);
+          dsa::umma_commit(&tfull[acc]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
+        dsa::umma_commit(qempty);
+      }
+    }
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int ew = warp - 2;                  // 0..7
+    const int quarter = warp & 3;             // TMEM lane quarter of this warp
+    const int half = ew >> 2;                 // column half: 0 or 1
+    const int et = threadIdx.x - 64;          // 0..255
+    const int key_lane = quarter * 32 + lane; // key within the tile
+    constexpr int QB = kNRows / HI;
+    constexpr int tok_per_half = QB / 2;
+    const int Hi = HI;
+    const int hist_words_row = FUSED ? (kHistWords / QB) : 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
+      const BlockRange br = block_range(p, blk);
+      named_bar(1, kEpiThreads);  // previous block's readers of w_s / tok_* are done
+      for (int i = et; i < kNRows; i += kEpiThreads) {
+        const int r = i / HI, h = i - r * HI;
+        const int t = br.t0 + r;
+        w_s[i] = t < p.T ? __ldg(p.w + static_cast<int64_t>(t) * Hi + h) : 0.f;
+      }
+      if (et < p.qb) {
+        const int t = br.t0 + et;
+        if (t < p.T) {
+          const int s = doc_start(p.cu, p.n_docs, t);
+          tok_start[et] = s;
+          tok_len[et] = t - s + 1;
+        } else {
+          tok_start[et] = INT_MAX;
+          tok_len[et] = 0;
+        }
+        if (FUSED) {
+          row_tau[et] = 0u;
+          row_cnt[et] = 0;
+          row_since[et] = 0;
+        }
+      }
+      if (FUSED)
+        for (int i = et; i < kHistWords; i += kEpiThreads) hist[i] = 0u;
+      named_bar(1, kEpiThreads);
+
+      for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+        if (!dsa::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) { ok = false; break; }
+        dsa::tc_fence_after();
+        const int s_key = kt * kKeyTile + key_lane;  // absolute key row
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows;
+        // columns [half*128, half*128+128) = tokens [half*tok_per_half, ...)
+        float score = 0.f;
+#pragma unroll
+        for (int chunk = 0; chunk < 4; ++chunk) {
+          uint32_t v[32];
+          dsa::tmem_ld32(t_addr + half * 128 + chunk * 32, v);
+          dsa::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int cl = chunk * 32 + i;            // column within this half (compile-time)
+            const int h = cl % HI;                    // 128 % HI == 0, so the half offset drops out
+            if (h == 0) score = 0.f;
+            score = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), score);
+            if (h == HI - 1) {
+              const int r = half * tok_per_half + cl / HI;
+              const int t = br.t0 + r;
+              const int st = tok_start[r];
+              const bool valid = (s_key >= st) && (s_key <= t) && (t < p.T);
+              if (!FUSED) {
+                if (valid) p.scores[static_cast<int64_t>(t) * p.ld + (s_key - st)] = score;
+              } else {
+                const uint32_t key = dsa::f32_key(score);
+                const bool emit = valid && key >= row_tau[r];
+                const int slot = dsa::warp_append(&row_cnt[r], emit);
+                const bool stored = slot >= 0 && slot < p.cap;
+                if (stored) {
+                  const int64_t o = static_cast<int64_t>(t) * p.cap + slot;
+                  p.cand_key[o] = key;
+                  p.cand_idx[o] = s_key - st;
+                }
+                const uint32_t bin = key >> (32 - p.hist_bits);
+                // bin b of this row lives in 16-bit half (b & 1) of word (b >> 1)
+                const uint32_t act = __ballot_sync(0xffffffffu, stored);
+                if (stored) {
+                  const uint32_t peers = __match_any_sync(act, bin);
+                  if (lane == __ffs(peers) - 1)
+                    atomicAdd(&hist[r * hist_words_row + (bin >> 1)], static_cast<uint32_t>(__popc(peers))
+                                                                          << (16 * (bin & 1)));
+                }
+                if (lane == 0 && act) atomicAdd(&row_since[r], __popc(act));
+              }
+            }
+          }
+        }
+        dsa::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) dsa::mbar_arrive(&tempty[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        if (FUSED) {
+          // raise tau of this half's rows once enough new candidates arrived
+          named_bar(2 + half, 128);
+          const int r0 = half * tok_per_half;
+          bool need = false;
+          for (int r = r0; r < r0 + tok_per_half; ++r) need |= row_since[r] >= kTauUpdateEvery;
+          if (need) {
+            named_bar(2 + half, 128);  // every warp of the half has read row_since
+            for (int r = r0 + (ew & 3); r < r0 + tok_per_half; r += 4) {
+              if (row_since[r] >= kTauUpdateEvery && row_cnt[r] <= p.cap) {
+                update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
+                if (lane == 0) row_since[r] = 0;
+              }
+            }
+            named_bar(2 + half, 128);
+          }
+        }
+      }
+      if (!ok) break;
+      named_bar(1, kEpiThreads);
+      if (!FUSED) {
+        // columns len[t] .. s_max-1 of the block's rows are -inf
+        for (int r = 0; r < p.qb; ++r) {
+          const int t = br.t0 + r;
+          if (t >= p.T) break;
+          float* row = p.scores + static_cast<int64_t>(t) * p.ld;
+          for (int j = tok_len[r] + et; j < p.s_max; j += kEpiThreads) row[j] = -INFINITY;
+        }
+      } else if (et < p.qb) {
+        const int t = br.t0 + et;
+        if (t < p.T) p.cand_cnt[t] = row_cnt[et];
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    dsa::tc_fence_after();
+    dsa::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Stage 2 of the fused path: exact top-k of each row's candidates.
+__global__ void __launch_bounds__(dsa::kTopkThreads)
+    fused_select_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint32_t* cand_key,
+                        const int32_t* cand_idx, const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx,
+                        int32_t* topk_length, uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t smem_raw2[];
+  dsa::TopkShared& S = *reinterpret_cast<dsa::TopkShared*>(smem_raw2);
+  const int t = blockIdx.x;
+  const int st = doc_start(cu, n_docs, t);
+  const int len = t - st + 1;
+  int32_t* out = idx + static_cast<int64_t>(t) * k;
+  if (len <= k) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < len ? st + j : -1;
+    if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
+    return;
+  }
+  int n = cand_cnt[t];
+  if (n > cap) {
+    if (threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
+    n = cap;
+  }
+  if (n < k) {  // only reachable after an overflow: keep the output well-formed
+    for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
+    if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
+    return;
+  }
+  const dsa::PairSrc src{cand_key + static_cast<int64_t>(t) * cap, cand_idx + static_cast<int64_t>(t) * cap, n};
+  dsa::select_topk(S, src, k);
+  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = st + S.sel[i];
+  if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
+}
+
+int validate_indexer(const void* qi, const void* ki, const float* w, const int32_t* cu, int n_docs, int T, int Hi,
+                     int d, int s_max, const char* fn) {
+  if (!qi || !ki || !w || !cu) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL input pointer", fn);
+  if (n_docs < 1 || T < 1) return dsa::set_error(DSA_ERR_VALUE, "%s: need n_docs >= 1 and T >= 1", fn);
+  if (d != 64 && d != 128) return dsa::set_error(DSA_ERR_VALUE, "%s: d must be 64 or 128 (got %d)", fn, d);
+  if (Hi != 8 && Hi != 16 && Hi != 32 && Hi != 64)
+    return dsa::set_error(DSA_ERR_VALUE, "%s: Hi must be 8, 16, 32 or 64 (got %d)", fn, Hi);
+  if (s_max < 1 || s_max > T) return dsa::set_error(DSA_ERR_VALUE, "%s: need 1 <= s_max <= T", fn);
+  if (!dsa::aligned(qi, 16) || !dsa::aligned(ki, 16))
+    return dsa::set_error(DSA_ERR_VALUE, "%s: qi and ki must be 16-byte aligned", fn);
+  if (static_cast<int64_t>(T) * Hi > INT_MAX) return dsa::set_error(DSA_ERR_VALUE, "%s: T*Hi too large", fn);
+  return DSA_OK;
+}
+
+int make_maps(const void* qi, const void* ki, int T, int Hi, int d, CUtensorMap* mq, CUtensorMap* mk) {
+  int rc = dsa::encode_tensor_map_2d(mq, qi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, static_cast<uint64_t>(T) * Hi,
+                                     static_cast<uint64_t>(d) * 2, 64, kNRows, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != DSA_OK) return rc;
+  return dsa::encode_tensor_map_2d(mk, ki, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, T, static_cast<uint64_t>(d) * 2, 64,
+                                   kKeyTile, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <int FUSED, int HI>
+int launch_indexer_hi(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count,
+                      cudaStream_t stream) {
+  const int max_stages = FUSED ? 3 : 4;
+  p.stages = p.d == 64 ? 6 : max_stages;
+  const SmemLayout L = smem_layout(p.d, p.stages, p.qb, FUSED);
+  const size_t smem = L.total + 1024;
+  if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return dsa::launch_error("indexer_kernel smem attribute");
+  const int grid = p.nblocks < sm_count ? p.nblocks : sm_count;
+  indexer_kernel<FUSED, HI><<<grid, kThreads, smem, stream>>>(mq, mk, p);
+  return dsa::launch_error("indexer_kernel");
+}
+
+template <int FUSED>
+int launch_indexer(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count, cudaStream_t stream) {
+  switch (p.Hi) {
+    case 8: return launch_indexer_hi<FUSED, 8>(mq, mk, p, sm_count, stream);
+    case 16: return launch_indexer_hi<FUSED, 16>(mq, mk, p, sm_count, stream);
+    case 32: return launch_indexer_hi<FUSED, 32>(mq, mk, p, sm_count, stream);
+    default: return launch_indexer_hi<FUSED, 64>(mq, mk, p, sm_count, stream);
+  }
+}
+
+int fused_cap(int s_max, int k) {
+  int cap = k * 8 > 16384 ? k * 8 : 16384;
+  if (s_max < cap) cap = s_max;
+  return (cap + 3) / 4 * 4;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" int dsa_indexer_scores(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                                  int n_docs, int T, int Hi, int d, int s_max, float* scores, int64_t ld,
+                                  cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_scores");
+  if (rc != DSA_OK) return rc;
+  if (!scores) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores: NULL scores");
+  if (ld < s_max || ld % 4 != 0) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores: need ld >= s_max, ld % 4 == 0");
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  CUtensorMap mq, mk;
+  rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
+  if (rc != DSA_OK) return rc;
+  IndexerParams p{};
+  p.w = w;
+  p.cu = cu_seqlens;
+  p.n_docs = n_docs;
+  p.T = T;
+  p.Hi = Hi;
+  p.d = d;
+  p.qb = kNRows / Hi;
+  p.nblocks = (T + p.qb - 1) / p.qb;
+  p.scores = scores;
+  p.ld = ld;
+  p.s_max = s_max;
+  p.status = dsa::device_status_ptr();
+  return launch_indexer<0>(mq, mk, p, sms, stream);
+}
+
+extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
+  if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1 || s_max > T) return 0;
+  const size_t cap = static_cast<size_t>(fused_cap(s_max, k));
+  return align256(static_cast<size_t>(T) * 4) + 2 * align256(static_cast<size_t>(T) * cap * 4);
+}
+
+extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
+                                int T, int Hi, int d, int k, int s_max, int32_t* idx, int32_t* topk_length,
+                                void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_topk");
+  if (rc != DSA_OK) return rc;
+  if (k < 1 || k > DSA_MAX_TOPK) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk: need 1 <= k <= %d", DSA_MAX_TOPK);
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk: NULL idx");
+  const size_t need = dsa_indexer_topk_workspace_size(T, Hi, d, k, s_max);
+  if (!workspace || ws_bytes < need || !dsa::aligned(workspace, 256))
+    return dsa::set_error(DSA_ERR_WORKSPACE, "dsa_indexer_topk: workspace must be 256-byte aligned and >= %zu bytes",
+                          need);
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  CUtensorMap mq, mk;
+  rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
+  if (rc != DSA_OK) return rc;
+  const int cap = fused_cap(s_max, k);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  IndexerParams p{};
+  p.w = w;
+  p.cu = cu_seqlens;
+  p.n_docs = n_docs;
+  p.T = T;
+  p.Hi = Hi;
+  p.d = d;
+  p.qb = kNRows / Hi;
+  p.nblocks = (T + p.qb - 1) / p.qb;
+  p.s_max = s_max;
+  p.cand_cnt = reinterpret_cast<int32_t*>(ws);
+  p.cand_key = reinterpret_cast<uint32_t*>(ws + align256(static_cast<size_t>(T) * 4));
+  p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(static_cast<size_t>(T) * 4) +
+                                          align256(static_cast<size_t>(T) * cap * 4));
+  p.cap = cap;
+  p.k = k;
+  int bins = 2 * kHistWords / p.qb;
+  int bits = 0;
+  while ((1 << bits) < bins) ++bits;
+  p.hist_bits = bits;
+  p.status = dsa::device_status_ptr();
+  rc = launch_indexer<1>(mq, mk, p, sms, stream);
+  if (rc != DSA_OK) return rc;
+  const size_t smem = sizeof(dsa::TopkShared);
+  if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return dsa::launch_error("fused_select_kernel smem attribute");
+  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand_key, p.cand_idx,
+                                                              p.cand_cnt, cap, idx, topk_length, p.status);
+  return dsa::launch_error("fused_select_kernel");
+}

@@ -1,0 +1,229 @@
+"""Thin Python binding of libdsa.so (include/dsa.h), same entry-point names.
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, outputs are allocated with torch (device memory is the caller's
+business on the C side), and every call goes straight to the C ABI on the
+current torch stream.  Every step of the path runs in the library's CUDA
+kernels; there is no fallback.  If the library is missing, the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libdsa.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "dsa.h")
+
+DSA_OK = 0
+DSA_ERR_VALUE = 1
+DSA_ERR_UNSUPPORTED = 2
+DSA_ERR_CUDA = 3
+DSA_ERR_WORKSPACE = 4
+DSA_STATUS_WAIT_TIMEOUT = 0x1
+DSA_STATUS_CAND_OVERFLOW = 0x2
+MAX_TOPK = 2048
+
+_lock = threading.Lock()
+_lib = None
+
+P = ctypes.c_void_p
+I = ctypes.c_int
+I64 = ctypes.c_int64
+F = ctypes.c_float
+SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "dsa_last_error": ([], ctypes.c_char_p),
+    "dsa_device_status": ([P, I], I),
+    "dsa_thd_metadata": ([P, I, I, P, P, P], I),
+    "dsa_indexer_scores": ([P, P, P, P, I, I, I, I, I, P, I64, P], I),
+    "dsa_topk": ([P, I64, P, P, I, I, P, P, P, P], I),
+    "dsa_compact_sort_indices": ([P, I, I, I64, P, P, P], I),
+    "dsa_indexer_topk_workspace_size": ([I, I, I, I, I], SZ),
+    "dsa_indexer_topk": ([P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P], I),
+    "dsa_sparse_attn_fwd": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P], I),
+    "dsa_pack_routes": ([P, I, I, I, P, P], I),
+}
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed ({code}): {msg}")
+        self.code = code
+
+
+def header_functions() -> list[str]:
+    """Names of the functions that include/dsa.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(dsa_\w+)\s*\(", text, re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdsa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libdsa.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGNATURES.items():
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != DSA_OK:
+        msg = lib().dsa_last_error().decode(errors="replace")
+        if rc in (DSA_ERR_VALUE, DSA_ERR_WORKSPACE):
+            raise ValueError(f"{fn}: {msg}")
+        raise DsaError(fn, rc, msg)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _need(t, name, dtype, dim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got {t.dim()}")
+    return t
+
+
+def device_status(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check("dsa_device_status", lib().dsa_device_status(ctypes.byref(v), 1 if clear else 0))
+    return int(v.value)
+
+
+def thd_metadata(cu_seqlens: torch.Tensor, T: int):
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    start = torch.empty(T, dtype=torch.int32, device=cu_seqlens.device)
+    length = torch.empty(T, dtype=torch.int32, device=cu_seqlens.device)
+    _check("dsa_thd_metadata", lib().dsa_thd_metadata(_p(cu_seqlens), cu_seqlens.numel() - 1, T, _p(start),
+                                                      _p(length), _stream()))
+    return start, length
+
+
+def indexer_scores(qi, ki, w, cu_seqlens, s_max: int, ld: int | None = None, out=None):
+    """Dense indexer scores fp32 [T, ld] (columns >= s_max untouched)."""
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, d = qi.shape
+    ld = ld or (s_max + 3) // 4 * 4
+    if out is None:
+        out = torch.empty((T, ld), dtype=torch.float32, device=qi.device)
+    _check("dsa_indexer_scores", lib().dsa_indexer_scores(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1,
+                                                          T, Hi, d, s_max, _p(out), ld, _stream()))
+    return out
+
+
+def topk(scores, lengths, k: int, row_start=None, want_vals: bool = False, idx=None, topk_length=None):
+    _need(scores, "scores", torch.float32, 2)
+    _need(lengths, "lengths", torch.int32, 1)
+    if row_start is not None:
+        _need(row_start, "row_start", torch.int32, 1)
+    T, ld = scores.shape
+    dev = scores.device
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev) if idx is None else idx
+    topk_length = torch.empty(T, dtype=torch.int32, device=dev) if topk_length is None else topk_length
+    vals = torch.empty((T, k), dtype=torch.float32, device=dev) if want_vals else None
+    _check("dsa_topk", lib().dsa_topk(_p(scores), ld, _p(lengths), _p(row_start), T, k, _p(idx), _p(topk_length),
+                                      _p(vals), _stream()))
+    return idx, topk_length, vals
+
+
+def compact_sort_indices(indices, key_count: int, out=None):
+    _need(indices, "indices", torch.int32, 2)
+    T, K = indices.shape
+    out = torch.empty_like(indices) if out is None else out
+    lengths = torch.empty(T, dtype=torch.int32, device=indices.device)
+    _check("dsa_compact_sort_indices", lib().dsa_compact_sort_indices(_p(indices), T, K, int(key_count), _p(out),
+                                                                      _p(lengths), _stream()))
+    return out, lengths
+
+
+def indexer_topk_workspace_size(T: int, Hi: int, d: int, k: int, s_max: int) -> int:
+    return int(lib().dsa_indexer_topk_workspace_size(T, Hi, d, k, s_max))
+
+
+def indexer_topk(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None, idx=None, topk_length=None):
+    """Fused indexer + top-k: (idx [T, k] ascending global ids, topk_length [T])."""
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, d = qi.shape
+    dev = qi.device
+    nbytes = indexer_topk_workspace_size(T, Hi, d, k, s_max)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev) if idx is None else idx
+    topk_length = torch.empty(T, dtype=torch.int32, device=dev) if topk_length is None else topk_length
+    _check("dsa_indexer_topk", lib().dsa_indexer_topk(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1,
+                                                      T, Hi, d, k, s_max, _p(idx), _p(topk_length), _p(workspace),
+                                                      workspace.numel() * workspace.element_size(), _stream()))
+    return idx, topk_length
+
+
+def sparse_attn_fwd(q, kv, idx, scale: float, topk_length=None, sink=None, v=None, want_lse_kv: bool = False,
+                    want_max_logits: bool = False, out=None, lse=None):
+    """Sparse MQA attention forward; returns dict(out, lse[, lse_kv][, max_logits])."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv, "kv", torch.bfloat16, 2)
+    _need(idx, "idx", torch.int32, 2)
+    if topk_length is not None:
+        _need(topk_length, "topk_length", torch.int32, 1)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    if v is not None:
+        _need(v, "v", torch.bfloat16, 2)
+    T, H, Dqk = q.shape
+    Tkv = kv.shape[0]
+    Dv = v.shape[1] if v is not None else 512
+    K = idx.shape[1]
+    dev = q.device
+    out = torch.empty((T, H, Dv), dtype=torch.bfloat16, device=dev) if out is None else out
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev) if lse is None else lse
+    lse_kv = torch.empty((T, H), dtype=torch.float32, device=dev) if want_lse_kv else None
+    ml = torch.empty((T, H), dtype=torch.float32, device=dev) if want_max_logits else None
+    _check("dsa_sparse_attn_fwd", lib().dsa_sparse_attn_fwd(_p(q), _p(kv), _p(v), _p(idx), _p(topk_length), _p(sink),
+                                                            T, Tkv, H, Dqk, Dv, K, float(scale), _p(out), _p(lse),
+                                                            _p(lse_kv), _p(ml), _stream()))
+    res = {"out": out, "lse": lse}
+    if lse_kv is not None:
+        res["lse_kv"] = lse_kv
+    if ml is not None:
+        res["max_logits"] = ml
+    return res
+
+
+def pack_routes(routes):
+    _need(routes, "routes", torch.int32, 3)
+    B, S, W = routes.shape
+    Wp = (W + 3) // 4 * 4
+    out = torch.empty((B * S, Wp), dtype=torch.int32, device=routes.device)
+    _check("dsa_pack_routes", lib().dsa_pack_routes(_p(routes), B, S, W, _p(out), _stream()))
+    return out

@@ -1,0 +1,81 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/dsa.h declares, and rejects invalid host arguments before touching
+the device (no compute call is made here)."""
+import ctypes
+
+import pytest
+
+import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+from sparse_attention_gemm_gb300 import build as dsa_build
+from sparse_attention_gemm_gb300 import ops
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dsa_build.build()
+    return ops.lib()
+
+
+def test_header_declares_the_hot_path():
+    names = ops.header_functions()
+    for must in ["dsa_thd_metadata", "dsa_indexer_scores", "dsa_topk", "dsa_compact_sort_indices",
+                 "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_sparse_attn_fwd", "dsa_pack_routes",
+                 "dsa_last_error", "dsa_device_status"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in ops.header_functions():
+        assert hasattr(lib, name), name
+        assert name in ops._SIGNATURES, f"binding lacks {name}"
+
+
+NULL = None
+FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+
+
+@pytest.mark.parametrize("call", [
+    lambda L: L.dsa_thd_metadata(FAKE, 0, 10, FAKE, FAKE, NULL),
+    lambda L: L.dsa_thd_metadata(NULL, 1, 10, FAKE, FAKE, NULL),
+    lambda L: L.dsa_topk(FAKE, 16, FAKE, NULL, 4, 0, FAKE, NULL, NULL, NULL),
+    lambda L: L.dsa_topk(FAKE, 16, FAKE, NULL, 4, 2049, FAKE, NULL, NULL, NULL),
+    lambda L: L.dsa_topk(NULL, 16, FAKE, NULL, 4, 8, FAKE, NULL, NULL, NULL),
+    lambda L: L.dsa_compact_sort_indices(FAKE, 4, 0, 10, FAKE, FAKE, NULL),
+    lambda L: L.dsa_compact_sort_indices(FAKE, 4, 16385, 10, FAKE, FAKE, NULL),
+    lambda L: L.dsa_indexer_scores(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 96, 128, FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_scores(FAKE, FAKE, FAKE, FAKE, 1, 128, 48, 128, 128, FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_scores(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 128, FAKE, 126, NULL),
+    lambda L: L.dsa_indexer_scores(ctypes.c_void_p(4097), FAKE, FAKE, FAKE, 1, 128, 64, 128, 128, FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 0, 128, FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 576, 256, 8, 0.1, FAKE, FAKE,
+                                    NULL, NULL, NULL),
+    lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 129, 576, 512, 8, 0.1, FAKE, FAKE,
+                                    NULL, NULL, NULL),
+    lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 576, 512, 8, 0.0, FAKE, FAKE,
+                                    NULL, NULL, NULL),
+    lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 576, 512, 8, float("inf"), FAKE,
+                                    FAKE, NULL, NULL, NULL),
+    lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 256, 256, 8, 0.1, FAKE, FAKE,
+                                    NULL, NULL, NULL),
+    lambda L: L.dsa_pack_routes(FAKE, 0, 4, 4, FAKE, NULL),
+])
+def test_invalid_arguments_are_rejected_before_launch(lib, call):
+    assert call(lib) == ops.DSA_ERR_VALUE
+    assert len(lib.dsa_last_error()) > 0
+
+
+def test_workspace_errors(lib):
+    need = lib.dsa_indexer_topk_workspace_size(4096, 64, 128, 2048, 4096)
+    assert need > 0
+    assert lib.dsa_indexer_topk_workspace_size(4096, 64, 128, 4096, 4096) == 0
+    rc = lib.dsa_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 128, 2048, 4096, FAKE, NULL, FAKE, need - 1, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+    rc = lib.dsa_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 128, 2048, 4096, FAKE, NULL,
+                              ctypes.c_void_p(4096 + 16), need, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+
+
+def test_workspace_size_depends_on_shapes_only(lib):
+    a = lib.dsa_indexer_topk_workspace_size(65536, 64, 128, 2048, 65536)
+    b = lib.dsa_indexer_topk_workspace_size(65536, 64, 128, 2048, 65536)
+    assert a == b and a % 256 == 0

@@ -1,0 +1,302 @@
+"""GPU parity of every hot-path step against the fp64 oracle, through the C ABI
+(ops.* marshals straight into libdsa.so).  Sizes span several tiles and a
+ragged tail while the oracle still finishes in seconds; edge cases cover
+empty/ragged inputs, ties, invalid ids and the padded-head paths."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (DEV, assert_attention_close, assert_scores_close, cu_from_lengths, dev, dev_bf16, f64,
+                      rand_bf16_bits)
+from sparse_attention_gemm_gb300 import ops
+from sparse_attention_gemm_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    ops.device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) == 0, "a kernel raised a device status flag"
+
+
+# ------------------------------------------------------------------ metadata
+@pytest.mark.parametrize("lengths", [[256], [1], [3, 1, 7, 1, 12], W.thd_16k().cu_seqlens[1:] - W.thd_16k().cu_seqlens[:-1]])
+def test_thd_metadata(lengths):
+    cu = cu_from_lengths(lengths)
+    T = int(cu[-1])
+    s, l = ops.thd_metadata(dev(cu), T)
+    rs, rl = oracle.thd_metadata(cu, T)
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(l.cpu().numpy(), rl)
+
+
+# -------------------------------------------------------------- route packing
+def test_pack_routes_gqa_workload():
+    r = W.gqa_routes().routes()
+    got = ops.pack_routes(dev(r)).cpu().numpy()
+    assert np.array_equal(got, oracle.pack_routes(r))
+
+
+@pytest.mark.parametrize("W_", [1, 3, 4, 6, 257])
+def test_pack_routes_ragged_width(W_):
+    rng = np.random.default_rng(W_)
+    r = rng.integers(-3, 40, size=(3, 37, W_)).astype(np.int32)
+    assert np.array_equal(ops.pack_routes(dev(r)).cpu().numpy(), oracle.pack_routes(r))
+
+
+# ---------------------------------------------------------------- compact/sort
+@pytest.mark.parametrize("K", [1, 7, 64, 512, 2052, 16384])
+def test_compact_sort(K):
+    rng = np.random.default_rng(K)
+    T, kc = 37, 3000
+    ind = rng.integers(-50, kc + 50, size=(T, K)).astype(np.int32)
+    ind[3] = -1
+    ind[4] = 5  # all duplicates
+    out, lengths = ops.compact_sort_indices(dev(ind), kc)
+    ro, rl = oracle.compact_sort(ind, kc)
+    assert np.array_equal(out.cpu().numpy(), ro) and np.array_equal(lengths.cpu().numpy(), rl)
+    # in place (out aliases in)
+    t = dev(ind)
+    ops.compact_sort_indices(t, kc, out=t)
+    assert np.array_equal(t.cpu().numpy(), ro)
+
+
+# -------------------------------------------------------------------- indexer
+def _indexer_inputs(rng, lengths, Hi, d, kind="normal"):
+    cu = cu_from_lengths(lengths)
+    T = int(cu[-1])
+    if kind == "int":
+        qi = W.f32_to_bf16_bits(rng.integers(-4, 5, size=(T, Hi, d)).astype(np.float32))
+        ki = W.f32_to_bf16_bits(rng.integers(-4, 5, size=(T, d)).astype(np.float32))
+        w = rng.integers(1, 5, size=(T, Hi)).astype(np.float32)
+    else:
+        qi = rand_bf16_bits(rng, (T, Hi, d))
+        ki = rand_bf16_bits(rng, (T, d))
+        w = (rng.random((T, Hi), dtype=np.float32) / np.float32(8)).astype(np.float32)
+    return cu, T, qi, ki, w
+
+
+def _oracle_scores(cu, T, qi, ki, w, s_max):
+    start, length = oracle.thd_metadata(cu, T)
+    sc, mag = oracle.indexer_scores(f64(qi), f64(ki), w, start, length, s_max, want_abs=True)
+    return start, length, sc, mag
+
+
+def test_indexer_integer_inputs_exact():
+    wl = W.tiny()
+    qi, ki, w = wl.qi_bits(), wl.ki_bits(), wl.w()
+    got = ops.indexer_scores(dev_bf16(qi), dev_bf16(ki), dev(w), dev(wl.cu_seqlens), wl.s_max).cpu().numpy()
+    _, length, sc, _ = _oracle_scores(wl.cu_seqlens, wl.T, qi, ki, w, wl.s_max)
+    fin = np.isfinite(sc)
+    assert np.array_equal(got[:, : wl.s_max][fin].astype(np.float64), sc[fin])
+    assert np.all(np.isneginf(got[:, : wl.s_max][~fin]))
+
+
+@pytest.mark.parametrize("Hi,d", [(64, 128), (32, 128), (16, 64), (8, 64), (64, 64), (8, 128)])
+@pytest.mark.parametrize("lengths", [[700], [129, 1, 300, 257]])
+def test_indexer_bf16_tolerance(Hi, d, lengths):
+    rng = np.random.default_rng(Hi * 1000 + d + len(lengths))
+    cu, T, qi, ki, w = _indexer_inputs(rng, lengths, Hi, d)
+    s_max = int(max(lengths))
+    got = ops.indexer_scores(dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu), s_max).cpu().numpy()[:, :s_max]
+    _, length, sc, mag = _oracle_scores(cu, T, qi, ki, w, s_max)
+    fin = np.isfinite(sc)
+    assert_scores_close(got, sc, mag, fin)
+    assert np.all(np.isneginf(got[~fin]))
+
+
+# ---------------------------------------------------------------------- top-k
+def test_topk_on_gpu_scores_is_exact():
+    rng = np.random.default_rng(5)
+    cu, T, qi, ki, w = _indexer_inputs(rng, [1500, 37, 900], 64, 128)
+    s_max = 1500
+    sc = ops.indexer_scores(dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu), s_max)
+    start, length = oracle.thd_metadata(cu, T)
+    for k in (1, 64, 512, 2048):
+        idx, tl, vals = ops.topk(sc, dev(length), k, row_start=dev(start), want_vals=True)
+        scn = sc.cpu().numpy().astype(np.float64)
+        ri, rt = oracle.topk(scn, length, k, start_rows=start)
+        assert np.array_equal(idx.cpu().numpy(), ri), k
+        assert np.array_equal(tl.cpu().numpy(), rt)
+        v = vals.cpu().numpy()
+        for t in (0, 5, T - 1):
+            n = rt[t]
+            assert np.array_equal(v[t, :n], scn[t, ri[t, :n] - start[t]].astype(np.float32))
+            assert np.all(np.isneginf(v[t, n:]))
+
+
+@pytest.mark.parametrize("case", ["all_equal", "three_values", "two_values_long", "normal", "neg_zero", "lengths"])
+def test_topk_ties_and_edges(case):
+    rng = np.random.default_rng(7)
+    T, ld = 24, 20000
+    if case == "all_equal":
+        sc = np.full((T, ld), 1.5, np.float32)
+    elif case == "three_values":
+        sc = rng.integers(0, 3, size=(T, ld)).astype(np.float32)
+    elif case == "two_values_long":
+        sc = (rng.random((T, ld)) < 0.02).astype(np.float32)  # ~400 ones, the rest tie at 0
+    elif case == "neg_zero":
+        sc = np.where(rng.random((T, ld)) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+        sc[:, ::97] = 1.0
+    else:
+        sc = rng.standard_normal((T, ld)).astype(np.float32)
+    lengths = np.full(T, ld, np.int32)
+    if case == "lengths":
+        lengths = rng.integers(0, ld + 1, size=T).astype(np.int32)
+        lengths[:4] = [0, 1, 2047, 2048]
+    for k in (1, 100, 2048):
+        idx, tl, _ = ops.topk(dev(sc), dev(lengths), k)
+        ri, rt = oracle.topk(sc.astype(np.float64), lengths, k)
+        assert np.array_equal(idx.cpu().numpy(), ri), (case, k)
+        assert np.array_equal(tl.cpu().numpy(), rt)
+
+
+def test_topk_unaligned_rows_use_scalar_path():
+    rng = np.random.default_rng(8)
+    sc = rng.integers(0, 50, size=(9, 3001)).astype(np.float32)
+    lengths = np.array([3001, 3000, 2999, 5, 0, 1, 3001, 2048, 2049], np.int32)
+    idx, tl, _ = ops.topk(dev(sc), dev(lengths), 2048)
+    ri, rt = oracle.topk(sc.astype(np.float64), lengths, 2048)
+    assert np.array_equal(idx.cpu().numpy(), ri) and np.array_equal(tl.cpu().numpy(), rt)
+
+
+# ------------------------------------------------------- fused indexer + top-k
+@pytest.mark.parametrize("lengths,Hi,d,k,kind", [
+    ([256], 8, 64, 64, "int"),
+    ([3000], 64, 128, 512, "normal"),
+    ([4096], 64, 128, 2048, "normal"),
+    ([700, 1, 1300, 129], 64, 128, 256, "normal"),
+    ([999, 513], 32, 128, 300, "int"),
+])
+def test_fused_indexer_topk_equals_unfused(lengths, Hi, d, k, kind):
+    rng = np.random.default_rng(sum(lengths) + k)
+    cu, T, qi, ki, w = _indexer_inputs(rng, lengths, Hi, d, kind)
+    s_max = int(max(lengths))
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    idx, tl = ops.indexer_topk(*a, k, s_max)
+    sc = ops.indexer_scores(*a, s_max)
+    start, length = oracle.thd_metadata(cu, T)
+    ui, ut, _ = ops.topk(sc, dev(length), k, row_start=dev(start))
+    assert np.array_equal(idx.cpu().numpy(), ui.cpu().numpy())
+    assert np.array_equal(tl.cpu().numpy(), ut.cpu().numpy())
+    # and the unfused result is the oracle's top-k of the GPU's own scores
+    ri, _ = oracle.topk(sc.cpu().numpy()[:, :s_max].astype(np.float64), length, k, start_rows=start)
+    assert np.array_equal(ui.cpu().numpy(), ri)
+    if kind == "int":  # exact scores: the oracle's own top-k matches too
+        _, _, osc, _ = _oracle_scores(cu, T, qi, ki, w, s_max)
+        oi, _ = oracle.topk(osc, length, k, start_rows=start)
+        assert np.array_equal(idx.cpu().numpy(), oi)
+
+
+# ------------------------------------------------------------------ attention
+def _attn_case(rng, T, H, Tkv, K, Dqk=576, Dv=512, sigma=0.1, qmul=1.0, sink_scale=1.0, sink=True, sep_v=False):
+    q = rand_bf16_bits(rng, (T, H, Dqk), sigma * qmul)
+    kv = rand_bf16_bits(rng, (Tkv, Dqk), sigma)
+    v = rand_bf16_bits(rng, (Tkv, Dv), sigma) if sep_v else None
+    sk = (rng.standard_normal(H) * sink_scale).astype(np.float32) if sink else None
+    return q, kv, v, sk
+
+
+def _run_attn(q, kv, v, idx, tl, sk, scale, want=True):
+    return ops.sparse_attn_fwd(dev_bf16(q), dev_bf16(kv), dev(idx), scale,
+                               topk_length=None if tl is None else dev(tl),
+                               sink=None if sk is None else dev(sk), v=None if v is None else dev_bf16(v),
+                               want_lse_kv=want, want_max_logits=want)
+
+
+def _ref_attn(q, kv, v, idx, tl, sk, scale, Dv=512):
+    return oracle.sparse_attn(f64(q), f64(kv), idx, scale, topk_length=tl, sink=sk,
+                              v=None if v is None else f64(v), dv=Dv)
+
+
+def test_attention_tiny_workload():
+    wl = W.tiny()
+    start, length = oracle.thd_metadata(wl.cu_seqlens, wl.T)
+    sc = oracle.indexer_scores(f64(wl.qi_bits()), f64(wl.ki_bits()), wl.w(), start, length, wl.s_max)
+    idx, tl = oracle.topk(sc, length, wl.K, start_rows=start)
+    q, kv, sk = wl.q_bits(), wl.kv_bits(), wl.sink()
+    got = _run_attn(q, kv, None, idx, tl, sk, wl.scale)
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, tl, sk, wl.scale))
+
+
+@pytest.mark.parametrize("qmul", [1.0, 30.0])
+def test_attention_all_keys_selected(qmul):
+    # every causal key selected (K >= len): sparse attention = dense causal attention with sink
+    rng = np.random.default_rng(int(qmul))
+    T, H = 300, 64
+    K = 384
+    q, kv, _, sk = _attn_case(rng, T, H, T, K, qmul=qmul, sink_scale=3.0)
+    idx = np.full((T, K), -1, np.int32)
+    for t in range(T):
+        idx[t, : t + 1] = np.arange(t + 1)
+    tl = np.minimum(np.arange(T) + 1, K).astype(np.int32)
+    scale = 1 / 24
+    got = _run_attn(q, kv, None, idx, tl, sk, scale)
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, tl, sk, scale))
+
+
+def test_attention_slot_edge_cases():
+    rng = np.random.default_rng(3)
+    T, H, Tkv, K = 96, 64, 500, 300
+    q, kv, _, sk = _attn_case(rng, T, H, Tkv, K, qmul=10.0, sink_scale=5.0)
+    idx = rng.integers(0, Tkv, size=(T, K)).astype(np.int32)
+    idx[:, 5] = -1                    # invalid inside the prefix
+    idx[:, 6] = Tkv + 3               # out of range
+    idx[:, 7] = idx[:, 8]             # duplicate slot
+    idx[10] = -1                      # row with no valid id
+    tl = rng.integers(0, K + 1, size=T).astype(np.int32)
+    tl[:6] = [0, 1, 127, 128, 129, K]
+    tl[6] = K + 50                    # clamped to K
+    tl[7] = -3                        # clamped to 0
+    scale = 0.05
+    got = _run_attn(q, kv, None, idx, tl, sk, scale)
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, tl, sk, scale))
+    # without lengths every slot is considered; no sink
+    got = _run_attn(q, kv, None, idx, None, None, scale)
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, None, None, scale))
+
+
+@pytest.mark.parametrize("H", [1, 12, 64, 100, 128])
+def test_attention_head_counts(H):
+    rng = np.random.default_rng(H)
+    T, Tkv, K = 70, 400, 200
+    q, kv, _, sk = _attn_case(rng, T, H, Tkv, K, qmul=5.0)
+    idx = rng.integers(-1, Tkv, size=(T, K)).astype(np.int32)
+    got = _run_attn(q, kv, None, idx, None, sk, 0.07)
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, None, sk, 0.07))
+
+
+def test_attention_dqk512():
+    rng = np.random.default_rng(11)
+    T, H, Tkv, K = 64, 64, 300, 256
+    q, kv, _, sk = _attn_case(rng, T, H, Tkv, K, Dqk=512)
+    idx = rng.integers(0, Tkv, size=(T, K)).astype(np.int32)
+    tl = rng.integers(1, K + 1, size=T).astype(np.int32)
+    got = _run_attn(q, kv, None, idx, tl, sk, 1 / math.sqrt(512))
+    assert_attention_close(got, _ref_attn(q, kv, None, idx, tl, sk, 1 / math.sqrt(512)))
+
+
+def test_attention_separate_v_gqa_shape():
+    rng = np.random.default_rng(12)
+    T, H, Tkv, K = 200, 12, 200, 260
+    q, kv, v, _ = _attn_case(rng, T, H, Tkv, K, Dqk=256, Dv=256, sink=False, sep_v=True, qmul=4.0)
+    routes = rng.integers(-1, Tkv, size=(T, K)).astype(np.int32)
+    got = _run_attn(q, kv, v, routes, None, None, 1 / 16)
+    assert_attention_close(got, _ref_attn(q, kv, v, routes, None, None, 1 / 16, Dv=256))
+
+
+def test_attention_empty_inputs():
+    rng = np.random.default_rng(13)
+    T, H, Tkv = 5, 64, 10
+    q, kv, _, sk = _attn_case(rng, T, H, Tkv, 0)
+    got = _run_attn(q, kv, None, np.zeros((T, 0), np.int32), None, sk, 0.1)
+    ref = _ref_attn(q, kv, None, np.zeros((T, 0), np.int32), None, sk, 0.1)
+    assert_attention_close(got, ref)
