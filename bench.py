@@ -1,0 +1,435 @@
+"""Benchmark of the DSA forward hot path on the long-context workload.
+
+One step = one pass of the whole path over one batch: THD metadata, fused
+indexer + top-k (no dense score matrix), sparse MQA attention.  Workload:
+T=65536 tokens in one document, H=64 heads, top-k 2048, indexer Hi=64, d=128,
+latent 576/512, synthetic seeded inputs (workloads.long_64k).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line.  N > 1 runs one replica per GPU (each rank
+processes its own full workload; no collective on the data path) and reports
+the whole-job aggregate with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA fwd tokens/s and sparse-attn TFLOP/s (% bf16 peak) at T=64K,H=64,k=2048"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p["bf16_tflops_sustained"], "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def work_counts(T: int, K: int, H: int, Hi: int, d: int, Dqk: int, Dv: int, lengths: np.ndarray):
+    """Algorithmic work: attention FLOPs over valid (t, slot) pairs and indexer
+    FLOPs over causal (t, s) pairs, from the per-token causal lengths."""
+    pairs_attn = int(np.minimum(lengths.astype(np.int64), K).sum())
+    pairs_idx = int(lengths.astype(np.int64).sum())
+    return {
+        "attn_flops": pairs_attn * H * 2 * (Dqk + Dv),
+        "indexer_flops": pairs_idx * Hi * d * 2,
+        "attn_pairs": pairs_attn,
+        "indexer_pairs": pairs_idx,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sample_rows(T: int, K: int, n: int, seed: int = 123) -> np.ndarray:
+    """Stratified query rows: first, last, around t = K, and random."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, K - 2, K - 1, K, K + 1, T // 2, T - 2, T - 1]
+    rest = rng.choice(T, size=max(0, n - len(fixed)), replace=False)
+    return np.unique(np.clip(np.concatenate([fixed, rest]), 0, T - 1)).astype(np.int64)
+
+
+def oracle_inputs(wl, rows, qi_all=None, q_all=None, w_all=None):
+    """fp64 oracle inputs for the given rows (sliced from full host arrays when
+    given, else regenerated from the seeded chunks)."""
+    qi = wl_f32(qi_all[rows] if qi_all is not None else wl.qi_bits(rows))
+    q = wl_f32(q_all[rows] if q_all is not None else wl.q_bits(rows))
+    w = w_all[rows] if w_all is not None else wl.w(rows)
+    return qi, q, w
+
+
+def oracle_rows_pass(wl, rows, ki64, kv64, qi, q, w):
+    """The fp64 oracle on the given rows: indexer -> top-k -> attention."""
+    import oracle
+
+    start, length = oracle.thd_metadata(wl.cu_seqlens, wl.T)
+    sc = oracle.indexer_scores(qi, ki64, w, start[rows], length[rows], wl.s_max)
+    idx, tl = oracle.topk(sc, length[rows], wl.K, start_rows=start[rows])
+    res = oracle.sparse_attn(q, kv64, idx, wl.scale, topk_length=tl, sink=wl.sink(), dv=wl.Dv)
+    return idx, tl, res
+
+
+def wl_f32(bits):
+    from sparse_attention_gemm_gb300 import workloads as W
+
+    return W.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def cpu_baseline(wl, n_rows: int, qi_all=None, q_all=None, w_all=None, ki_all=None, kv_all=None):
+    """Times the oracle on a bounded stratified sample of query rows (input
+    preparation outside the timed region)."""
+    import oracle
+
+    oracle.build()
+    ki64 = wl_f32(ki_all if ki_all is not None else wl.ki_bits())
+    kv64 = wl_f32(kv_all if kv_all is not None else wl.kv_bits())
+    rows = sample_rows(wl.T, wl.K, n_rows)
+    qi, q, w = oracle_inputs(wl, rows, qi_all, q_all, w_all)
+    t0 = time.perf_counter()
+    oracle_rows_pass(wl, rows, ki64, kv64, qi, q, w)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} stratified query rows of the T=65536 workload (indexer+top-k+attention, fp64)",
+            "seconds": dt}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if os.environ.get("DSA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: bounded samples timed on host cores."""
+    if rank != 0:
+        return
+    from sparse_attention_gemm_gb300 import workloads as W
+
+    wl = W.long_64k()
+    import oracle
+
+    oracle.build()
+    ki64 = wl_f32(wl.ki_bits())
+    kv64 = wl_f32(wl.kv_bits())
+    n_rows = args.ref_rows
+    for i in range(args.warmup):
+        rows = sample_rows(wl.T, wl.K, 4, seed=1000 + i)
+        oracle_rows_pass(wl, rows, ki64, kv64, *oracle_inputs(wl, rows))
+    times = []
+    for i in range(args.steps):
+        rows = sample_rows(wl.T, wl.K, n_rows, seed=2000 + i)
+        inputs = oracle_inputs(wl, rows)
+        t0 = time.perf_counter()
+        oracle_rows_pass(wl, rows, ki64, kv64, *inputs)
+        times.append((time.perf_counter() - t0, len(rows)))
+    tot_s = sum(t for t, _ in times)
+    tot_rows = sum(n for _, n in times)
+    value = tot_rows / tot_s
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "k": wl.K},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n_rows} stratified query rows per step (indexer+top-k+attention, fp64)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-rows", type=int, default=48)
+    ap.add_argument("--ref-rows", type=int, default=16)
+    ap.add_argument("--no-topk-standalone", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        barrier(world)
+        return
+
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from sparse_attention_gemm_gb300 import ops
+    from sparse_attention_gemm_gb300 import workloads as W
+
+    wl = W.long_64k()
+    T, K, H = wl.T, wl.K, wl.H
+    lengths = (np.arange(T) - np.repeat(wl.cu_seqlens[:-1], np.diff(wl.cu_seqlens)) + 1).astype(np.int64)
+    work = work_counts(T, K, H, wl.Hi, wl.d, wl.Dqk, wl.Dv, lengths)
+    pk = peaks()
+
+    # ---- inputs (seeded, host), pinned for the end-to-end leg
+    host = {
+        "qi": wl.qi_bits(), "ki": wl.ki_bits(), "w": wl.w(), "q": wl.q_bits(), "kv": wl.kv_bits(),
+        "sink": wl.sink(), "cu": wl.cu_seqlens,
+    }
+
+    def pin(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a))
+        return t.pin_memory()
+
+    hpin = {k: pin(v) for k, v in host.items()}
+    d = {k: v.to(dev, non_blocking=True) for k, v in hpin.items()}
+    for k in ("qi", "ki", "q", "kv"):
+        d[k] = d[k].view(torch.bfloat16)
+    ws_bytes = ops.indexer_topk_workspace_size(T, wl.Hi, wl.d, K, wl.s_max)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    tl = torch.empty(T, dtype=torch.int32, device=dev)
+    out = torch.empty((T, H, wl.Dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 4  # metadata, fused indexer stage 1, stage 2 selection, attention
+    start_t = torch.empty(T, dtype=torch.int32, device=dev)
+    len_t = torch.empty(T, dtype=torch.int32, device=dev)
+
+    def step(ev=None):
+        L = ops.lib()
+        ops._check("dsa_thd_metadata", L.dsa_thd_metadata(ops._p(d["cu"]), wl.n_docs, T, ops._p(start_t),
+                                                          ops._p(len_t), ops._stream()))
+        if ev:
+            ev[0].record(stream)
+        ops.indexer_topk(d["qi"], d["ki"], d["w"], d["cu"], K, wl.s_max, workspace=ws, idx=idx, topk_length=tl)
+        if ev:
+            ev[1].record(stream)
+        ops.sparse_attn_fwd(d["q"], d["kv"], idx, wl.scale, topk_length=tl, sink=d["sink"], out=out, lse=lse)
+        if ev:
+            ev[2].record(stream)
+
+    ops.device_status(clear=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region
+    E = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between timed steps (outside the events)
+        E[i][0].record(stream)
+        step(ev=E[i][1:])
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [E[i][0].elapsed_time(E[i][3]) for i in range(args.steps)]
+    idx_ms = [E[i][1].elapsed_time(E[i][2]) for i in range(args.steps)]
+    attn_ms = [E[i][2].elapsed_time(E[i][3]) for i in range(args.steps)]
+    tot_ms = reduce_max(sum(step_ms), world, dev)
+    ms_per_step = tot_ms / args.steps
+    value = world * T * args.steps / (tot_ms / 1e3)
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    idx_avg = sum(idx_ms) / len(idx_ms)
+    attn_tflops = work["attn_flops"] / (attn_avg / 1e3) / 1e12
+    idx_tflops = work["indexer_flops"] / (idx_avg / 1e3) / 1e12
+    status = ops.device_status(clear=True)
+
+    # ---- end to end through host buffers (H2D inputs + D2H results inside the timed region)
+    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    idx_h = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    tl_h = torch.empty(tl.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hpin.values())
+    d2h = sum(t.numel() * t.element_size() for t in (out, lse, idx, tl))
+    e2e_ms = []
+    for i in range(args.e2e_steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k, v in hpin.items():
+            dst = d[k].view(torch.int16) if d[k].dtype == torch.bfloat16 else d[k]
+            dst.copy_(v, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        idx_h.copy_(idx, non_blocking=True)
+        tl_h.copy_(tl, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_tot = reduce_max(sum(e2e_ms), world, dev)
+    e2e_value = world * T * args.e2e_steps / (e2e_tot / 1e3)
+
+    # ---- standalone top-k on a materialised causal score matrix (HBM-bound step)
+    topk_line = None
+    if not args.no_topk_standalone:
+        del ws
+        torch.cuda.empty_cache()
+        scores = torch.empty((T, wl.s_max), dtype=torch.float32, device=dev)
+        ops.indexer_scores(d["qi"], d["ki"], d["w"], d["cu"], wl.s_max, out=scores)
+        tk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        tk_tl = torch.empty(T, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            ops.topk(scores, len_t, K, row_start=start_t, idx=tk_idx, topk_length=tk_tl)
+        torch.cuda.synchronize()
+        tms = []
+        for _ in range(3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ops.topk(scores, len_t, K, row_start=start_t, idx=tk_idx, topk_length=tk_tl)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tms.append(a.elapsed_time(b))
+        same = bool(torch.equal(tk_idx, idx))
+        tbytes = int(lengths.sum()) * 4 + T * K * 4  # scores read once + ids written
+        tavg = sum(tms) / len(tms)
+        topk_line = {"ms": tavg, "algorithmic_bytes": tbytes, "achieved_gbs": tbytes / (tavg / 1e3) / 1e9,
+                     "peak_gbs": pk["hbm_gbs"], "frac": tbytes / (tavg / 1e3) / 1e9 / pk["hbm_gbs"],
+                     "equals_fused_indices": same}
+        del scores
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_rows, host["qi"], host["q"], host["w"], host["ki"], host["kv"])
+    del host
+
+    if rank == 0:
+        peak_t = pk["bf16_tflops_sustained"]
+        dominant = "indexer" if idx_avg >= attn_avg else "attention"
+        if dominant == "indexer":
+            roof = {"kernel": "dsa_indexer_topk (fused stage 1 + stage-2 selection, one call)",
+                    "bound": "tensor", "achieved": idx_tflops, "peak": peak_t, "unit": "TFLOP/s",
+                    "frac": idx_tflops / peak_t, "traffic": None}
+        else:
+            roof = {"kernel": "sparse_attn_kernel", "bound": "tensor", "achieved": attn_tflops, "peak": peak_t,
+                    "unit": "TFLOP/s", "frac": attn_tflops / peak_t, "traffic": None}
+        roof["peak_source"] = f"{pk['source']} bf16 sustained"
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded PCG64 draws shaped like the long-context workload)",
+            "config": {"workload": wl.name, "T": T, "H": H, "k": K, "Hi": wl.Hi, "d": wl.d, "Dqk": wl.Dqk,
+                       "Dv": wl.Dv, "docs": wl.n_docs,
+                       "l2": "inputs larger than L2 (q 4.8 GB) and L2 flushed between timed steps",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "attn_ms": attn_avg, "attn_tflops": attn_tflops, "attn_frac_peak": attn_tflops / peak_t,
+            "indexer_topk_ms": idx_avg, "indexer_tflops": idx_tflops, "indexer_frac_peak": idx_tflops / peak_t,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_tot / args.e2e_steps},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "device_status": status,
+            "topk_standalone": topk_line,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

@@ -260,8 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // MMA2: O^T += V^T . P^T, 128 value dims per instruction group
           if (!dsa::mbar_wait(p_full, ph, abort_flag, p.status)) { ok = false; break; }
           dsa::tc_fence_after();
-          for (int mb = 0; mb < p.n_v / 2; ++mb) {
+          for (int mb = 0; mb < p.n_v / 2 && ok; ++mb) {
             const int c0 = p.v_first + 2 * mb;
+            if (c0 >= p.n_qk) {  // separate V: these chunks were not waited for by MMA1
+              if (!dsa::mbar_wait(&kv_full[c0], ph, abort_flag, p.status) ||
+                  !dsa::mbar_wait(&kv_full[c0 + 1], ph, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+              dsa::tc_fence_after();
+            }
             const uint32_t tO = tmem_base + kOCol + mb * kHG;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -273,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dsa::umma_commit(&kv_empty[c0]);
             dsa::umma_commit(&kv_empty[c0 + 1]);
           }
+          if (!ok) break;
           dsa::umma_commit(o_done);
           if (p.p_alias >= 0) dsa::umma_commit(&kv_empty[p.p_alias]);
         }

@@ -1,0 +1,126 @@
+"""Parity at the full workload sizes, in the launch configuration the bench
+times.  Every row is checked where the check is exact and cheap (fused top-k
+against dense scores + top-k, top-k against the oracle's top-k of the GPU's
+own scores); indexer scores and attention outputs are checked against the
+fp64 oracle on stratified samples of rows (first, last, around t = k, random).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import DEV, assert_attention_close, assert_scores_close, dev, dev_bf16, f64
+from sparse_attention_gemm_gb300 import ops
+from sparse_attention_gemm_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    ops.device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) == 0, "a kernel raised a device status flag"
+
+
+def _rows(T, K, n, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, K - 2, K - 1, K, K + 1, T // 2, T - 2, T - 1]
+    extra = rng.choice(T, size=n, replace=False)
+    return np.unique(np.clip(np.concatenate([fixed, extra]), 0, T - 1))
+
+
+def _boundary_tolerant_topk(got_idx, ref_scores, start, length, k):
+    """Against oracle scores: ids that differ from the oracle's exact top-k must
+    lie within the score tolerance of the k-th value (ties near the boundary)."""
+    for r in range(got_idx.shape[0]):
+        n = min(k, length[r])
+        g = got_idx[r, :n] - start[r]
+        s = ref_scores[r, : length[r]]
+        assert np.all(np.diff(g) > 0) and np.all(got_idx[r, n:] == -1)
+        if n == length[r]:
+            assert np.array_equal(g, np.arange(n))
+            continue
+        kth = np.sort(s)[::-1][n - 1]
+        ref = set(np.argsort(-s, kind="stable")[:n].tolist())
+        diff = set(g.tolist()) ^ ref
+        tol = 1e-4 * abs(kth) + 1e-6
+        assert all(abs(s[j] - kth) <= tol for j in diff), f"row {r}: {len(diff)} ids off the boundary"
+
+
+def _indexer_workload_check(wl, n_sample, seed):
+    T, K = wl.T, wl.K
+    qi, ki, w = wl.qi_bits(), wl.ki_bits(), wl.w()
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(wl.cu_seqlens))
+    start, length = oracle.thd_metadata(wl.cu_seqlens, T)
+    idx, tl = ops.indexer_topk(*a, K, wl.s_max)
+    scores = ops.indexer_scores(*a, wl.s_max)
+    ui, ut, _ = ops.topk(scores, dev(length), K, row_start=dev(start))
+    # fused == dense + top-k on every row (bit-exact)
+    assert torch.equal(idx, ui) and torch.equal(tl, ut)
+    rows = _rows(T, K, n_sample, seed)
+    sc_rows = scores[torch.from_numpy(rows).to(DEV)].cpu().numpy()[:, : wl.s_max]
+    # top-k = the oracle's top-k of the GPU's own scores (exact), sampled rows
+    ri, rt = oracle.topk(sc_rows.astype(np.float64), length[rows], K, start_rows=start[rows])
+    gi = idx[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    assert np.array_equal(gi, ri) and np.array_equal(tl.cpu().numpy()[rows], rt)
+    # scores against the fp64 oracle, and top-k against the oracle's scores
+    osc, mag = oracle.indexer_scores(f64(qi[rows]), f64(ki), w[rows], start[rows], length[rows], wl.s_max,
+                                     want_abs=True)
+    fin = np.isfinite(osc)
+    assert_scores_close(sc_rows, osc, mag, fin)
+    assert np.all(np.isneginf(sc_rows[~fin]))
+    _boundary_tolerant_topk(gi, osc, start[rows], length[rows], K)
+    del scores
+    return idx, tl, rows
+
+
+def _attention_check(wl, idx, tl, rows, v=None):
+    q, kv, sk = wl.q_bits(), wl.kv_bits(), wl.sink()
+    got = ops.sparse_attn_fwd(dev_bf16(q), dev_bf16(kv), idx, wl.scale, topk_length=tl,
+                              sink=None if sk is None else dev(sk), v=None if v is None else dev_bf16(v),
+                              want_lse_kv=True, want_max_logits=True)
+    r = torch.from_numpy(rows).to(DEV)
+    sub = {k: t[r] for k, t in got.items()}
+    ref = oracle.sparse_attn(f64(q[rows]), f64(kv), idx[r].cpu().numpy(), wl.scale,
+                             topk_length=tl[r].cpu().numpy(), sink=sk, v=None if v is None else f64(v), dv=wl.Dv)
+    assert_attention_close(sub, ref)
+
+
+def test_single_doc_4k_workload():
+    wl = W.single_doc_4k()
+    idx, tl, rows = _indexer_workload_check(wl, 96, 1)
+    _attention_check(wl, idx, tl, _rows(wl.T, wl.K, 48, 11))
+
+
+def test_thd_16k_workload():
+    wl = W.thd_16k()
+    idx, tl, rows = _indexer_workload_check(wl, 96, 2)
+    # sample rows at every document boundary too
+    extra = np.concatenate([wl.cu_seqlens[:-1], wl.cu_seqlens[1:] - 1])
+    _attention_check(wl, idx, tl, np.unique(np.concatenate([_rows(wl.T, wl.K, 48, 12), extra])))
+
+
+def test_long_64k_workload():
+    wl = W.long_64k()
+    idx, tl, rows = _indexer_workload_check(wl, 40, 3)
+    _attention_check(wl, idx, tl, _rows(wl.T, wl.K, 24, 13))
+
+
+def test_gqa_routes_workload():
+    wl = W.gqa_routes()
+    routes = wl.routes()
+    packed = ops.pack_routes(dev(routes))
+    assert np.array_equal(packed.cpu().numpy(), oracle.pack_routes(routes))
+    q, k, v = wl.q_bits(), wl.kv_bits(), wl.v_bits()
+    got = ops.sparse_attn_fwd(dev_bf16(q), dev_bf16(k), packed, wl.scale, v=dev_bf16(v), want_lse_kv=True,
+                              want_max_logits=True)
+    rows = np.unique(np.concatenate([_rows(wl.T, 4, 64, 14), np.arange(0, wl.T, wl.S), np.arange(3, wl.T, wl.S)]))
+    r = torch.from_numpy(rows).to(DEV)
+    sub = {key: t[r] for key, t in got.items()}
+    ref = oracle.sparse_attn(f64(q[rows]), f64(k), packed[r].cpu().numpy(), wl.scale, v=f64(v))
+    assert_attention_close(sub, ref)
