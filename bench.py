@@ -186,6 +186,13 @@ def reduce_max(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def aggregate(local_total_ms: float, world: int, tokens_per_rank: int, steps: int, device=None):
+    """Whole-job throughput: every rank processed tokens_per_rank per step; the
+    job took the slowest rank's time."""
+    tot = reduce_max(local_total_ms, world, device)
+    return tot, world * tokens_per_rank * steps / (tot / 1e3)
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -327,9 +334,8 @@ def main():
     step_ms = [E[i][0].elapsed_time(E[i][3]) for i in range(args.steps)]
     idx_ms = [E[i][1].elapsed_time(E[i][2]) for i in range(args.steps)]
     attn_ms = [E[i][2].elapsed_time(E[i][3]) for i in range(args.steps)]
-    tot_ms = reduce_max(sum(step_ms), world, dev)
+    tot_ms, value = aggregate(sum(step_ms), world, T, args.steps, dev)
     ms_per_step = tot_ms / args.steps
-    value = world * T * args.steps / (tot_ms / 1e3)
     attn_avg = sum(attn_ms) / len(attn_ms)
     idx_avg = sum(idx_ms) / len(idx_ms)
     attn_tflops = work["attn_flops"] / (attn_avg / 1e3) / 1e12
@@ -359,8 +365,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_tot = reduce_max(sum(e2e_ms), world, dev)
-    e2e_value = world * T * args.e2e_steps / (e2e_tot / 1e3)
+    e2e_tot, e2e_value = aggregate(sum(e2e_ms), world, T, args.e2e_steps, dev)
 
     # ---- standalone top-k on a materialised causal score matrix (HBM-bound step)
     topk_line = None
