@@ -148,6 +148,39 @@ int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32
                      int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
                      int32_t* topk_length, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of the fixed device array used by dsa_indexer_topk_noalloc (64 MiB). */
+#define DSA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* dsa_indexer_topk for callers that cannot allocate device memory.  (The pages
+ * have no counterpart; this is a convenience of this library.)
+ * Some callers cannot call cudaMalloc at all: code running inside a host
+ * framework whose own allocator owns the device memory, plug-ins of
+ * inference runtimes that are handed only their input and output buffers,
+ * and latency-critical loops where an allocation is not allowed because
+ * cudaMalloc/cudaFree may synchronise the device.  This entry point takes the
+ * same arguments as dsa_indexer_topk minus the workspace; its scratch lives
+ * in one file-scope device array of DSA_NOALLOC_SCRATCH_BYTES, which every GPU
+ * that loads this library keeps until the process exits.  The caller still
+ * owns qi, ki, w, cu_seqlens, idx and topk_length.
+ *  - Shapes whose workspace (dsa_indexer_topk_workspace_size) exceeds
+ *    DSA_NOALLOC_SCRATCH_BYTES are rejected with DSA_ERR_WORKSPACE before
+ *    anything is launched (e.g. T = s_max = 2048 fits, T = s_max = 4096
+ *    does not).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and it keeps whatever the
+ *    last call left there.  Nothing needs clearing: each word the kernels read
+ *    is written earlier in the same call.  Calls that overlap on the GPU
+ *    (other streams, other host threads) race on the array and corrupt each
+ *    other's results: serialise them.
+ *  - Results are identical to dsa_indexer_topk.  It calls no allocating
+ *    routine.  Errors: as dsa_indexer_topk, plus DSA_ERR_WORKSPACE for shapes
+ *    beyond the fixed size. */
+int dsa_indexer_topk_noalloc(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                             int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
+                             int32_t* topk_length, cudaStream_t stream);
+
 /* Sparse MQA attention forward ([cuDNN-DSA] 1; THD shapes of [NeMo-GLM]
  * cudnn_sparse_attention).  For row t, head h and valid slot j (j <
  * clamp(topk_length[t], 0, K) when lengths are given, and 0 <= idx[t,j] <

@@ -30,6 +30,7 @@
 // member of the final top-k (ties included) is emitted.  Stage 2 then
 // selects exactly from the candidates (topk.cu).
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "topk_select.cuh"
@@ -586,4 +587,60 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand_key, p.cand_idx,
                                                               p.cand_cnt, cap, idx, topk_length, p.status);
   return dsa::launch_error("fused_select_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// dsa_indexer_topk_noalloc: the fused call with its scratch in a fixed,
+// file-scope device array instead of a caller-provided workspace.  The array
+// is DSA_NOALLOC_SCRATCH_BYTES long and exists on every GPU that loads this
+// library until the process exits.  Host code cannot pass the array's name to
+// a kernel (on the host it is only a stand-in symbol), so the first call on
+// each device looks up its device address with cudaGetSymbolAddress while that
+// device is current and caches it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kNoAllocMaxDevices];
+}  // namespace
+
+extern "C" int dsa_indexer_topk_noalloc(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                                        int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
+                                        int32_t* topk_length, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_topk_noalloc");
+  if (rc != DSA_OK) return rc;
+  if (k < 1 || k > DSA_MAX_TOPK)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_noalloc: need 1 <= k <= %d", DSA_MAX_TOPK);
+  const size_t need = dsa_indexer_topk_workspace_size(T, Hi, d, k, s_max);
+  if (need > DSA_NOALLOC_SCRATCH_BYTES)
+    return dsa::set_error(DSA_ERR_WORKSPACE,
+                          "dsa_indexer_topk_noalloc: these shapes need %zu bytes of scratch but the fixed array holds "
+                          "%zu; call dsa_indexer_topk with a workspace instead",
+                          need, static_cast<size_t>(DSA_NOALLOC_SCRATCH_BYTES));
+  rc = dsa::check_device(nullptr);
+  if (rc != DSA_OK) return rc;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    cudaGetLastError();
+    return dsa::set_error(DSA_ERR_UNSUPPORTED, "dsa_indexer_topk_noalloc: unusable device ordinal");
+  }
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p) {
+        cudaGetLastError();
+        return dsa::set_error(DSA_ERR_CUDA, "dsa_indexer_topk_noalloc: cannot resolve the scratch array: %s",
+                              cudaGetErrorString(e));
+      }
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  return dsa_indexer_topk(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, idx, topk_length, scratch,
+                          DSA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -47,6 +47,7 @@ _SIGNATURES = {
     "dsa_compact_sort_indices": ([P, I, I, I64, P, P, P], I),
     "dsa_indexer_topk_workspace_size": ([I, I, I, I, I], SZ),
     "dsa_indexer_topk": ([P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P], I),
+    "dsa_indexer_topk_noalloc": ([P, P, P, P, I, I, I, I, I, I, P, P, P], I),
     "dsa_sparse_attn_fwd": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P], I),
     "dsa_pack_routes": ([P, I, I, I, P, P], I),
 }
@@ -185,6 +186,22 @@ def indexer_topk(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None, idx=
     _check("dsa_indexer_topk", lib().dsa_indexer_topk(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1,
                                                       T, Hi, d, k, s_max, _p(idx), _p(topk_length), _p(workspace),
                                                       workspace.numel() * workspace.element_size(), _stream()))
+    return idx, topk_length
+
+
+def indexer_topk_noalloc(qi, ki, w, cu_seqlens, k: int, s_max: int, idx=None, topk_length=None):
+    """indexer_topk with the library's fixed scratch array (no workspace)."""
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, d = qi.shape
+    dev = qi.device
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev) if idx is None else idx
+    topk_length = torch.empty(T, dtype=torch.int32, device=dev) if topk_length is None else topk_length
+    _check("dsa_indexer_topk_noalloc",
+           lib().dsa_indexer_topk_noalloc(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hi, d,
+                                          k, s_max, _p(idx), _p(topk_length), _stream()))
     return idx, topk_length
 
 
