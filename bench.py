@@ -248,6 +248,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-topk-standalone", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
+                    help="2: single doc T=4096, 3: THD T=16384, 4: long T=65536 (the headline workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -268,7 +270,7 @@ def main():
     from sparse_attention_gemm_gb300 import ops
     from sparse_attention_gemm_gb300 import workloads as W
 
-    wl = W.long_64k()
+    wl = W.ALL[args.workload]()
     T, K, H = wl.T, wl.K, wl.H
     lengths = (np.arange(T) - np.repeat(wl.cu_seqlens[:-1], np.diff(wl.cu_seqlens)) + 1).astype(np.int64)
     work = work_counts(T, K, H, wl.Hi, wl.d, wl.Dqk, wl.Dv, lengths)
@@ -350,6 +352,7 @@ def main():
     h2d = sum(v.numel() * v.element_size() for v in hpin.values())
     d2h = sum(t.numel() * t.element_size() for t in (out, lse, idx, tl))
     e2e_ms = []
+    e2e_line = None
     for i in range(args.e2e_steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -365,7 +368,10 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_tot, e2e_value = aggregate(sum(e2e_ms), world, T, args.e2e_steps, dev)
+    if args.e2e_steps > 0:
+        e2e_tot, e2e_value = aggregate(sum(e2e_ms), world, T, args.e2e_steps, dev)
+        e2e_line = {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_tot / args.e2e_steps}
 
     # ---- standalone top-k on a materialised causal score matrix (HBM-bound step)
     topk_line = None
@@ -397,7 +403,7 @@ def main():
         del scores
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.workload == 4:
         cpu = cpu_baseline(wl, args.cpu_rows, host["qi"], host["q"], host["w"], host["ki"], host["kv"])
     del host
 
@@ -425,8 +431,7 @@ def main():
             "indexer_topk_ms": idx_avg, "indexer_tflops": idx_tflops, "indexer_frac_peak": idx_tflops / peak_t,
             "roofline": roof,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_tot / args.e2e_steps},
+            "e2e": e2e_line,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "device_status": status,

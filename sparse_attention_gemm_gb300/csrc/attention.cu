@@ -5,54 +5,70 @@
 // invalid or out-of-range ids are absent; duplicates are separate slots; the
 // sink enters only the denominator.  Shapes follow NeMo glm_moe_dsa
 // cudnn_sparse_attention (q [T,H,576], latent kv [T,1,576], V = first 512
-// dims) and, with a separate V of 256 dims, NeMo qwen3_8_flash_next
+// dims) and, with a separate 256-dim V, NeMo qwen3_8_flash_next
 // cudnn_sparse_gqa_attention.
 //
-// Work unit = (token t, group g of 64 heads).  Per unit the selected KV rows
-// are gathered once (TMA tile::gather4, four rows per instruction) into a
-// 128-key tile and shared by all 64 heads of the group (MQA).  Both products
-// are "swap AB" so that the 128-wide M of tcgen05.mma is keys or value dims,
-// never the 64 heads:
-//   MMA1  S^T[key, head]  = KV[key, 0:Dqk] . Q[head, 0:Dqk]^T   (M=128, N=64)
-//   MMA2  O^T[dim, head] += V^T[dim, key] . P^T[key, head]      (M=128 per
-//         128 value dims, N=64, K=16 keys per instruction)
-// S^T and O^T live in TMEM.  Softmax threads own one key (one TMEM lane):
-// they scale the 64 scores, keep a running per-head reference maximum
-// (online softmax; the accumulator is rescaled only when the maximum grows by
-// more than 2^8, which leaves the result exact), exponentiate, accumulate
-// per-thread row sums and write P^T (bf16) to shared memory for MMA2.
-// The epilogue reduces the row sums, adds the sink to the denominator and
-// writes out (bf16), lse (sink included), and optionally lse_kv and
-// max_logits.
+// Work unit = (token t, group g of 64 heads).  The selected KV rows are
+// gathered once per unit, in tiles of 64 keys, and shared by all 64 heads
+// (MQA).  At 64 heads the step needs ~120 FLOP per gathered byte, so the
+// kernel is organised around keeping the gather streaming: two 64-key tile
+// buffers alternate (a 128-key tile would not fit twice next to the resident
+// query), and four warps gather with cp.async, each warp instruction moving
+// four 128-byte row segments into their 128-byte-swizzled slots (rows of
+// invalid slots are zero-filled without reading memory).
 //
-// Warp roles (192 threads): warp 0 gathers (all 32 lanes issue gather4 for 4
-// keys each) and loads Q; warp 1 allocates TMEM and issues MMAs; warps 2..5
-// run softmax and epilogue.  The KV tile is split into 16 KB chunks of 64
-// dims, each with its own full/empty barrier, so the next tile's gather
-// starts as soon as MMA2 releases the chunks it no longer reads.
+// Products ("swap AB", the 64 heads are the N side of both):
+//   MMA1  S^T[key, head]  = KV[key, 0:Dqk] . Q[head, 0:Dqk]^T  (M=64 keys, N=64)
+//   MMA2  O^T[dim, head] += V^T[dim, key] . P^T[key, head]     (M=128 value
+//         dims per instruction group, N=64, K=16 keys per instruction)
+// S^T (two buffers) and O^T live in TMEM.  An M=64 accumulator occupies
+// lanes 0..15 of each 32-lane quarter (row r in lane 32*(r/16) + r%16).
+// MMA issue order runs one tile ahead: MMA1 of tile i+1 is issued before
+// MMA2 of tile i, so the tensor core has work while softmax(i) runs.
+//
+// Softmax: 8 warps, two per TMEM lane quarter; lanes 0..15 of a warp own one
+// key each and 32 heads (the warp's head half).  Per head a reference maximum
+// is kept (online softmax); the running sums and O^T are rescaled only when
+// a tile's maximum exceeds the reference by more than 2^8, which leaves the
+// result exact because numerator and denominator use the same reference.
+// p = 2^(x - m) with x = s*scale*log2(e); P^T goes to shared memory as bf16.
+// The epilogue reduces the per-thread sums, adds the sink to the
+// denominator and writes out (bf16), lse (sink included) and optionally
+// lse_kv and max_logits.
+//
+// Warps: 0..3 gather, 4 = TMEM allocation, MMA issue (lane 0) and query
+// loads (lane 1, TMA), 5..12 softmax and epilogue.  Persistent CTAs take
+// units from the longest rows down.
 #include <climits>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int kKeys = 128;
-constexpr int kHG = 64;
-constexpr int kThreads = 192;
-constexpr int kSoftWarps = 4;
-constexpr uint32_t kChunkBytes = kKeys * 128;  // 128 keys x 64 bf16
-constexpr uint32_t kQChunkBytes = kHG * 128;   // 64 heads x 64 bf16
+constexpr int kKeys = 64;                       // keys per tile
+constexpr int kHG = 64;                         // heads per group
+constexpr int kGatherWarps = 4;
+constexpr int kGatherThreads = kGatherWarps * 32;
+constexpr int kMmaWarp = 4;
+constexpr int kSoftWarp0 = 5;
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kThreads = (kSoftWarp0 + kSoftWarps) * 32;  // 416
+constexpr uint32_t kChunkBytes = kKeys * 128;   // 64 keys x 64 bf16
+constexpr uint32_t kQChunkBytes = kHG * 128;    // 64 heads x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTheta = 8.0f;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSCol = 0;
-constexpr int kOCol = 64;
+constexpr int kSCol = 0;     // S^T buffers at columns 0 and 64
+constexpr int kOCol = 128;   // O^T blocks at 128 + 64*m
 
 struct AttnParams {
   const int32_t* idx;
   const int32_t* topk_length;
   const float* sink;
+  const uint8_t* kv;   // latent (or K) rows of kv_row_bytes
+  const uint8_t* v;    // separate V rows of v_row_bytes, or nullptr
   __nv_bfloat16* out;
   float* lse;
   float* lse_kv;
@@ -61,14 +77,16 @@ struct AttnParams {
   int T, Tkv, H, G, K, Dv;
   int n_qk;      // Dqk / 64
   int n_v;       // Dv / 64
-  int n_chunks;  // KV chunks per tile
+  int n_chunks;  // 64-dim chunks per tile buffer
   int v_first;   // chunk index of value dims 0..63
-  int p_alias;   // chunk whose buffer holds P^T, or -1 (separate buffer)
+  int p_alias;   // chunk whose space holds P^T, or -1 (separate buffers)
+  int kv_row_bytes, v_row_bytes;
   float scale_log2;
 };
 
 struct Layout {
   uint32_t q, kv, p, small, bars, misc, total;
+  uint32_t buf_bytes;
 };
 
 __host__ __device__ inline Layout make_layout(int n_qk, int n_chunks, int p_alias) {
@@ -77,17 +95,18 @@ __host__ __device__ inline Layout make_layout(int n_qk, int n_chunks, int p_alia
   L.q = o;
   o += n_qk * kQChunkBytes;
   L.kv = o;
-  o += n_chunks * kChunkBytes;
+  L.buf_bytes = n_chunks * kChunkBytes;
+  o += 2 * L.buf_bytes;
   if (p_alias >= 0) {
-    L.p = L.kv + p_alias * kChunkBytes;
+    L.p = 0xFFFFFFFFu;  // P^T of buffer b lives in chunk p_alias of buffer b
   } else {
     L.p = o;
-    o += kChunkBytes;
+    o += 2 * kChunkBytes;
   }
   L.small = o;
-  o += (64 * 4 + 4 * 64 + 4 * 64 + 8) * 4;  // m_cur m_max alpha fac | wmax | red | exflag
+  o += (4 * 64 + 4 * 64 + 64 + 64 + 64 + 16) * 4;  // wmax | red | alpha | mref | fac | exflag
   L.bars = o;
-  o += (16 + 16 + 6) * 8;
+  o += 16 * 8;
   L.misc = o;
   o += 16;
   L.total = o;
@@ -100,18 +119,23 @@ __device__ __forceinline__ int ord_f32(float f) {
 }
 __device__ __forceinline__ float unord_f32(int i) { return __int_as_float(i >= 0 ? i : (i ^ 0x7FFFFFFF)); }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ int unit_tiles(const AttnParams& p, int t, int* len_out) {
+__device__ __forceinline__ int unit_len(const AttnParams& p, int t) {
   int L = p.K;
   if (p.topk_length) {
     L = __ldg(p.topk_length + t);
     L = L < 0 ? 0 : (L > p.K ? p.K : L);
   }
-  *len_out = L;
-  return (L + kKeys - 1) / kKeys;
+  return L;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -119,32 +143,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dsa::smem_u32(bar)) : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                       const __grid_constant__ CUtensorMap map_v, const AttnParams p) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap map_q, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dsa::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const Layout L = make_layout(p.n_qk, p.n_chunks, p.p_alias);
   uint8_t* qbuf = smem + L.q;
   uint8_t* kvbuf = smem + L.kv;
-  uint8_t* pbuf = smem + L.p;
-  float* m_cur = reinterpret_cast<float*>(smem + L.small);
-  float* m_max = m_cur + 64;
-  float* alpha = m_cur + 128;
-  float* fac = m_cur + 192;
-  int* wmax = reinterpret_cast<int*>(m_cur + 256);
-  float* red = m_cur + 512;
-  int* exflag = reinterpret_cast<int*>(m_cur + 768);
+  int* wmax = reinterpret_cast<int*>(smem + L.small);  // [4 quarters][64 heads]
+  float* red = reinterpret_cast<float*>(wmax + 256);   // [4][64]
+  float* alpha = red + 256;                            // [64]
+  float* mref = alpha + 64;                            // [64]
+  float* fac = mref + 64;                              // [64]
+  int* exflag = reinterpret_cast<int*>(fac + 64);      // [2][8]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* kv_full = bars;
-  uint64_t* kv_empty = bars + 16;
-  uint64_t* q_full = bars + 32;
-  uint64_t* q_empty = bars + 33;
-  uint64_t* s_full = bars + 34;
-  uint64_t* s_empty = bars + 35;
-  uint64_t* p_full = bars + 36;
-  uint64_t* o_done = bars + 37;
+  uint64_t* kv_full = bars;        // [2]
+  uint64_t* kv_empty = bars + 2;   // [2]
+  uint64_t* s_full = bars + 4;     // [2]
+  uint64_t* s_empty = bars + 6;    // [2]
+  uint64_t* p_full = bars + 8;     // [2]
+  uint64_t* q_full = bars + 10;
+  uint64_t* q_empty = bars + 11;
+  uint64_t* o_done = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -152,148 +180,157 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = p.T * p.G;
 
   if (threadIdx.x == 0) {
-    for (int c = 0; c < p.n_chunks; ++c) {
-      dsa::mbar_init(&kv_full[c], 1);
-      dsa::mbar_init(&kv_empty[c], 1);
+    for (int b = 0; b < 2; ++b) {
+      dsa::mbar_init(&kv_full[b], kGatherThreads);
+      dsa::mbar_init(&kv_empty[b], 1);
+      dsa::mbar_init(&s_full[b], 1);
+      dsa::mbar_init(&s_empty[b], kSoftWarps);
+      dsa::mbar_init(&p_full[b], kSoftWarps);
     }
     dsa::mbar_init(q_full, 1);
     dsa::mbar_init(q_empty, 1);
-    dsa::mbar_init(s_full, 1);
-    dsa::mbar_init(s_empty, kSoftWarps);
-    dsa::mbar_init(p_full, kSoftWarps);
     dsa::mbar_init(o_done, 1);
     *abort_flag = 0;
     dsa::fence_barrier_init();
   }
-  if (warp == 1) dsa::tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kMmaWarp) dsa::tmem_alloc(tmem_slot, kTmemCols);
   dsa::tc_fence_before();
   __syncthreads();
   dsa::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < kGatherWarps) {
     // ------------------------------------------------------------ gather
-    if (lane == 0) {
-      dsa::tma_prefetch_desc(&map_q);
-      dsa::tma_prefetch_desc(&map_k);
-      dsa::tma_prefetch_desc(&map_v);
-    }
-    uint32_t tile_ctr = 0, unit_ctr = 0;
+    // Thread g covers piece (g & 7) (16 bytes) of key (g >> 3) + 16*kg, for
+    // kg = 0..3 and every 64-dim chunk: one warp instruction = 4 keys x 128 B.
+    const int g = threadIdx.x;
+    const int piece = g & 7;
+    uint32_t tile_ctr = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int uu = n_units - 1 - u;
-      const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
-      int len;
-      const int nt = unit_tiles(p, t, &len);
-      if (nt == 0) continue;
-      int good = 1;
-      if (lane == 0) {
-        if (unit_ctr > 0 && !dsa::mbar_wait(q_empty, (unit_ctr - 1) & 1, abort_flag, p.status)) good = 0;
-        if (good) {
-          dsa::mbar_expect_tx(q_full, p.n_qk * kQChunkBytes);
-          for (int c = 0; c < p.n_qk; ++c) dsa::tma_load_3d(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full);
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
-      ++unit_ctr;
+      const int t = uu / p.G;
+      const int len = unit_len(p, t);
+      const int nt = (len + kKeys - 1) / kKeys;
       const int32_t* irow = p.idx + static_cast<int64_t>(t) * p.K;
-      for (int i = 0; i < nt && ok; ++i, ++tile_ctr) {
-        int y[4];
+      for (int i = 0; i < nt; ++i, ++tile_ctr) {
+        const int b = tile_ctr & 1;
+        int id[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = i * kKeys + lane * 4 + e;
-          int id = j < len ? __ldg(irow + j) : -1;
-          y[e] = (id >= 0 && id < p.Tkv) ? id : -1;
+        for (int kg = 0; kg < 4; ++kg) {
+          const int j = i * kKeys + kg * 16 + (g >> 3);
+          const int v = j < len ? __ldg(irow + j) : -1;
+          id[kg] = (v >= 0 && v < p.Tkv) ? v : -1;
         }
-        for (int c = 0; c < p.n_chunks; ++c) {
-          if (lane == 0) {
-            good = dsa::mbar_wait(&kv_empty[c], (tile_ctr & 1) ^ 1, abort_flag, p.status);
-            if (good) dsa::mbar_expect_tx(&kv_full[c], kChunkBytes);
+        if (!dsa::mbar_wait(&kv_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        dsa::fence_proxy_async_smem();
+        const uint32_t buf = dsa::smem_u32(kvbuf) + b * L.buf_bytes;
+#pragma unroll
+        for (int kg = 0; kg < 4; ++kg) {
+          const int key = kg * 16 + (g >> 3);
+          const uint32_t nbytes = id[kg] >= 0 ? 16u : 0u;
+          const int64_t row = id[kg] >= 0 ? id[kg] : 0;
+          const uint8_t* krow = p.kv + row * p.kv_row_bytes + piece * 16;
+          for (int c = 0; c < p.n_qk; ++c)
+            cp_async16(buf + c * kChunkBytes + dsa::sw128_offset(key, piece * 16), krow + c * 128, nbytes);
+          if (p.v) {
+            const uint8_t* vrow = p.v + row * p.v_row_bytes + piece * 16;
+            for (int c = 0; c < p.n_v; ++c)
+              cp_async16(buf + (p.n_qk + c) * kChunkBytes + dsa::sw128_offset(key, piece * 16), vrow + c * 128,
+                         nbytes);
           }
-          if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
-          const bool is_v = c >= p.n_qk;
-          const CUtensorMap* m = is_v ? &map_v : &map_k;
-          const int x = (is_v ? c - p.n_qk : c) * 64;
-          dsa::tma_gather4(kvbuf + c * kChunkBytes + lane * 512, m, x, y[0], y[1], y[2], y[3], &kv_full[c]);
         }
+        cp_async_arrive(&kv_full[b]);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
+      // ------------------------------------------------------------ MMA issue
       constexpr uint32_t idesc1 = dsa::idesc_bf16(kKeys, kHG, 0, 0);
-      constexpr uint32_t idesc2 = dsa::idesc_bf16(kKeys, kHG, 1, 1);
-      const uint32_t q_addr = dsa::smem_u32(qbuf), kv_addr = dsa::smem_u32(kvbuf), p_addr = dsa::smem_u32(pbuf);
-      const uint32_t tS = tmem_base + kSCol;
+      constexpr uint32_t idesc2 = dsa::idesc_bf16(128, kHG, 1, 1);
+      const uint32_t q_addr = dsa::smem_u32(qbuf), kv_addr = dsa::smem_u32(kvbuf);
+      const uint32_t p_sep = dsa::smem_u32(smem) + L.p;
       uint32_t tile_ctr = 0, unit_ctr = 0;
       bool ok = true;
+      auto mma1 = [&](uint32_t tc) -> bool {
+        const int b = tc & 1;
+        const uint32_t ph = (tc >> 1) & 1;
+        if (!dsa::mbar_wait(&s_empty[b], ph ^ 1, abort_flag, p.status)) return false;
+        if (!dsa::mbar_wait(&kv_full[b], ph, abort_flag, p.status)) return false;
+        dsa::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05 reads
+        dsa::tc_fence_after();
+        const uint32_t a0 = kv_addr + b * L.buf_bytes;
+        for (int c = 0; c < p.n_qk; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = dsa::smem_desc(a0 + c * kChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
+            const uint64_t bd = dsa::smem_desc(q_addr + c * kQChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
+            dsa::umma_bf16(tmem_base + kSCol + b * 64, ad, bd, idesc1, (c | kk) != 0);
+          }
+        }
+        dsa::umma_commit(&s_full[b]);
+        return true;
+      };
+      auto mma2 = [&](uint32_t tc, bool first) -> bool {
+        const int b = tc & 1;
+        const uint32_t ph = (tc >> 1) & 1;
+        if (!dsa::mbar_wait(&p_full[b], ph, abort_flag, p.status)) return false;
+        dsa::tc_fence_after();
+        const uint32_t a0 = kv_addr + b * L.buf_bytes;
+        const uint32_t pb = p.p_alias >= 0 ? a0 + p.p_alias * kChunkBytes : p_sep + b * kChunkBytes;
+        for (int mb = 0; mb < p.n_v / 2; ++mb) {
+          const uint32_t c0 = a0 + (p.v_first + 2 * mb) * kChunkBytes;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t ad = dsa::smem_desc(c0 + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
+            const uint64_t bd = dsa::smem_desc(pb + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
+            dsa::umma_bf16(tmem_base + kOCol + mb * kHG, ad, bd, idesc2, (!first || kk > 0) ? 1u : 0u);
+          }
+        }
+        dsa::umma_commit(o_done);
+        dsa::umma_commit(&kv_empty[b]);
+        return true;
+      };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int uu = n_units - 1 - u;
         const int t = uu / p.G;
-        int len;
-        const int nt = unit_tiles(p, t, &len);
+        const int nt = (unit_len(p, t) + kKeys - 1) / kKeys;
         if (nt == 0) continue;
         if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
         ++unit_ctr;
-        for (int i = 0; i < nt; ++i, ++tile_ctr) {
-          const uint32_t ph = tile_ctr & 1;
-          // MMA1: S^T = KV . Q^T over the Dqk chunks
-          if (!dsa::mbar_wait(s_empty, ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          for (int c = 0; c < p.n_qk; ++c) {
-            if (!dsa::mbar_wait(&kv_full[c], ph, abort_flag, p.status)) { ok = false; break; }
-            dsa::tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = dsa::smem_desc(kv_addr + c * kChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
-              const uint64_t bd = dsa::smem_desc(q_addr + c * kQChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
-              dsa::umma_bf16(tS, ad, bd, idesc1, (c | kk) != 0);
-            }
-          }
-          if (!ok) break;
-          dsa::umma_commit(s_full);
-          // chunks read only by MMA1 (and not holding P^T) are free now
-          for (int c = 0; c < p.n_qk; ++c) {
-            const bool is_value = (c >= p.v_first && c < p.v_first + p.n_v);
-            if (!is_value && c != p.p_alias) dsa::umma_commit(&kv_empty[c]);
-          }
+        const uint32_t t0 = tile_ctr;
+        // MMA1(i+1) is issued before MMA2(i); the unit's last MMA2 drains.
+        for (int i = 0; i < nt && ok; ++i) {
+          if (!mma1(t0 + i)) { ok = false; break; }
           if (i == nt - 1) dsa::umma_commit(q_empty);
-          // MMA2: O^T += V^T . P^T, 128 value dims per instruction group
-          if (!dsa::mbar_wait(p_full, ph, abort_flag, p.status)) { ok = false; break; }
-          dsa::tc_fence_after();
-          for (int mb = 0; mb < p.n_v / 2 && ok; ++mb) {
-            const int c0 = p.v_first + 2 * mb;
-            if (c0 >= p.n_qk) {  // separate V: these chunks were not waited for by MMA1
-              if (!dsa::mbar_wait(&kv_full[c0], ph, abort_flag, p.status) ||
-                  !dsa::mbar_wait(&kv_full[c0 + 1], ph, abort_flag, p.status)) {
-                ok = false;
-                break;
-              }
-              dsa::tc_fence_after();
-            }
-            const uint32_t tO = tmem_base + kOCol + mb * kHG;
-#pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-              const uint64_t ad =
-                  dsa::smem_desc(kv_addr + c0 * kChunkBytes + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
-              const uint64_t bd = dsa::smem_desc(p_addr + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
-              dsa::umma_bf16(tO, ad, bd, idesc2, (i > 0 || kk > 0) ? 1u : 0u);
-            }
-            dsa::umma_commit(&kv_empty[c0]);
-            dsa::umma_commit(&kv_empty[c0 + 1]);
-          }
-          if (!ok) break;
-          dsa::umma_commit(o_done);
-          if (p.p_alias >= 0) dsa::umma_commit(&kv_empty[p.p_alias]);
+          if (i > 0 && !mma2(t0 + i - 1, i == 1)) { ok = false; break; }
         }
+        if (ok && !mma2(t0 + nt - 1, nt == 1)) ok = false;
+        tile_ctr = t0 + nt;
+      }
+    } else if (lane == 1) {
+      // ------------------------------------------------------------ query loads
+      dsa::tma_prefetch_desc(&map_q);
+      uint32_t unit_ctr = 0;
+      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int uu = n_units - 1 - u;
+        const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
+        if (unit_len(p, t) == 0) continue;
+        if (unit_ctr > 0 && !dsa::mbar_wait(q_empty, (unit_ctr - 1) & 1, abort_flag, p.status)) break;
+        dsa::mbar_expect_tx(q_full, p.n_qk * kQChunkBytes);
+        for (int c = 0; c < p.n_qk; ++c) dsa::tma_load_3d(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full);
+        ++unit_ctr;
       }
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int st = threadIdx.x - 64;  // 0..127
-    const int wq = warp - 2;          // softmax warp 0..3
-    const int quarter = warp & 3;     // TMEM lane quarter
-    const int key_lane = quarter * 32 + lane;
+    const int sw = warp - kSoftWarp0;           // 0..7
+    const int st = threadIdx.x - kSoftWarp0 * 32;  // 0..255
+    const int quarter = warp & 3;               // TMEM lane quarter
+    const int hh = sw >> 2;                     // head half: heads hh*32 .. hh*32+31
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int key_in_tile = quarter * 16 + (lane & 15);  // meaningful for lanes 0..15
+    const bool key_lane = lane < 16;
     const bool want_max = p.max_logits != nullptr;
     uint32_t tile_ctr = 0;
     bool ok = true;
@@ -301,12 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int uu = n_units - 1 - u;
       const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
       const int hv = min(kHG, p.H - g * kHG);
-      int len;
-      const int nt = unit_tiles(p, t, &len);
-      const int64_t orow = static_cast<int64_t>(t) * p.H + g * kHG;  // first (t, head) row of the group
+      const int len = unit_len(p, t);
+      const int nt = (len + kKeys - 1) / kKeys;
+      const int64_t orow = static_cast<int64_t>(t) * p.H + g * kHG;
       if (nt == 0) {
         for (int h = 0; h < hv; ++h)
-          for (int d = st; d < p.Dv; d += 128) p.out[(orow + h) * p.Dv + d] = __float2bfloat16_rn(0.f);
+          for (int d = st; d < p.Dv; d += kSoftThreads) p.out[(orow + h) * p.Dv + d] = __float2bfloat16_rn(0.f);
         if (st < hv) {
           p.lse[orow + st] = p.sink ? __ldg(p.sink + g * kHG + st) : -INFINITY;
           if (p.lse_kv) p.lse_kv[orow + st] = INFINITY;
@@ -314,127 +351,136 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      if (st < 64) {
-        m_cur[st] = -INFINITY;
-        m_max[st] = -INFINITY;
-      }
-      float l_part[64];
+      float l_part[32];
+      float m_max = -INFINITY;  // exact maximum of head st (threads st < 64), for max_logits
 #pragma unroll
-      for (int h = 0; h < 64; ++h) l_part[h] = 0.f;
-      named_bar(1, 128);
+      for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
+      const float4* mref4 = reinterpret_cast<const float4*>(mref + hh * 32);
+      if (st < 64) mref[st] = -INFINITY;  // ordered before its readers by the first tile's barriers
       const int32_t* irow = p.idx + static_cast<int64_t>(t) * p.K;
-
+      int next_id = -1;
+      {
+        const int j = key_in_tile;
+        next_id = (key_lane && j < len) ? __ldg(irow + j) : -1;
+      }
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
-        const uint32_t ph = tile_ctr & 1;
-        if (!dsa::mbar_wait(s_full, ph, abort_flag, p.status)) { ok = false; break; }
+        const int b = tile_ctr & 1;
+        const uint32_t ph = (tile_ctr >> 1) & 1;
+        const int j = i * kKeys + key_in_tile;
+        const int id = next_id;
+        if (i + 1 < nt) {
+          const int jn = j + kKeys;
+          next_id = (key_lane && jn < len) ? __ldg(irow + jn) : -1;
+        }
+        const bool valid = key_lane && j < len && id >= 0 && id < p.Tkv;
+        if (!dsa::mbar_wait(&s_full[b], ph, abort_flag, p.status)) { ok = false; break; }
         dsa::tc_fence_after();
-        float x[64];
+        float x[32];
         {
-          uint32_t va[32], vb[32];
-          dsa::tmem_ld32(tmem_base + lane_off + kSCol, va);
-          dsa::tmem_ld32(tmem_base + lane_off + kSCol + 32, vb);
+          uint32_t v[32];
+          dsa::tmem_ld32(tmem_base + lane_off + kSCol + b * 64 + hh * 32, v);
           dsa::tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            x[h] = __uint_as_float(va[h]);
-            x[h + 32] = __uint_as_float(vb[h]);
-          }
+          for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(v[h]);
         }
         dsa::tc_fence_before();
         __syncwarp();
-        if (lane == 0) dsa::mbar_arrive(s_empty);
-
-        const int j = i * kKeys + key_lane;
-        const int id = j < len ? __ldg(irow + j) : -1;
-        const bool valid = j < len && id >= 0 && id < p.Tkv;
+        if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
         bool ex = false;
 #pragma unroll
-        for (int h = 0; h < 64; ++h) {
-          x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-          ex |= x[h] > m_cur[h] + kTheta;
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 m4 = mref4[h4];
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = h4 * 4 + e;
+            x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
+            ex |= x[h] > mm[e] + kTheta;
+          }
         }
         const bool ex_warp = __any_sync(0xffffffffu, ex);
-        if (lane == 0) exflag[(ph << 2) + wq] = ex_warp ? 1 : 0;
-        named_bar(1, 128);
-        const bool reduce = want_max || exflag[ph << 2] || exflag[(ph << 2) + 1] || exflag[(ph << 2) + 2] ||
-                            exflag[(ph << 2) + 3];
+        if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = ex_warp ? 1 : 0;
+        named_bar(1, kSoftThreads);
+        bool reduce = want_max;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) reduce |= exflag[(tile_ctr & 1) * 8 + w] != 0;
         if (reduce) {
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
+          for (int h = 0; h < 32; ++h) {
             const int r = __reduce_max_sync(0xffffffffu, ord_f32(x[h]));
-            if (lane == (h & 31)) wmax[wq * 64 + h] = r;
+            if (lane == h) wmax[quarter * 64 + hh * 32 + h] = r;
           }
-          named_bar(1, 128);
+          named_bar(1, kSoftThreads);
           if (st < 64) {
-            int r = wmax[st];
-            r = max(r, wmax[64 + st]);
-            r = max(r, wmax[128 + st]);
-            r = max(r, wmax[192 + st]);
+            int r = max(max(wmax[st], wmax[64 + st]), max(wmax[128 + st], wmax[192 + st]));
             const float tmax = unord_f32(r);
-            m_max[st] = fmaxf(m_max[st], tmax);
-            const float mo = m_cur[st];
+            const float mo = mref[st];
             const float mn = (tmax > mo + kTheta) ? tmax : mo;
-            alpha[st] = (mn == mo) ? 1.f : exp2f(mo - mn);
-            m_cur[st] = mn;
+            alpha[st] = (mn == mo) ? 1.f : ex2(mo - mn);
+            mref[st] = mn;
+            m_max = fmaxf(m_max, tmax);
           }
-          named_bar(1, 128);
+          named_bar(1, kSoftThreads);
           bool rescale = false;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            const float a = alpha[h];
+          for (int h = 0; h < 32; ++h) {
+            const float a = alpha[hh * 32 + h];
             rescale |= a != 1.f;
             l_part[h] *= a;
           }
           if (rescale && i > 0) {
-            // O^T columns of heads whose reference maximum moved get alpha[h];
-            // MMA2 of the previous tile must have landed first.
-            if (!dsa::mbar_wait(o_done, ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+            // MMA2 of the previous tile must have landed before O^T is scaled
+            if (!dsa::mbar_wait(o_done, ((tile_ctr - 1) & 1), abort_flag, p.status)) { ok = false; break; }
             dsa::tc_fence_after();
+            const float* a32 = alpha + hh * 32;
             for (int mb = 0; mb < p.n_v / 2; ++mb) {
-              for (int half = 0; half < 2; ++half) {
-                const uint32_t ta = tmem_base + lane_off + kOCol + mb * kHG + half * 32;
-                uint32_t v[32];
-                dsa::tmem_ld32(ta, v);
-                dsa::tmem_wait_ld();
+              const uint32_t ta = tmem_base + lane_off + kOCol + mb * kHG + hh * 32;
+              uint32_t v[32];
+              dsa::tmem_ld32(ta, v);
+              dsa::tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha[half * 32 + c]);
-                dsa::tmem_st32(ta, v);
-              }
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a32[c]);
+              dsa::tmem_st32(ta, v);
             }
             dsa::tmem_wait_st();
           }
         }
-        // P^T row of this key: 64 bf16 = 8 chunks of 16 bytes, 128-byte swizzle
-        uint8_t* prow = pbuf + key_lane * 128;
+        // P^T row of this key: heads hh*32 .. hh*32+31 = 4 chunks of 16 bytes
+        uint8_t* prow = (p.p_alias >= 0 ? kvbuf + b * L.buf_bytes + p.p_alias * kChunkBytes
+                                        : smem + L.p + b * kChunkBytes) +
+                        key_in_tile * 128;
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
+        for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t w4[4];
+          const float4 ma = mref4[c4 * 2], mb4 = mref4[c4 * 2 + 1];
+          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int h0 = c16 * 8 + e * 2;
-            const float p0 = valid ? exp2f(x[h0] - m_cur[h0]) : 0.f;
-            const float p1 = valid ? exp2f(x[h0 + 1] - m_cur[h0 + 1]) : 0.f;
+            const int h0 = c4 * 8 + e * 2;
+            const float p0 = valid ? ex2(x[h0] - mm[e * 2]) : 0.f;
+            const float p1 = valid ? ex2(x[h0 + 1] - mm[e * 2 + 1]) : 0.f;
             l_part[h0] += p0;
             l_part[h0 + 1] += p1;
             w4[e] = pack_bf16x2(p0, p1);
           }
-          const int pos = (c16 ^ (key_lane & 7)) * 16;
-          *reinterpret_cast<uint4*>(prow + pos) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          if (key_lane) {
+            const int c16 = hh * 4 + c4;
+            *reinterpret_cast<uint4*>(prow + ((c16 ^ (key_in_tile & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
         }
         dsa::fence_proxy_async_smem();
         dsa::tc_fence_before();
         __syncwarp();
-        if (lane == 0) dsa::mbar_arrive(p_full);
+        if (lane == 0) dsa::mbar_arrive(&p_full[b]);
       }
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
       if (!dsa::mbar_wait(o_done, (tile_ctr - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       dsa::tc_fence_after();
-      // l_part summed over the 128 key threads: transpose-reduce within the
-      // warp (lane ends with heads 2*lane, 2*lane+1), then across warps.
+      // per-thread sums over this warp's keys: transpose-reduce, lane l ends with head hh*32 + l
 #pragma unroll
-      for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+      for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
         for (int k = 0; k < n; ++k) {
@@ -443,14 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_part[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
         }
       }
-      red[wq * 64 + 2 * lane] = l_part[0];
-      red[wq * 64 + 2 * lane + 1] = l_part[1];
-      named_bar(1, 128);
+      red[quarter * 64 + hh * 32 + lane] = l_part[0];
+      named_bar(1, kSoftThreads);
       if (st < 64) {
         const float l = red[st] + red[64 + st] + red[128 + st] + red[192 + st];
-        const float mc = m_cur[st];
+        const float mc = mref[st];
         const float sk = (p.sink && st < hv) ? __ldg(p.sink + g * kHG + st) * kLog2e : -INFINITY;
-        float f = 0.f, lse_v, lkv, mlog;
+        float f = 0.f, lse_v, lkv, mlog = -INFINITY;
         if (l > 0.f) {
           const float M = fmaxf(mc, sk);
           const float a = exp2f(mc - M);
@@ -458,11 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           f = a / z;
           lse_v = (M + log2f(z)) * kLn2;
           lkv = (mc + log2f(l)) * kLn2;
-          mlog = m_max[st] * kLn2;  // x = s * log2(e), so max s = max x * ln(2)
+          if (want_max) mlog = m_max * kLn2;  // x = s*log2(e), so max s = max x * ln(2)
         } else {
           lse_v = sk * kLn2;
           lkv = INFINITY;
-          mlog = -INFINITY;
         }
         fac[st] = f;
         if (st < hv) {
@@ -471,27 +515,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.max_logits) p.max_logits[orow + st] = mlog;
         }
       }
-      named_bar(1, 128);
-      for (int mb = 0; mb < p.n_v / 2; ++mb) {
-        for (int half = 0; half < 2; ++half) {
+      named_bar(1, kSoftThreads);
+      {
+        const float* f32 = fac + hh * 32;
+        for (int mb = 0; mb < p.n_v / 2; ++mb) {
           uint32_t v[32];
-          dsa::tmem_ld32(tmem_base + lane_off + kOCol + mb * kHG + half * 32, v);
+          dsa::tmem_ld32(tmem_base + lane_off + kOCol + mb * kHG + hh * 32, v);
           dsa::tmem_wait_ld();
-          const int d = mb * 128 + key_lane;
+          const int d = mb * 128 + quarter * 32 + lane;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int h = half * 32 + c;
-            if (h < hv) p.out[(orow + h) * p.Dv + d] = __float2bfloat16_rn(__uint_as_float(v[c]) * fac[h]);
+            const int h = hh * 32 + c;
+            if (h < hv) p.out[(orow + h) * p.Dv + d] = __float2bfloat16_rn(__uint_as_float(v[c]) * f32[c]);
           }
         }
       }
       dsa::tc_fence_before();
-      named_bar(1, 128);
+      named_bar(1, kSoftThreads);
     }
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     dsa::tc_fence_after();
     dsa::tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -526,6 +571,8 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
   p.idx = idx;
   p.topk_length = topk_length;
   p.sink = sink;
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.v = static_cast<const uint8_t*>(v);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.lse_kv = lse_kv;
@@ -539,6 +586,8 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
   p.Dv = Dv;
   p.n_qk = Dqk / 64;
   p.n_v = Dv / 64;
+  p.kv_row_bytes = Dqk * 2;
+  p.v_row_bytes = Dv * 2;
   p.scale_log2 = scale * kLog2e;
   if (latent) {
     p.n_chunks = p.n_qk;
@@ -549,20 +598,10 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
     p.v_first = p.n_qk;
     p.p_alias = -1;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq;
   rc = dsa::encode_tensor_map_3d(&mq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Dqk, H, T, static_cast<uint64_t>(Dqk) * 2,
                                  static_cast<uint64_t>(Dqk) * H * 2, 64, kHG, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != DSA_OK) return rc;
-  rc = dsa::encode_tensor_map_2d(&mk, kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Dqk, Tkv, static_cast<uint64_t>(Dqk) * 2,
-                                 64, 1, CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc != DSA_OK) return rc;
-  if (separate) {
-    rc = dsa::encode_tensor_map_2d(&mv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Dv, Tkv, static_cast<uint64_t>(Dv) * 2, 64,
-                                   1, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (rc != DSA_OK) return rc;
-  } else {
-    mv = mk;
-  }
   const Layout L = make_layout(p.n_qk, p.n_chunks, p.p_alias);
   const size_t smem = L.total + 1024;
   if (cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -570,6 +609,6 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
     return dsa::launch_error("sparse_attn_kernel smem attribute");
   const int units = T * p.G;
   const int grid = units < sms ? units : sms;
-  sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(mq, p);
   return dsa::launch_error("sparse_attn_kernel");
 }
