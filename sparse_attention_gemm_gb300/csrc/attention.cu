@@ -143,8 +143,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+// 16-byte global -> shared copy; src_bytes = 0 fills zeros without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dsa::smem_u32(bar)) : "memory");
@@ -205,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // kg = 0..3 and every 64-dim chunk: one warp instruction = 4 keys x 128 B.
     const int g = threadIdx.x;
     const int piece = g & 7;
+    // The gathered rows (kv, v) are re-read by every query row: keep them in L2
+    // while the streamed q, ids and outputs pass through.
+    const uint64_t keep = dsa::l2_policy_evict_last();
     uint32_t tile_ctr = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -213,14 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int len = unit_len(p, t);
       const int nt = (len + kKeys - 1) / kKeys;
       const int32_t* irow = p.idx + static_cast<int64_t>(t) * p.K;
+      // ids are loaded one tile ahead so that their latency hides behind the
+      // previous tile's copies
+      int nxt[4];
+#pragma unroll
+      for (int kg = 0; kg < 4; ++kg) {
+        const int j = kg * 16 + (g >> 3);
+        nxt[kg] = j < len ? __ldcs(irow + j) : -1;
+      }
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
         const int b = tile_ctr & 1;
         int id[4];
 #pragma unroll
         for (int kg = 0; kg < 4; ++kg) {
-          const int j = i * kKeys + kg * 16 + (g >> 3);
-          const int v = j < len ? __ldg(irow + j) : -1;
-          id[kg] = (v >= 0 && v < p.Tkv) ? v : -1;
+          id[kg] = (nxt[kg] >= 0 && nxt[kg] < p.Tkv) ? nxt[kg] : -1;
+          const int j = (i + 1) * kKeys + kg * 16 + (g >> 3);
+          nxt[kg] = (i + 1 < nt && j < len) ? __ldcs(irow + j) : -1;
         }
         if (!dsa::mbar_wait(&kv_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         dsa::fence_proxy_async_smem();
@@ -232,12 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t row = id[kg] >= 0 ? id[kg] : 0;
           const uint8_t* krow = p.kv + row * p.kv_row_bytes + piece * 16;
           for (int c = 0; c < p.n_qk; ++c)
-            cp_async16(buf + c * kChunkBytes + dsa::sw128_offset(key, piece * 16), krow + c * 128, nbytes);
+            cp_async16(buf + c * kChunkBytes + dsa::sw128_offset(key, piece * 16), krow + c * 128, nbytes, keep);
           if (p.v) {
             const uint8_t* vrow = p.v + row * p.v_row_bytes + piece * 16;
             for (int c = 0; c < p.n_v; ++c)
               cp_async16(buf + (p.n_qk + c) * kChunkBytes + dsa::sw128_offset(key, piece * 16), vrow + c * 128,
-                         nbytes);
+                         nbytes, keep);
           }
         }
         cp_async_arrive(&kv_full[b]);
@@ -252,11 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t p_sep = dsa::smem_u32(smem) + L.p;
       uint32_t tile_ctr = 0, unit_ctr = 0;
       bool ok = true;
-      auto mma1 = [&](uint32_t tc) -> bool {
+      // MMA1(tc): S^T[tc&1] = KV(tile tc) . Q^T; needs the tile and a free S buffer.
+      auto mma1 = [&](uint32_t tc) {
         const int b = tc & 1;
-        const uint32_t ph = (tc >> 1) & 1;
-        if (!dsa::mbar_wait(&s_empty[b], ph ^ 1, abort_flag, p.status)) return false;
-        if (!dsa::mbar_wait(&kv_full[b], ph, abort_flag, p.status)) return false;
         dsa::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05 reads
         dsa::tc_fence_after();
         const uint32_t a0 = kv_addr + b * L.buf_bytes;
@@ -269,12 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         dsa::umma_commit(&s_full[b]);
-        return true;
       };
-      auto mma2 = [&](uint32_t tc, bool first) -> bool {
+      // MMA2(tc): O^T += V^T(tile tc) . P^T(tile tc); releases the tile buffer.
+      auto mma2 = [&](uint32_t tc, bool first) {
         const int b = tc & 1;
-        const uint32_t ph = (tc >> 1) & 1;
-        if (!dsa::mbar_wait(&p_full[b], ph, abort_flag, p.status)) return false;
         dsa::tc_fence_after();
         const uint32_t a0 = kv_addr + b * L.buf_bytes;
         const uint32_t pb = p.p_alias >= 0 ? a0 + p.p_alias * kChunkBytes : p_sep + b * kChunkBytes;
@@ -289,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         dsa::umma_commit(o_done);
         dsa::umma_commit(&kv_empty[b]);
-        return true;
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int uu = n_units - 1 - u;
@@ -298,19 +307,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nt == 0) continue;
         if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
         ++unit_ctr;
-        const uint32_t t0 = tile_ctr;
-        // MMA1(i+1) is issued before MMA2(i); the unit's last MMA2 drains.
-        for (int i = 0; i < nt && ok; ++i) {
-          if (!mma1(t0 + i)) { ok = false; break; }
-          if (i == nt - 1) dsa::umma_commit(q_empty);
-          if (i > 0 && !mma2(t0 + i - 1, i == 1)) { ok = false; break; }
+        const uint32_t t0 = tile_ctr, tend = tile_ctr + nt;
+        // Issue whichever product is ready first: MMA1 of the next tile once its
+        // gather landed and its S buffer is free, or MMA2 of the oldest tile
+        // whose P is written.  MMA1 may run at most two tiles ahead of MMA2
+        // (two tile buffers, two S buffers).
+        uint32_t n1 = t0, n2 = t0;
+        uint64_t t_wait = 0;
+        while (n2 < tend) {
+          bool progressed = false;
+          if (n1 < tend && n1 < n2 + 2 && dsa::mbar_test_wait(&s_empty[n1 & 1], (((n1 >> 1) & 1) ^ 1)) &&
+              dsa::mbar_test_wait(&kv_full[n1 & 1], (n1 >> 1) & 1)) {
+            mma1(n1);
+            if (n1 == tend - 1) dsa::umma_commit(q_empty);
+            ++n1;
+            progressed = true;
+          }
+          if (n2 < n1 && dsa::mbar_test_wait(&p_full[n2 & 1], (n2 >> 1) & 1)) {
+            mma2(n2, n2 == t0);
+            ++n2;
+            progressed = true;
+          }
+          if (progressed) {
+            t_wait = 0;
+          } else {
+            if (*abort_flag) { ok = false; break; }
+            const uint64_t now = dsa::globaltimer();
+            if (t_wait == 0) {
+              t_wait = now;
+            } else if (now - t_wait > DSA_WAIT_TIMEOUT_NS) {
+              atomicOr(p.status, DSA_STATUS_WAIT_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
         }
-        if (ok && !mma2(t0 + nt - 1, nt == 1)) ok = false;
-        tile_ctr = t0 + nt;
+        tile_ctr = tend;
       }
     } else if (lane == 1) {
       // ------------------------------------------------------------ query loads
       dsa::tma_prefetch_desc(&map_q);
+      const uint64_t stream = dsa::l2_policy_evict_first();  // each query tile is read once
       uint32_t unit_ctr = 0;
       for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const int uu = n_units - 1 - u;
@@ -318,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (unit_len(p, t) == 0) continue;
         if (unit_ctr > 0 && !dsa::mbar_wait(q_empty, (unit_ctr - 1) & 1, abort_flag, p.status)) break;
         dsa::mbar_expect_tx(q_full, p.n_qk * kQChunkBytes);
-        for (int c = 0; c < p.n_qk; ++c) dsa::tma_load_3d(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full);
+        for (int c = 0; c < p.n_qk; ++c)
+          dsa::tma_load_3d_hint(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full, stream);
         ++unit_ctr;
       }
     }
@@ -361,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int next_id = -1;
       {
         const int j = key_in_tile;
-        next_id = (key_lane && j < len) ? __ldg(irow + j) : -1;
+        next_id = (key_lane && j < len) ? __ldcs(irow + j) : -1;
       }
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
         const int b = tile_ctr & 1;
@@ -370,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int id = next_id;
         if (i + 1 < nt) {
           const int jn = j + kKeys;
-          next_id = (key_lane && jn < len) ? __ldg(irow + jn) : -1;
+          next_id = (key_lane && jn < len) ? __ldcs(irow + jn) : -1;
         }
         const bool valid = key_lane && j < len && id >= 0 && id < p.Tkv;
         if (!dsa::mbar_wait(&s_full[b], ph, abort_flag, p.status)) { ok = false; break; }
@@ -402,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = ex_warp ? 1 : 0;
         named_bar(1, kSoftThreads);
         bool reduce = want_max;
+        bool need_rescale = false;
 #pragma unroll
         for (int w = 0; w < 8; ++w) reduce |= exflag[(tile_ctr & 1) * 8 + w] != 0;
         if (reduce) {
@@ -428,22 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rescale |= a != 1.f;
             l_part[h] *= a;
           }
-          if (rescale && i > 0) {
-            // MMA2 of the previous tile must have landed before O^T is scaled
-            if (!dsa::mbar_wait(o_done, ((tile_ctr - 1) & 1), abort_flag, p.status)) { ok = false; break; }
-            dsa::tc_fence_after();
-            const float* a32 = alpha + hh * 32;
-            for (int mb = 0; mb < p.n_v / 2; ++mb) {
-              const uint32_t ta = tmem_base + lane_off + kOCol + mb * kHG + hh * 32;
-              uint32_t v[32];
-              dsa::tmem_ld32(ta, v);
-              dsa::tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a32[c]);
-              dsa::tmem_st32(ta, v);
-            }
-            dsa::tmem_wait_st();
-          }
+          need_rescale = rescale && i > 0;
         }
         // P^T row of this key: heads hh*32 .. hh*32+31 = 4 chunks of 16 bytes
         uint8_t* prow = (p.p_alias >= 0 ? kvbuf + b * L.buf_bytes + p.p_alias * kChunkBytes
@@ -468,6 +493,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(prow + ((c16 ^ (key_in_tile & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
+        // O^T columns of heads whose reference moved get alpha[h]; this runs after
+        // P is written so that the scores are no longer live.
+        if (need_rescale) {
+          // MMA2 of the previous tile must have landed before O^T is scaled
+          if (!dsa::mbar_wait(o_done, ((tile_ctr - 1) & 1), abort_flag, p.status)) { ok = false; break; }
+          dsa::tc_fence_after();
+          const float* a32 = alpha + hh * 32;
+          for (int mb = 0; mb < p.n_v / 2; ++mb) {
+            const uint32_t ta = tmem_base + lane_off + kOCol + mb * kHG + hh * 32;
+            uint32_t v[32];
+            dsa::tmem_ld32(ta, v);
+            dsa::tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * a32[c]);
+            dsa::tmem_st32(ta, v);
+          }
+          dsa::tmem_wait_st();
+        }
         dsa::fence_proxy_async_smem();
         dsa::tc_fence_before();
         __syncwarp();
@@ -478,18 +521,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       if (!dsa::mbar_wait(o_done, (tile_ctr - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       dsa::tc_fence_after();
-      // per-thread sums over this warp's keys: transpose-reduce, lane l ends with head hh*32 + l
+      // per-head sums over this warp's 16 key lanes (lanes 16..31 hold zeros)
 #pragma unroll
-      for (int off = 16, n = 16; off >= 1; off >>= 1, n >>= 1) {
-        const bool upper = (lane & off) != 0;
-#pragma unroll
-        for (int k = 0; k < n; ++k) {
-          const float send = upper ? l_part[k] : l_part[k + n];
-          const float keep = upper ? l_part[k + n] : l_part[k];
-          l_part[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
+      for (int h = 0; h < 32; ++h) {
+        float v = l_part[h];
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if (lane == 0) red[quarter * 64 + hh * 32 + h] = v;
       }
-      red[quarter * 64 + hh * 32 + lane] = l_part[0];
       named_bar(1, kSoftThreads);
       if (st < 64) {
         const float l = red[st] + red[64 + st] + red[128 + st] + red[192 + st];
@@ -518,15 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(1, kSoftThreads);
       {
         const float* f32 = fac + hh * 32;
+        const int hcount = min(32, hv - hh * 32);  // real heads in this warp's half
         for (int mb = 0; mb < p.n_v / 2; ++mb) {
           uint32_t v[32];
           dsa::tmem_ld32(tmem_base + lane_off + kOCol + mb * kHG + hh * 32, v);
           dsa::tmem_wait_ld();
-          const int d = mb * 128 + quarter * 32 + lane;
+          __nv_bfloat16* o = p.out + (orow + hh * 32) * p.Dv + mb * 128 + quarter * 32 + lane;
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int h = hh * 32 + c;
-            if (h < hv) p.out[(orow + h) * p.Dv + d] = __float2bfloat16_rn(__uint_as_float(v[c]) * f32[c]);
+            if (c < hcount) __stcs(o, __float2bfloat16_rn(__uint_as_float(v[c]) * f32[c]));
+            o += p.Dv;
           }
         }
       }

@@ -216,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------ TMA producer
       dsa::tma_prefetch_desc(&map_q);
       dsa::tma_prefetch_desc(&map_k);
+      // key tiles are re-read by every query block; query blocks are read once
+      const uint64_t keep = dsa::l2_policy_evict_last();
+      const uint64_t stream = dsa::l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int iter = 0;
@@ -225,13 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
         for (int c = 0; c < nch; ++c)
-          dsa::tma_load_2d(qbuf + c * kNRows * 128, &map_q, c * 64, br.t0 * p.Hi, qfull);
+          dsa::tma_load_2d_hint(qbuf + c * kNRows * 128, &map_q, c * 64, br.t0 * p.Hi, qfull, stream);
         for (int kt = br.kt0; kt <= br.kt1; ++kt) {
           if (!dsa::mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           dsa::mbar_expect_tx(&full[stage], nch * kKeyTile * 128);
           uint8_t* dst = kbuf + stage * nch * kKeyTile * 128;
           for (int c = 0; c < nch; ++c)
-            dsa::tma_load_2d(dst + c * kKeyTile * 128, &map_k, c * 64, kt * kKeyTile, &full[stage]);
+            dsa::tma_load_2d_hint(dst + c * kKeyTile * 128, &map_k, c * 64, kt * kKeyTile, &full[stage], keep);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int st = tok_start[r];
               const bool valid = (s_key >= st) && (s_key <= t) && (t < p.T);
               if (!FUSED) {
-                if (valid) p.scores[static_cast<int64_t>(t) * p.ld + (s_key - st)] = score;
+                if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
                 const uint32_t key = dsa::f32_key(score);
                 const bool emit = valid && key >= row_tau[r];
@@ -348,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool stored = slot >= 0 && slot < p.cap;
                 if (stored) {
                   const int64_t o = static_cast<int64_t>(t) * p.cap + slot;
-                  p.cand_key[o] = key;
-                  p.cand_idx[o] = s_key - st;
+                  __stcs(p.cand_key + o, key);
+                  __stcs(p.cand_idx + o, s_key - st);
                 }
                 const uint32_t bin = key >> (32 - p.hist_bits);
                 // bin b of this row lives in 16-bit half (b & 1) of word (b >> 1)
