@@ -61,10 +61,9 @@ struct IndexerParams {
   int64_t ld;
   int s_max;
   // fused
-  uint32_t* cand_key;
-  int32_t* cand_idx;
-  int32_t* cand_cnt;
-  int cap;
+  uint2* cand;        // [T][4 segments][cap/4] (key, column) pairs
+  int32_t* cand_cnt;  // [T][4] candidates written per segment
+  int cap;            // per row, a multiple of 16
   int k;
   int hist_bits;  // log2(bins per row)
   uint32_t* status;
@@ -89,7 +88,7 @@ __host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int
   L.hist_off = o;
   if (fused) o += kHistWords * 4;
   L.row_off = o;
-  o += 4 * 32 * 4;  // tau, cnt, since, spare per row
+  o += (32 + 128 + 32 + 64) * 4;  // tau, per-segment counts, since, spare
   L.bar_off = o;
   o += (2 * 8 + 6) * 8;
   L.misc_off = o;
@@ -151,7 +150,8 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, 
       else if (acc + hi_c + lo_c >= k) bin = 2 * i;
       if (bin >= 0) {
         const uint32_t t = static_cast<uint32_t>(bin) << (32 - hist_bits);
-        if (t > *tau) *tau = t;
+        volatile uint32_t* vt = tau;
+        if (t > *vt) *vt = t;
         break;
       }
       acc += hi_c + lo_c;
@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* tok_len = tok_start + 32;
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist_off);
   uint32_t* row_tau = reinterpret_cast<uint32_t*>(smem + L.row_off);
-  int32_t* row_cnt = reinterpret_cast<int32_t*>(row_tau + 32);
-  int32_t* row_since = row_cnt + 32;
+  int32_t* seg_cnt = reinterpret_cast<int32_t*>(row_tau + 32);  // [32 rows][4 segments], one writer each
+  int32_t* row_since = seg_cnt + 128;  // candidate count at the row's last tau update (owner warp only)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* full = bars;
   uint64_t* empty = bars + 8;
@@ -291,8 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    const int seg = quarter;              // this warp writes segment `quarter` of its rows
+    const int cap_seg = FUSED ? p.cap / 4 : 0;
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
       const BlockRange br = block_range(p, blk);
+      int wcnt[tok_per_half];              // candidates this warp wrote per row (warp-uniform)
+#pragma unroll
+      for (int q = 0; q < tok_per_half; ++q) wcnt[q] = 0;
       named_bar(1, kEpiThreads);  // previous block's readers of w_s / tok_* are done
       for (int i = et; i < kNRows; i += kEpiThreads) {
         const int r = i / HI, h = i - r * HI;
@@ -311,8 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (FUSED) {
           row_tau[et] = 0u;
-          row_cnt[et] = 0;
           row_since[et] = 0;
+#pragma unroll
+          for (int sg = 0; sg < 4; ++sg) seg_cnt[et * 4 + sg] = 0;
         }
       }
       if (FUSED)
@@ -346,24 +352,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
                 const uint32_t key = dsa::f32_key(score);
-                const bool emit = valid && key >= row_tau[r];
-                const int slot = dsa::warp_append(&row_cnt[r], emit);
-                const bool stored = slot >= 0 && slot < p.cap;
+                const bool emit = valid && key >= *reinterpret_cast<volatile uint32_t*>(&row_tau[r]);
+                // append to this warp's own segment of row t: no atomics, the
+                // warp-uniform counter lives in a register
+                const uint32_t em = __ballot_sync(0xffffffffu, emit);
+                const int q = cl / HI;  // row index within this half (compile-time)
+                const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
+                const bool stored = emit && slot < cap_seg;
                 if (stored) {
-                  const int64_t o = static_cast<int64_t>(t) * p.cap + slot;
-                  __stcs(p.cand_key + o, key);
-                  __stcs(p.cand_idx + o, s_key - st);
+                  __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
+                  // histogram of stored keys; bin b lives in 16-bit half (b & 1) of word (b >> 1);
+                  // the result is unused, so this is a fire-and-forget reduction
+                  const uint32_t bin = key >> (32 - p.hist_bits);
+                  atomicAdd(&hist[r * hist_words_row + (bin >> 1)], 1u << (16 * (bin & 1)));
                 }
-                const uint32_t bin = key >> (32 - p.hist_bits);
-                // bin b of this row lives in 16-bit half (b & 1) of word (b >> 1)
-                const uint32_t act = __ballot_sync(0xffffffffu, stored);
-                if (stored) {
-                  const uint32_t peers = __match_any_sync(act, bin);
-                  if (lane == __ffs(peers) - 1)
-                    atomicAdd(&hist[r * hist_words_row + (bin >> 1)], static_cast<uint32_t>(__popc(peers))
-                                                                          << (16 * (bin & 1)));
-                }
-                if (lane == 0 && act) atomicAdd(&row_since[r], __popc(act));
+                wcnt[q] += __popc(em);
               }
             }
           }
@@ -374,20 +377,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
         if (FUSED) {
-          // raise tau of this half's rows once enough new candidates arrived
-          named_bar(2 + half, 128);
+          // Raise tau of the rows this warp owns once enough new candidates
+          // arrived.  No barrier: tau only has to stay a lower bound of the
+          // row's k-th largest key, and a histogram read while other warps
+          // still add to it can only undercount, which lowers the bound.
           const int r0 = half * tok_per_half;
-          bool need = false;
-          for (int r = r0; r < r0 + tok_per_half; ++r) need |= row_since[r] >= kTauUpdateEvery;
-          if (need) {
-            named_bar(2 + half, 128);  // every warp of the half has read row_since
-            for (int r = r0 + (ew & 3); r < r0 + tok_per_half; r += 4) {
-              if (row_since[r] >= kTauUpdateEvery && row_cnt[r] <= p.cap) {
-                update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
-                if (lane == 0) row_since[r] = 0;
+          if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < tok_per_half; ++q)
+              reinterpret_cast<volatile int32_t*>(seg_cnt)[(r0 + q) * 4 + seg] = wcnt[q];
+          }
+          for (int r = r0 + (ew & 3); r < r0 + tok_per_half; r += 4) {
+            int cnt = 0, worst = 0;
+            if (lane == 0) {
+              const volatile int32_t* sc = reinterpret_cast<volatile int32_t*>(seg_cnt) + r * 4;
+              for (int sg = 0; sg < 4; ++sg) {
+                const int c = sc[sg];
+                cnt += c;
+                worst = max(worst, c);
               }
             }
-            named_bar(2 + half, 128);
+            cnt = __shfl_sync(0xffffffffu, cnt, 0);
+            worst = __shfl_sync(0xffffffffu, worst, 0);
+            if (cnt - row_since[r] >= kTauUpdateEvery && worst <= cap_seg) {
+              update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
+              if (lane == 0) row_since[r] = cnt;  // row_since: candidate count at the last update
+              __syncwarp();
+            }
           }
         }
       }
@@ -401,9 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* row = p.scores + static_cast<int64_t>(t) * p.ld;
           for (int j = tok_len[r] + et; j < p.s_max; j += kEpiThreads) row[j] = -INFINITY;
         }
-      } else if (et < p.qb) {
-        const int t = br.t0 + et;
-        if (t < p.T) p.cand_cnt[t] = row_cnt[et];
+      } else if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < tok_per_half; ++q) {
+          const int t = br.t0 + half * tok_per_half + q;
+          if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
+        }
       }
     }
   }
@@ -415,11 +434,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Candidates of one row: four segments of (key, column) pairs.
+struct SegmentedPairSrc {
+  const uint2* base;  // row's first segment
+  int cap_seg;
+  int n0, n1, n2, n3;  // valid pairs per segment
+  int n;
+  __device__ __forceinline__ uint32_t key_at(int i) const {
+    const int e1 = n0, e2 = n0 + n1, e3 = n0 + n1 + n2;
+    const int sg = (i >= e1) + (i >= e2) + (i >= e3);
+    const int off = i - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
+    return __ldg(&base[sg * cap_seg + off].x);
+  }
+  template <class F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    const int e1 = n0, e2 = n0 + n1, e3 = n0 + n1 + n2;
+    for (int b = 0; b < n; b += blockDim.x) {
+      const int i = b + threadIdx.x;
+      const bool a = i < n;
+      uint2 v = make_uint2(0u, 0u);
+      if (a) {
+        const int sg = (i >= e1) + (i >= e2) + (i >= e3);
+        const int off = i - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
+        v = __ldcs(base + sg * cap_seg + off);
+      }
+      f(v.x, static_cast<int32_t>(v.y), a);
+    }
+  }
+};
+
 // Stage 2 of the fused path: exact top-k of each row's candidates.
 __global__ void __launch_bounds__(dsa::kTopkThreads)
-    fused_select_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint32_t* cand_key,
-                        const int32_t* cand_idx, const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx,
-                        int32_t* topk_length, uint32_t* status) {
+    fused_select_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint2* cand,
+                        const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
+                        uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem_raw2[];
   dsa::TopkShared& S = *reinterpret_cast<dsa::TopkShared*>(smem_raw2);
   const int t = blockIdx.x;
@@ -431,19 +479,31 @@ __global__ void __launch_bounds__(dsa::kTopkThreads)
     if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
     return;
   }
-  int n = cand_cnt[t];
-  if (n > cap) {
-    if (threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
-    n = cap;
+  const int cap_seg = cap / 4;
+  int c[4];
+  bool overflow = false;
+#pragma unroll
+  for (int sg = 0; sg < 4; ++sg) {
+    c[sg] = __ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg);
+    if (c[sg] > cap_seg) {
+      overflow = true;
+      c[sg] = cap_seg;
+    }
   }
+  if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
+  const int n = c[0] + c[1] + c[2] + c[3];
   if (n < k) {  // only reachable after an overflow: keep the output well-formed
     for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = -1;
     if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
     return;
   }
-  const dsa::PairSrc src{cand_key + static_cast<int64_t>(t) * cap, cand_idx + static_cast<int64_t>(t) * cap, n};
-  dsa::select_topk(S, src, k);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = st + S.sel[i];
+  const SegmentedPairSrc src{cand + static_cast<int64_t>(t) * cap, cap_seg, c[0], c[1], c[2], c[3], n};
+  if (len <= 32 * dsa::kBitmapWords && dsa::select_topk_sampled(S, src, n, k, len)) {
+    dsa::emit_bits_ascending(S, len, [&](int pos, int j) { out[pos] = st + j; });
+  } else {
+    dsa::select_topk(S, src, k);
+    for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = st + S.sel[i];
+  }
   if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
 }
 
@@ -494,10 +554,14 @@ int launch_indexer(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& 
   }
 }
 
+// Candidate capacity per row: four equal segments, one per key quarter of a
+// 128-key tile.  A row touches at most ceil(s_max/128)+1 tiles and a segment
+// receives at most 32 keys per tile, so short rows can never overflow; long
+// rows get max(4096, 2k) per segment (the threshold keeps them far below).
 int fused_cap(int s_max, int k) {
-  int cap = k * 8 > 16384 ? k * 8 : 16384;
-  if (s_max < cap) cap = s_max;
-  return (cap + 3) / 4 * 4;
+  const int64_t whole = 32ll * ((s_max + kKeyTile - 1) / kKeyTile + 1);
+  const int64_t bound = 2ll * k > 4096 ? 2ll * k : 4096;
+  return static_cast<int>(4 * (whole < bound ? whole : bound));
 }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -537,7 +601,7 @@ extern "C" int dsa_indexer_scores(const void* qi, const void* ki, const float* w
 extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
   if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1 || s_max > T) return 0;
   const size_t cap = static_cast<size_t>(fused_cap(s_max, k));
-  return align256(static_cast<size_t>(T) * 4) + 2 * align256(static_cast<size_t>(T) * cap * 4);
+  return align256(static_cast<size_t>(T) * 16) + align256(static_cast<size_t>(T) * cap * 8);
 }
 
 extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
@@ -571,9 +635,7 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   p.nblocks = (T + p.qb - 1) / p.qb;
   p.s_max = s_max;
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
-  p.cand_key = reinterpret_cast<uint32_t*>(ws + align256(static_cast<size_t>(T) * 4));
-  p.cand_idx = reinterpret_cast<int32_t*>(ws + align256(static_cast<size_t>(T) * 4) +
-                                          align256(static_cast<size_t>(T) * cap * 4));
+  p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(T) * 16));
   p.cap = cap;
   p.k = k;
   int bins = 2 * kHistWords / p.qb;
@@ -587,8 +649,8 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return dsa::launch_error("fused_select_kernel smem attribute");
-  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand_key, p.cand_idx,
-                                                              p.cand_cnt, cap, idx, topk_length, p.status);
+  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand, p.cand_cnt, cap,
+                                                              idx, topk_length, p.status);
   return dsa::launch_error("fused_select_kernel");
 }
 

@@ -33,11 +33,19 @@ __global__ void __launch_bounds__(dsa::kTopkThreads)
     if (threadIdx.x == 0 && topk_length) topk_length[row] = n;
     return;
   }
-  dsa::select_topk(S, dsa::DenseRowSrc<VEC4>{r, n}, k);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) {
-    const int j = S.sel[i];
-    out[i] = base + j;
-    if (vout) vout[i] = __ldg(r + j);
+  const dsa::DenseRowSrc<VEC4> src{r, n};
+  if (n <= 32 * dsa::kBitmapWords && dsa::select_topk_sampled(S, src, n, k, n)) {
+    dsa::emit_bits_ascending(S, n, [&](int pos, int j) {
+      out[pos] = base + j;
+      if (vout) vout[pos] = __ldg(r + j);
+    });
+  } else {
+    dsa::select_topk(S, src, k);
+    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+      const int j = S.sel[i];
+      out[i] = base + j;
+      if (vout) vout[i] = __ldg(r + j);
+    }
   }
   if (threadIdx.x == 0 && topk_length) topk_length[row] = k;
 }

@@ -25,9 +25,14 @@ namespace dsa {
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 2048;
 constexpr int kTopkCandCap = 8192;
+constexpr int kSampleBins = 4096;     // 12-bit histogram of the sampled keys
+constexpr int kSample = 2048;         // keys sampled to place the collection threshold
+constexpr int kBitmapWords = 2048;    // selected-column bitmap: rows of up to 65536 columns
 
 struct TopkShared {
-  uint32_t hist[kTopkBins];
+  uint32_t hist[kSampleBins];
+  uint32_t bits[kBitmapWords];
+  uint32_t tiebits[kBitmapWords];
   int32_t sel[DSA_MAX_TOPK];
   uint32_t ckey[kTopkCandCap];
   int32_t cidx[kTopkCandCap];
@@ -100,6 +105,7 @@ struct PairSrc {
   const uint32_t* key;  // may be shared or global memory
   const int32_t* idx;
   int n;
+  __device__ __forceinline__ uint32_t key_at(int i) const { return key[i]; }
   template <class F>
   __device__ __forceinline__ void for_each(F&& f) const {
     for (int base = 0; base < n; base += blockDim.x) {
@@ -116,6 +122,7 @@ template <bool VEC4>
 struct DenseRowSrc {
   const float* row;
   int n;
+  __device__ __forceinline__ uint32_t key_at(int i) const { return f32_key(__ldg(row + i)); }
   template <class F>
   __device__ __forceinline__ void for_each(F&& f) const {
     if constexpr (VEC4) {
@@ -301,6 +308,123 @@ __device__ void select_topk(TopkShared& S, const Src& src, int k) {
   while (P < k) P <<= 1;
   for (int i = k + threadIdx.x; i < P; i += blockDim.x) S.sel[i] = INT_MAX;
   bitonic_sort_smem(S.sel, P);
+}
+
+// ---------------------------------------------------------------------------
+// Faster exact path with a sampled threshold and a bitmap output.
+//
+// 1. A 12-bit histogram of kSample evenly spaced keys places a threshold
+//    tau_s at or below the key whose sample rank is about 1.25 * k * m / n
+//    (with m = n every key is sampled and tau_s is at or below the k-th key).
+// 2. One pass over the source copies the pairs with key >= tau_s into shared
+//    memory.  When at least k and at most kTopkCandCap were copied, tau_s is
+//    at or below the k-th key (at least k keys reach it), so every member of
+//    the top-k, ties included, is among the copies; otherwise the function
+//    returns false and the caller runs select_topk instead.
+// 3. The exact k-th key tau follows from radix digits over the copies; keys
+//    above tau and the `need` smallest-index keys equal to tau are marked in
+//    the column bitmap S.bits.
+// The block then reads the bitmap in column order (emit_bits_ascending).
+// Requires every column index < 32 * kBitmapWords.
+template <class Src>
+__device__ bool select_topk_sampled(TopkShared& S, const Src& src, int n, int k, int len) {
+  const int m = n < kSample ? n : kSample;
+  for (int i = threadIdx.x; i < kSampleBins; i += blockDim.x) S.hist[i] = 0;
+  if (threadIdx.x == 0) S.n_cand = 0;
+  __syncthreads();
+  for (int sidx = threadIdx.x; sidx < m; sidx += blockDim.x) {
+    const int pos = static_cast<int>((static_cast<int64_t>(sidx) * n) / m);
+    atomicAdd(&S.hist[src.key_at(pos) >> 20], 1u);
+  }
+  int r = m == n ? k : static_cast<int>((static_cast<int64_t>(k) * m * 5) / (static_cast<int64_t>(n) * 4)) + 16;
+  if (r > m) r = m;
+  find_threshold_bin(S, kSampleBins, r);
+  const uint32_t tau_s = static_cast<uint32_t>(S.bin) << 20;
+  src.for_each([&](uint32_t key, int32_t idx, bool a) {
+    const int pc = warp_append(&S.n_cand, a && key >= tau_s);
+    if (pc >= 0 && pc < kTopkCandCap) {
+      S.ckey[pc] = key;
+      S.cidx[pc] = idx;
+    }
+  });
+  __syncthreads();
+  const int nc = S.n_cand;
+  __syncthreads();  // every thread has read n_cand before a fallback resets it
+  if (nc < k || nc > kTopkCandCap) return false;
+  // exact k-th key among the copies
+  const PairSrc cand{S.ckey, S.cidx, nc};
+  digit_pass(S, cand, 0u, 0u, 21, kTopkBins, k);
+  const uint32_t b1 = static_cast<uint32_t>(S.bin);
+  int k_rem = k - S.above;
+  digit_pass(S, cand, 0xFFE00000u, b1 << 21, 10, kTopkBins, k_rem);
+  const uint32_t b2 = static_cast<uint32_t>(S.bin);
+  k_rem -= S.above;
+  digit_pass(S, cand, 0xFFFFFC00u, (b1 << 21) | (b2 << 10), 0, 1024, k_rem);
+  const uint32_t tau = (b1 << 21) | (b2 << 10) | static_cast<uint32_t>(S.bin);
+  const int need = k_rem - S.above;  // how many keys equal to tau are taken
+  const int words = (len + 31) >> 5;
+  for (int w = threadIdx.x; w < words; w += blockDim.x) {
+    S.bits[w] = 0u;
+    S.tiebits[w] = 0u;
+  }
+  __syncthreads();
+  int mine_eq = 0;
+  for (int i = threadIdx.x; i < nc; i += blockDim.x) {
+    const uint32_t key = S.ckey[i];
+    const int j = S.cidx[i];
+    if (key > tau) atomicOr(&S.bits[j >> 5], 1u << (j & 31));
+    else if (key == tau) {
+      atomicOr(&S.tiebits[j >> 5], 1u << (j & 31));
+      ++mine_eq;
+    }
+  }
+  int n_eq = 0;
+  block_inclusive_scan(mine_eq, S.scan, &n_eq);  // ends with __syncthreads
+  // the `need` tied columns with the smallest indices: walk the tie bitmap in order
+  const int per = (words + blockDim.x - 1) / blockDim.x;
+  const int w0 = threadIdx.x * per;
+  int cnt = 0;
+  for (int w = w0; w < w0 + per && w < words; ++w) cnt += __popc(S.tiebits[w]);
+  int total = 0;
+  const int excl = block_inclusive_scan(cnt, S.scan, &total) - cnt;
+  if (n_eq == need) {
+    for (int w = w0; w < w0 + per && w < words; ++w) S.bits[w] |= S.tiebits[w];
+  } else if (excl < need) {
+    int taken = excl;
+    for (int w = w0; w < w0 + per && w < words && taken < need; ++w) {
+      uint32_t v = S.tiebits[w], keep = 0u;
+      while (v && taken < need) {
+        const uint32_t low = v & (0u - v);
+        keep |= low;
+        v ^= low;
+        ++taken;
+      }
+      S.bits[w] |= keep;
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+// Calls emit(position, column) for every set bit of S.bits[0 .. words) in
+// increasing column order (positions 0, 1, ...).
+template <class F>
+__device__ __forceinline__ void emit_bits_ascending(TopkShared& S, int len, F&& emit) {
+  const int words = (len + 31) >> 5;
+  const int per = (words + blockDim.x - 1) / blockDim.x;
+  const int w0 = threadIdx.x * per;
+  int cnt = 0;
+  for (int w = w0; w < w0 + per && w < words; ++w) cnt += __popc(S.bits[w]);
+  int total = 0;
+  int pos = block_inclusive_scan(cnt, S.scan, &total) - cnt;
+  for (int w = w0; w < w0 + per && w < words; ++w) {
+    uint32_t v = S.bits[w];
+    while (v) {
+      const int b = __ffs(v) - 1;
+      v &= v - 1;
+      emit(pos++, (w << 5) + b);
+    }
+  }
 }
 
 }  // namespace dsa
