@@ -214,6 +214,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+// 32 lanes x 64 consecutive columns (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+  uint32_t(&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(

@@ -9,10 +9,10 @@
 // rows (N), contracting over d (K) in steps of 16.  The accumulator lives in
 // TMEM (2 x 256 fp32 columns, double-buffered) so that the epilogue of one key
 // tile overlaps the MMAs of the next.  Each epilogue thread owns one key (a
-// TMEM lane) and reduces over the heads of its tokens:
-//     score = fma(w[h], max(D, 0), score), h = 0 .. Hi-1 in order,
-// which is the same instruction sequence in both modes, so the fused mode
-// sees exactly the scores that the dense mode writes.
+// TMEM lane) and reduces over the heads of its tokens with fma(w[h],
+// max(D, 0), acc) in two interleaved chains over even and odd heads, added
+// at the end; both modes run this same instruction sequence, so the fused
+// mode sees exactly the scores that the dense mode writes.
 //
 // Warp roles (320 threads): warp 0 issues TMA loads (qi block once per block,
 // ki tiles through a multi-stage ring), warp 1 allocates TMEM and issues the
@@ -44,7 +44,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHistWords = 8192;   // 16384 16-bit bin counters shared by the block's rows
-constexpr int kTauUpdateEvery = 256;
+constexpr int kTauUpdateEvery = 512;
 
 struct IndexerParams {
   const float* w;
@@ -123,39 +123,58 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Raise tau of one row from its packed 16-bit histogram (one warp).
+// Raise tau of one row from its packed 16-bit histogram (one warp): find the
+// highest bin b at which the counts of bins >= b reach k and set tau to b's
+// lower edge (only ever raised).  Two warp scans: first over 32 contiguous
+// groups of words (lane 0 = highest), then over the words of the crossing
+// group spread across the lanes.
 __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, int hist_bits, int k, uint32_t* tau) {
   const int lane = threadIdx.x & 31;
-  const int per = words / 32;  // words per lane; lane 0 owns the highest bins
+  const int per = words / 32;  // words per group; group 0 holds the highest bins
   const int w_hi = words - lane * per;
   int s = 0;
-  for (int i = w_hi - 1; i >= w_hi - per; --i) {
-    const uint32_t v = hist_row[i];
+  // the sum does not depend on order: start each lane at a different offset so
+  // that the 32 lanes read 32 different banks (per is a multiple of 32)
+  for (int j = 0; j < per; ++j) {
+    const uint32_t v = hist_row[w_hi - 1 - ((j + lane) & (per - 1))];
     s += static_cast<int>((v & 0xFFFFu) + (v >> 16));
   }
   int incl = s;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  const int excl = incl - s;
-  if (excl < k && incl >= k) {
-    int acc = excl;
-    for (int i = w_hi - 1; i >= w_hi - per; --i) {
-      const uint32_t v = hist_row[i];
-      const int hi_c = static_cast<int>(v >> 16), lo_c = static_cast<int>(v & 0xFFFFu);
-      int bin = -1;
-      if (acc + hi_c >= k) bin = 2 * i + 1;
-      else if (acc + hi_c + lo_c >= k) bin = 2 * i;
-      if (bin >= 0) {
+  const uint32_t hit = __ballot_sync(0xffffffffu, incl >= k);
+  if (hit == 0u) return;               // fewer than k candidates so far
+  const int g = __ffs(hit) - 1;        // crossing group
+  int before = __shfl_sync(0xffffffffu, incl - s, g);
+  // words of group g, top down, spread over the lanes in rounds of 32
+  const int g_hi = words - g * per;
+  for (int r0 = 0; r0 < per; r0 += 32) {
+    const int wi = g_hi - 1 - r0 - lane;  // lane 0 takes the highest word of the round
+    const uint32_t v = (r0 + lane < per) ? hist_row[wi] : 0u;  // groups narrower than 32 words
+    const int hi_c = static_cast<int>(v >> 16), lo_c = static_cast<int>(v & 0xFFFFu);
+    const int c = hi_c + lo_c;
+    int inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    const uint32_t h2 = __ballot_sync(0xffffffffu, before + inc >= k);
+    if (h2 != 0u) {
+      const int l2 = __ffs(h2) - 1;
+      if (lane == l2) {
+        const int ex = before + inc - c;     // count of bins above this word
+        const int bin = (ex + hi_c >= k) ? 2 * wi + 1 : 2 * wi;
         const uint32_t t = static_cast<uint32_t>(bin) << (32 - hist_bits);
         volatile uint32_t* vt = tau;
         if (t > *vt) *vt = t;
-        break;
       }
-      acc += hi_c + lo_c;
+      break;
     }
+    before += __shfl_sync(0xffffffffu, inc, 31);
   }
   __syncwarp();
 }
@@ -331,19 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
         const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows;
         // columns [half*128, half*128+128) = tokens [half*tok_per_half, ...)
-        float score = 0.f;
+        // score = sum_h w[h] * max(D[h], 0), as two interleaved fma chains
+        // (even and odd heads) added at the end; fused and dense modes run
+        // this same sequence, so their scores are identical
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
-        for (int chunk = 0; chunk < 4; ++chunk) {
-          uint32_t v[32];
-          dsa::tmem_ld32(t_addr + half * 128 + chunk * 32, v);
+        for (int pair = 0; pair < 2; ++pair) {
+          uint32_t v[64];
+          dsa::tmem_ld64(t_addr + half * 128 + pair * 64, v);
           dsa::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int cl = chunk * 32 + i;            // column within this half (compile-time)
+          for (int i = 0; i < 64; ++i) {
+            const int cl = pair * 64 + i;             // column within this half (compile-time)
             const int h = cl % HI;                    // 128 % HI == 0, so the half offset drops out
-            if (h == 0) score = 0.f;
-            score = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), score);
+            if (h == 0) {
+              acc0 = 0.f;
+              acc1 = 0.f;
+            }
+            if (h & 1) acc1 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc1);
+            else acc0 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc0);
             if (h == HI - 1) {
+              const float score = acc0 + acc1;
               const int r = half * tok_per_half + cl / HI;
               const int t = br.t0 + r;
               const int st = tok_start[r];
@@ -376,11 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) dsa::mbar_arrive(&tempty[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
-        if (FUSED) {
-          // Raise tau of the rows this warp owns once enough new candidates
-          // arrived.  No barrier: tau only has to stay a lower bound of the
-          // row's k-th largest key, and a histogram read while other warps
-          // still add to it can only undercount, which lowers the bound.
+        if (FUSED && ((kt - br.kt0) & 3) == 3) {
+          // Every fourth tile, raise tau of the rows this warp owns once enough
+          // new candidates arrived.  No barrier: tau only has to stay a lower
+          // bound of the row's k-th largest key, and a histogram read while
+          // other warps still add to it can only undercount, which lowers it.
           const int r0 = half * tok_per_half;
           if (lane == 0) {
 #pragma unroll
@@ -449,16 +476,24 @@ struct SegmentedPairSrc {
   template <class F>
   __device__ __forceinline__ void for_each(F&& f) const {
     const int e1 = n0, e2 = n0 + n1, e3 = n0 + n1 + n2;
-    for (int b = 0; b < n; b += blockDim.x) {
-      const int i = b + threadIdx.x;
-      const bool a = i < n;
-      uint2 v = make_uint2(0u, 0u);
-      if (a) {
-        const int sg = (i >= e1) + (i >= e2) + (i >= e3);
-        const int off = i - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
-        v = __ldcs(base + sg * cap_seg + off);
+    constexpr int U = 4;  // loads in flight per thread before processing
+    for (int b = 0; b < n; b += blockDim.x * U) {
+      uint2 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = b + u * blockDim.x + threadIdx.x;
+        v[u] = make_uint2(0u, 0u);
+        if (i < n) {
+          const int sg = (i >= e1) + (i >= e2) + (i >= e3);
+          const int off = i - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
+          v[u] = __ldcs(base + sg * cap_seg + off);
+        }
       }
-      f(v.x, static_cast<int32_t>(v.y), a);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = b + u * blockDim.x + threadIdx.x;
+        f(v[u].x, static_cast<int32_t>(v[u].y), i < n);
+      }
     }
   }
 };

@@ -126,20 +126,40 @@ struct DenseRowSrc {
   template <class F>
   __device__ __forceinline__ void for_each(F&& f) const {
     if constexpr (VEC4) {
-      for (int base = 0; base < n; base += blockDim.x * 4) {
-        const int j = base + threadIdx.x * 4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < n) v = __ldg(reinterpret_cast<const float4*>(row + j));
-        f(f32_key(v.x), j, j < n);
-        f(f32_key(v.y), j + 1, j + 1 < n);
-        f(f32_key(v.z), j + 2, j + 2 < n);
-        f(f32_key(v.w), j + 3, j + 3 < n);
+      // four independent 16-byte loads per thread are in flight before any
+      // element is processed, so a step costs one memory latency, not four
+      constexpr int U = 4;
+      const int step = blockDim.x * 4;
+      for (int base = 0; base < n; base += step * U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = base + u * step + threadIdx.x * 4;
+          v[u] = j < n ? __ldcs(reinterpret_cast<const float4*>(row + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = base + u * step + threadIdx.x * 4;
+          f(f32_key(v[u].x), j, j < n);
+          f(f32_key(v[u].y), j + 1, j + 1 < n);
+          f(f32_key(v[u].z), j + 2, j + 2 < n);
+          f(f32_key(v[u].w), j + 3, j + 3 < n);
+        }
       }
     } else {
-      for (int base = 0; base < n; base += blockDim.x) {
-        const int j = base + threadIdx.x;
-        const bool a = j < n;
-        f(a ? f32_key(__ldg(row + j)) : 0u, j, a);
+      constexpr int U = 8;
+      for (int base = 0; base < n; base += blockDim.x * U) {
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = base + u * blockDim.x + threadIdx.x;
+          v[u] = j < n ? __ldcs(row + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = base + u * blockDim.x + threadIdx.x;
+          f(f32_key(v[u]), j, j < n);
+        }
       }
     }
   }
