@@ -140,10 +140,12 @@ size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max);
  *   ids, -1 suffix); topk_length int32 [T] or NULL (out);
  *   workspace: device buffer of ws_bytes >= dsa_indexer_topk_workspace_size,
  *   256-byte aligned, contents ignored on entry.
- * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE.  If a row's candidates exceed
- * the workspace's per-row capacity the row is recomputed through a dense
- * fallback inside the workspace; DSA_STATUS_CAND_OVERFLOW records that it
- * happened. */
+ * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE.  The result is exact for any
+ * data: a row's candidate space never overflows, because a segment of it
+ * that fills up (scores rising along the row, long runs of equal scores) is
+ * cut down in place to the keys that can still reach the row's top-k.
+ * DSA_STATUS_CAND_OVERFLOW is therefore never expected; if it were ever set,
+ * the flagged rows would hold -1 or an inexact selection. */
 int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
                      int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
                      int32_t* topk_length, void* workspace, size_t ws_bytes, cudaStream_t stream);

@@ -29,6 +29,16 @@
 // keys seen, that edge never exceeds the final k-th largest key, so every
 // member of the final top-k (ties included) is emitted.  Stage 2 then
 // selects exactly from the candidates (topk.cu).
+//
+// Rows never overflow their candidate space.  A row's candidates sit in four
+// segments, one per key quarter of a tile, each written by one warp in
+// ascending key order.  When a segment could overflow on the next tile, its
+// warp cuts it down to its own top-k (key descending, column ascending) and
+// from then on appends only keys above the k-th key it kept: any key that k
+// others of the same row beat cannot be in the row's top-k, and a later key
+// that ties the k-th loses the tie to the k earlier columns.  Scores that keep
+// rising along the row (every key beats the running threshold) are the case
+// this exists for.
 #include <climits>
 #include <mutex>
 
@@ -64,13 +74,14 @@ struct IndexerParams {
   uint2* cand;        // [T][4 segments][cap/4] (key, column) pairs
   int32_t* cand_cnt;  // [T][4] candidates written per segment
   int cap;            // per row, a multiple of 16
+  int compact;        // segments may fill up (cap below the longest row's keys per segment)
   int k;
   int hist_bits;  // log2(bins per row)
   uint32_t* status;
 };
 
 struct SmemLayout {
-  uint32_t q_off, k_off, w_off, tok_off, hist_off, row_off, bar_off, misc_off, total;
+  uint32_t q_off, k_off, w_off, tok_off, hist_off, row_off, cmp_off, bar_off, misc_off, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int fused) {
@@ -88,7 +99,9 @@ __host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int
   L.hist_off = o;
   if (fused) o += kHistWords * 4;
   L.row_off = o;
-  o += (32 + 128 + 32 + 64) * 4;  // tau, per-segment counts, since, spare
+  o += (32 + 128 + 32 + 128 + 128) * 4;  // tau, segment counts, since, segment floors, segment drops
+  L.cmp_off = o;
+  if (fused) o += kEpiWarps * 256 * 4;  // one 256-bin histogram per epilogue warp (segment compaction)
   L.bar_off = o;
   o += (2 * 8 + 6) * 8;
   L.misc_off = o;
@@ -121,6 +134,79 @@ __device__ __forceinline__ BlockRange block_range(const IndexerParams& p, int bl
 
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Cut one candidate segment (n > k pairs in ascending column order, in
+// global memory) down to its top-k by (key descending, column ascending),
+// keeping the column order, and return the smallest key a later (larger)
+// column must reach to enter it: one above the k-th key kept.  One warp;
+// hist is a 256-word scratch of this warp.  The k-th key comes from a
+// four-pass radix select on 8-bit digits, the ties at it from the front.
+__device__ __noinline__ uint32_t compact_segment(uint2* seg, int n, int k, uint32_t* hist) {
+  const int lane = threadIdx.x & 31;
+  uint32_t prefix = 0u, mask = 0u;
+  int need = k;  // rank of the k-th key among the keys matching prefix
+  __syncwarp();
+  for (int shift = 24; shift >= 0; shift -= 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
+    __syncwarp();
+    for (int b = 0; b < n; b += 32) {
+      const int i = b + lane;
+      const uint32_t key = i < n ? __ldcg(&seg[i].x) : 0u;
+      const bool in = i < n && (key & mask) == prefix;
+      const uint32_t digit = in ? (key >> shift) & 255u : 256u + lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], static_cast<uint32_t>(__popc(peers)));
+    }
+    __syncwarp();
+    // lane l sums bins 255-8l down to 248-8l; the first lane whose running
+    // total from the top reaches need holds the digit
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += static_cast<int>(hist[255 - lane * 8 - i]);
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int g = __ffs(__ballot_sync(0xffffffffu, incl >= need)) - 1;
+    int digit = 0, above = 0;
+    if (lane == g) {
+      int run = incl - s;
+      for (int i = 0; i < 8; ++i) {
+        const int c = static_cast<int>(hist[255 - lane * 8 - i]);
+        if (run + c >= need) {
+          digit = 255 - lane * 8 - i;
+          above = run;
+          break;
+        }
+        run += c;
+      }
+    }
+    digit = __shfl_sync(0xffffffffu, digit, g);
+    need -= __shfl_sync(0xffffffffu, above, g);
+    prefix |= static_cast<uint32_t>(digit) << shift;
+    mask |= 255u << shift;
+    __syncwarp();
+  }
+  // keep keys above the k-th, and the first `need` keys equal to it
+  int out = 0, eq_seen = 0;
+  for (int b = 0; b < n; b += 32) {
+    const int i = b + lane;
+    const uint2 e = i < n ? __ldcg(&seg[i]) : make_uint2(0u, 0u);
+    const bool eq = i < n && e.x == prefix;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+    const bool keep = (i < n && e.x > prefix) || (eq && eq_seen + __popc(eqm & dsa::lanemask_lt()) < need);
+    const uint32_t km = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();  // every lane has read this round before any lane writes
+    if (keep) seg[out + __popc(km & dsa::lanemask_lt())] = e;
+    out += __popc(km);
+    eq_seen += __popc(eqm);
+  }
+  __syncwarp();
+  return prefix == 0xFFFFFFFFu ? prefix : prefix + 1u;
 }
 
 // Raise tau of one row from its packed 16-bit histogram (one warp): find the
@@ -196,6 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* row_tau = reinterpret_cast<uint32_t*>(smem + L.row_off);
   int32_t* seg_cnt = reinterpret_cast<int32_t*>(row_tau + 32);  // [32 rows][4 segments], one writer each
   int32_t* row_since = seg_cnt + 128;  // candidate count at the row's last tau update (owner warp only)
+  uint32_t* seg_floor = reinterpret_cast<uint32_t*>(row_since + 32);  // [32][4] entry floor after a compaction
+  int32_t* seg_drop = reinterpret_cast<int32_t*>(seg_floor + 128);    // [32][4] candidates dropped by compactions
+  uint32_t* cmp_hist = reinterpret_cast<uint32_t*>(smem + L.cmp_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* full = bars;
   uint64_t* empty = bars + 8;
@@ -314,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cap_seg = FUSED ? p.cap / 4 : 0;
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
       const BlockRange br = block_range(p, blk);
+      uint32_t cmask = 0u;                 // bit q: this warp's segment of row q was compacted
       int wcnt[tok_per_half];              // candidates this warp wrote per row (warp-uniform)
 #pragma unroll
       for (int q = 0; q < tok_per_half; ++q) wcnt[q] = 0;
@@ -337,7 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           row_tau[et] = 0u;
           row_since[et] = 0;
 #pragma unroll
-          for (int sg = 0; sg < 4; ++sg) seg_cnt[et * 4 + sg] = 0;
+          for (int sg = 0; sg < 4; ++sg) {
+            seg_cnt[et * 4 + sg] = 0;
+            seg_floor[et * 4 + sg] = 0u;
+            seg_drop[et * 4 + sg] = 0;
+          }
         }
       }
       if (FUSED)
@@ -379,14 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
                 const uint32_t key = dsa::f32_key(score);
-                const bool emit = valid && key >= *reinterpret_cast<volatile uint32_t*>(&row_tau[r]);
+                const uint32_t fl = ((cmask >> (cl / HI)) & 1u) ? reinterpret_cast<volatile uint32_t*>(seg_floor)[r * 4 + seg] : 0u;
+                const bool emit = valid && key >= *reinterpret_cast<volatile uint32_t*>(&row_tau[r]) && key >= fl;
                 // append to this warp's own segment of row t: no atomics, the
-                // warp-uniform counter lives in a register
+                // warp-uniform counter lives in a register; the segment has
+                // room for a whole tile (compaction below)
                 const uint32_t em = __ballot_sync(0xffffffffu, emit);
                 const int q = cl / HI;  // row index within this half (compile-time)
                 const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
-                const bool stored = emit && slot < cap_seg;
-                if (stored) {
+                if (emit) {
                   __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
                   // histogram of stored keys; bin b lives in 16-bit half (b & 1) of word (b >> 1);
                   // the result is unused, so this is a fire-and-forget reduction
@@ -403,6 +498,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) dsa::mbar_arrive(&tempty[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
+        if (FUSED && p.compact) {
+          // a segment that might not hold the next tile's 32 keys is cut to its top-k
+#pragma unroll
+          for (int q = 0; q < tok_per_half; ++q) {
+            if (wcnt[q] > cap_seg - 32) {
+              const int r = half * tok_per_half + q;
+              const int64_t t = br.t0 + r;
+              const uint32_t fl = compact_segment(p.cand + (t * 4 + seg) * cap_seg, wcnt[q], p.k, cmp_hist + ew * 256);
+              if (lane == 0) {
+                seg_floor[r * 4 + seg] = fl;
+                seg_drop[r * 4 + seg] += wcnt[q] - p.k;
+              }
+              wcnt[q] = p.k;
+              cmask |= 1u << q;
+              __syncwarp();
+            }
+          }
+        }
         if (FUSED && ((kt - br.kt0) & 3) == 3) {
           // Every fourth tile, raise tau of the rows this warp owns once enough
           // new candidates arrived.  No barrier: tau only has to stay a lower
@@ -412,21 +525,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
 #pragma unroll
             for (int q = 0; q < tok_per_half; ++q)
-              reinterpret_cast<volatile int32_t*>(seg_cnt)[(r0 + q) * 4 + seg] = wcnt[q];
+              reinterpret_cast<volatile int32_t*>(seg_cnt)[(r0 + q) * 4 + seg] = wcnt[q] + seg_drop[(r0 + q) * 4 + seg];
           }
           for (int r = r0 + (ew & 3); r < r0 + tok_per_half; r += 4) {
-            int cnt = 0, worst = 0;
+            int cnt = 0;  // candidates emitted so far (stored or since dropped)
             if (lane == 0) {
               const volatile int32_t* sc = reinterpret_cast<volatile int32_t*>(seg_cnt) + r * 4;
-              for (int sg = 0; sg < 4; ++sg) {
-                const int c = sc[sg];
-                cnt += c;
-                worst = max(worst, c);
-              }
+              for (int sg = 0; sg < 4; ++sg) cnt += sc[sg];
             }
             cnt = __shfl_sync(0xffffffffu, cnt, 0);
-            worst = __shfl_sync(0xffffffffu, worst, 0);
-            if (cnt - row_since[r] >= kTauUpdateEvery && worst <= cap_seg) {
+            if (cnt - row_since[r] >= kTauUpdateEvery) {
               update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
               if (lane == 0) row_since[r] = cnt;  // row_since: candidate count at the last update
               __syncwarp();
@@ -591,13 +699,17 @@ int launch_indexer(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& 
 
 // Candidate capacity per row: four equal segments, one per key quarter of a
 // 128-key tile.  A row touches at most ceil(s_max/128)+1 tiles and a segment
-// receives at most 32 keys per tile, so short rows can never overflow; long
-// rows get max(4096, 2k) per segment (the threshold keeps them far below).
+// receives at most 32 keys per tile, so short rows hold every key they could
+// emit; long rows get max(4096, 2k) per segment, which the running threshold
+// normally keeps far from full, and a segment that does fill is compacted to
+// its top-k in place (fused_compact says when that can happen).
+int64_t fused_whole(int s_max) { return 32ll * ((s_max + kKeyTile - 1) / kKeyTile + 1); }
+int64_t fused_bound(int k) { return 2ll * k > 4096 ? 2ll * k : 4096; }
 int fused_cap(int s_max, int k) {
-  const int64_t whole = 32ll * ((s_max + kKeyTile - 1) / kKeyTile + 1);
-  const int64_t bound = 2ll * k > 4096 ? 2ll * k : 4096;
+  const int64_t whole = fused_whole(s_max), bound = fused_bound(k);
   return static_cast<int>(4 * (whole < bound ? whole : bound));
 }
+int fused_compact(int s_max, int k) { return fused_whole(s_max) > fused_bound(k) ? 1 : 0; }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -672,6 +784,7 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
   p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(T) * 16));
   p.cap = cap;
+  p.compact = fused_compact(s_max, k);
   p.k = k;
   int bins = 2 * kHistWords / p.qb;
   int bits = 0;

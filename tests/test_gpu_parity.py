@@ -196,6 +196,70 @@ def test_fused_indexer_topk_equals_unfused(lengths, Hi, d, k, kind):
         assert np.array_equal(idx.cpu().numpy(), oi)
 
 
+def _ordered_scores_inputs(T, pattern, Hi=8, d=64):
+    """Integer inputs whose exact scores follow a pattern along the key axis:
+    score[j] = 256 * a[j] + b[j] from one head (q = (256, 1, 0, ...) against
+    k[j] = (a[j], b[j], 0, ...)), exact in bf16 and in fp32 accumulation."""
+    j = np.arange(T)
+    if pattern == "rising":
+        a, b = j >> 8, j & 255
+    elif pattern == "falling":
+        a, b = 255 - (j >> 8), 255 - (j & 255)
+    elif pattern == "equal":
+        a, b = np.zeros(T, np.int64), np.zeros(T, np.int64)
+    elif pattern == "plateaus":  # rising steps of 1024 equal keys
+        a, b = j >> 10, np.zeros(T, np.int64)
+    else:
+        raise ValueError(pattern)
+    qi = np.zeros((T, Hi, d), np.float32)
+    qi[:, 0, 0], qi[:, 0, 1] = 256.0, 1.0
+    ki = np.zeros((T, d), np.float32)
+    ki[:, 0], ki[:, 1] = a, b
+    w = np.zeros((T, Hi), np.float32)
+    w[:, 0] = 1.0
+    return W.f32_to_bf16_bits(qi), W.f32_to_bf16_bits(ki), w, (256 * a + b).astype(np.float64)
+
+
+@pytest.mark.parametrize("pattern", ["rising", "falling", "equal", "plateaus"])
+@pytest.mark.parametrize("k", [2048, 64])
+def test_fused_topk_exact_when_every_key_beats_the_running_threshold(pattern, k):
+    """Rows of 32768 keys whose scores rise along the row emit every key as a
+    candidate (each beats the k-th largest seen so far), far more than a row's
+    candidate segments hold; equal scores and plateaus do the same through
+    ties.  The fused call must still give the exact top-k, with no status flag."""
+    T = 32768
+    qi, ki, w, sc = _ordered_scores_inputs(T, pattern)
+    cu = np.array([0, T], np.int32)
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    ops.device_status(clear=True)
+    idx, tl = ops.indexer_topk(*a, k, T)
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) == 0
+    got = idx.cpu().numpy()
+    # the same result as the unfused path on every row
+    dsc = ops.indexer_scores(*a, T)
+    start, length = oracle.thd_metadata(cu, T)
+    ui, ut, _ = ops.topk(dsc, dev(length), k, row_start=dev(start))
+    assert np.array_equal(got, ui.cpu().numpy())
+    assert np.array_equal(tl.cpu().numpy(), ut.cpu().numpy())
+    del dsc
+    # closed forms: rising -> the last k keys; falling or equal -> the first k
+    t = np.arange(T)
+    long_rows = t + 1 > k
+    if pattern == "rising":
+        want = (t[long_rows, None] - k + 1) + np.arange(k)[None, :]
+        assert np.array_equal(got[long_rows], want)
+    elif pattern in ("falling", "equal"):
+        assert np.array_equal(got[long_rows], np.broadcast_to(np.arange(k), (long_rows.sum(), k)))
+    # and the oracle's top-k of the exact scores on sampled rows
+    rows = np.array([k - 1, k, 16383, 16384, 20000, 30001, T - 1])
+    ref = np.full((rows.size, T), -np.inf)
+    for i, r in enumerate(rows):
+        ref[i, :r + 1] = sc[:r + 1]
+    oi, _ = oracle.topk(ref, (rows + 1).astype(np.int32), k)
+    assert np.array_equal(got[rows], oi)
+
+
 # ------------------------------------------------------------------ attention
 def _attn_case(rng, T, H, Tkv, K, Dqk=576, Dv=512, sigma=0.1, qmul=1.0, sink_scale=1.0, sink=True, sep_v=False):
     q = rand_bf16_bits(rng, (T, H, Dqk), sigma * qmul)
