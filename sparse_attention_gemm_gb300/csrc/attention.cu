@@ -368,8 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;               // TMEM lane quarter
     const int hh = sw >> 2;                     // head half: heads hh*32 .. hh*32+31
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int key_in_tile = quarter * 16 + (lane & 15);  // meaningful for lanes 0..15
-    const bool key_lane = lane < 16;
+    // S^T is read with 16-lane loads (shape 16x256b) so that all 32 threads
+    // of a warp hold scores: thread `lane` gets keys kA = lane/4 and kB =
+    // lane/4 + 8 of its quarter's 16 and heads hbase + 8j + e (j = 0..3,
+    // e = 0..1) of its head half; register 4j+e is (kA, head), 4j+2+e is (kB, head).
+    const int kA = quarter * 16 + (lane >> 2), kB = kA + 8;
+    const int hbase = hh * 32 + 2 * (lane & 3);
     const bool want_max = p.max_logits != nullptr;
     uint32_t tile_ctr = 0;
     bool ok = true;
@@ -390,71 +394,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      float l_part[32];
+      float l_part[8];  // [j*2 + e]: running sum of p for head hbase + 8j + e over this thread's keys
       float m_max = -INFINITY;  // exact maximum of head st (threads st < 64), for max_logits
 #pragma unroll
-      for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
-      const float4* mref4 = reinterpret_cast<const float4*>(mref + hh * 32);
-      if (st < 64) mref[st] = -INFINITY;  // ordered before its readers by the first tile's barriers
+      for (int h = 0; h < 8; ++h) l_part[h] = 0.f;
       const int32_t* irow = p.idx + static_cast<int64_t>(t) * p.K;
-      int next_id = -1;
-      {
-        const int j = key_in_tile;
-        next_id = (key_lane && j < len) ? __ldcs(irow + j) : -1;
-      }
+      int nA = kA < len ? __ldcs(irow + kA) : -1;
+      int nB = kB < len ? __ldcs(irow + kB) : -1;
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
         const int b = tile_ctr & 1;
         const uint32_t ph = (tile_ctr >> 1) & 1;
-        const int j = i * kKeys + key_in_tile;
-        const int id = next_id;
+        const int jA = i * kKeys + kA, jB = i * kKeys + kB;
+        const bool vA = jA < len && nA >= 0 && nA < p.Tkv;
+        const bool vB = jB < len && nB >= 0 && nB < p.Tkv;
         if (i + 1 < nt) {
-          const int jn = j + kKeys;
-          next_id = (key_lane && jn < len) ? __ldcs(irow + jn) : -1;
+          nA = jA + kKeys < len ? __ldcs(irow + jA + kKeys) : -1;
+          nB = jB + kKeys < len ? __ldcs(irow + jB + kKeys) : -1;
         }
-        const bool valid = key_lane && j < len && id >= 0 && id < p.Tkv;
         if (!dsa::mbar_wait(&s_full[b], ph, abort_flag, p.status)) { ok = false; break; }
         dsa::tc_fence_after();
-        float x[32];
+        float x[16];
         {
-          uint32_t v[32];
-          dsa::tmem_ld32(tmem_base + lane_off + kSCol + b * 64 + hh * 32, v);
+          uint32_t v[16];
+          dsa::tmem_ld16x256b_x4(tmem_base + lane_off + kSCol + b * 64 + hh * 32, v);
           dsa::tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(v[h]);
+          for (int r = 0; r < 16; ++r) x[r] = __uint_as_float(v[r]);
         }
         dsa::tc_fence_before();
         __syncwarp();
         if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
+        // y = s*log2(e) - m for the current reference m of each head; a tile
+        // whose scores pass m + theta anywhere moves the reference first
+        float y[16];
         bool ex = false;
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 m4 = mref4[h4];
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int j = 0; j < 4; ++j) {
+          const float2 m2 = *reinterpret_cast<const float2*>(mref + hbase + 8 * j);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int h = h4 * 4 + e;
-            x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-            ex |= x[h] > mm[e] + kTheta;
+          for (int e = 0; e < 2; ++e) {
+            const float m = e ? m2.y : m2.x;
+            y[4 * j + e] = vA ? fmaf(x[4 * j + e], p.scale_log2, -m) : -INFINITY;
+            y[4 * j + 2 + e] = vB ? fmaf(x[4 * j + 2 + e], p.scale_log2, -m) : -INFINITY;
+            ex |= (y[4 * j + e] > kTheta) || (y[4 * j + 2 + e] > kTheta);
           }
         }
         const bool ex_warp = __any_sync(0xffffffffu, ex);
         if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = ex_warp ? 1 : 0;
         named_bar(1, kSoftThreads);
-        bool reduce = want_max;
+        // the first tile of a unit always sets the reference (mref still holds
+        // the previous unit's, so its y above are discarded)
+        bool reduce = want_max || i == 0;
         bool need_rescale = false;
 #pragma unroll
         for (int w = 0; w < 8; ++w) reduce |= exflag[(tile_ctr & 1) * 8 + w] != 0;
         if (reduce) {
+          // tile maximum per head: this thread's two keys, then the 8 threads
+          // that share its heads (lane bits 2..4)
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const int r = __reduce_max_sync(0xffffffffu, ord_f32(x[h]));
-            if (lane == h) wmax[quarter * 64 + hh * 32 + h] = r;
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float mx = fmaxf(vA ? x[4 * j + e] * p.scale_log2 : -INFINITY,
+                               vB ? x[4 * j + 2 + e] * p.scale_log2 : -INFINITY);
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              if (lane < 4) wmax[quarter * 64 + hbase + 8 * j + e] = ord_f32(mx);
+            }
           }
           named_bar(1, kSoftThreads);
           if (st < 64) {
             int r = max(max(wmax[st], wmax[64 + st]), max(wmax[128 + st], wmax[192 + st]));
             const float tmax = unord_f32(r);
-            const float mo = mref[st];
+            const float mo = i == 0 ? -INFINITY : mref[st];
             const float mn = (tmax > mo + kTheta) ? tmax : mo;
             alpha[st] = (mn == mo) ? 1.f : ex2(mo - mn);
             mref[st] = mn;
@@ -463,35 +476,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar(1, kSoftThreads);
           bool rescale = false;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const float a = alpha[hh * 32 + h];
-            rescale |= a != 1.f;
-            l_part[h] *= a;
+          for (int j = 0; j < 4; ++j) {
+            const float2 a2 = *reinterpret_cast<const float2*>(alpha + hbase + 8 * j);
+            const float2 m2 = *reinterpret_cast<const float2*>(mref + hbase + 8 * j);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float a = e ? a2.y : a2.x;
+              const float m = e ? m2.y : m2.x;
+              rescale |= a != 1.f;
+              l_part[2 * j + e] *= a;
+              y[4 * j + e] = vA ? fmaf(x[4 * j + e], p.scale_log2, -m) : -INFINITY;
+              y[4 * j + 2 + e] = vB ? fmaf(x[4 * j + 2 + e], p.scale_log2, -m) : -INFINITY;
+            }
           }
           need_rescale = rescale && i > 0;
         }
-        // P^T row of this key: heads hh*32 .. hh*32+31 = 4 chunks of 16 bytes
-        uint8_t* prow = (p.p_alias >= 0 ? kvbuf + b * L.buf_bytes + p.p_alias * kChunkBytes
-                                        : smem + L.p + b * kChunkBytes) +
-                        key_in_tile * 128;
+        // P^T rows kA and kB: heads hbase + 8j + {0, 1} are 4 bytes at 16-byte
+        // unit hh*4 + j of the row (128-byte swizzle: unit ^ (key & 7))
+        uint8_t* pbase = p.p_alias >= 0 ? kvbuf + b * L.buf_bytes + p.p_alias * kChunkBytes : smem + L.p + b * kChunkBytes;
+        uint8_t* prowA = pbase + kA * 128 + 4 * (lane & 3);
+        uint8_t* prowB = pbase + kB * 128 + 4 * (lane & 3);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t w4[4];
-          const float4 ma = mref4[c4 * 2], mb4 = mref4[c4 * 2 + 1];
-          const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int h0 = c4 * 8 + e * 2;
-            const float p0 = valid ? ex2(x[h0] - mm[e * 2]) : 0.f;
-            const float p1 = valid ? ex2(x[h0 + 1] - mm[e * 2 + 1]) : 0.f;
-            l_part[h0] += p0;
-            l_part[h0 + 1] += p1;
-            w4[e] = pack_bf16x2(p0, p1);
-          }
-          if (key_lane) {
-            const int c16 = hh * 4 + c4;
-            *reinterpret_cast<uint4*>(prow + ((c16 ^ (key_in_tile & 7)) * 16)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
+        for (int j = 0; j < 4; ++j) {
+          const float a0 = ex2(y[4 * j]), a1 = ex2(y[4 * j + 1]);
+          const float b0 = ex2(y[4 * j + 2]), b1 = ex2(y[4 * j + 3]);
+          l_part[2 * j] += a0 + b0;
+          l_part[2 * j + 1] += a1 + b1;
+          const int u = hh * 4 + j;
+          *reinterpret_cast<uint32_t*>(prowA + ((u ^ (kA & 7)) * 16)) = pack_bf16x2(a0, a1);
+          *reinterpret_cast<uint32_t*>(prowB + ((u ^ (kB & 7)) * 16)) = pack_bf16x2(b0, b1);
         }
         // O^T columns of heads whose reference moved get alpha[h]; this runs after
         // P is written so that the scores are no longer live.
@@ -521,15 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- epilogue
       if (!dsa::mbar_wait(o_done, (tile_ctr - 1) & 1, abort_flag, p.status)) { ok = false; break; }
       dsa::tc_fence_after();
-      // per-head sums over this warp's 16 key lanes (lanes 16..31 hold zeros)
+      // per-head sums over the quarter's 16 keys: the 8 threads sharing a head
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        float v = l_part[h];
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (lane == 0) red[quarter * 64 + hh * 32 + h] = v;
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = l_part[2 * j + e];
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 8);
+          v += __shfl_xor_sync(0xffffffffu, v, 16);
+          if (lane < 4) red[quarter * 64 + hbase + 8 * j + e] = v;
+        }
       }
       named_bar(1, kSoftThreads);
       if (st < 64) {
