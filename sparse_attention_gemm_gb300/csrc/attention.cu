@@ -23,8 +23,9 @@
 //         dims per instruction group, N=64, K=16 keys per instruction)
 // S^T (two buffers) and O^T live in TMEM.  An M=64 accumulator occupies
 // lanes 0..15 of each 32-lane quarter (row r in lane 32*(r/16) + r%16).
-// MMA issue order runs one tile ahead: MMA1 of tile i+1 is issued before
-// MMA2 of tile i, so the tensor core has work while softmax(i) runs.
+// MMA1 and MMA2 are issued by two different warps, each as soon as its
+// inputs are ready, so MMA1 of tile i+1 (two S buffers) can run while
+// softmax(i) does and MMA2(i) never queues behind a whole MMA1.
 //
 // Softmax: 8 warps, two per TMEM lane quarter; lanes 0..15 of a warp own one
 // key each and 32 heads (the warp's head half).  Per head a reference maximum
@@ -36,9 +37,9 @@
 // denominator and writes out (bf16), lse (sink included) and optionally
 // lse_kv and max_logits.
 //
-// Warps: 0..3 gather, 4 = TMEM allocation, MMA issue (lane 0) and query
-// loads (lane 1, TMA), 5..12 softmax and epilogue.  Persistent CTAs take
-// units from the longest rows down.
+// Warps: 0..3 gather, 4 = TMEM allocation, MMA1 issue and query loads (TMA),
+// 5..12 softmax and epilogue, 13 = MMA2 issue.  Persistent CTAs take units
+// from the longest rows down.
 #include <climits>
 
 #include "common.cuh"
@@ -49,11 +50,12 @@ constexpr int kKeys = 64;                       // keys per tile
 constexpr int kHG = 64;                         // heads per group
 constexpr int kGatherWarps = 4;
 constexpr int kGatherThreads = kGatherWarps * 32;
-constexpr int kMmaWarp = 4;
+constexpr int kMmaWarp = 4;     // MMA1 and query loads
 constexpr int kSoftWarp0 = 5;
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kThreads = (kSoftWarp0 + kSoftWarps) * 32;  // 416
+constexpr int kMma2Warp = kSoftWarp0 + kSoftWarps;  // 13: MMA2
+constexpr int kThreads = (kMma2Warp + 1) * 32;       // 448
 constexpr uint32_t kChunkBytes = kKeys * 128;   // 64 keys x 64 bf16
 constexpr uint32_t kQChunkBytes = kHG * 128;    // 64 heads x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
@@ -123,6 +125,14 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// One lane of the (converged) warp: true there, false elsewhere.
+__device__ __forceinline__ bool elect_sync() {
+  uint32_t is = 0;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}" : "=r"(is));
+  return is != 0;
 }
 
 __device__ __forceinline__ void named_bar(int id, int n) {
@@ -257,108 +267,117 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_arrive(&kv_full[b]);
       }
     }
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issue
+  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+    // ------------------------------------------------------------ MMA issue
+    // Two issuing warps, one per product, so that neither waits behind the
+    // other's instructions: warp kMmaWarp issues MMA1 (and loads the query),
+    // warp kMma2Warp issues MMA2 as soon as a tile's P is written, which
+    // frees the tile buffer for the next gather sooner.  Each warp runs its
+    // loop converged, so that control flow and the operand descriptors stay
+    // warp-uniform, and one elected lane issues each instruction.  The
+    // descriptors are built once and advanced by constant offsets (the
+    // start-address field counts 16-byte units): with 64-key tiles the tensor
+    // core finishes an instruction in a few dozen cycles, so issue cost counts.
+    const bool leader = elect_sync();
+    const uint32_t kv_addr = dsa::smem_u32(kvbuf);
+    const uint32_t buf16 = L.buf_bytes >> 4;
+    // next unit of this CTA that has at least one tile (n_units if none)
+    auto next_unit = [&](int u) {
+      for (; u < n_units; u += gridDim.x)
+        if (unit_len(p, (n_units - 1 - u) / p.G) > 0) return u;
+      return n_units;
+    };
+    auto unit_tiles = [&](int u) { return (unit_len(p, (n_units - 1 - u) / p.G) + kKeys - 1) / kKeys; };
+    if (warp == kMmaWarp) {
       constexpr uint32_t idesc1 = dsa::idesc_bf16(kKeys, kHG, 0, 0);
-      constexpr uint32_t idesc2 = dsa::idesc_bf16(128, kHG, 1, 1);
-      const uint32_t q_addr = dsa::smem_u32(qbuf), kv_addr = dsa::smem_u32(kvbuf);
-      const uint32_t p_sep = dsa::smem_u32(smem) + L.p;
-      uint32_t tile_ctr = 0, unit_ctr = 0;
-      bool ok = true;
-      // MMA1(tc): S^T[tc&1] = KV(tile tc) . Q^T; needs the tile and a free S buffer.
-      auto mma1 = [&](uint32_t tc) {
-        const int b = tc & 1;
-        dsa::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05 reads
-        dsa::tc_fence_after();
-        const uint32_t a0 = kv_addr + b * L.buf_bytes;
-        for (int c = 0; c < p.n_qk; ++c) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = dsa::smem_desc(a0 + c * kChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
-            const uint64_t bd = dsa::smem_desc(q_addr + c * kQChunkBytes + kk * 32, 16, 1024, dsa::kSwizzle128B);
-            dsa::umma_bf16(tmem_base + kSCol + b * 64, ad, bd, idesc1, (c | kk) != 0);
-          }
-        }
-        dsa::umma_commit(&s_full[b]);
-      };
-      // MMA2(tc): O^T += V^T(tile tc) . P^T(tile tc); releases the tile buffer.
-      auto mma2 = [&](uint32_t tc, bool first) {
-        const int b = tc & 1;
-        dsa::tc_fence_after();
-        const uint32_t a0 = kv_addr + b * L.buf_bytes;
-        const uint32_t pb = p.p_alias >= 0 ? a0 + p.p_alias * kChunkBytes : p_sep + b * kChunkBytes;
-        for (int mb = 0; mb < p.n_v / 2; ++mb) {
-          const uint32_t c0 = a0 + (p.v_first + 2 * mb) * kChunkBytes;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t ad = dsa::smem_desc(c0 + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
-            const uint64_t bd = dsa::smem_desc(pb + kk * 2048, kChunkBytes, 1024, dsa::kSwizzle128B);
-            dsa::umma_bf16(tmem_base + kOCol + mb * kHG, ad, bd, idesc2, (!first || kk > 0) ? 1u : 0u);
-          }
-        }
-        dsa::umma_commit(o_done);
-        dsa::umma_commit(&kv_empty[b]);
-      };
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int uu = n_units - 1 - u;
-        const int t = uu / p.G;
-        const int nt = (unit_len(p, t) + kKeys - 1) / kKeys;
-        if (nt == 0) continue;
-        if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
-        ++unit_ctr;
-        const uint32_t t0 = tile_ctr, tend = tile_ctr + nt;
-        // Issue whichever product is ready first: MMA1 of the next tile once its
-        // gather landed and its S buffer is free, or MMA2 of the oldest tile
-        // whose P is written.  MMA1 may run at most two tiles ahead of MMA2
-        // (two tile buffers, two S buffers).
-        uint32_t n1 = t0, n2 = t0;
-        uint64_t t_wait = 0;
-        while (n2 < tend) {
-          bool progressed = false;
-          if (n1 < tend && n1 < n2 + 2 && dsa::mbar_test_wait(&s_empty[n1 & 1], (((n1 >> 1) & 1) ^ 1)) &&
-              dsa::mbar_test_wait(&kv_full[n1 & 1], (n1 >> 1) & 1)) {
-            mma1(n1);
-            if (n1 == tend - 1) dsa::umma_commit(q_empty);
-            ++n1;
-            progressed = true;
-          }
-          if (n2 < n1 && dsa::mbar_test_wait(&p_full[n2 & 1], (n2 >> 1) & 1)) {
-            mma2(n2, n2 == t0);
-            ++n2;
-            progressed = true;
-          }
-          if (progressed) {
-            t_wait = 0;
-          } else {
-            if (*abort_flag) { ok = false; break; }
-            const uint64_t now = dsa::globaltimer();
-            if (t_wait == 0) {
-              t_wait = now;
-            } else if (now - t_wait > DSA_WAIT_TIMEOUT_NS) {
-              atomicOr(p.status, DSA_STATUS_WAIT_TIMEOUT);
-              *abort_flag = 1;
-              ok = false;
-              break;
-            }
-          }
-        }
-        tile_ctr = tend;
-      }
-    } else if (lane == 1) {
-      // ------------------------------------------------------------ query loads
-      dsa::tma_prefetch_desc(&map_q);
-      const uint64_t stream = dsa::l2_policy_evict_first();  // each query tile is read once
-      uint32_t unit_ctr = 0;
-      for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const uint64_t q_desc = dsa::smem_desc(dsa::smem_u32(qbuf), 16, 1024, dsa::kSwizzle128B);
+      const uint64_t kv_desc = dsa::smem_desc(kv_addr, 16, 1024, dsa::kSwizzle128B);
+      const uint64_t q_policy = dsa::l2_policy_evict_first();  // each query tile is read once
+      if (leader) dsa::tma_prefetch_desc(&map_q);
+      auto load_q = [&](int u) {
         const int uu = n_units - 1 - u;
         const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
-        if (unit_len(p, t) == 0) continue;
-        if (unit_ctr > 0 && !dsa::mbar_wait(q_empty, (unit_ctr - 1) & 1, abort_flag, p.status)) break;
-        dsa::mbar_expect_tx(q_full, p.n_qk * kQChunkBytes);
-        for (int c = 0; c < p.n_qk; ++c)
-          dsa::tma_load_3d_hint(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full, stream);
+        if (leader) {
+          dsa::mbar_expect_tx(q_full, p.n_qk * kQChunkBytes);
+          for (int c = 0; c < p.n_qk; ++c)
+            dsa::tma_load_3d_hint(qbuf + c * kQChunkBytes, &map_q, c * 64, g * kHG, t, q_full, q_policy);
+        }
+        __syncwarp();
+      };
+      uint32_t tile_ctr = 0, unit_ctr = 0;
+      bool ok = true;
+      int u = next_unit(blockIdx.x);
+      if (u < n_units) load_q(u);
+      while (u < n_units && ok) {
+        const int nt = unit_tiles(u);
+        const int u_next = next_unit(u + gridDim.x);
+        if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
+        // MMA1(tc): S^T[tc&1] = KV(tile tc) . Q^T; needs the tile and a free S buffer
+        for (int i = 0; i < nt; ++i, ++tile_ctr) {
+          const int b = tile_ctr & 1;
+          if (!dsa::mbar_wait(&s_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status) ||
+              !dsa::mbar_wait(&kv_full[b], (tile_ctr >> 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          dsa::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05 reads
+          dsa::tc_fence_after();
+          const uint64_t a0 = kv_desc + b * buf16;
+          const uint32_t d = tmem_base + kSCol + b * 64;
+          for (int c = 0; c < p.n_qk; ++c) {
+            const uint64_t ac = a0 + c * (kChunkBytes >> 4), bc = q_desc + c * (kQChunkBytes >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              if (leader) dsa::umma_bf16(d, ac + kk * 2, bc + kk * 2, idesc1, (c | kk) != 0);
+          }
+          if (leader) dsa::umma_commit(&s_full[b]);
+          __syncwarp();
+        }
+        if (!ok) break;
+        // the query buffer is free once this unit's MMA1 have run
+        if (leader) dsa::umma_commit(q_empty);
+        __syncwarp();
+        if (u_next < n_units) {
+          if (!dsa::mbar_wait(q_empty, unit_ctr & 1, abort_flag, p.status)) break;
+          load_q(u_next);
+        }
         ++unit_ctr;
+        u = u_next;
+      }
+    } else {
+      constexpr uint32_t idesc2 = dsa::idesc_bf16(128, kHG, 1, 1);
+      const uint64_t v_desc = dsa::smem_desc(kv_addr + p.v_first * kChunkBytes, kChunkBytes, 1024, dsa::kSwizzle128B);
+      const uint64_t p_desc =
+          p.p_alias >= 0 ? dsa::smem_desc(kv_addr + p.p_alias * kChunkBytes, kChunkBytes, 1024, dsa::kSwizzle128B)
+                         : dsa::smem_desc(dsa::smem_u32(smem) + L.p, kChunkBytes, 1024, dsa::kSwizzle128B);
+      const uint32_t pbuf16 = p.p_alias >= 0 ? buf16 : (kChunkBytes >> 4);
+      uint32_t tile_ctr = 0;
+      bool ok = true;
+      for (int u = next_unit(blockIdx.x); u < n_units && ok; u = next_unit(u + gridDim.x)) {
+        const int nt = unit_tiles(u);
+        // MMA2(tc): O^T += V^T(tile tc) . P^T(tile tc); releases the tile buffer
+        for (int i = 0; i < nt; ++i, ++tile_ctr) {
+          const int b = tile_ctr & 1;
+          if (!dsa::mbar_wait(&p_full[b], (tile_ctr >> 1) & 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          dsa::tc_fence_after();
+          const uint64_t a0 = v_desc + b * buf16, b0 = p_desc + b * pbuf16;
+          for (int mb = 0; mb < p.n_v / 2; ++mb) {
+            const uint64_t am = a0 + mb * (2 * kChunkBytes >> 4);
+            const uint32_t d = tmem_base + kOCol + mb * kHG;
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk)
+              if (leader)
+                dsa::umma_bf16(d, am + kk * (2048 >> 4), b0 + kk * (2048 >> 4), idesc2, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (leader) {
+            dsa::umma_commit(o_done);
+            dsa::umma_commit(&kv_empty[b]);
+          }
+          __syncwarp();
+        }
       }
     }
   } else {
