@@ -650,6 +650,322 @@ __global__ void __launch_bounds__(dsa::kTopkThreads)
   if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
 }
 
+// Stage 2, fast form: one persistent 1024-thread CTA per SM, one row at a
+// time.  While a row is being selected, the TMA unit copies the next row's
+// candidate segments into shared memory, from where they are moved into
+// registers (16 per thread, columns packed in 16 bits; the per-row capacity
+// is at most 16384).  The exact k-th key tau comes from a radix pass over the
+// key range the row actually spans (its minimum to its maximum, at most 11
+// bits), which spreads the histogram over its bins instead of piling onto the
+// few bins that the top bits of similar scores share.  The few keys of the
+// bin that holds the k-th key are then ranked by one warp; when that bin
+// holds more than 32 keys, further radix passes resolve the remaining bits.
+// The selected columns are set in a shared-memory bitmap over the row, which
+// one block scan turns into ascending ids; among keys equal to tau the
+// smallest columns are taken.  Histogram bins and bitmap words are zeroed by
+// the thread that reads them.
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelPer = 16;
+constexpr int kSelMax = kSelThreads * kSelPer;  // >= the per-row candidate capacity
+constexpr int kSelBins = 2048;
+constexpr int kSelMaxLen = 65536;  // columns must fit 16 bits; longer rows use fused_select_kernel
+constexpr int kSelWords = kSelMaxLen / 32;
+
+struct SelShared {
+  uint32_t hist[kSelBins];
+  uint32_t sel[kSelWords];
+  uint32_t tie[kSelWords];
+  int wsum[2][kSelWarps];
+  uint32_t wlo[kSelWarps], whi[kSelWarps];
+  uint32_t lkey[32];  // keys of the bin that holds the k-th key
+  int lcnt;
+  int bin, above, n_eq, need;
+  uint32_t tau;
+  int abort;
+  uint64_t full;  // staging buffer filled
+};
+
+__host__ __device__ inline size_t sel_stage_offset() { return (sizeof(SelShared) + 127) / 128 * 128; }
+
+// Exclusive prefix of v over the block (one barrier); wsum buffer `par`
+// must not be in use by another scan between two barriers.
+__device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[par][warp] = incl;
+  __syncthreads();
+  const int x = lane < kSelWarps ? wsum[par][lane] : 0;
+  int wincl = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+    if (lane >= o) wincl += y;
+  }
+  const int before = __shfl_sync(0xffffffffu, wincl - x, warp);
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kSelThreads, 1)
+    fused_select_fast_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint2* cand,
+                             const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
+                             uint32_t* status) {
+  extern __shared__ __align__(128) uint8_t smem_sel[];
+  SelShared& S = *reinterpret_cast<SelShared*>(smem_sel);
+  uint2* stage = reinterpret_cast<uint2*>(smem_sel + sel_stage_offset());
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cap_seg = cap / 4;
+  for (int i = threadIdx.x; i < kSelBins; i += kSelThreads) S.hist[i] = 0u;
+  for (int i = threadIdx.x; i < kSelWords; i += kSelThreads) {
+    S.sel[i] = 0u;
+    S.tie[i] = 0u;
+  }
+  // counts of a row's segments, clamped to the capacity
+  auto seg_counts = [&](int t, int (&c)[4]) {
+    bool over = false;
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) {
+      c[sg] = __ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg);
+      if (c[sg] > cap_seg) {
+        over = true;
+        c[sg] = cap_seg;
+      }
+    }
+    return over;
+  };
+  auto row_len = [&](int r, int* st) {
+    const int t = T - 1 - r;
+    const int s0 = doc_start(cu, n_docs, t);
+    if (st) *st = s0;
+    return t - s0 + 1;
+  };
+  // thread 0: the copy of row r's segments into the staging buffer
+  const uint64_t once = dsa::l2_policy_evict_first();
+  auto issue = [&](int r) {
+    const int t = T - 1 - r;
+    int c[4];
+    seg_counts(t, c);
+    uint32_t total = 0;
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) total += static_cast<uint32_t>((c[sg] + 1) & ~1) * 8u;
+    dsa::mbar_expect_tx(&S.full, total);
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) {
+      const uint32_t bytes = static_cast<uint32_t>((c[sg] + 1) & ~1) * 8u;
+      if (bytes)
+        dsa::bulk_load_hint(stage + sg * cap_seg, cand + (static_cast<int64_t>(t) * 4 + sg) * cap_seg, bytes, &S.full,
+                            once);
+    }
+  };
+  // next row of this CTA after r that needs its candidates (T if none)
+  auto next_row = [&](int r) {
+    for (r += gridDim.x; r < T; r += gridDim.x)
+      if (row_len(r, nullptr) > k) return r;
+    return T;
+  };
+  if (threadIdx.x == 0) {
+    dsa::mbar_init(&S.full, 1);
+    S.abort = 0;
+    dsa::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int r0 = row_len(blockIdx.x, nullptr) > k ? blockIdx.x : next_row(blockIdx.x);
+    if (r0 < T) issue(r0);
+  }
+  uint32_t phase = 0;
+  // longest rows first
+  for (int r = blockIdx.x; r < T; r += gridDim.x) {
+    const int t = T - 1 - r;
+    int st = 0;
+    const int len = row_len(r, &st);
+    int32_t* out = idx + static_cast<int64_t>(t) * k;
+    if (len <= k) {
+      for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = j < len ? st + j : -1;
+      if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
+      continue;
+    }
+    int c[4];
+    const bool overflow = seg_counts(t, c);
+    if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
+    const int n = c[0] + c[1] + c[2] + c[3];
+    if (!dsa::mbar_wait(&S.full, phase, &S.abort, status)) break;
+    phase ^= 1;
+    // ---- staging buffer -> registers: element e = i*1024 + thread of the concatenated segments
+    const int e1 = c[0], e2 = e1 + c[1], e3 = e2 + c[2];
+    uint32_t key[kSelPer];
+    uint32_t colp[kSelPer / 2];  // two 16-bit columns per word
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int i = 0; i < kSelPer; ++i) {
+      const int e = i * kSelThreads + threadIdx.x;
+      uint2 v = make_uint2(0u, 0u);
+      if (e < n) {
+        const int sg = (e >= e1) + (e >= e2) + (e >= e3);
+        const int off = e - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
+        v = stage[sg * cap_seg + off];
+        lo = min(lo, v.x);
+        hi = max(hi, v.x);
+      }
+      key[i] = v.x;
+      if (i & 1) colp[i >> 1] |= v.y << 16;
+      else colp[i >> 1] = v.y & 0xFFFFu;
+    }
+    auto valid = [&](int i) { return i * kSelThreads + static_cast<int>(threadIdx.x) < n; };
+    auto column = [&](int i) { return static_cast<int>((colp[i >> 1] >> (16 * (i & 1))) & 0xFFFFu); };
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    if (lane == 0) {
+      S.wlo[warp] = lo;
+      S.whi[warp] = hi;
+    }
+    if (threadIdx.x == 0) S.lcnt = 0;
+    __syncthreads();  // every thread has its candidates: the staging buffer is free
+    if (threadIdx.x == 0) {
+      const int rn = next_row(r);
+      if (rn < T) {
+        dsa::fence_proxy_async_smem();  // the generic reads above before the async overwrite
+        issue(rn);
+      }
+    }
+    if (n < k) {  // only reachable after an overflow: keep the output well-formed
+      for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = -1;
+      if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
+      __syncthreads();
+      continue;
+    }
+    lo = __reduce_min_sync(0xffffffffu, S.wlo[lane]);
+    hi = __reduce_max_sync(0xffffffffu, S.whi[lane]);
+    const int nbits = hi > lo ? 32 - __clz(hi - lo) : 0;
+    // ---- radix passes over v = key - lo, at most 11 bits each, top down
+    uint32_t prefix = 0u, mask = 0u;
+    int k_rem = k, n_eq = n, shift = nbits, par = 0;
+    auto run_pass = [&](int db) {
+      shift -= db;
+      const int nb = 1 << db;
+#pragma unroll
+      for (int i = 0; i < kSelPer; ++i) {
+        const uint32_t v = key[i] - lo;
+        if (valid(i) && (v & mask) == prefix) atomicAdd(&S.hist[(v >> shift) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      // thread i holds bins nb-1-2i and nb-2-2i (the top bins first)
+      const int b0 = nb - 1 - 2 * static_cast<int>(threadIdx.x);
+      const uint32_t c0 = b0 >= 0 ? S.hist[b0] : 0u;
+      const uint32_t c1 = b0 >= 1 ? S.hist[b0 - 1] : 0u;
+      if (b0 >= 0) S.hist[b0] = 0u;  // ready for the next pass
+      if (b0 >= 1) S.hist[b0 - 1] = 0u;
+      const int sum = static_cast<int>(c0 + c1);
+      const int excl = sel_scan(sum, S.wsum, par);
+      if (excl < k_rem && excl + sum >= k_rem) {
+        const bool first = excl + static_cast<int>(c0) >= k_rem;
+        S.bin = first ? b0 : b0 - 1;
+        S.above = first ? excl : excl + static_cast<int>(c0);
+        S.n_eq = static_cast<int>(first ? c0 : c1);
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(S.bin) << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
+      k_rem -= S.above;
+      n_eq = S.n_eq;
+      par ^= 1;
+    };
+    if (shift > 0) run_pass(shift < 11 ? shift : 11);
+    uint32_t tau;
+    int need;
+    if (shift > 0 && n_eq <= 32) {
+      // rank the keys of the bin that holds the k-th key within one warp
+#pragma unroll
+      for (int i = 0; i < kSelPer; ++i) {
+        const uint32_t v = key[i] - lo;
+        if (valid(i) && (v & mask) == prefix) S.lkey[atomicAdd(&S.lcnt, 1)] = key[i];
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const uint32_t mine = lane < n_eq ? S.lkey[lane] : 0u;
+        int greater = 0, equal = 0;
+        for (int j = 0; j < n_eq; ++j) {
+          const uint32_t o = S.lkey[j];
+          greater += o > mine;
+          equal += o == mine;
+        }
+        const bool hit = lane < n_eq && greater < k_rem && k_rem <= greater + equal;
+        const uint32_t hits = __ballot_sync(0xffffffffu, hit);
+        if (hits && lane == __ffs(hits) - 1) {
+          S.tau = mine;
+          S.need = k_rem - greater;
+          S.n_eq = equal;
+        }
+      }
+      __syncthreads();
+      tau = S.tau;
+      need = S.need;
+      n_eq = S.n_eq;
+    } else {
+      while (shift > 0) run_pass(shift < 11 ? shift : 11);
+      tau = lo + prefix;
+      need = k_rem;
+    }
+    // ---- bitmap of the selected columns
+#pragma unroll
+    for (int i = 0; i < kSelPer; ++i) {
+      if (!valid(i)) continue;
+      const int col = column(i);
+      if (key[i] > tau) atomicOr(&S.sel[col >> 5], 1u << (col & 31));
+      else if (key[i] == tau) atomicOr(&S.tie[col >> 5], 1u << (col & 31));
+    }
+    __syncthreads();
+    // this thread's two words, in column order
+    const int w0 = 2 * threadIdx.x;
+    uint32_t m0 = S.sel[w0], m1 = S.sel[w0 + 1];
+    uint32_t t0 = S.tie[w0], t1 = S.tie[w0 + 1];
+    S.sel[w0] = 0u;  // ready for the next row
+    S.sel[w0 + 1] = 0u;
+    S.tie[w0] = 0u;
+    S.tie[w0 + 1] = 0u;
+    if (n_eq != need) {
+      // only the `need` tied columns with the smallest indices
+      int taken = sel_scan(__popc(t0) + __popc(t1), S.wsum, par);
+      par ^= 1;
+      uint32_t keep0 = 0u, keep1 = 0u;
+      while (t0 && taken < need) {
+        const uint32_t low = t0 & (0u - t0);
+        keep0 |= low;
+        t0 ^= low;
+        ++taken;
+      }
+      while (t1 && taken < need) {
+        const uint32_t low = t1 & (0u - t1);
+        keep1 |= low;
+        t1 ^= low;
+        ++taken;
+      }
+      t0 = keep0;
+      t1 = keep1;
+    }
+    m0 |= t0;
+    m1 |= t1;
+    int pos = sel_scan(__popc(m0) + __popc(m1), S.wsum, par);
+    while (m0) {
+      const int b = __ffs(m0) - 1;
+      m0 &= m0 - 1;
+      out[pos++] = st + (w0 << 5) + b;
+    }
+    while (m1) {
+      const int b = __ffs(m1) - 1;
+      m1 &= m1 - 1;
+      out[pos++] = st + ((w0 + 1) << 5) + b;
+    }
+    if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
+    __syncthreads();  // the next row reuses the shared words above
+  }
+}
+
 int validate_indexer(const void* qi, const void* ki, const float* w, const int32_t* cu, int n_docs, int T, int Hi,
                      int d, int s_max, const char* fn) {
   if (!qi || !ki || !w || !cu) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL input pointer", fn);
@@ -793,6 +1109,16 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   p.status = dsa::device_status_ptr();
   rc = launch_indexer<1>(mq, mk, p, sms, stream);
   if (rc != DSA_OK) return rc;
+  if (s_max <= kSelMaxLen && cap <= kSelMax) {
+    const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
+    if (cudaFuncSetAttribute(fused_select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return dsa::launch_error("fused_select_fast_kernel smem attribute");
+    const int grid = T < sms ? T : sms;
+    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand, p.cand_cnt, cap,
+                                                                  idx, topk_length, p.status);
+    return dsa::launch_error("fused_select_fast_kernel");
+  }
   const size_t smem = sizeof(dsa::TopkShared);
   if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)

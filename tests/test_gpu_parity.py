@@ -260,6 +260,25 @@ def test_fused_topk_exact_when_every_key_beats_the_running_threshold(pattern, k)
     assert np.array_equal(got[rows], oi)
 
 
+def test_fused_topk_rows_longer_than_65536_columns():
+    """Rows past 65536 columns take the other stage-2 selection (its column
+    bitmap has no 16-bit limit); the result must still equal the unfused path."""
+    rng = np.random.default_rng(70001)
+    T, Hi, d, k = 70001, 8, 64, 256
+    qi = rand_bf16_bits(rng, (T, Hi, d))
+    ki = rand_bf16_bits(rng, (T, d))
+    w = (rng.random((T, Hi), dtype=np.float32) / np.float32(8)).astype(np.float32)
+    cu = np.array([0, T], np.int32)
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    idx, tl = ops.indexer_topk(*a, k, T)
+    sc = ops.indexer_scores(*a, T)
+    start, length = oracle.thd_metadata(cu, T)
+    ui, ut, _ = ops.topk(sc, dev(length), k, row_start=dev(start))
+    del sc
+    assert torch.equal(idx, ui)
+    assert torch.equal(tl, ut)
+
+
 # ------------------------------------------------------------------ attention
 def _attn_case(rng, T, H, Tkv, K, Dqk=576, Dv=512, sigma=0.1, qmul=1.0, sink_scale=1.0, sink=True, sep_v=False):
     q = rand_bf16_bits(rng, (T, H, Dqk), sigma * qmul)
