@@ -150,6 +150,26 @@ int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32
                      int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
                      int32_t* topk_length, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* The two stages of dsa_indexer_topk as separate calls, for callers that
+ * schedule or time them apart ([cuDNN-DSA] "Limitations": the selection
+ * over the candidate buffer is a stage of its own).  dsa_indexer_candidates
+ * followed by dsa_select_candidates on the same workspace and stream gives
+ * exactly the result of dsa_indexer_topk.
+ *   dsa_indexer_candidates: arguments as dsa_indexer_topk without idx and
+ *   topk_length; fills the workspace with the candidate buffer (stage 1).
+ *   dsa_select_candidates: cu_seqlens, n_docs, T, Hi, d, k and s_max as
+ *   given to dsa_indexer_candidates (they fix the workspace layout), the
+ *   workspace it filled (read only), idx and topk_length as in
+ *   dsa_indexer_topk (stage 2).
+ * What the workspace holds between the two calls is private to this library.
+ * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE. */
+int dsa_indexer_candidates(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
+                           int T, int Hi, int d, int k, int s_max, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int T, int Hi, int d, int k, int s_max,
+                          const void* workspace, size_t ws_bytes, int32_t* idx, int32_t* topk_length,
+                          cudaStream_t stream);
+
 /* Bytes of the fixed device array used by dsa_indexer_topk_noalloc (64 MiB). */
 #define DSA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

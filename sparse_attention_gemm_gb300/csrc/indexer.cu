@@ -1067,25 +1067,22 @@ extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, i
   return align256(static_cast<size_t>(T) * 16) + align256(static_cast<size_t>(T) * cap * 8);
 }
 
-extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
-                                int T, int Hi, int d, int k, int s_max, int32_t* idx, int32_t* topk_length,
-                                void* workspace, size_t ws_bytes, cudaStream_t stream) {
-  dsa::clear_error();
-  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_topk");
-  if (rc != DSA_OK) return rc;
-  if (k < 1 || k > DSA_MAX_TOPK) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk: need 1 <= k <= %d", DSA_MAX_TOPK);
-  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk: NULL idx");
+namespace {
+
+int check_workspace(int T, int Hi, int d, int k, int s_max, const void* workspace, size_t ws_bytes, const char* fn) {
+  if (k < 1 || k > DSA_MAX_TOPK) return dsa::set_error(DSA_ERR_VALUE, "%s: need 1 <= k <= %d", fn, DSA_MAX_TOPK);
   const size_t need = dsa_indexer_topk_workspace_size(T, Hi, d, k, s_max);
   if (!workspace || ws_bytes < need || !dsa::aligned(workspace, 256))
-    return dsa::set_error(DSA_ERR_WORKSPACE, "dsa_indexer_topk: workspace must be 256-byte aligned and >= %zu bytes",
-                          need);
-  int sms = 0;
-  rc = dsa::check_device(&sms);
-  if (rc != DSA_OK) return rc;
+    return dsa::set_error(DSA_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned and >= %zu bytes", fn, need);
+  return DSA_OK;
+}
+
+// Stage 1 launch (arguments already validated).
+int run_candidates(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs, int T,
+                   int Hi, int d, int k, int s_max, void* workspace, int sms, cudaStream_t stream) {
   CUtensorMap mq, mk;
-  rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
+  int rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
   if (rc != DSA_OK) return rc;
-  const int cap = fused_cap(s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   IndexerParams p{};
   p.w = w;
@@ -1099,7 +1096,7 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   p.s_max = s_max;
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
   p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(T) * 16));
-  p.cap = cap;
+  p.cap = fused_cap(s_max, k);
   p.compact = fused_compact(s_max, k);
   p.k = k;
   int bins = 2 * kHistWords / p.qb;
@@ -1107,25 +1104,83 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   while ((1 << bits) < bins) ++bits;
   p.hist_bits = bits;
   p.status = dsa::device_status_ptr();
-  rc = launch_indexer<1>(mq, mk, p, sms, stream);
-  if (rc != DSA_OK) return rc;
+  return launch_indexer<1>(mq, mk, p, sms, stream);
+}
+
+// Stage 2 launch (arguments already validated).
+int run_select(const int32_t* cu_seqlens, int n_docs, int T, int k, int s_max, void* workspace, int32_t* idx,
+               int32_t* topk_length, int sms, cudaStream_t stream) {
+  const int cap = fused_cap(s_max, k);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
+  const uint2* cand = reinterpret_cast<const uint2*>(ws + align256(static_cast<size_t>(T) * 16));
+  uint32_t* status = dsa::device_status_ptr();
   if (s_max <= kSelMaxLen && cap <= kSelMax) {
     const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
     if (cudaFuncSetAttribute(fused_select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return dsa::launch_error("fused_select_fast_kernel smem attribute");
     const int grid = T < sms ? T : sms;
-    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand, p.cand_cnt, cap,
-                                                                  idx, topk_length, p.status);
+    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, cand, cand_cnt, cap, idx,
+                                                                  topk_length, status);
     return dsa::launch_error("fused_select_fast_kernel");
   }
   const size_t smem = sizeof(dsa::TopkShared);
   if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return dsa::launch_error("fused_select_kernel smem attribute");
-  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, p.cand, p.cand_cnt, cap,
-                                                              idx, topk_length, p.status);
+  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, cand, cand_cnt, cap, idx,
+                                                              topk_length, status);
   return dsa::launch_error("fused_select_kernel");
+}
+
+}  // namespace
+
+extern "C" int dsa_indexer_candidates(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                                      int n_docs, int T, int Hi, int d, int k, int s_max, void* workspace,
+                                      size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_candidates");
+  if (rc != DSA_OK) return rc;
+  rc = check_workspace(T, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_candidates");
+  if (rc != DSA_OK) return rc;
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  return run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
+}
+
+extern "C" int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int T, int Hi, int d, int k, int s_max,
+                                     const void* workspace, size_t ws_bytes, int32_t* idx, int32_t* topk_length,
+                                     cudaStream_t stream) {
+  dsa::clear_error();
+  if (!cu_seqlens) return dsa::set_error(DSA_ERR_VALUE, "dsa_select_candidates: NULL cu_seqlens");
+  if (n_docs < 1 || T < 1) return dsa::set_error(DSA_ERR_VALUE, "dsa_select_candidates: need n_docs >= 1 and T >= 1");
+  if (s_max < 1 || s_max > T) return dsa::set_error(DSA_ERR_VALUE, "dsa_select_candidates: need 1 <= s_max <= T");
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_select_candidates: NULL idx");
+  int rc = check_workspace(T, Hi, d, k, s_max, workspace, ws_bytes, "dsa_select_candidates");
+  if (rc != DSA_OK) return rc;
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  return run_select(cu_seqlens, n_docs, T, k, s_max, const_cast<void*>(workspace), idx, topk_length, sms, stream);
+}
+
+extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
+                                int T, int Hi, int d, int k, int s_max, int32_t* idx, int32_t* topk_length,
+                                void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_topk");
+  if (rc != DSA_OK) return rc;
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk: NULL idx");
+  rc = check_workspace(T, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_topk");
+  if (rc != DSA_OK) return rc;
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  rc = run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
+  if (rc != DSA_OK) return rc;
+  return run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, sms, stream);
 }
 
 // ---------------------------------------------------------------------------

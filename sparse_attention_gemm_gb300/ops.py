@@ -48,6 +48,8 @@ _SIGNATURES = {
     "dsa_indexer_topk_workspace_size": ([I, I, I, I, I], SZ),
     "dsa_indexer_topk": ([P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P], I),
     "dsa_indexer_topk_noalloc": ([P, P, P, P, I, I, I, I, I, I, P, P, P], I),
+    "dsa_indexer_candidates": ([P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
+    "dsa_select_candidates": ([P, I, I, I, I, I, I, P, SZ, P, P, P], I),
     "dsa_sparse_attn_fwd": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P], I),
     "dsa_pack_routes": ([P, I, I, I, P, P], I),
 }
@@ -186,6 +188,36 @@ def indexer_topk(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None, idx=
     _check("dsa_indexer_topk", lib().dsa_indexer_topk(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1,
                                                       T, Hi, d, k, s_max, _p(idx), _p(topk_length), _p(workspace),
                                                       workspace.numel() * workspace.element_size(), _stream()))
+    return idx, topk_length
+
+
+def indexer_candidates(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None):
+    """Stage 1 of indexer_topk: fills and returns the candidate workspace."""
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, d = qi.shape
+    if workspace is None:
+        workspace = torch.empty(indexer_topk_workspace_size(T, Hi, d, k, s_max), dtype=torch.uint8, device=qi.device)
+    _check("dsa_indexer_candidates",
+           lib().dsa_indexer_candidates(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hi, d, k,
+                                        s_max, _p(workspace), workspace.numel() * workspace.element_size(),
+                                        _stream()))
+    return workspace
+
+
+def select_candidates(cu_seqlens, T: int, Hi: int, d: int, k: int, s_max: int, workspace, idx=None,
+                      topk_length=None):
+    """Stage 2 of indexer_topk over a workspace filled by indexer_candidates."""
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(workspace, "workspace", torch.uint8, 1)
+    dev = workspace.device
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev) if idx is None else idx
+    topk_length = torch.empty(T, dtype=torch.int32, device=dev) if topk_length is None else topk_length
+    _check("dsa_select_candidates",
+           lib().dsa_select_candidates(_p(cu_seqlens), cu_seqlens.numel() - 1, T, Hi, d, k, s_max, _p(workspace),
+                                       workspace.numel(), _p(idx), _p(topk_length), _stream()))
     return idx, topk_length
 
 

@@ -58,6 +58,11 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     lambda L: L.dsa_sparse_attn_fwd(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 256, 256, 8, 0.1, FAKE, FAKE,
                                     NULL, NULL, NULL),
     lambda L: L.dsa_pack_routes(FAKE, 0, 4, 4, FAKE, NULL),
+    lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 64, 129, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, NULL, NULL, NULL),
+    lambda L: L.dsa_select_candidates(NULL, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
+    lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
 ])
 def test_invalid_arguments_are_rejected_before_launch(lib, call):
     assert call(lib) == ops.DSA_ERR_VALUE
@@ -72,6 +77,15 @@ def test_workspace_errors(lib):
     assert rc == ops.DSA_ERR_WORKSPACE
     rc = lib.dsa_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 128, 2048, 4096, FAKE, NULL,
                               ctypes.c_void_p(4096 + 16), need, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+
+
+def test_stage_calls_check_the_workspace(lib):
+    need = lib.dsa_indexer_topk_workspace_size(4096, 64, 128, 2048, 4096)
+    rc = lib.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 128, 2048, 4096, FAKE, need - 1, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+    rc = lib.dsa_select_candidates(FAKE, 1, 4096, 64, 128, 2048, 4096, ctypes.c_void_p(4096 + 16), need, FAKE, NULL,
+                                   NULL)
     assert rc == ops.DSA_ERR_WORKSPACE
 
 

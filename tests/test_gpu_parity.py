@@ -196,6 +196,18 @@ def test_fused_indexer_topk_equals_unfused(lengths, Hi, d, k, kind):
         assert np.array_equal(idx.cpu().numpy(), oi)
 
 
+@pytest.mark.parametrize("lengths,Hi,k,kind", [([3000], 64, 512, "normal"), ([700, 1, 300, 2049], 16, 256, "int")])
+def test_stage_calls_equal_the_fused_call(lengths, Hi, k, kind):
+    rng = np.random.default_rng(sum(lengths) + 7)
+    cu, T, qi, ki, w = _indexer_inputs(rng, lengths, Hi, 128, kind)
+    s_max = int(max(lengths))
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    idx, tl = ops.indexer_topk(*a, k, s_max)
+    ws = ops.indexer_candidates(*a, k, s_max)
+    si, stl = ops.select_candidates(a[3], T, Hi, 128, k, s_max, ws)
+    assert torch.equal(idx, si) and torch.equal(tl, stl)
+
+
 def _ordered_scores_inputs(T, pattern, Hi=8, d=64):
     """Integer inputs whose exact scores follow a pattern along the key axis:
     score[j] = 256 * a[j] + b[j] from one head (q = (256, 1, 0, ...) against
