@@ -159,6 +159,75 @@ def test_topk_ties_and_edges(case):
         assert np.array_equal(tl.cpu().numpy(), rt)
 
 
+def _sampled_columns(n):
+    """Columns that the streaming top-k samples in a row of n > 4096 columns:
+    512 runs of 8 adjacent columns, run j starting at floor(j*n/512) rounded
+    down to a multiple of 4 (the kernel's sampling rule, restated here so the
+    test can plant values that the sample sees or misses)."""
+    starts = (np.arange(512, dtype=np.int64) * n // 512) & ~3
+    return np.unique((starts[:, None] + np.arange(8)[None, :]).ravel())
+
+
+@pytest.mark.parametrize("case", ["normal_long", "rising", "falling", "sample_misses_the_top",
+                                  "sample_overestimates", "sample_sees_only_ties", "short_rows"])
+def test_topk_streaming_paths(case):
+    """Rows up to 65536 columns take the sampled single-pass kernel; these
+    cases drive its run sample, its whole-row sample, and both ways the sample
+    can misjudge a row (too few candidates, too many), each of which must
+    fall back to the exact passes with the same result."""
+    rng = np.random.default_rng(11)
+    T, ld = 12, 65536
+    sc = rng.standard_normal((T, ld)).astype(np.float32)
+    lengths = np.full(T, ld, np.int32)
+    lengths[1:6] = [65535, 40000, 4097, 9001, 30000]
+    if case == "rising":
+        sc = np.sort(sc, axis=1)
+    elif case == "falling":
+        sc = -np.sort(sc, axis=1)
+    elif case == "sample_misses_the_top":
+        # every sampled column is 0 and most others are 1: the sample sees
+        # only the bottom, tau0 admits the whole row and the buffer overflows
+        sc = (1.0 + 0.01 * rng.standard_normal((T, ld))).astype(np.float32)
+        for t in range(T):
+            sc[t, _sampled_columns(int(lengths[t]))] = 0.0
+    elif case == "sample_overestimates":
+        # 300 sampled columns hold the row's largest values: tau0 lands above
+        # the k-th key, so fewer than k keys pass
+        sc = rng.random((T, ld)).astype(np.float32)
+        for t in range(T):
+            cols = _sampled_columns(int(lengths[t]))
+            sc[t, rng.choice(cols, 300, replace=False)] = 10.0 + rng.random(300).astype(np.float32)
+    elif case == "sample_sees_only_ties":
+        sc = np.zeros((T, ld), np.float32)
+        sc[:, ::101] = 2.0
+    elif case == "short_rows":
+        lengths = rng.integers(2049, 4097, size=T).astype(np.int32)
+        lengths[:3] = [2049, 4096, 4095]
+    for k in (2048, 777, 64):
+        idx, tl, vals = ops.topk(dev(sc), dev(lengths), k, want_vals=True)
+        ri, rt = oracle.topk(sc.astype(np.float64), lengths, k)
+        assert np.array_equal(idx.cpu().numpy(), ri), (case, k)
+        assert np.array_equal(tl.cpu().numpy(), rt)
+        v = vals.cpu().numpy()
+        for t in (0, 3, T - 1):
+            n = rt[t]
+            assert np.array_equal(v[t, :n], sc[t, ri[t, :n]])
+
+
+def test_topk_streaming_unaligned_output():
+    """k not a multiple of 4 and an id buffer that is not 16-byte aligned:
+    the staged ids are stored one by one."""
+    rng = np.random.default_rng(12)
+    sc = rng.standard_normal((5, 8192)).astype(np.float32)
+    lengths = np.array([8192, 8000, 3000, 2050, 7], np.int32)
+    buf = torch.full((5 * 2046 + 1,), -7, dtype=torch.int32, device=DEV)
+    out = buf[1:].view(5, 2046)
+    idx, tl, _ = ops.topk(dev(sc), dev(lengths), 2046, idx=out)
+    ri, rt = oracle.topk(sc.astype(np.float64), lengths, 2046)
+    assert np.array_equal(idx.cpu().numpy(), ri) and np.array_equal(tl.cpu().numpy(), rt)
+    assert int(buf[0]) == -7
+
+
 def test_topk_unaligned_rows_use_scalar_path():
     rng = np.random.default_rng(8)
     sc = rng.integers(0, 50, size=(9, 3001)).astype(np.float32)
