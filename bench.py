@@ -41,7 +41,7 @@ L2_BYTES = 129 * 1024 * 1024
 TRAFFIC = {
     "indexer_kernel": (5952405248, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
                        "8949f9ae7a391d31"),
-    "sparse_attn_kernel": (11327277824, ("attention.cu", "common.cuh"), "e0ad7bd892a3bf0b"),
+    "sparse_attn_kernel": (11349792000, ("attention.cu", "common.cuh"), "64143baaa6e1d26b"),
 }
 
 

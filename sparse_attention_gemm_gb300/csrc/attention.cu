@@ -48,14 +48,20 @@ namespace {
 
 constexpr int kKeys = 64;                       // keys per tile
 constexpr int kHG = 64;                         // heads per group
-constexpr int kGatherWarps = 4;
+// cp.async gather bandwidth grows with the warps issuing it (measured on
+// GB300, random 1152-byte rows into 64-key tiles: 4 warps 30 B/clk/SM,
+// 6 warps 36, 8 warps 49), so the gather gets six warps; with 16 warps in
+// all, a thread keeps up to 128 registers.
+constexpr int kGatherWarps = 6;
 constexpr int kGatherThreads = kGatherWarps * 32;
-constexpr int kMmaWarp = 4;     // MMA1 and query loads
-constexpr int kSoftWarp0 = 5;
+constexpr int kGatherKeys = kGatherThreads / 8;                   // keys one gather step covers
+constexpr int kGatherSteps = (kKeys + kGatherKeys - 1) / kGatherKeys;  // steps per tile
+constexpr int kMmaWarp = kGatherWarps;  // MMA1 and query loads
+constexpr int kSoftWarp0 = kMmaWarp + 1;
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kMma2Warp = kSoftWarp0 + kSoftWarps;  // 13: MMA2
-constexpr int kThreads = (kMma2Warp + 1) * 32;       // 448
+constexpr int kMma2Warp = kSoftWarp0 + kSoftWarps;  // MMA2
+constexpr int kThreads = (kMma2Warp + 1) * 32;       // 512
 constexpr uint32_t kChunkBytes = kKeys * 128;   // 64 keys x 64 bf16
 constexpr uint32_t kQChunkBytes = kHG * 128;    // 64 heads x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
@@ -214,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kGatherWarps) {
     // ------------------------------------------------------------ gather
-    // Thread g covers piece (g & 7) (16 bytes) of key (g >> 3) + 16*kg, for
-    // kg = 0..3 and every 64-dim chunk: one warp instruction = 4 keys x 128 B.
+    // Thread g covers piece (g & 7) (16 bytes) of key (g >> 3) + kGatherKeys*kg
+    // (keys below 64 only), for every step kg and every 64-dim chunk: one warp
+    // instruction = 4 keys x 128 B.
     const int g = threadIdx.x;
     const int piece = g & 7;
     // The gathered rows (kv, v) are re-read by every query row: keep them in L2
@@ -231,27 +238,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* irow = p.idx + static_cast<int64_t>(t) * p.K;
       // ids are loaded one tile ahead so that their latency hides behind the
       // previous tile's copies
-      int nxt[4];
+      int nxt[kGatherSteps];
 #pragma unroll
-      for (int kg = 0; kg < 4; ++kg) {
-        const int j = kg * 16 + (g >> 3);
-        nxt[kg] = j < len ? __ldcs(irow + j) : -1;
+      for (int kg = 0; kg < kGatherSteps; ++kg) {
+        const int j = kg * kGatherKeys + (g >> 3);
+        nxt[kg] = (j < kKeys && j < len) ? __ldcs(irow + j) : -1;
       }
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
         const int b = tile_ctr & 1;
-        int id[4];
+        int id[kGatherSteps];
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
+        for (int kg = 0; kg < kGatherSteps; ++kg) {
           id[kg] = (nxt[kg] >= 0 && nxt[kg] < p.Tkv) ? nxt[kg] : -1;
-          const int j = (i + 1) * kKeys + kg * 16 + (g >> 3);
-          nxt[kg] = (i + 1 < nt && j < len) ? __ldcs(irow + j) : -1;
+          const int jk = kg * kGatherKeys + (g >> 3);
+          const int j = (i + 1) * kKeys + jk;
+          nxt[kg] = (i + 1 < nt && jk < kKeys && j < len) ? __ldcs(irow + j) : -1;
         }
         if (!dsa::mbar_wait(&kv_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
         dsa::fence_proxy_async_smem();
         const uint32_t buf = dsa::smem_u32(kvbuf) + b * L.buf_bytes;
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
-          const int key = kg * 16 + (g >> 3);
+        for (int kg = 0; kg < kGatherSteps; ++kg) {
+          const int key = kg * kGatherKeys + (g >> 3);
+          if (key >= kKeys) continue;
           const uint32_t nbytes = id[kg] >= 0 ? 16u : 0u;
           const int64_t row = id[kg] >= 0 ? id[kg] : 0;
           const uint8_t* krow = p.kv + row * p.kv_row_bytes + piece * 16;

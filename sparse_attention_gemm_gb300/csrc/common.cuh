@@ -105,36 +105,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// try_wait with a suspend-time hint: the thread may sleep in hardware until
-// the phase completes or about `ns` nanoseconds pass, instead of returning at
-// once, so a waiting warp takes no issue slots from the warps doing work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait for waits that may be long: the same bound and abort protocol,
-// with the thread suspended between checks.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > DSA_WAIT_TIMEOUT_NS) {
-      atomicOr(status, DSA_STATUS_WAIT_TIMEOUT);
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
