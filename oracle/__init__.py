@@ -64,7 +64,7 @@ def _load():
             lib.oracle_compact_sort.restype = None
             lib.oracle_pack_routes.argtypes = [P, I, I, I, P]
             lib.oracle_pack_routes.restype = None
-            lib.oracle_sparse_attn.argtypes = [P, P, L, P, P, P, P, I, I, I, I, I, I, D, P, P, P, P]
+            lib.oracle_sparse_attn.argtypes = [P, P, L, P, P, P, P, I, I, I, I, I, I, D, P, P, P, P, I, P]
             lib.oracle_sparse_attn.restype = None
             _lib = lib
     return _lib
@@ -141,8 +141,11 @@ def pack_routes(routes):
     return out
 
 
-def sparse_attn(q_rows, kv, idx_rows, scale: float, topk_length=None, sink=None, v=None, dqk=None, dv=None):
-    """Returns dict(out [n,H,Dv], lse, lse_kv, max_logits) in fp64.
+def sparse_attn(q_rows, kv, idx_rows, scale: float, topk_length=None, sink=None, v=None, dqk=None, dv=None,
+                indexer_topk: int = 0):
+    """Returns dict(out [n,H,Dv], lse, lse_kv, max_logits) in fp64, plus
+    lse_indexer [n,H] when indexer_topk > 0 (the LSE of the logits of the
+    first indexer_topk slots, cuDNN DSA page section 1).
 
     kv is [Tkv, kv_ld]; QK uses its first ``dqk`` columns (default: q's last
     dim); V is ``v`` when given, else the first ``dv`` columns of kv.
@@ -162,6 +165,11 @@ def sparse_attn(q_rows, kv, idx_rows, scale: float, topk_length=None, sink=None,
     lse = np.empty((n, H), np.float64)
     lse_kv = np.empty((n, H), np.float64)
     ml = np.empty((n, H), np.float64)
+    li = np.empty((n, H), np.float64) if indexer_topk > 0 else None
     _load().oracle_sparse_attn(_ptr(q_rows), _ptr(kv), kv_ld, _ptr(vv), _ptr(idx_rows), _ptr(tl), _ptr(sk),
-                               n, Tkv, H, Dqk, Dv, K, float(scale), _ptr(out), _ptr(lse), _ptr(lse_kv), _ptr(ml))
-    return {"out": out, "lse": lse, "lse_kv": lse_kv, "max_logits": ml}
+                               n, Tkv, H, Dqk, Dv, K, float(scale), _ptr(out), _ptr(lse), _ptr(lse_kv), _ptr(ml),
+                               int(indexer_topk), _ptr(li))
+    res = {"out": out, "lse": lse, "lse_kv": lse_kv, "max_logits": ml}
+    if li is not None:
+        res["lse_indexer"] = li
+    return res

@@ -237,11 +237,13 @@ void oracle_sparse_attn(const double* q_rows, const double* kv, int64_t kv_ld,
                         const int32_t* len_rows, const double* sink, int n_rows,
                         int Tkv, int H, int Dqk, int Dv, int K, double scale,
                         double* out, double* lse, double* lse_kv,
-                        double* max_logits) {
+                        double* max_logits, int indexer_topk,
+                        double* lse_indexer) {
 #pragma omp parallel
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
+    int32_t* slot = (int32_t*)malloc(sizeof(int32_t) * (size_t)(K > 0 ? K : 1));
 #pragma omp for schedule(dynamic, 1)
     for (int64_t rh = 0; rh < (int64_t)n_rows * H; ++rh) {
       int r = (int)(rh / H), h = (int)(rh % H);
@@ -254,7 +256,10 @@ void oracle_sparse_attn(const double* q_rows, const double* kv, int64_t kv_ld,
       int n = 0;
       for (int j = 0; j < lim; ++j) {
         int32_t id = idx_rows[(int64_t)r * K + j];
-        if (id >= 0 && id < Tkv) ids[n++] = id;
+        if (id >= 0 && id < Tkv) {
+          slot[n] = j;
+          ids[n++] = id;
+        }
       }
       const double* qh = q_rows + ((int64_t)r * H + h) * Dqk;
       double m = -INFINITY;
@@ -268,6 +273,18 @@ void oracle_sparse_attn(const double* q_rows, const double* kv, int64_t kv_ld,
       double sk = sink ? sink[h] : -INFINITY;
       double* o = out + ((int64_t)r * H + h) * Dv;
       for (int c = 0; c < Dv; ++c) o[c] = 0.0;
+      if (lse_indexer) {
+        /* cuDNN DSA page, section 1: the LSE of the KV logits of the first
+         * indexer_topk slots (valid ids only, sink excluded); +inf when
+         * there are none, as for an empty row. */
+        int np = 0;  /* valid ids in slots below indexer_topk */
+        while (np < n && slot[np] < indexer_topk) ++np;
+        double mp = -INFINITY, zp = 0.0;
+        for (int j = 0; j < np; ++j)
+          if (s[j] > mp) mp = s[j];
+        for (int j = 0; j < np; ++j) zp += exp(s[j] - mp);
+        lse_indexer[rh] = zp > 0.0 ? mp + log(zp) : INFINITY;
+      }
       if (n == 0) {
         if (lse) lse[rh] = sk;
         if (lse_kv) lse_kv[rh] = INFINITY;
@@ -290,5 +307,6 @@ void oracle_sparse_attn(const double* q_rows, const double* kv, int64_t kv_ld,
     }
     free(s);
     free(ids);
+    free(slot);
   }
 }

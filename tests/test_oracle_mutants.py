@@ -31,6 +31,12 @@ MUTANTS = {
     "attn_sign_in_exp": ("double p = exp(s[j] - ref);", "double p = exp(ref - s[j]);"),
     "attn_drop_scale": ("s[j] = scale * dot;", "s[j] = dot;"),
     "attn_lse_kv_with_sink": ("if (lse_kv) lse_kv[rh] = ref + log(zkv);", "if (lse_kv) lse_kv[rh] = ref + log(z);"),
+    "lse_indexer_prefix_off_by_one": ("while (np < n && slot[np] < indexer_topk) ++np;",
+                                      "while (np < n && slot[np] <= indexer_topk) ++np;"),
+    "lse_indexer_counts_valid_ids": ("while (np < n && slot[np] < indexer_topk) ++np;",
+                                     "while (np < n && np < indexer_topk) ++np;"),
+    "lse_indexer_with_sink": ("lse_indexer[rh] = zp > 0.0 ? mp + log(zp) : INFINITY;",
+                              "lse_indexer[rh] = zp > 0.0 ? mp + log(zp + exp(sk - mp)) : INFINITY;"),
     "compact_keeps_key_count": ("(int64_t)id < key_count", "(int64_t)id <= key_count"),
     "pack_wrong_batch_stride": ("v = b * S + id;", "v = b * W + id;"),
     "metadata_len_off_by_one": ("len[t] = t - cu[b] + 1;", "len[t] = t - cu[b];"),

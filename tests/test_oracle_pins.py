@@ -386,3 +386,53 @@ def test_attention_separate_v_equals_latent_layout():
     b = oracle.sparse_attn(q2, kv2, idx, 0.6, dv=Dv)
     np.testing.assert_allclose(a["out"], b["out"], rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(a["lse"], b["lse"], rtol=1e-12)
+
+
+# ---------------------------------------------------- attention: lse_indexer
+def test_lse_indexer_golden_hand_example():
+    g = _gold("attention_hand.json")
+    for P, ln_arg in g["lse_indexer_ln"].items():
+        res = oracle.sparse_attn(np.array(g["q"]), np.array(g["kv"]), np.array(g["idx"]), math.log(3) / 2,
+                                 sink=np.array(g["sink"]), dv=1, indexer_topk=int(P))
+        assert res["lse_indexer"][0, 0] == pytest.approx(math.log(ln_arg), rel=1e-14), P
+
+
+def test_lse_indexer_prefix_and_suffix_make_lse_kv():
+    """The prefix LSE and the LSE of the remaining slots combine to the
+    KV-only LSE of the whole row; a full prefix is that LSE itself; the prefix
+    LSE grows with the prefix."""
+    rng = np.random.default_rng(56)
+    T, H, D, Tkv, K = 7, 3, 9, 40, 16
+    q = rng.standard_normal((T, H, D)) * 2
+    kv = rng.standard_normal((Tkv, D))
+    sink = rng.standard_normal(H)
+    idx = rng.integers(-2, Tkv + 2, size=(T, K)).astype(np.int32)  # some invalid ids
+    idx[:, 0] = rng.integers(0, Tkv, size=T)                        # every row has a valid slot
+    full = oracle.sparse_attn(q, kv, idx, 0.4, sink=sink, dv=4, indexer_topk=K)
+    np.testing.assert_allclose(full["lse_indexer"], full["lse_kv"], rtol=1e-13)
+    prev = None
+    for P in (1, 5, 8, 13):
+        pre = oracle.sparse_attn(q, kv, idx, 0.4, sink=sink, dv=4, indexer_topk=P)["lse_indexer"]
+        suf_idx = idx.copy()
+        suf_idx[:, :P] = -1
+        suf = oracle.sparse_attn(q, kv, suf_idx, 0.4, sink=sink, dv=4)["lse_kv"]
+        both = np.logaddexp(pre, np.where(np.isinf(suf), -np.inf, suf))
+        np.testing.assert_allclose(both, full["lse_kv"], rtol=1e-12)
+        if prev is not None:
+            assert np.all(pre >= prev - 1e-12)
+        prev = pre
+
+
+def test_lse_indexer_empty_and_truncated():
+    rng = np.random.default_rng(57)
+    q = rng.standard_normal((3, 2, 5))
+    kv = rng.standard_normal((6, 5))
+    idx = np.array([[-1, -1, -1, -1], [-1, 2, 3, 4], [1, 2, 3, 4]], np.int32)
+    res = oracle.sparse_attn(q, kv, idx, 1.0, dv=3, indexer_topk=1)
+    assert np.all(np.isposinf(res["lse_indexer"][:2]))   # empty row; prefix of invalid ids only
+    assert np.all(np.isfinite(res["lse_indexer"][2]))
+    # topk_length shorter than the prefix: the prefix covers every valid slot
+    tl = np.array([0, 2, 3], np.int32)
+    r2 = oracle.sparse_attn(q, kv, idx, 1.0, dv=3, topk_length=tl, indexer_topk=4)
+    np.testing.assert_allclose(r2["lse_indexer"][1:], r2["lse_kv"][1:], rtol=1e-13)
+    assert np.all(np.isposinf(r2["lse_indexer"][0]))
