@@ -228,6 +228,23 @@ int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int3
                         int Dqk, int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
                         float* max_logits, cudaStream_t stream);
 
+/* dsa_sparse_attn_fwd plus the indexer-prefix statistic ([cuDNN-DSA] 1,
+ * outputs "lse_indexer" and compile-time "indexer_topk"):
+ *   lse_indexer fp32 [T, H] (out): log sum exp(s_j) over the valid slots j <
+ *       indexer_topk (KV only, sink excluded), +inf when there are none
+ *       (empty row, or a prefix of invalid ids).  A row whose topk_length is
+ *       below indexer_topk uses all of its valid slots (the pages require
+ *       topk_length >= indexer_topk; this is the plain reading otherwise).
+ *   indexer_topk: 0 (no lse_indexer; the pointer is ignored) or a multiple
+ *       of 64 in [64, K] (the pages' variants use 512, 1024, 2048).
+ * Other arguments, results and errors as dsa_sparse_attn_fwd; lse_indexer
+ * NULL with indexer_topk > 0, or an indexer_topk outside the rule above, is
+ * DSA_ERR_VALUE. */
+int dsa_sparse_attn_fwd_ex(const void* q, const void* kv, const void* v, const int32_t* idx,
+                           const int32_t* topk_length, const float* sink, int T, int Tkv, int H,
+                           int Dqk, int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
+                           float* max_logits, int indexer_topk, float* lse_indexer, cudaStream_t stream);
+
 /* Route packing ([NeMo-QSA] _pack_indices): routes int32 [B, S, W] hold
  * batch-local ids; out int32 [B*S, Wp] with Wp = ceil(W/4)*4 receives
  * b*S + id for 0 <= id < S and -1 otherwise (including slots W..Wp-1).

@@ -81,8 +81,10 @@ struct AttnParams {
   float* lse;
   float* lse_kv;
   float* max_logits;
+  float* lse_indexer;  // [T, H] or nullptr
   uint32_t* status;
   int T, Tkv, H, G, K, Dv;
+  int snap_tiles;  // indexer_topk / 64: lse_indexer is taken after this many tiles (0: off)
   int n_qk;      // Dqk / 64
   int n_v;       // Dv / 64
   int n_chunks;  // 64-dim chunks per tile buffer
@@ -419,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.lse[orow + st] = p.sink ? __ldg(p.sink + g * kHG + st) : -INFINITY;
           if (p.lse_kv) p.lse_kv[orow + st] = INFINITY;
           if (p.max_logits) p.max_logits[orow + st] = -INFINITY;
+          if (p.lse_indexer) p.lse_indexer[orow + st] = INFINITY;
         }
         continue;
       }
@@ -556,6 +559,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsa::tc_fence_before();
         __syncwarp();
         if (lane == 0) dsa::mbar_arrive(&p_full[b]);
+        // lse_indexer: the LSE of the slots of the first snap_tiles tiles (all
+        // of a shorter row), from the sums so far, relative to the current
+        // reference like the final statistics
+        if (p.snap_tiles > 0 && i == min(p.snap_tiles, nt) - 1) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float v = l_part[2 * j + e];
+              v += __shfl_xor_sync(0xffffffffu, v, 4);
+              v += __shfl_xor_sync(0xffffffffu, v, 8);
+              v += __shfl_xor_sync(0xffffffffu, v, 16);
+              if (lane < 4) red[quarter * 64 + hbase + 8 * j + e] = v;
+            }
+          }
+          named_bar(1, kSoftThreads);
+          if (st < hv) {
+            const float l = red[st] + red[64 + st] + red[128 + st] + red[192 + st];
+            p.lse_indexer[orow + st] = l > 0.f ? (mref[st] + log2f(l)) * kLn2 : INFINITY;
+          }
+          named_bar(1, kSoftThreads);  // red is read before the epilogue reuses it
+        }
       }
       if (!ok) break;
 
@@ -629,11 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int32_t* idx,
-                                   const int32_t* topk_length, const float* sink, int T, int Tkv, int H, int Dqk,
-                                   int Dv, int K, float scale, void* out, float* lse, float* lse_kv, float* max_logits,
-                                   cudaStream_t stream) {
+extern "C" int dsa_sparse_attn_fwd_ex(const void* q, const void* kv, const void* v, const int32_t* idx,
+                                      const int32_t* topk_length, const float* sink, int T, int Tkv, int H, int Dqk,
+                                      int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
+                                      float* max_logits, int indexer_topk, float* lse_indexer, cudaStream_t stream) {
   dsa::clear_error();
+  if (indexer_topk < 0 || indexer_topk % 64 != 0 || indexer_topk > K)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_sparse_attn_fwd: indexer_topk must be a multiple of 64 in [0, K]");
+  if (indexer_topk > 0 && T > 0 && !lse_indexer)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_sparse_attn_fwd: lse_indexer is NULL while indexer_topk > 0");
   const bool latent = (Dqk == 576 || Dqk == 512) && Dv == 512 && v == nullptr;
   const bool separate = Dqk == 256 && Dv == 256 && v != nullptr;
   if (!latent && !separate)
@@ -662,6 +691,8 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
   p.lse = lse;
   p.lse_kv = lse_kv;
   p.max_logits = max_logits;
+  p.lse_indexer = indexer_topk > 0 ? lse_indexer : nullptr;
+  p.snap_tiles = indexer_topk / kKeys;
   p.status = dsa::device_status_ptr();
   p.T = T;
   p.Tkv = Tkv;
@@ -696,4 +727,12 @@ extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v,
   const int grid = units < sms ? units : sms;
   sparse_attn_kernel<<<grid, kThreads, smem, stream>>>(mq, p);
   return dsa::launch_error("sparse_attn_kernel");
+}
+
+extern "C" int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int32_t* idx,
+                                   const int32_t* topk_length, const float* sink, int T, int Tkv, int H, int Dqk,
+                                   int Dv, int K, float scale, void* out, float* lse, float* lse_kv, float* max_logits,
+                                   cudaStream_t stream) {
+  return dsa_sparse_attn_fwd_ex(q, kv, v, idx, topk_length, sink, T, Tkv, H, Dqk, Dv, K, scale, out, lse, lse_kv,
+                                max_logits, 0, nullptr, stream);
 }

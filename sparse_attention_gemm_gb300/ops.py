@@ -51,6 +51,7 @@ _SIGNATURES = {
     "dsa_indexer_candidates": ([P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
     "dsa_select_candidates": ([P, I, I, I, I, I, I, P, SZ, P, P, P], I),
     "dsa_sparse_attn_fwd": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P], I),
+    "dsa_sparse_attn_fwd_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, I, P, P], I),
     "dsa_pack_routes": ([P, I, I, I, P, P], I),
 }
 
@@ -238,8 +239,9 @@ def indexer_topk_noalloc(qi, ki, w, cu_seqlens, k: int, s_max: int, idx=None, to
 
 
 def sparse_attn_fwd(q, kv, idx, scale: float, topk_length=None, sink=None, v=None, want_lse_kv: bool = False,
-                    want_max_logits: bool = False, out=None, lse=None):
-    """Sparse MQA attention forward; returns dict(out, lse[, lse_kv][, max_logits])."""
+                    want_max_logits: bool = False, out=None, lse=None, indexer_topk: int = 0):
+    """Sparse MQA attention forward; returns dict(out, lse[, lse_kv][, max_logits][, lse_indexer]).
+    indexer_topk > 0 adds lse_indexer (dsa_sparse_attn_fwd_ex)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(kv, "kv", torch.bfloat16, 2)
     _need(idx, "idx", torch.int32, 2)
@@ -258,10 +260,20 @@ def sparse_attn_fwd(q, kv, idx, scale: float, topk_length=None, sink=None, v=Non
     lse = torch.empty((T, H), dtype=torch.float32, device=dev) if lse is None else lse
     lse_kv = torch.empty((T, H), dtype=torch.float32, device=dev) if want_lse_kv else None
     ml = torch.empty((T, H), dtype=torch.float32, device=dev) if want_max_logits else None
-    _check("dsa_sparse_attn_fwd", lib().dsa_sparse_attn_fwd(_p(q), _p(kv), _p(v), _p(idx), _p(topk_length), _p(sink),
-                                                            T, Tkv, H, Dqk, Dv, K, float(scale), _p(out), _p(lse),
-                                                            _p(lse_kv), _p(ml), _stream()))
+    if indexer_topk:
+        li = torch.empty((T, H), dtype=torch.float32, device=dev)
+        _check("dsa_sparse_attn_fwd_ex",
+               lib().dsa_sparse_attn_fwd_ex(_p(q), _p(kv), _p(v), _p(idx), _p(topk_length), _p(sink), T, Tkv, H, Dqk,
+                                            Dv, K, float(scale), _p(out), _p(lse), _p(lse_kv), _p(ml),
+                                            int(indexer_topk), _p(li), _stream()))
+    else:
+        li = None
+        _check("dsa_sparse_attn_fwd",
+               lib().dsa_sparse_attn_fwd(_p(q), _p(kv), _p(v), _p(idx), _p(topk_length), _p(sink), T, Tkv, H, Dqk,
+                                         Dv, K, float(scale), _p(out), _p(lse), _p(lse_kv), _p(ml), _stream()))
     res = {"out": out, "lse": lse}
+    if li is not None:
+        res["lse_indexer"] = li
     if lse_kv is not None:
         res["lse_kv"] = lse_kv
     if ml is not None:

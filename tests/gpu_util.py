@@ -62,7 +62,7 @@ def assert_attention_close(got: dict, ref: dict, hv=None):
     if nrm > 0:
         fro = np.linalg.norm(out - rout) / nrm
         assert fro <= OUT_FRO_REL, f"out relative Frobenius err {fro:.3g}"
-    for key, tol in (("lse", LSE_ABS), ("lse_kv", LSE_ABS), ("max_logits", LSE_ABS)):
+    for key, tol in (("lse", LSE_ABS), ("lse_kv", LSE_ABS), ("max_logits", LSE_ABS), ("lse_indexer", LSE_ABS)):
         if key in got:
             g = got[key].cpu().numpy().astype(np.float64)
             r = ref[key]

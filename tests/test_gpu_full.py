@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import DEV, assert_attention_close, assert_scores_close, dev, dev_bf16, f64
+from gpu_util import DEV, LSE_ABS, assert_attention_close, assert_scores_close, dev, dev_bf16, f64
 from sparse_attention_gemm_gb300 import ops
 from sparse_attention_gemm_gb300 import workloads as W
 
@@ -108,7 +108,23 @@ def test_thd_16k_workload():
 def test_long_64k_workload():
     wl = W.long_64k()
     idx, tl, rows = _indexer_workload_check(wl, 40, 3)
-    _attention_check(wl, idx, tl, _rows(wl.T, wl.K, 24, 13))
+    rows = _rows(wl.T, wl.K, 24, 13)
+    _attention_check(wl, idx, tl, rows)
+    # lse_indexer over the first 1024 slots (a prefix length the pages list for
+    # 64 heads): the other results are those of the call without it, bit for
+    # bit, and lse_indexer matches the oracle on the sampled rows
+    q, kv, sk = wl.q_bits(), wl.kv_bits(), wl.sink()
+    a = (dev_bf16(q), dev_bf16(kv), idx, wl.scale)
+    plain = ops.sparse_attn_fwd(*a, topk_length=tl, sink=dev(sk))
+    ext = ops.sparse_attn_fwd(*a, topk_length=tl, sink=dev(sk), indexer_topk=1024)
+    assert torch.equal(plain["out"], ext["out"]) and torch.equal(plain["lse"], ext["lse"])
+    r = torch.from_numpy(rows).to(DEV)
+    ref = oracle.sparse_attn(f64(q[rows]), f64(kv), idx[r].cpu().numpy(), wl.scale, topk_length=tl[r].cpu().numpy(),
+                             sink=sk, dv=wl.Dv, indexer_topk=1024)
+    got = ext["lse_indexer"][r].cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref["lse_indexer"])
+    assert np.array_equal(np.isposinf(got), ~fin)
+    assert np.abs(got[fin] - ref["lse_indexer"][fin]).max() <= LSE_ABS
 
 
 def test_gqa_routes_workload():

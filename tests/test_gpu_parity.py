@@ -428,6 +428,31 @@ def test_attention_slot_edge_cases():
     assert_attention_close(got, _ref_attn(q, kv, None, idx, None, None, scale))
 
 
+@pytest.mark.parametrize("H,P,sep_v", [(64, 64, False), (64, 128, False), (128, 256, False), (12, 192, False),
+                                       (12, 256, True)])
+def test_attention_lse_indexer(H, P, sep_v):
+    """lse_indexer over the first P slots: prefixes with invalid ids, rows
+    shorter than the prefix, an empty row and a prefix of invalid ids only."""
+    rng = np.random.default_rng(20 + P + H)
+    T, Tkv, K = 80, 600, 320
+    Dqk, Dv = (256, 256) if sep_v else (576, 512)
+    q, kv, v, sk = _attn_case(rng, T, H, Tkv, K, Dqk=Dqk, Dv=Dv, qmul=8.0, sink=not sep_v, sep_v=sep_v)
+    idx = rng.integers(0, Tkv, size=(T, K)).astype(np.int32)
+    idx[:, 3] = -1
+    idx[:, 70] = Tkv + 1
+    idx[9] = -1
+    idx[11, :P] = -1
+    tl = rng.integers(0, K + 1, size=T).astype(np.int32)
+    tl[:5] = [0, 1, P - 1, P, P + 1]
+    scale = 1 / math.sqrt(Dqk)
+    got = ops.sparse_attn_fwd(dev_bf16(q), dev_bf16(kv), dev(idx), scale, topk_length=dev(tl),
+                              sink=None if sk is None else dev(sk), v=None if v is None else dev_bf16(v),
+                              want_lse_kv=True, want_max_logits=True, indexer_topk=P)
+    ref = oracle.sparse_attn(f64(q), f64(kv), idx, scale, topk_length=tl, sink=sk,
+                             v=None if v is None else f64(v), dv=Dv, indexer_topk=P)
+    assert_attention_close(got, ref, hv=H)
+
+
 @pytest.mark.parametrize("H", [1, 12, 64, 100, 128])
 def test_attention_head_counts(H):
     rng = np.random.default_rng(H)
