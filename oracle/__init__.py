@@ -60,6 +60,8 @@ def _load():
             lib.oracle_indexer_scores.restype = None
             lib.oracle_topk.argtypes = [P, L, P, P, I, I, P, P]
             lib.oracle_topk.restype = I
+            lib.oracle_topk_softmax.argtypes = [P, L, P, P, P, I, I, P, P, P]
+            lib.oracle_topk_softmax.restype = None
             lib.oracle_compact_sort.argtypes = [P, I, I, L, P, P]
             lib.oracle_compact_sort.restype = None
             lib.oracle_pack_routes.argtypes = [P, I, I, I, P]
@@ -121,6 +123,25 @@ def topk(scores, len_rows, k: int, start_rows=None):
     if rc != 0:
         raise MemoryError("oracle_topk: allocation failed")
     return idx, tl
+
+
+def topk_softmax(scores, idx, topk_len, start_rows=None):
+    """(logits [n, k], softmax [n, k], lse [n]) of the selected slots, cuDNN
+    DSA page section 4: logits aligned with idx (-inf in padded slots), their
+    softmax over the row's selected slots (0 elsewhere) and its log-sum-exp
+    (-inf for a row with no slot)."""
+    scores = _f64(scores)
+    n, ld = scores.shape
+    idx = _i32(idx)
+    k = idx.shape[1]
+    tl = _i32(topk_len)
+    st = None if start_rows is None else _i32(start_rows)
+    logits = np.empty((n, k), np.float64)
+    sm = np.empty((n, k), np.float64)
+    lse = np.empty(n, np.float64)
+    _load().oracle_topk_softmax(_ptr(scores), ld, _ptr(idx), _ptr(st), _ptr(tl), n, k, _ptr(logits), _ptr(sm),
+                                _ptr(lse))
+    return logits, sm, lse
 
 
 def compact_sort(indices, key_count: int):

@@ -177,6 +177,35 @@ int oracle_topk(const double* scores, int64_t ld, const int32_t* len_rows,
  * valid ids form the prefix, every later slot holds -1, the id convention
  * is preserved].  Valid ids are sorted ascending; duplicates are kept.
  * ------------------------------------------------------------------------ */
+/* cuDNN Frontend DSA page, section 4 (Combined Indexer Forward + Top-K):
+ * with the indices come the aligned logits (the selected scores, -inf in
+ * padded slots), their softmax and its log-sum-exp.  Reading: the softmax
+ * and lse run over the row's selected slots j < topk_len[r]; padded slots
+ * have probability 0; a row with no slot has lse = -inf. */
+void oracle_topk_softmax(const double* scores, int64_t ld, const int32_t* idx,
+                         const int32_t* start_rows, const int32_t* topk_len,
+                         int n_rows, int K, double* logits, double* softmax,
+                         double* lse) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < n_rows; ++r) {
+    const int n = topk_len[r];
+    const int32_t base = start_rows ? start_rows[r] : 0;
+    double m = -INFINITY;
+    for (int j = 0; j < K; ++j) {
+      double l = -INFINITY;
+      if (j < n) l = scores[(int64_t)r * ld + (idx[(int64_t)r * K + j] - base)];
+      logits[(int64_t)r * K + j] = l;
+      if (l > m) m = l;
+    }
+    double z = 0.0;
+    for (int j = 0; j < n; ++j) z += exp(logits[(int64_t)r * K + j] - m);
+    const double lz = n > 0 ? m + log(z) : -INFINITY;
+    lse[r] = lz;
+    for (int j = 0; j < K; ++j)
+      softmax[(int64_t)r * K + j] = j < n ? exp(logits[(int64_t)r * K + j] - lz) : 0.0;
+  }
+}
+
 void oracle_compact_sort(const int32_t* in, int T, int K, int64_t key_count,
                          int32_t* out, int32_t* lengths) {
 #pragma omp parallel for schedule(static)

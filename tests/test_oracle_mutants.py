@@ -37,6 +37,12 @@ MUTANTS = {
                                      "while (np < n && np < indexer_topk) ++np;"),
     "lse_indexer_with_sink": ("lse_indexer[rh] = zp > 0.0 ? mp + log(zp) : INFINITY;",
                               "lse_indexer[rh] = zp > 0.0 ? mp + log(zp + exp(sk - mp)) : INFINITY;"),
+    "topk_softmax_ignores_start": ("l = scores[(int64_t)r * ld + (idx[(int64_t)r * K + j] - base)];",
+                                   "l = scores[(int64_t)r * ld + idx[(int64_t)r * K + j]];"),
+    "topk_softmax_lse_over_all_slots": ("for (int j = 0; j < n; ++j) z += exp(logits[(int64_t)r * K + j] - m);",
+                                        "for (int j = 0; j < K; ++j) z += exp(logits[(int64_t)r * K + j] - m) + 1e-3;"),
+    "topk_softmax_divides_by_max": ("softmax[(int64_t)r * K + j] = j < n ? exp(logits[(int64_t)r * K + j] - lz) : 0.0;",
+                                    "softmax[(int64_t)r * K + j] = j < n ? exp(logits[(int64_t)r * K + j] - m) : 0.0;"),
     "compact_keeps_key_count": ("(int64_t)id < key_count", "(int64_t)id <= key_count"),
     "pack_wrong_batch_stride": ("v = b * S + id;", "v = b * W + id;"),
     "metadata_len_off_by_one": ("len[t] = t - cu[b] + 1;", "len[t] = t - cu[b];"),

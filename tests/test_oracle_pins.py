@@ -436,3 +436,56 @@ def test_lse_indexer_empty_and_truncated():
     r2 = oracle.sparse_attn(q, kv, idx, 1.0, dv=3, topk_length=tl, indexer_topk=4)
     np.testing.assert_allclose(r2["lse_indexer"][1:], r2["lse_kv"][1:], rtol=1e-13)
     assert np.all(np.isposinf(r2["lse_indexer"][0]))
+
+
+# ------------------------------------------------- top-k logits and softmax
+def _ln(v):
+    return {"ln2": math.log(2), "ln3": math.log(3), "ln7": math.log(7)}.get(v, v)
+
+
+def test_topk_softmax_golden():
+    g = _gold("topk_softmax.json")
+    sc = np.array([[_ln(v) for v in row] for row in g["scores"]], np.float64)
+    idx, tl = oracle.topk(sc, np.array(g["length"], np.int32), g["k"], start_rows=np.array(g["start"], np.int32))
+    assert idx.tolist() == g["idx"]
+    logits, sm, lse = oracle.topk_softmax(sc, idx, tl, start_rows=np.array(g["start"], np.int32))
+    for r in range(3):
+        for j in range(2):
+            want = g["logits_ln"][r][j]
+            if want is None:
+                assert np.isneginf(logits[r, j])
+            else:
+                assert logits[r, j] == pytest.approx(math.log(want), rel=1e-15)
+            assert sm[r, j] == pytest.approx(g["softmax"][r][j], rel=1e-14, abs=1e-300)
+        if g["lse_ln"][r] is None:
+            assert np.isneginf(lse[r])
+        else:
+            assert lse[r] == pytest.approx(math.log(g["lse_ln"][r]), rel=1e-14)
+
+
+def test_topk_softmax_invariants():
+    rng = np.random.default_rng(58)
+    T, ld, k = 40, 300, 64
+    sc = rng.standard_normal((T, ld)) * 3
+    lengths = rng.integers(0, ld + 1, size=T).astype(np.int32)
+    lengths[:3] = [0, 1, k]
+    idx, tl = oracle.topk(sc, lengths, k)
+    logits, sm, lse = oracle.topk_softmax(sc, idx, tl)
+    for t in range(T):
+        n = tl[t]
+        assert np.all(np.isneginf(logits[t, n:])) and np.all(sm[t, n:] == 0.0)
+        if n == 0:
+            assert np.isneginf(lse[t])
+            continue
+        assert sm[t, :n].sum() == pytest.approx(1.0, rel=1e-12)
+        # the selected logits are the top-n scores of the row, aligned with the ids
+        np.testing.assert_array_equal(logits[t, :n], sc[t, idx[t, :n]])
+        assert logits[t, :n].min() >= np.sort(sc[t, : lengths[t]])[::-1][n - 1]
+        # probability ratios are exponentials of logit differences
+        np.testing.assert_allclose(sm[t, 1:n] / sm[t, 0], np.exp(logits[t, 1:n] - logits[t, 0]), rtol=1e-12)
+        assert lse[t] >= logits[t, :n].max()
+    # shifting every score shifts the lse and leaves the softmax alone
+    l2, s2, e2 = oracle.topk_softmax(sc + 2.5, idx, tl)
+    np.testing.assert_allclose(s2, sm, rtol=1e-12, atol=1e-300)
+    fin = np.isfinite(lse)
+    np.testing.assert_allclose(e2[fin], lse[fin] + 2.5, rtol=1e-13)
