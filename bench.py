@@ -39,9 +39,9 @@ L2_BYTES = 129 * 1024 * 1024
 # bench (command and figures in profiles/).  A figure only stands for the
 # kernel sources it measured: when their hash differs it is reported as null.
 TRAFFIC = {
-    "indexer_kernel": (5952405248, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
-                       "8949f9ae7a391d31"),
-    "sparse_attn_kernel": (11349792000, ("attention.cu", "common.cuh"), "64143baaa6e1d26b"),
+    "indexer_kernel": (5954639872, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
+                       "34a59eb369377138"),
+    "sparse_attn_kernel": (11351404288, ("attention.cu", "common.cuh"), "5d7dcd228735d363"),
 }
 
 
@@ -272,6 +272,7 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=16)
     ap.add_argument("--no-topk-standalone", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip timing the optional outputs")
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
                     help="2: single doc T=4096, 3: THD T=16384, 4: long T=65536 (the headline workload)")
     args = ap.parse_args()
@@ -376,6 +377,44 @@ def main():
     cand_tflops = work["indexer_flops"] / (cand_avg / 1e3) / 1e12
     status = ops.device_status(clear=True)
 
+    # ---- the optional outputs, timed on their own (not part of the step)
+    def timed(fn, reps=3):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return sum(ts) / len(ts)
+
+    extras = None
+    if not args.no_extras:
+        P = 1024 if K >= 1024 else (K // 64) * 64
+        extras = {}
+        if P > 0:
+            li = torch.empty((T, H), dtype=torch.float32, device=dev)
+            L = ops.lib()
+
+            def attn_li():
+                ops._check("dsa_sparse_attn_fwd_ex", L.dsa_sparse_attn_fwd_ex(
+                    ops._p(d["q"]), ops._p(d["kv"]), None, ops._p(idx), ops._p(tl), ops._p(d["sink"]), T, T, H,
+                    wl.Dqk, wl.Dv, K, float(wl.scale), ops._p(out), ops._p(lse), None, None, P, ops._p(li),
+                    ops._stream()))
+            extras["attn_with_lse_indexer_ms"] = timed(attn_li)
+            extras["lse_indexer_prefix"] = P
+            extras["attn_ms_same_run"] = timed(lambda: ops.sparse_attn_fwd(
+                d["q"], d["kv"], idx, wl.scale, topk_length=tl, sink=d["sink"], out=out, lse=lse))
+            del li
+        if wl.s_max <= 65536:
+            extras["indexer_topk_logits_softmax_lse_ms"] = timed(lambda: ops.indexer_topk_ex(
+                d["qi"], d["ki"], d["w"], d["cu"], K, wl.s_max, workspace=ws))
+            extras["indexer_topk_ms_same_run"] = timed(lambda: ops.indexer_topk(
+                d["qi"], d["ki"], d["w"], d["cu"], K, wl.s_max, workspace=ws, idx=idx, topk_length=tl))
+        ops.device_status(clear=True)
+
     # ---- end to end through host buffers (H2D inputs + D2H results inside the timed region)
     out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -470,6 +509,7 @@ def main():
             "clocks": clk,
             "device_status": status,
             "topk_standalone": topk_line,
+            "optional_outputs": extras,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

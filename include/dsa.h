@@ -116,6 +116,19 @@ int dsa_indexer_scores(const void* qi, const void* ki, const float* w, const int
 int dsa_topk(const float* scores, int64_t ld, const int32_t* len, const int32_t* row_start, int T,
              int k, int32_t* idx, int32_t* topk_length, float* vals, cudaStream_t stream);
 
+/* Softmax of the top-k logits ([cuDNN-DSA] 4: the combined indexer + top-k
+ * returns aligned logits, their softmax and an LSE).  Over the slots of a row
+ * whose id is valid (idx >= 0):
+ *   lse[t] = log sum_j exp(logits[t, j]);  softmax[t, j] = exp(logits[t, j] - lse[t]);
+ * slots with idx < 0 get probability 0; a row with no valid slot has lse
+ * -inf and probability 0 everywhere.  fp32 arithmetic (CUDA's expf/logf).
+ *   logits fp32 [T, k] (e.g. dsa_topk's vals); idx int32 [T, k] (the ids
+ *   they are aligned with); softmax fp32 [T, k] or NULL (out); lse fp32 [T]
+ *   or NULL (out), not both NULL.  Shapes: T >= 0, k >= 1.
+ * Errors: DSA_ERR_VALUE. */
+int dsa_topk_softmax(const float* logits, const int32_t* idx, int T, int k, float* softmax, float* lse,
+                     cudaStream_t stream);
+
 /* Compact and sort ([NeMo-common] _compact_and_sort_indices; [cuDNN-DSA]
  * "Compact vs. non-compact sparse indices"): per row, ids with
  * 0 <= id < key_count are sorted ascending into a prefix (duplicates kept),
@@ -149,6 +162,20 @@ size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max);
 int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
                      int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
                      int32_t* topk_length, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* dsa_indexer_topk with the other outputs of the pages' combined indexer +
+ * top-k ([cuDNN-DSA] 4): logits fp32 [T, k] (out, required): the score of
+ * each selected id, aligned with idx, -inf in padded slots -- bit for bit
+ * the value dsa_indexer_scores computes for that key; softmax fp32 [T, k]
+ * and lse fp32 [T] (out, each may be NULL): as dsa_topk_softmax over those
+ * logits.  Other arguments and results as dsa_indexer_topk.
+ * Errors: as dsa_indexer_topk, plus DSA_ERR_VALUE for NULL logits and
+ * DSA_ERR_UNSUPPORTED when s_max exceeds 65536 (rows that long select
+ * through a form that does not keep the values). */
+int dsa_indexer_topk_ex(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                        int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
+                        int32_t* topk_length, float* logits, float* softmax, float* lse,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* The two stages of dsa_indexer_topk as separate calls, for callers that
  * schedule or time them apart ([cuDNN-DSA] "Limitations": the selection

@@ -714,7 +714,7 @@ __device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) 
 __global__ void __launch_bounds__(kSelThreads, 1)
     fused_select_fast_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint2* cand,
                              const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
-                             uint32_t* status) {
+                             float* logits, uint32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared& S = *reinterpret_cast<SelShared*>(smem_sel);
   uint2* stage = reinterpret_cast<uint2*>(smem_sel + sel_stage_offset());
@@ -785,9 +785,23 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     int st = 0;
     const int len = row_len(r, &st);
     int32_t* out = idx + static_cast<int64_t>(t) * k;
+    float* lout = logits ? logits + static_cast<int64_t>(t) * k : nullptr;
     if (len <= k) {
       for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = j < len ? st + j : -1;
       if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
+      if (lout) {
+        // every key of a row this short is a candidate: its value goes to the
+        // slot of its column
+        int c[4];
+        seg_counts(t, c);
+        for (int j = len + threadIdx.x; j < k; j += kSelThreads) lout[j] = -INFINITY;
+#pragma unroll
+        for (int sg = 0; sg < 4; ++sg)
+          for (int i = threadIdx.x; i < c[sg]; i += kSelThreads) {
+            const uint2 v = cand[(static_cast<int64_t>(t) * 4 + sg) * cap_seg + i];
+            if (static_cast<int>(v.y) < len) lout[v.y] = dsa::key_f32(v.x);
+          }
+      }
       continue;
     }
     int c[4];
@@ -834,7 +848,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       }
     }
     if (n < k) {  // only reachable after an overflow: keep the output well-formed
-      for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = -1;
+      for (int j = threadIdx.x; j < k; j += kSelThreads) {
+        out[j] = -1;
+        if (lout) lout[j] = -INFINITY;
+      }
       if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
       __syncthreads();
       continue;
@@ -951,6 +968,13 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     m0 |= t0;
     m1 |= t1;
     int pos = sel_scan(__popc(m0) + __popc(m1), S.wsum, par);
+    if (lout) {
+      // the final bitmap and each word's first output slot, for the logits
+      S.sel[w0] = m0;
+      S.sel[w0 + 1] = m1;
+      S.tie[w0] = static_cast<uint32_t>(pos);
+      S.tie[w0 + 1] = static_cast<uint32_t>(pos + __popc(m0));
+    }
     while (m0) {
       const int b = __ffs(m0) - 1;
       m0 &= m0 - 1;
@@ -962,6 +986,23 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       out[pos++] = st + ((w0 + 1) << 5) + b;
     }
     if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
+    if (lout) {
+      // each selected candidate's value at the slot of its column: the slot is
+      // its word's first slot plus the selected columns below it in the word
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < kSelPer; ++i) {
+        if (!valid(i)) continue;
+        const int col = column(i);
+        const uint32_t word = S.sel[col >> 5], below = (1u << (col & 31)) - 1u;
+        if ((word >> (col & 31)) & 1u) lout[S.tie[col >> 5] + __popc(word & below)] = dsa::key_f32(key[i]);
+      }
+      __syncthreads();
+      S.sel[w0] = 0u;
+      S.sel[w0 + 1] = 0u;
+      S.tie[w0] = 0u;
+      S.tie[w0 + 1] = 0u;
+    }
     __syncthreads();  // the next row reuses the shared words above
   }
 }
@@ -1108,21 +1149,24 @@ int run_candidates(const void* qi, const void* ki, const float* w, const int32_t
 }
 
 // Stage 2 launch (arguments already validated).
+// True when stage 2 runs its fast form (the only form that can also write logits).
+bool select_is_fast(int s_max, int k) { return s_max <= kSelMaxLen && fused_cap(s_max, k) <= kSelMax; }
+
 int run_select(const int32_t* cu_seqlens, int n_docs, int T, int k, int s_max, void* workspace, int32_t* idx,
-               int32_t* topk_length, int sms, cudaStream_t stream) {
+               int32_t* topk_length, float* logits, int sms, cudaStream_t stream) {
   const int cap = fused_cap(s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
   const uint2* cand = reinterpret_cast<const uint2*>(ws + align256(static_cast<size_t>(T) * 16));
   uint32_t* status = dsa::device_status_ptr();
-  if (s_max <= kSelMaxLen && cap <= kSelMax) {
+  if (select_is_fast(s_max, k)) {
     const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
     if (cudaFuncSetAttribute(fused_select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return dsa::launch_error("fused_select_fast_kernel smem attribute");
     const int grid = T < sms ? T : sms;
     fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, cand, cand_cnt, cap, idx,
-                                                                  topk_length, status);
+                                                                  topk_length, logits, status);
     return dsa::launch_error("fused_select_fast_kernel");
   }
   const size_t smem = sizeof(dsa::TopkShared);
@@ -1163,7 +1207,8 @@ extern "C" int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_select(cu_seqlens, n_docs, T, k, s_max, const_cast<void*>(workspace), idx, topk_length, sms, stream);
+  return run_select(cu_seqlens, n_docs, T, k, s_max, const_cast<void*>(workspace), idx, topk_length, nullptr, sms,
+                    stream);
 }
 
 extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
@@ -1180,7 +1225,33 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   if (rc != DSA_OK) return rc;
   rc = run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
   if (rc != DSA_OK) return rc;
-  return run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, sms, stream);
+  return run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, nullptr, sms, stream);
+}
+
+// The fused call with the outputs that come with the indices on the pages'
+// combined indexer + top-k: aligned logits, and optionally their softmax and
+// log-sum-exp (dsa_topk_softmax over the logits).
+extern "C" int dsa_indexer_topk_ex(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
+                                   int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
+                                   int32_t* topk_length, float* logits, float* softmax, float* lse, void* workspace,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_indexer(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, s_max, "dsa_indexer_topk_ex");
+  if (rc != DSA_OK) return rc;
+  if (!idx || !logits) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_ex: NULL idx or logits");
+  rc = check_workspace(T, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_topk_ex");
+  if (rc != DSA_OK) return rc;
+  if (!select_is_fast(s_max, k))
+    return dsa::set_error(DSA_ERR_UNSUPPORTED,
+                          "dsa_indexer_topk_ex: logits need rows of at most %d columns (s_max = %d)", kSelMaxLen, s_max);
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  rc = run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
+  if (rc != DSA_OK) return rc;
+  rc = run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, logits, sms, stream);
+  if (rc != DSA_OK || (!softmax && !lse)) return rc;
+  return dsa_topk_softmax(logits, idx, T, k, softmax, lse, stream);
 }
 
 // ---------------------------------------------------------------------------

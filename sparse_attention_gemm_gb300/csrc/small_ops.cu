@@ -1,8 +1,10 @@
-// small_ops.cu -- THD metadata, route packing and compact+sort.
+// small_ops.cu -- THD metadata, route packing, compact+sort and the softmax
+// of the top-k logits.
 //
 // These are small, latency-bound steps: one thread per element for the
 // metadata and the route packing, one CTA per row for compact+sort (the row
-// is sorted in shared memory with a bitonic network).
+// is sorted in shared memory with a bitonic network), one warp per row for
+// the top-k softmax.
 #include <climits>
 
 #include "block_sort.cuh"
@@ -101,6 +103,55 @@ extern "C" int dsa_pack_routes(const int32_t* routes, int B, int S, int W, int32
   const int64_t n = static_cast<int64_t>(B) * S * Wp;
   pack_routes_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(routes, S, W, Wp, n, out);
   return dsa::launch_error("pack_routes_kernel");
+}
+
+namespace {
+
+// cuDNN Frontend DSA page, section 4: the softmax of a row's top-k logits and
+// its log-sum-exp, over the slots whose id is valid (>= 0); other slots get
+// probability 0.  One warp per row: the maximum, then the sum of exp(l - max)
+// (fp32, CUDA's expf/logf), then the probabilities.  A row with no valid slot
+// has lse = -inf.
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits,
+                                                           const int32_t* __restrict__ idx, int T, int k,
+                                                           float* __restrict__ softmax, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* l = logits + t * k;
+  const int32_t* id = idx + t * k;
+  float m = -INFINITY;
+  for (int j = lane; j < k; j += 32)
+    if (__ldg(id + j) >= 0) m = fmaxf(m, __ldg(l + j));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float z = 0.f;
+  if (m > -INFINITY)
+    for (int j = lane; j < k; j += 32)
+      if (__ldg(id + j) >= 0) z += expf(__ldg(l + j) - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float lz = z > 0.f ? m + logf(z) : -INFINITY;
+  if (lse && lane == 0) lse[t] = lz;
+  if (softmax) {
+    float* s = softmax + t * k;
+    for (int j = lane; j < k; j += 32) s[j] = (z > 0.f && __ldg(id + j) >= 0) ? expf(__ldg(l + j) - lz) : 0.f;
+  }
+}
+
+}  // namespace
+
+extern "C" int dsa_topk_softmax(const float* logits, const int32_t* idx, int T, int k, float* softmax, float* lse,
+                                cudaStream_t stream) {
+  dsa::clear_error();
+  if (T < 0 || k < 1) return dsa::set_error(DSA_ERR_VALUE, "dsa_topk_softmax: need T >= 0 and k >= 1");
+  if (T > 0 && (!logits || !idx || (!softmax && !lse)))
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_topk_softmax: NULL logits or idx, or neither softmax nor lse");
+  int rc = dsa::check_device(nullptr);
+  if (rc != DSA_OK) return rc;
+  if (T == 0) return DSA_OK;
+  topk_softmax_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, idx, T, k, softmax, lse);
+  return dsa::launch_error("topk_softmax_kernel");
 }
 
 extern "C" int dsa_compact_sort_indices(const int32_t* in, int T, int K, int64_t key_count, int32_t* out,

@@ -47,6 +47,8 @@ _SIGNATURES = {
     "dsa_compact_sort_indices": ([P, I, I, I64, P, P, P], I),
     "dsa_indexer_topk_workspace_size": ([I, I, I, I, I], SZ),
     "dsa_indexer_topk": ([P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P], I),
+    "dsa_indexer_topk_ex": ([P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
+    "dsa_topk_softmax": ([P, P, I, I, P, P, P], I),
     "dsa_indexer_topk_noalloc": ([P, P, P, P, I, I, I, I, I, I, P, P, P], I),
     "dsa_indexer_candidates": ([P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
     "dsa_select_candidates": ([P, I, I, I, I, I, I, P, SZ, P, P, P], I),
@@ -190,6 +192,46 @@ def indexer_topk(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None, idx=
                                                       T, Hi, d, k, s_max, _p(idx), _p(topk_length), _p(workspace),
                                                       workspace.numel() * workspace.element_size(), _stream()))
     return idx, topk_length
+
+
+def indexer_topk_ex(qi, ki, w, cu_seqlens, k: int, s_max: int, want_softmax: bool = True, want_lse: bool = True,
+                    workspace=None):
+    """Fused indexer + top-k with its aligned logits, and optionally their
+    softmax and lse: dict(idx, topk_length, logits[, softmax][, lse])."""
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hi, d = qi.shape
+    dev = qi.device
+    if workspace is None:
+        workspace = torch.empty(indexer_topk_workspace_size(T, Hi, d, k, s_max), dtype=torch.uint8, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    tl = torch.empty(T, dtype=torch.int32, device=dev)
+    logits = torch.empty((T, k), dtype=torch.float32, device=dev)
+    sm = torch.empty((T, k), dtype=torch.float32, device=dev) if want_softmax else None
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if want_lse else None
+    _check("dsa_indexer_topk_ex",
+           lib().dsa_indexer_topk_ex(_p(qi), _p(ki), _p(w), _p(cu_seqlens), cu_seqlens.numel() - 1, T, Hi, d, k, s_max,
+                                     _p(idx), _p(tl), _p(logits), _p(sm), _p(lse), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream()))
+    res = {"idx": idx, "topk_length": tl, "logits": logits}
+    if sm is not None:
+        res["softmax"] = sm
+    if lse is not None:
+        res["lse"] = lse
+    return res
+
+
+def topk_softmax(logits, idx, want_softmax: bool = True, want_lse: bool = True):
+    """Softmax and lse of top-k logits over the slots with a valid id: (softmax or None, lse or None)."""
+    _need(logits, "logits", torch.float32, 2)
+    _need(idx, "idx", torch.int32, 2)
+    T, k = logits.shape
+    sm = torch.empty_like(logits) if want_softmax else None
+    lse = torch.empty(T, dtype=torch.float32, device=logits.device) if want_lse else None
+    _check("dsa_topk_softmax", lib().dsa_topk_softmax(_p(logits), _p(idx), T, k, _p(sm), _p(lse), _stream()))
+    return sm, lse
 
 
 def indexer_candidates(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None):

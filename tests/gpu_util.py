@@ -22,6 +22,24 @@ SCORE_FLOOR = 1e-6
 # (2^-9), so 1e-2 leaves a 2.5x margin; it catches systematic errors that the
 # loose absolute bound would miss on small outputs.
 OUT_FRO_REL = 1e-2
+# Derived (not stated): the top-k softmax runs in fp32 with CUDA's expf/logf
+# (a few ulp each) over at most 2048 terms, so its lse is off by a few fp32
+# ulp of its magnitude plus ~1e-6 from the sum, and each probability by the
+# same relative amount; 1e-4 relative leaves a wide margin.
+TOPK_SOFTMAX_REL = 1e-4
+
+
+def assert_topk_softmax_close(sm, lse, ref_sm, ref_lse):
+    sm = sm.cpu().numpy().astype(np.float64) if sm is not None else None
+    lse = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(lse), ~fin), "lse: -inf rows differ"
+    if fin.any():
+        e = np.abs(lse[fin] - ref_lse[fin]) / np.maximum(1.0, np.abs(ref_lse[fin]))
+        assert e.max() <= TOPK_SOFTMAX_REL, f"lse rel err {e.max():.3g}"
+    if sm is not None:
+        bad = np.abs(sm - ref_sm) > TOPK_SOFTMAX_REL * ref_sm + 1e-7
+        assert not bad.any(), f"{bad.sum()} probabilities out of tolerance"
 
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:

@@ -19,7 +19,8 @@ def lib():
 def test_header_declares_the_hot_path():
     names = ops.header_functions()
     for must in ["dsa_thd_metadata", "dsa_indexer_scores", "dsa_topk", "dsa_compact_sort_indices",
-                 "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex",
+                 "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_topk_ex", "dsa_topk_softmax",
+                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex",
                  "dsa_pack_routes",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
@@ -64,6 +65,10 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
                                        NULL, NULL, 192, FAKE, NULL),
     lambda L: L.dsa_sparse_attn_fwd_ex(FAKE, FAKE, NULL, FAKE, NULL, NULL, 4, 4, 64, 576, 512, 128, 0.1, FAKE, FAKE,
                                        NULL, NULL, 64, NULL, NULL),
+    lambda L: L.dsa_topk_softmax(FAKE, FAKE, 4, 0, FAKE, FAKE, NULL),
+    lambda L: L.dsa_topk_softmax(FAKE, FAKE, 4, 8, NULL, NULL, NULL),
+    lambda L: L.dsa_indexer_topk_ex(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 64, 128, FAKE, NULL, NULL, NULL, NULL,
+                                    FAKE, 1 << 30, NULL),
     lambda L: L.dsa_pack_routes(FAKE, 0, 4, 4, FAKE, NULL),
     lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 64, 129, FAKE, 1 << 30, NULL),

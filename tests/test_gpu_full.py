@@ -4,6 +4,8 @@ against dense scores + top-k, top-k against the oracle's top-k of the GPU's
 own scores); indexer scores and attention outputs are checked against the
 fp64 oracle on stratified samples of rows (first, last, around t = k, random).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -59,6 +61,15 @@ def _indexer_workload_check(wl, n_sample, seed):
     start, length = oracle.thd_metadata(wl.cu_seqlens, T)
     idx, tl = ops.indexer_topk(*a, K, wl.s_max)
     scores = ops.indexer_scores(*a, wl.s_max)
+    if wl.s_max <= 65536:
+        # the fused call's logits are the dense scores at the selected ids, every row
+        ext = ops.indexer_topk_ex(*a, K, wl.s_max, want_softmax=False)
+        assert torch.equal(ext["idx"], idx)
+        st = torch.from_numpy(start).to(DEV).long()
+        col = (idx.long() - st[:, None]).clamp(min=0)
+        want = torch.where(idx >= 0, torch.gather(scores, 1, col), torch.full_like(ext["logits"], -math.inf))
+        assert torch.equal(ext["logits"], want)
+        del ext, st, col, want
     ui, ut, _ = ops.topk(scores, dev(length), K, row_start=dev(start))
     # fused == dense + top-k on every row (bit-exact)
     assert torch.equal(idx, ui) and torch.equal(tl, ut)

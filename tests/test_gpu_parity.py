@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (DEV, assert_attention_close, assert_scores_close, cu_from_lengths, dev, dev_bf16, f64,
-                      rand_bf16_bits)
+from gpu_util import (DEV, assert_attention_close, assert_scores_close, assert_topk_softmax_close, cu_from_lengths,
+                      dev, dev_bf16, f64, rand_bf16_bits)
 from sparse_attention_gemm_gb300 import ops
 from sparse_attention_gemm_gb300 import workloads as W
 
@@ -131,6 +131,41 @@ def test_topk_on_gpu_scores_is_exact():
             n = rt[t]
             assert np.array_equal(v[t, :n], scn[t, ri[t, :n] - start[t]].astype(np.float32))
             assert np.all(np.isneginf(v[t, n:]))
+
+
+def test_topk_softmax_of_dense_topk():
+    """dsa_topk's values are the selected scores; dsa_topk_softmax over them
+    against the oracle's softmax and lse of the same selection."""
+    rng = np.random.default_rng(6)
+    cu, T, qi, ki, w = _indexer_inputs(rng, [1500, 37, 900], 64, 128)
+    sc = ops.indexer_scores(dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu), 1500)
+    start, length = oracle.thd_metadata(cu, T)
+    scn = sc.cpu().numpy().astype(np.float64)
+    for k in (1, 64, 2048):
+        idx, tl, vals = ops.topk(sc, dev(length), k, row_start=dev(start), want_vals=True)
+        sm, lse = ops.topk_softmax(vals, idx)
+        rl, rs, re = oracle.topk_softmax(scn, idx.cpu().numpy(), tl.cpu().numpy(), start_rows=start)
+        assert np.array_equal(vals.cpu().numpy().astype(np.float64), rl), k
+        assert_topk_softmax_close(sm, lse, rs, re)
+
+
+@pytest.mark.parametrize("lengths,k", [([3000], 512), ([300, 2100, 40, 1500], 1024), ([4096], 2048),
+                                       ([256], 64)])
+def test_fused_topk_logits_softmax(lengths, k):
+    """The fused call's logits are the dense scores of the selected keys, bit
+    for bit (-inf on padding); its softmax and lse match the oracle's."""
+    rng = np.random.default_rng(sum(lengths) + k)
+    cu, T, qi, ki, w = _indexer_inputs(rng, lengths, 64, 128)
+    s_max = int(max(lengths))
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    ext = ops.indexer_topk_ex(*a, k, s_max)
+    idx, tl = ops.indexer_topk(*a, k, s_max)
+    assert torch.equal(ext["idx"], idx) and torch.equal(ext["topk_length"], tl)
+    sc = ops.indexer_scores(*a, s_max).cpu().numpy().astype(np.float64)
+    start, _ = oracle.thd_metadata(cu, T)
+    rl, rs, re = oracle.topk_softmax(sc, idx.cpu().numpy(), tl.cpu().numpy(), start_rows=start)
+    assert np.array_equal(ext["logits"].cpu().numpy().astype(np.float64), rl)
+    assert_topk_softmax_close(ext["softmax"], ext["lse"], rs, re)
 
 
 @pytest.mark.parametrize("case", ["all_equal", "three_values", "two_values_long", "normal", "neg_zero", "lengths"])
