@@ -272,6 +272,62 @@ int dsa_sparse_attn_fwd_ex(const void* q, const void* kv, const void* v, const i
                            int Dqk, int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
                            float* max_logits, int indexer_topk, float* lse_indexer, cudaStream_t stream);
 
+/* One forward step from host buffers: the fused indexer + top-k
+ * (dsa_indexer_topk) and sparse attention (dsa_sparse_attn_fwd, latent
+ * kv of the same T rows, ids global) with the host-device copies overlapped
+ * with the kernels.  Not a step of the pages' method: the path of
+ * dsa_indexer_topk and dsa_sparse_attn_fwd, enqueued so that the upload of q
+ * and kv runs under the indexer and the download of each of `chunks` token
+ * ranges of out/lse runs under the attention of the next range.
+ *   b: host inputs qi [T,Hi,d] bf16, ki [T,d] bf16, w [T,Hi], cu_seqlens
+ *      [n_docs+1], q [T,H,Dqk] bf16, kv [T,Dqk] bf16, sink [H] or NULL;
+ *      caller-owned device buffers of the same shapes (*_d; sink_d NULL iff
+ *      sink is NULL); device results idx_d [T,k], topk_length_d [T], out_d
+ *      [T,H,Dv] bf16, lse_d [T,H]; the indexer workspace (as for
+ *      dsa_indexer_topk); host results idx, topk_length, out, lse.  Host
+ *      buffers should be page-locked: pageable ones are still correct but
+ *      their copies do not overlap.
+ *   chunks: 1..16 (and <= T) token ranges for attention.
+ *   compute, copy: two streams; the call enqueues on both and returns.
+ *      When `compute` has finished, every result is in the host buffers.
+ * Results equal those of the two device calls on the same inputs, bit for
+ * bit.  Shapes as those calls (Dqk in {576, 512}, Dv = 512, no separate v).
+ * Events: a fixed set per device, created by the first call on that device
+ * (make it before any stream capture); a lock serialises the enqueueing of
+ * calls from several host threads.  Errors: DSA_ERR_VALUE,
+ * DSA_ERR_WORKSPACE, DSA_ERR_CUDA, DSA_ERR_UNSUPPORTED; every argument is
+ * validated before the first copy is enqueued. */
+typedef struct dsa_forward_buffers {
+  const void* qi;
+  const void* ki;
+  const float* w;
+  const int32_t* cu_seqlens;
+  const void* q;
+  const void* kv;
+  const float* sink;
+  void* qi_d;
+  void* ki_d;
+  float* w_d;
+  int32_t* cu_seqlens_d;
+  void* q_d;
+  void* kv_d;
+  float* sink_d;
+  int32_t* idx_d;
+  int32_t* topk_length_d;
+  void* out_d;
+  float* lse_d;
+  void* workspace;
+  size_t ws_bytes;
+  int32_t* idx;
+  int32_t* topk_length;
+  void* out;
+  float* lse;
+} dsa_forward_buffers;
+
+int dsa_forward_host(const dsa_forward_buffers* b, int n_docs, int T, int Hi, int d, int k, int s_max,
+                     int H, int Dqk, int Dv, float scale, int chunks, cudaStream_t compute,
+                     cudaStream_t copy);
+
 /* Route packing ([NeMo-QSA] _pack_indices): routes int32 [B, S, W] hold
  * batch-local ids; out int32 [B*S, Wp] with Wp = ceil(W/4)*4 receives
  * b*S + id for 0 <= id < S and -1 otherwise (including slots W..Wp-1).

@@ -49,6 +49,7 @@ _SIGNATURES = {
     "dsa_indexer_topk": ([P, P, P, P, I, I, I, I, I, I, P, P, P, SZ, P], I),
     "dsa_indexer_topk_ex": ([P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
     "dsa_topk_softmax": ([P, P, I, I, P, P, P], I),
+    "dsa_forward_host": ([P, I, I, I, I, I, I, I, I, I, F, I, P, P], I),
     "dsa_indexer_topk_noalloc": ([P, P, P, P, I, I, I, I, I, I, P, P, P], I),
     "dsa_indexer_candidates": ([P, P, P, P, I, I, I, I, I, I, P, SZ, P], I),
     "dsa_select_candidates": ([P, I, I, I, I, I, I, P, SZ, P, P, P], I),
@@ -232,6 +233,42 @@ def topk_softmax(logits, idx, want_softmax: bool = True, want_lse: bool = True):
     lse = torch.empty(T, dtype=torch.float32, device=logits.device) if want_lse else None
     _check("dsa_topk_softmax", lib().dsa_topk_softmax(_p(logits), _p(idx), T, k, _p(sm), _p(lse), _stream()))
     return sm, lse
+
+
+class ForwardBuffers(ctypes.Structure):
+    """dsa_forward_buffers (include/dsa.h), field for field."""
+    _fields_ = [(name, ctypes.c_void_p) for name in (
+        "qi", "ki", "w", "cu_seqlens", "q", "kv", "sink", "qi_d", "ki_d", "w_d", "cu_seqlens_d", "q_d", "kv_d",
+        "sink_d", "idx_d", "topk_length_d", "out_d", "lse_d", "workspace")] + [("ws_bytes", ctypes.c_size_t)] + [
+        (name, ctypes.c_void_p) for name in ("idx", "topk_length", "out", "lse")]
+
+
+def forward_host(host: dict, dev: dict, res_dev: dict, res_host: dict, workspace, n_docs: int, k: int, s_max: int,
+                 scale: float, chunks: int = 4, copy_stream=None):
+    """One forward step from host buffers through dsa_forward_host.
+
+    host: qi, ki, w, cu_seqlens, q, kv, sink (page-locked CPU tensors; sink may
+    be None); dev: device tensors of the same shapes; res_dev / res_host: idx,
+    topk_length, out, lse on the device / in page-locked host memory.  Enqueues
+    on the current stream and `copy_stream` and returns at once."""
+    T, Hi, d = host["qi"].shape
+    _, H, Dqk = host["q"].shape
+    Dv = res_dev["out"].shape[2]
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=dev["qi"].device)
+    b = ForwardBuffers()
+    for name in ("qi", "ki", "w", "cu_seqlens", "q", "kv", "sink"):
+        setattr(b, name, None if host.get(name) is None else host[name].data_ptr())
+        setattr(b, name + "_d", None if dev.get(name) is None else dev[name].data_ptr())
+    for name in ("idx", "topk_length", "out", "lse"):
+        setattr(b, name + "_d", res_dev[name].data_ptr())
+        setattr(b, name, res_host[name].data_ptr())
+    b.workspace = workspace.data_ptr()
+    b.ws_bytes = workspace.numel() * workspace.element_size()
+    _check("dsa_forward_host", lib().dsa_forward_host(ctypes.byref(b), n_docs, T, Hi, d, k, s_max, H, Dqk, Dv,
+                                                      float(scale), chunks, _stream(),
+                                                      ctypes.c_void_p(copy_stream.cuda_stream)))
+    return copy_stream
 
 
 def indexer_candidates(qi, ki, w, cu_seqlens, k: int, s_max: int, workspace=None):

@@ -20,7 +20,7 @@ def test_header_declares_the_hot_path():
     names = ops.header_functions()
     for must in ["dsa_thd_metadata", "dsa_indexer_scores", "dsa_topk", "dsa_compact_sort_indices",
                  "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_topk_ex", "dsa_topk_softmax",
-                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex",
+                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex", "dsa_forward_host",
                  "dsa_pack_routes",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
@@ -69,6 +69,11 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     lambda L: L.dsa_topk_softmax(FAKE, FAKE, 4, 8, NULL, NULL, NULL),
     lambda L: L.dsa_indexer_topk_ex(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 64, 128, FAKE, NULL, NULL, NULL, NULL,
                                     FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_forward_host(NULL, 1, 128, 64, 128, 64, 128, 64, 576, 512, 0.1, 4, NULL, NULL),
+    lambda L: L.dsa_forward_host(ctypes.byref(ops.ForwardBuffers()), 1, 128, 64, 128, 64, 128, 64, 576, 512, 0.1, 0,
+                                 NULL, NULL),
+    lambda L: L.dsa_forward_host(ctypes.byref(ops.ForwardBuffers()), 1, 128, 64, 128, 64, 128, 64, 576, 512, 0.1, 4,
+                                 NULL, NULL),
     lambda L: L.dsa_pack_routes(FAKE, 0, 4, 4, FAKE, NULL),
     lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_indexer_candidates(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 128, 64, 129, FAKE, 1 << 30, NULL),

@@ -151,3 +151,37 @@ def test_gqa_routes_workload():
     sub = {key: t[r] for key, t in got.items()}
     ref = oracle.sparse_attn(f64(q[rows]), f64(k), packed[r].cpu().numpy(), wl.scale, v=f64(v))
     assert_attention_close(sub, ref)
+
+
+@pytest.mark.parametrize("name,chunks", [("single_doc_4k", 1), ("single_doc_4k", 3), ("thd_16k", 4)])
+def test_forward_from_host_buffers(name, chunks):
+    """dsa_forward_host (copies overlapped with the kernels) gives the results
+    of the device calls on the same inputs, bit for bit."""
+    wl = getattr(W, name)()
+    T, K = wl.T, wl.K
+
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    host = {"qi": pinned(wl.qi_bits()), "ki": pinned(wl.ki_bits()), "w": pinned(wl.w()),
+            "cu_seqlens": pinned(wl.cu_seqlens), "q": pinned(wl.q_bits()), "kv": pinned(wl.kv_bits()),
+            "sink": pinned(wl.sink())}
+    dev_in = {k: torch.empty_like(v, device=DEV) for k, v in host.items()}
+    res_dev = {"idx": torch.empty((T, K), dtype=torch.int32, device=DEV),
+               "topk_length": torch.empty(T, dtype=torch.int32, device=DEV),
+               "out": torch.empty((T, wl.H, wl.Dv), dtype=torch.bfloat16, device=DEV),
+               "lse": torch.empty((T, wl.H), dtype=torch.float32, device=DEV)}
+    res_host = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in res_dev.items()}
+    ws = torch.empty(ops.indexer_topk_workspace_size(T, wl.Hi, wl.d, K, wl.s_max), dtype=torch.uint8, device=DEV)
+    ops.forward_host(host, dev_in, res_dev, res_host, ws, wl.n_docs, K, wl.s_max, wl.scale, chunks=chunks)
+    torch.cuda.current_stream().synchronize()
+    # the same step through the device calls
+    bf = lambda t: t.to(DEV).view(torch.bfloat16)
+    idx, tl = ops.indexer_topk(bf(host["qi"]), bf(host["ki"]), host["w"].to(DEV), host["cu_seqlens"].to(DEV), K,
+                               wl.s_max)
+    ref = ops.sparse_attn_fwd(bf(host["q"]), bf(host["kv"]), idx, wl.scale, topk_length=tl, sink=host["sink"].to(DEV))
+    assert torch.equal(res_host["idx"], idx.cpu()) and torch.equal(res_host["topk_length"], tl.cpu())
+    assert torch.equal(res_host["out"].view(torch.int16), ref["out"].cpu().view(torch.int16))
+    assert torch.equal(res_host["lse"], ref["lse"].cpu())
