@@ -167,9 +167,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                "r"(src_bytes), "l"(policy)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(dsa::smem_u32(bar)) : "memory");
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap map_q, const AttnParams p) {
@@ -275,7 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                          nbytes, keep);
           }
         }
-        cp_async_arrive(&kv_full[b]);
+        // the tile is signalled with a plain release arrive once this thread's
+        // copies have landed (cp.async.mbarrier.arrive, which signals from the
+        // copy engine, gave stale tiles on GB300 when other warps arrived on
+        // other barriers meanwhile; waiting here costs nothing measurable,
+        // the next tile's buffer is not free before these copies land anyway)
+        cp_async_wait_all();
+        dsa::mbar_arrive(&kv_full[b]);
       }
     }
   } else if (warp == kMmaWarp || warp == kMma2Warp) {
