@@ -56,6 +56,8 @@ def _load():
             lib.oracle_num_threads.restype = I
             lib.oracle_thd_metadata.argtypes = [P, I, I, P, P]
             lib.oracle_thd_metadata.restype = I
+            lib.oracle_ratio_metadata.argtypes = [P, P, P, I, I, I, I, P, P]
+            lib.oracle_ratio_metadata.restype = I
             lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
             lib.oracle_indexer_scores.restype = None
             lib.oracle_topk.argtypes = [P, L, P, P, I, I, P, P]
@@ -96,6 +98,23 @@ def thd_metadata(cu_seqlens, T: int):
     rc = _load().oracle_thd_metadata(_ptr(cu), cu.size - 1, T, _ptr(start), _ptr(length))
     if rc != 0:
         raise ValueError("cu_seqlens is not a valid prefix array over [0, T)")
+    return start, length
+
+
+def ratio_metadata(cu_q, cu_k, q_causal_offsets, ratio: int, Tq: int, Tk: int):
+    """start[t], len[t] of the ratio-causal compressed-key mask (cuDNN DSA
+    page, section 3: k_local < clamp((q_causal_offsets[b] + q_local + 1) //
+    ratio, 0, seqlen_k_b)); keys of segment b start at cu_k[b]."""
+    cq, ck = _i32(cu_q), _i32(cu_k)
+    off = None if q_causal_offsets is None else _i32(q_causal_offsets)
+    if cq.size != ck.size or (off is not None and off.size != cq.size - 1):
+        raise ValueError("cu_q, cu_k and q_causal_offsets disagree on the number of segments")
+    start = np.empty(Tq, np.int32)
+    length = np.empty(Tq, np.int32)
+    rc = _load().oracle_ratio_metadata(_ptr(cq), _ptr(ck), _ptr(off), cq.size - 1, Tq, Tk, int(ratio), _ptr(start),
+                                       _ptr(length))
+    if rc != 0:
+        raise ValueError("cu_q / cu_k are not valid prefix arrays over [0, Tq) / [0, Tk), or ratio < 1")
     return start, length
 
 

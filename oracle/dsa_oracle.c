@@ -69,6 +69,44 @@ int oracle_thd_metadata(const int32_t* cu, int n_docs, int T, int32_t* start,
 }
 
 /* ------------------------------------------------------------------------
+ * Ratio-causal metadata of a compressed-key indexer [P5 section 3,
+ * "ratio-causal mask" and q_causal_offsets; section 4, compact addressing
+ * clamps rows that extend past the key prefix].  Query segment b occupies
+ * rows cu_q[b] .. cu_q[b+1]-1 and its compressed keys rows cu_k[b] ..
+ * cu_k[b+1]-1 (a prefix of the segment's compressed timeline, from
+ * compressed column 0).  Local query row q (q = t - cu_q[b]) sees key
+ * column j iff
+ *     j < clamp( floor((q_off[b] + q + 1) / ratio), 0, cu_k[b+1] - cu_k[b] ),
+ * q_off[b] being the global position of the segment's first query (0 when
+ * q_off is NULL).  start[t] = cu_k[b] and len[t] = that bound.
+ * Returns 0, or -1 when cu_q / cu_k are not valid prefix arrays over
+ * [0, Tq) / [0, Tk) or ratio < 1.
+ * ------------------------------------------------------------------------ */
+int oracle_ratio_metadata(const int32_t* cu_q, const int32_t* cu_k,
+                          const int32_t* q_off, int n_docs, int Tq, int Tk,
+                          int ratio, int32_t* start, int32_t* len) {
+  if (n_docs < 1 || ratio < 1 || cu_q[0] != 0 || cu_q[n_docs] != Tq ||
+      cu_k[0] != 0 || cu_k[n_docs] != Tk)
+    return -1;
+  for (int b = 0; b < n_docs; ++b)
+    if (cu_q[b + 1] < cu_q[b] || cu_k[b + 1] < cu_k[b]) return -1;
+  for (int b = 0; b < n_docs; ++b) {
+    const int64_t seqlen_k = cu_k[b + 1] - cu_k[b];
+    const int64_t off = q_off ? q_off[b] : 0;
+    for (int t = cu_q[b]; t < cu_q[b + 1]; ++t) {
+      const int64_t num = off + (t - cu_q[b]) + 1;
+      /* floor division (num may be negative for a negative offset) */
+      int64_t bound = num >= 0 ? num / ratio : -((-num + ratio - 1) / ratio);
+      if (bound < 0) bound = 0;
+      if (bound > seqlen_k) bound = seqlen_k;
+      start[t] = cu_k[b];
+      len[t] = (int32_t)bound;
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
  * Lightning-indexer scores [P5 section 3; P1 cudnn_indexer_topk].
  * For one query row with inputs qi_row [Hi, d], w_row [Hi] and keys
  * ki [*, d]:

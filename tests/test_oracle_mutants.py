@@ -46,6 +46,13 @@ MUTANTS = {
     "compact_keeps_key_count": ("(int64_t)id < key_count", "(int64_t)id <= key_count"),
     "pack_wrong_batch_stride": ("v = b * S + id;", "v = b * W + id;"),
     "metadata_len_off_by_one": ("len[t] = t - cu[b] + 1;", "len[t] = t - cu[b];"),
+    "ratio_drop_plus_one": ("const int64_t num = off + (t - cu_q[b]) + 1;",
+                            "const int64_t num = off + (t - cu_q[b]);"),
+    "ratio_ceil_not_floor": ("int64_t bound = num >= 0 ? num / ratio : -((-num + ratio - 1) / ratio);",
+                             "int64_t bound = num >= 0 ? (num + ratio - 1) / ratio : -((-num) / ratio);"),
+    "ratio_no_clamp_to_prefix": ("if (bound > seqlen_k) bound = seqlen_k;", ""),
+    "ratio_ignores_offset": ("const int64_t off = q_off ? q_off[b] : 0;", "const int64_t off = 0;"),
+    "ratio_start_from_queries": ("start[t] = cu_k[b];", "start[t] = cu_q[b];"),
 }
 
 

@@ -42,6 +42,59 @@ def test_metadata_rejects_invalid(cu, T):
 
 
 # ----------------------------------------------------------------- indexer
+def test_ratio_metadata_golden():
+    g = _gold("ratio_metadata.json")
+    for c in g["cases"]:
+        s, l = oracle.ratio_metadata(np.array(c["cu_q"]), np.array(c["cu_k"]),
+                                     None if c["q_causal_offsets"] is None else np.array(c["q_causal_offsets"]),
+                                     c["ratio"], c["Tq"], c["Tk"])
+        assert s.tolist() == c["start"] and l.tolist() == c["len"]
+
+
+def test_ratio_metadata_ratio_one_is_thd_metadata():
+    """ratio 1, zero offsets and keys stored like the queries: the plain
+    causal THD metadata."""
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        lens = rng.integers(0, 40, size=rng.integers(1, 6))
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        if T == 0:
+            continue
+        assert [a.tolist() for a in oracle.ratio_metadata(cu, cu, None, 1, T, T)] == \
+            [a.tolist() for a in oracle.thd_metadata(cu, T)]
+
+
+def test_ratio_metadata_brute_force():
+    """Key j of segment b is visible to local row q iff every token it
+    compresses, (j+1)*ratio - 1 at the latest, is at or before the query's
+    global position offset + q, and j is one of the segment's keys."""
+    rng = np.random.default_rng(12)
+    for _ in range(40):
+        nb = int(rng.integers(1, 5))
+        ratio = int(rng.integers(1, 6))
+        lq = rng.integers(0, 30, size=nb)
+        off = rng.integers(-3, 40, size=nb)
+        lk = np.array([max(0, int((o + q) // ratio) + int(rng.integers(-3, 3))) for o, q in zip(off, lq)])
+        cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+        ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+        Tq, Tk = int(cq[-1]), int(ck[-1])
+        s, l = oracle.ratio_metadata(cq, ck, off.astype(np.int32), ratio, Tq, Tk)
+        for b in range(nb):
+            for q in range(int(lq[b])):
+                t = int(cq[b]) + q
+                vis = [j for j in range(int(lk[b])) if (j + 1) * ratio - 1 <= int(off[b]) + q]
+                assert vis == list(range(len(vis))), "the visible keys form a prefix"
+                assert l[t] == len(vis) and s[t] == ck[b], (b, q, ratio, int(off[b]))
+
+
+@pytest.mark.parametrize("cu_q,cu_k,ratio,Tq,Tk", [([0, 4], [0, 2], 0, 4, 2), ([0, 4], [1, 2], 2, 4, 2),
+                                                     ([0, 3, 2], [0, 1, 2], 2, 2, 2), ([0, 4], [0, 3], 2, 4, 2)])
+def test_ratio_metadata_rejects_invalid(cu_q, cu_k, ratio, Tq, Tk):
+    with pytest.raises(ValueError):
+        oracle.ratio_metadata(np.array(cu_q), np.array(cu_k), None, ratio, Tq, Tk)
+
+
 def _rand_bf16_like(rng, shape, lo=-4, hi=4):
     return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
 
