@@ -140,8 +140,9 @@ int dsa_topk_softmax(const float* logits, const int32_t* idx, int T, int k, floa
 int dsa_compact_sort_indices(const int32_t* in, int T, int K, int64_t key_count, int32_t* out,
                              int32_t* lengths, cudaStream_t stream);
 
-/* Workspace bytes that dsa_indexer_topk needs for these shapes (0 on invalid
- * shapes).  Depends on shapes only, never on data. */
+/* Workspace bytes that dsa_indexer_topk (and dsa_indexer_topk_ratio, with
+ * T = Tq) needs for these shapes: 0 when T, Hi, d or s_max is below 1 or k is
+ * outside [1, DSA_MAX_TOPK].  Depends on shapes only, never on data. */
 size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max);
 
 /* Fused indexer + top-k ([cuDNN-DSA] 4: one call, no dense [T, S] score
@@ -176,6 +177,61 @@ int dsa_indexer_topk_ex(const void* qi, const void* ki, const float* w, const in
                         int n_docs, int T, int Hi, int d, int k, int s_max, int32_t* idx,
                         int32_t* topk_length, float* logits, float* softmax, float* lse,
                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* ---- Compressed-key (ratio-causal) indexer ([cuDNN-DSA] 3 Indexer Forward
+ * with ratio and q_causal_offsets; [cuDNN-DSA] 4 for the combined call).
+ * Query segment b holds query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1;
+ * its keys are a compressed prefix, ki rows cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1]-1, starting at compressed column 0.  Local query row q
+ * sees key columns
+ *     j < len = clamp( floor((q_causal_offsets[b] + q + 1) / ratio), 0,
+ *                      cu_seqlens_k[b+1] - cu_seqlens_k[b] ),
+ * q_causal_offsets[b] being the global position of the segment's first
+ * query (all 0 when the pointer is NULL; the pages require offsets >= 0,
+ * a negative one only shortens rows).  ratio = 1, zero offsets and
+ * cu_seqlens_k = cu_seqlens_q give the plain causal form above.
+ * cu_seqlens_q / cu_seqlens_k: int32 [n_docs + 1], device, non-decreasing,
+ * from 0 to Tq / Tk (not checked: the call reads no device data on the host);
+ * q_causal_offsets: int32 [n_docs], device, or NULL. */
+
+/* Per-query-row start (= cu_seqlens_k[b]) and len of the mask above.
+ *   start, len int32 [T] (out).  Errors: DSA_ERR_VALUE for n_docs < 1,
+ *   T < 0, ratio < 1 or NULL pointers (T = 0 is a no-op). */
+int dsa_thd_metadata_ratio(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           const int32_t* q_causal_offsets, int n_docs, int T, int ratio,
+                           int32_t* start, int32_t* len, cudaStream_t stream);
+
+/* Dense scores over the compressed keys:
+ *   scores[t, j] = sum_h w[t, h] * ReLU( qi[t, h, :] . ki[start[t] + j, :] )
+ * for j < min(len[t], s_max), -inf for the other columns below s_max.
+ *   qi bf16 [Tq, Hi, d], ki bf16 [Tk, d], w fp32 [Tq, Hi]; s_max: a host
+ *   bound on the longest row, 1 <= s_max <= Tk (rows are cut at s_max);
+ *   scores fp32 [Tq, ld] (out), ld >= s_max, ld % 4 == 0.
+ * Shapes and errors as dsa_indexer_scores, plus DSA_ERR_VALUE for Tk < 1,
+ * ratio < 1 or NULL cu_seqlens_k. */
+int dsa_indexer_scores_ratio(const void* qi, const void* ki, const float* w,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi,
+                             int d, int ratio, int s_max, float* scores, int64_t ld,
+                             cudaStream_t stream);
+
+/* The combined indexer + top-k over the compressed keys: identical (bit for
+ * bit) to dsa_indexer_scores_ratio followed by dsa_topk with row_start =
+ * start[t] and len = min(len[t], s_max), without the dense matrix.  ids are
+ * global ki rows (start[t] + j), ascending, -1 suffix.
+ *   idx int32 [Tq, k] (out); topk_length int32 [Tq] or NULL (out);
+ *   logits fp32 [Tq, k] or NULL (out, as dsa_indexer_topk_ex); softmax fp32
+ *   [Tq, k] and lse fp32 [Tq] or NULL (out; need logits);
+ *   workspace: dsa_indexer_topk_workspace_size(Tq, Hi, d, k, s_max) bytes,
+ *   256-byte aligned.
+ * Errors: as dsa_indexer_scores_ratio, plus DSA_ERR_WORKSPACE, and
+ * DSA_ERR_UNSUPPORTED for logits with s_max > 65536. */
+int dsa_indexer_topk_ratio(const void* qi, const void* ki, const float* w,
+                           const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                           int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length,
+                           float* logits, float* softmax, float* lse, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
 
 /* The two stages of dsa_indexer_topk as separate calls, for callers that
  * schedule or time them apart ([cuDNN-DSA] "Limitations": the selection

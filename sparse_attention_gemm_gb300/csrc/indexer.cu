@@ -1,8 +1,13 @@
 // indexer.cu -- lightning-indexer scores on tcgen05 (dense and fused top-k).
 //
 // score[t, j] = sum_h w[t, h] * ReLU(qi[t, h, :] . ki[start[t] + j, :])
-// (cuDNN Frontend DSA page, section 3 Indexer Forward, ratio 1; THD shapes of
-// NeMo glm_moe_dsa cudnn_indexer_topk; head weights arrive pre-scaled).
+// for j < len[t] (cuDNN Frontend DSA page, section 3 Indexer Forward; THD
+// shapes of NeMo glm_moe_dsa cudnn_indexer_topk; head weights arrive
+// pre-scaled).  Row geometry (Geom): query segment b holds rows cu_q[b] ..
+// cu_q[b+1]-1 and its keys rows cu_k[b] .. cu_k[b+1]-1 of ki; local row q
+// sees key columns j < clamp((q_off[b] + q + 1) / ratio, 0, keys of b), the
+// section's ratio-causal mask over a compressed key prefix.  The plain causal
+// form is cu_k = cu_q, no offsets, ratio 1 (len = q + 1).
 //
 // Tiling ("swap AB"): one tcgen05.mma computes D[key, (token, head)] for a
 // tile of 128 keys (M) against a block of QB tokens x Hi heads = 256 query
@@ -56,10 +61,20 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kHistWords = 8192;   // 16384 16-bit bin counters shared by the block's rows
 constexpr int kTauUpdateEvery = 512;
 
+// Which keys each query row sees (see the file comment).  Row lengths are
+// also clamped to s_max, the caller's bound on the longest row.
+struct Geom {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* q_off;  // or nullptr: all offsets 0
+  int n_docs;
+  int ratio;
+  int s_max;
+};
+
 struct IndexerParams {
   const float* w;
-  const int32_t* cu;
-  int n_docs;
+  Geom g;
   int T;
   int Hi;
   int d;
@@ -110,25 +125,45 @@ __host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int
   return L;
 }
 
-__device__ __forceinline__ int doc_start(const int32_t* __restrict__ cu, int n_docs, int t) {
+__device__ __forceinline__ int doc_index(const int32_t* __restrict__ cu, int n_docs, int t) {
   int lo = 0, hi = n_docs - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
     if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
   }
-  return __ldg(cu + lo);
+  return lo;
+}
+
+// Number of keys query row t sees; *start receives the row of its first key.
+__device__ __forceinline__ int row_geom(const Geom& g, int t, int* start) {
+  const int b = doc_index(g.cu_q, g.n_docs, t);
+  const int k0 = __ldg(g.cu_k + b);
+  const int64_t nk = __ldg(g.cu_k + b + 1) - k0;
+  const int64_t num = (g.q_off ? static_cast<int64_t>(__ldg(g.q_off + b)) : 0) + (t - __ldg(g.cu_q + b)) + 1;
+  int64_t len = num > 0 ? num / g.ratio : 0;  // a non-positive bound clamps to 0 either way
+  len = len < nk ? len : nk;
+  len = len < g.s_max ? len : g.s_max;
+  *start = k0;
+  return len > 0 ? static_cast<int>(len) : 0;
 }
 
 struct BlockRange {
   int t0, t1, kt0, kt1;
 };
 
+// Key tiles of a block of query rows: from the first row's first key to the
+// last row's last key (both ends grow with the row, within and across
+// segments); kt1 < kt0 when no row of the block sees a key.
 __device__ __forceinline__ BlockRange block_range(const IndexerParams& p, int blk) {
   BlockRange r;
   r.t0 = blk * p.qb;
   r.t1 = min(r.t0 + p.qb, p.T);
-  r.kt0 = doc_start(p.cu, p.n_docs, r.t0) / kKeyTile;
-  r.kt1 = (r.t1 - 1) / kKeyTile;
+  int s0, s1;
+  row_geom(p.g, r.t0, &s0);
+  const int l1 = row_geom(p.g, r.t1 - 1, &s1);
+  r.kt0 = s0 / kKeyTile;
+  const int last = s1 + l1;  // one past the block's last key
+  r.kt1 = last > r.kt0 * kKeyTile ? (last - 1) / kKeyTile : r.kt0 - 1;
   return r;
 }
 
@@ -416,9 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (et < p.qb) {
         const int t = br.t0 + et;
         if (t < p.T) {
-          const int s = doc_start(p.cu, p.n_docs, t);
+          int s;
+          tok_len[et] = row_geom(p.g, t, &s);
           tok_start[et] = s;
-          tok_len[et] = t - s + 1;
         } else {
           tok_start[et] = INT_MAX;
           tok_len[et] = 0;
@@ -468,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int r = half * tok_per_half + cl / HI;
               const int t = br.t0 + r;
               const int st = tok_start[r];
-              const bool valid = (s_key >= st) && (s_key <= t) && (t < p.T);
+              const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(tok_len[r]);
               if (!FUSED) {
                 if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
@@ -608,14 +643,14 @@ struct SegmentedPairSrc {
 
 // Stage 2 of the fused path: exact top-k of each row's candidates.
 __global__ void __launch_bounds__(dsa::kTopkThreads)
-    fused_select_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint2* cand,
+    fused_select_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
                         const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
                         uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem_raw2[];
   dsa::TopkShared& S = *reinterpret_cast<dsa::TopkShared*>(smem_raw2);
   const int t = blockIdx.x;
-  const int st = doc_start(cu, n_docs, t);
-  const int len = t - st + 1;
+  int st;
+  const int len = row_geom(g, t, &st);
   int32_t* out = idx + static_cast<int64_t>(t) * k;
   if (len <= k) {
     for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < len ? st + j : -1;
@@ -712,7 +747,7 @@ __device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) 
 }
 
 __global__ void __launch_bounds__(kSelThreads, 1)
-    fused_select_fast_kernel(const int32_t* __restrict__ cu, int n_docs, int T, int k, const uint2* cand,
+    fused_select_fast_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
                              const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
                              float* logits, uint32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_sel[];
@@ -739,10 +774,10 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     return over;
   };
   auto row_len = [&](int r, int* st) {
-    const int t = T - 1 - r;
-    const int s0 = doc_start(cu, n_docs, t);
+    int s0;
+    const int len = row_geom(g, T - 1 - r, &s0);
     if (st) *st = s0;
-    return t - s0 + 1;
+    return len;
   };
   // thread 0: the copy of row r's segments into the staging buffer
   const uint64_t once = dsa::l2_policy_evict_first();
@@ -1007,25 +1042,47 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   }
 }
 
-int validate_indexer(const void* qi, const void* ki, const float* w, const int32_t* cu, int n_docs, int T, int Hi,
-                     int d, int s_max, const char* fn) {
-  if (!qi || !ki || !w || !cu) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL input pointer", fn);
-  if (n_docs < 1 || T < 1) return dsa::set_error(DSA_ERR_VALUE, "%s: need n_docs >= 1 and T >= 1", fn);
+int validate_common(const void* qi, const void* ki, const float* w, int n_docs, int Tq, int Hi, int d,
+                    const char* fn) {
+  if (!qi || !ki || !w) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL input pointer", fn);
+  if (n_docs < 1 || Tq < 1) return dsa::set_error(DSA_ERR_VALUE, "%s: need n_docs >= 1 and T >= 1", fn);
   if (d != 64 && d != 128) return dsa::set_error(DSA_ERR_VALUE, "%s: d must be 64 or 128 (got %d)", fn, d);
   if (Hi != 8 && Hi != 16 && Hi != 32 && Hi != 64)
     return dsa::set_error(DSA_ERR_VALUE, "%s: Hi must be 8, 16, 32 or 64 (got %d)", fn, Hi);
-  if (s_max < 1 || s_max > T) return dsa::set_error(DSA_ERR_VALUE, "%s: need 1 <= s_max <= T", fn);
   if (!dsa::aligned(qi, 16) || !dsa::aligned(ki, 16))
     return dsa::set_error(DSA_ERR_VALUE, "%s: qi and ki must be 16-byte aligned", fn);
-  if (static_cast<int64_t>(T) * Hi > INT_MAX) return dsa::set_error(DSA_ERR_VALUE, "%s: T*Hi too large", fn);
+  if (static_cast<int64_t>(Tq) * Hi > INT_MAX) return dsa::set_error(DSA_ERR_VALUE, "%s: T*Hi too large", fn);
   return DSA_OK;
 }
 
-int make_maps(const void* qi, const void* ki, int T, int Hi, int d, CUtensorMap* mq, CUtensorMap* mk) {
-  int rc = dsa::encode_tensor_map_2d(mq, qi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, static_cast<uint64_t>(T) * Hi,
+// The plain causal THD form: keys stored like the queries, ratio 1.
+int validate_indexer(const void* qi, const void* ki, const float* w, const int32_t* cu, int n_docs, int T, int Hi,
+                     int d, int s_max, const char* fn) {
+  int rc = validate_common(qi, ki, w, n_docs, T, Hi, d, fn);
+  if (rc != DSA_OK) return rc;
+  if (!cu) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL cu_seqlens", fn);
+  if (s_max < 1 || s_max > T) return dsa::set_error(DSA_ERR_VALUE, "%s: need 1 <= s_max <= T", fn);
+  return DSA_OK;
+}
+
+// The ratio-causal form over a compressed key prefix.
+int validate_ratio(const void* qi, const void* ki, const float* w, const int32_t* cu_q, const int32_t* cu_k,
+                   int n_docs, int Tq, int Tk, int Hi, int d, int ratio, int s_max, const char* fn) {
+  int rc = validate_common(qi, ki, w, n_docs, Tq, Hi, d, fn);
+  if (rc != DSA_OK) return rc;
+  if (!cu_q || !cu_k) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL cu_seqlens_q or cu_seqlens_k", fn);
+  if (Tk < 1 || ratio < 1) return dsa::set_error(DSA_ERR_VALUE, "%s: need Tk >= 1 and ratio >= 1", fn);
+  if (s_max < 1 || s_max > Tk) return dsa::set_error(DSA_ERR_VALUE, "%s: need 1 <= s_max <= Tk", fn);
+  return DSA_OK;
+}
+
+Geom plain_geom(const int32_t* cu, int n_docs, int s_max) { return Geom{cu, cu, nullptr, n_docs, 1, s_max}; }
+
+int make_maps(const void* qi, const void* ki, int Tq, int Tk, int Hi, int d, CUtensorMap* mq, CUtensorMap* mk) {
+  int rc = dsa::encode_tensor_map_2d(mq, qi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, static_cast<uint64_t>(Tq) * Hi,
                                      static_cast<uint64_t>(d) * 2, 64, kNRows, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != DSA_OK) return rc;
-  return dsa::encode_tensor_map_2d(mk, ki, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, T, static_cast<uint64_t>(d) * 2, 64,
+  return dsa::encode_tensor_map_2d(mk, ki, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, Tk, static_cast<uint64_t>(d) * 2, 64,
                                    kKeyTile, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -1070,6 +1127,27 @@ int fused_compact(int s_max, int k) { return fused_whole(s_max) > fused_bound(k)
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Dense scores (arguments already validated).
+int run_dense(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d,
+              float* scores, int64_t ld, int sms, cudaStream_t stream) {
+  CUtensorMap mq, mk;
+  int rc = make_maps(qi, ki, Tq, Tk, Hi, d, &mq, &mk);
+  if (rc != DSA_OK) return rc;
+  IndexerParams p{};
+  p.w = w;
+  p.g = g;
+  p.T = Tq;
+  p.Hi = Hi;
+  p.d = d;
+  p.qb = kNRows / Hi;
+  p.nblocks = (Tq + p.qb - 1) / p.qb;
+  p.scores = scores;
+  p.ld = ld;
+  p.s_max = g.s_max;
+  p.status = dsa::device_status_ptr();
+  return launch_indexer<0>(mq, mk, p, sms, stream);
+}
+
 }  // namespace
 
 extern "C" int dsa_indexer_scores(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens,
@@ -1083,27 +1161,29 @@ extern "C" int dsa_indexer_scores(const void* qi, const void* ki, const float* w
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  CUtensorMap mq, mk;
-  rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
+  return run_dense(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, scores, ld, sms, stream);
+}
+
+extern "C" int dsa_indexer_scores_ratio(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens_q,
+                                        const int32_t* cu_seqlens_k, const int32_t* q_causal_offsets, int n_docs,
+                                        int Tq, int Tk, int Hi, int d, int ratio, int s_max, float* scores, int64_t ld,
+                                        cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_ratio(qi, ki, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                          "dsa_indexer_scores_ratio");
   if (rc != DSA_OK) return rc;
-  IndexerParams p{};
-  p.w = w;
-  p.cu = cu_seqlens;
-  p.n_docs = n_docs;
-  p.T = T;
-  p.Hi = Hi;
-  p.d = d;
-  p.qb = kNRows / Hi;
-  p.nblocks = (T + p.qb - 1) / p.qb;
-  p.scores = scores;
-  p.ld = ld;
-  p.s_max = s_max;
-  p.status = dsa::device_status_ptr();
-  return launch_indexer<0>(mq, mk, p, sms, stream);
+  if (!scores) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_ratio: NULL scores");
+  if (ld < s_max || ld % 4 != 0)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_ratio: need ld >= s_max, ld % 4 == 0");
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_dense(qi, ki, w, g, Tq, Tk, Hi, d, scores, ld, sms, stream);
 }
 
 extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
-  if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1 || s_max > T) return 0;
+  if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1) return 0;
   const size_t cap = static_cast<size_t>(fused_cap(s_max, k));
   return align256(static_cast<size_t>(T) * 16) + align256(static_cast<size_t>(T) * cap * 8);
 }
@@ -1119,26 +1199,25 @@ int check_workspace(int T, int Hi, int d, int k, int s_max, const void* workspac
 }
 
 // Stage 1 launch (arguments already validated).
-int run_candidates(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs, int T,
-                   int Hi, int d, int k, int s_max, void* workspace, int sms, cudaStream_t stream) {
+int run_candidates(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d, int k,
+                   void* workspace, int sms, cudaStream_t stream) {
   CUtensorMap mq, mk;
-  int rc = make_maps(qi, ki, T, Hi, d, &mq, &mk);
+  int rc = make_maps(qi, ki, Tq, Tk, Hi, d, &mq, &mk);
   if (rc != DSA_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   IndexerParams p{};
   p.w = w;
-  p.cu = cu_seqlens;
-  p.n_docs = n_docs;
-  p.T = T;
+  p.g = g;
+  p.T = Tq;
   p.Hi = Hi;
   p.d = d;
   p.qb = kNRows / Hi;
-  p.nblocks = (T + p.qb - 1) / p.qb;
-  p.s_max = s_max;
+  p.nblocks = (Tq + p.qb - 1) / p.qb;
+  p.s_max = g.s_max;
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
-  p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(T) * 16));
-  p.cap = fused_cap(s_max, k);
-  p.compact = fused_compact(s_max, k);
+  p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(Tq) * 16));
+  p.cap = fused_cap(g.s_max, k);
+  p.compact = fused_compact(g.s_max, k);
   p.k = k;
   int bins = 2 * kHistWords / p.qb;
   int bits = 0;
@@ -1152,30 +1231,41 @@ int run_candidates(const void* qi, const void* ki, const float* w, const int32_t
 // True when stage 2 runs its fast form (the only form that can also write logits).
 bool select_is_fast(int s_max, int k) { return s_max <= kSelMaxLen && fused_cap(s_max, k) <= kSelMax; }
 
-int run_select(const int32_t* cu_seqlens, int n_docs, int T, int k, int s_max, void* workspace, int32_t* idx,
-               int32_t* topk_length, float* logits, int sms, cudaStream_t stream) {
-  const int cap = fused_cap(s_max, k);
+int run_select(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32_t* topk_length, float* logits,
+               int sms, cudaStream_t stream) {
+  const int cap = fused_cap(g.s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
   const uint2* cand = reinterpret_cast<const uint2*>(ws + align256(static_cast<size_t>(T) * 16));
   uint32_t* status = dsa::device_status_ptr();
-  if (select_is_fast(s_max, k)) {
+  if (select_is_fast(g.s_max, k)) {
     const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
     if (cudaFuncSetAttribute(fused_select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return dsa::launch_error("fused_select_fast_kernel smem attribute");
     const int grid = T < sms ? T : sms;
-    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, cand, cand_cnt, cap, idx,
-                                                                  topk_length, logits, status);
+    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length,
+                                                                  logits, status);
     return dsa::launch_error("fused_select_fast_kernel");
   }
   const size_t smem = sizeof(dsa::TopkShared);
   if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return dsa::launch_error("fused_select_kernel smem attribute");
-  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(cu_seqlens, n_docs, T, k, cand, cand_cnt, cap, idx,
-                                                              topk_length, status);
+  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length, status);
   return dsa::launch_error("fused_select_kernel");
+}
+
+// Both stages plus the optional outputs of the pages' combined call (arguments
+// already validated; logits may be NULL only when softmax and lse are).
+int run_fused(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d, int k,
+              int32_t* idx, int32_t* topk_length, float* logits, float* softmax, float* lse, void* workspace,
+              int sms, cudaStream_t stream) {
+  int rc = run_candidates(qi, ki, w, g, Tq, Tk, Hi, d, k, workspace, sms, stream);
+  if (rc != DSA_OK) return rc;
+  rc = run_select(g, Tq, k, workspace, idx, topk_length, logits, sms, stream);
+  if (rc != DSA_OK || (!softmax && !lse)) return rc;
+  return dsa_topk_softmax(logits, idx, Tq, k, softmax, lse, stream);
 }
 
 }  // namespace
@@ -1191,7 +1281,7 @@ extern "C" int dsa_indexer_candidates(const void* qi, const void* ki, const floa
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
+  return run_candidates(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, workspace, sms, stream);
 }
 
 extern "C" int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int T, int Hi, int d, int k, int s_max,
@@ -1207,8 +1297,8 @@ extern "C" int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_select(cu_seqlens, n_docs, T, k, s_max, const_cast<void*>(workspace), idx, topk_length, nullptr, sms,
-                    stream);
+  return run_select(plain_geom(cu_seqlens, n_docs, s_max), T, k, const_cast<void*>(workspace), idx, topk_length,
+                    nullptr, sms, stream);
 }
 
 extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens, int n_docs,
@@ -1223,9 +1313,8 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  rc = run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
-  if (rc != DSA_OK) return rc;
-  return run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, nullptr, sms, stream);
+  return run_fused(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, idx, topk_length, nullptr,
+                   nullptr, nullptr, workspace, sms, stream);
 }
 
 // The fused call with the outputs that come with the indices on the pages'
@@ -1247,11 +1336,35 @@ extern "C" int dsa_indexer_topk_ex(const void* qi, const void* ki, const float* 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  rc = run_candidates(qi, ki, w, cu_seqlens, n_docs, T, Hi, d, k, s_max, workspace, sms, stream);
+  return run_fused(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, idx, topk_length, logits,
+                   softmax, lse, workspace, sms, stream);
+}
+
+// The combined call over a compressed key prefix with the ratio-causal mask
+// (cuDNN DSA page, sections 3 and 4): ids are global key rows cu_k[b] + j.
+extern "C" int dsa_indexer_topk_ratio(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, const int32_t* q_causal_offsets, int n_docs, int Tq,
+                                      int Tk, int Hi, int d, int ratio, int k, int s_max, int32_t* idx,
+                                      int32_t* topk_length, float* logits, float* softmax, float* lse,
+                                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_ratio(qi, ki, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                          "dsa_indexer_topk_ratio");
   if (rc != DSA_OK) return rc;
-  rc = run_select(cu_seqlens, n_docs, T, k, s_max, workspace, idx, topk_length, logits, sms, stream);
-  if (rc != DSA_OK || (!softmax && !lse)) return rc;
-  return dsa_topk_softmax(logits, idx, T, k, softmax, lse, stream);
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_ratio: NULL idx");
+  if ((softmax || lse) && !logits)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_ratio: softmax and lse need logits");
+  rc = check_workspace(Tq, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_topk_ratio");
+  if (rc != DSA_OK) return rc;
+  if (logits && !select_is_fast(s_max, k))
+    return dsa::set_error(DSA_ERR_UNSUPPORTED,
+                          "dsa_indexer_topk_ratio: logits need rows of at most %d columns (s_max = %d)", kSelMaxLen,
+                          s_max);
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_fused(qi, ki, w, g, Tq, Tk, Hi, d, k, idx, topk_length, logits, softmax, lse, workspace, sms, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -33,6 +33,24 @@ __global__ void thd_metadata_kernel(const int32_t* __restrict__ cu, int n_docs, 
   len[t] = t - s + 1;
 }
 
+// cuDNN DSA page, section 3 Indexer Forward, ratio-causal mask: query segment
+// b's keys start at cu_k[b]; local row q sees
+// clamp((q_off[b] + q + 1) / ratio, 0, cu_k[b+1] - cu_k[b]) of them.
+__global__ void ratio_metadata_kernel(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ cu_k,
+                                      const int32_t* __restrict__ q_off, int n_docs, int T, int ratio,
+                                      int32_t* __restrict__ start, int32_t* __restrict__ len) {
+  int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int b = doc_of(cu_q, n_docs, t);
+  const int k0 = __ldg(cu_k + b);
+  const int64_t nk = __ldg(cu_k + b + 1) - k0;
+  const int64_t num = (q_off ? static_cast<int64_t>(__ldg(q_off + b)) : 0) + (t - __ldg(cu_q + b)) + 1;
+  int64_t n = num > 0 ? num / ratio : 0;
+  n = n < nk ? n : nk;
+  start[t] = k0;
+  len[t] = n > 0 ? static_cast<int32_t>(n) : 0;
+}
+
 // NeMo qwen3_8_flash_next.cudnn_qsa _pack_indices: batch-local ids -> packed
 // coordinates b*S + id; invalid ids and the width padding become -1.
 __global__ void pack_routes_kernel(const int32_t* __restrict__ routes, int S, int W, int Wp, int64_t n_out,
@@ -89,6 +107,22 @@ extern "C" int dsa_thd_metadata(const int32_t* cu_seqlens, int n_docs, int T, in
   if (T == 0) return DSA_OK;
   thd_metadata_kernel<<<(T + 255) / 256, 256, 0, stream>>>(cu_seqlens, n_docs, T, start, len);
   return dsa::launch_error("thd_metadata_kernel");
+}
+
+extern "C" int dsa_thd_metadata_ratio(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                      const int32_t* q_causal_offsets, int n_docs, int T, int ratio, int32_t* start,
+                                      int32_t* len, cudaStream_t stream) {
+  dsa::clear_error();
+  if (n_docs < 1 || T < 0 || ratio < 1)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_thd_metadata_ratio: need n_docs >= 1, T >= 0, ratio >= 1");
+  if (!cu_seqlens_q || !cu_seqlens_k || (T > 0 && (!start || !len)))
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_thd_metadata_ratio: NULL pointer");
+  int rc = dsa::check_device(nullptr);
+  if (rc != DSA_OK) return rc;
+  if (T == 0) return DSA_OK;
+  ratio_metadata_kernel<<<(T + 255) / 256, 256, 0, stream>>>(cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, T,
+                                                             ratio, start, len);
+  return dsa::launch_error("ratio_metadata_kernel");
 }
 
 extern "C" int dsa_pack_routes(const int32_t* routes, int B, int S, int W, int32_t* out, cudaStream_t stream) {

@@ -56,6 +56,9 @@ _SIGNATURES = {
     "dsa_sparse_attn_fwd": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, P], I),
     "dsa_sparse_attn_fwd_ex": ([P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, I, P, P], I),
     "dsa_pack_routes": ([P, I, I, I, P, P], I),
+    "dsa_thd_metadata_ratio": ([P, P, P, I, I, I, P, P, P], I),
+    "dsa_indexer_scores_ratio": ([P, P, P, P, P, P, I, I, I, I, I, I, I, P, I64, P], I),
+    "dsa_indexer_topk_ratio": ([P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
 }
 
 
@@ -130,6 +133,73 @@ def thd_metadata(cu_seqlens: torch.Tensor, T: int):
     _check("dsa_thd_metadata", lib().dsa_thd_metadata(_p(cu_seqlens), cu_seqlens.numel() - 1, T, _p(start),
                                                       _p(length), _stream()))
     return start, length
+
+
+def thd_metadata_ratio(cu_seqlens_q, cu_seqlens_k, q_causal_offsets, ratio: int, T: int):
+    """start, len [T] of the ratio-causal compressed-key mask."""
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    if q_causal_offsets is not None:
+        _need(q_causal_offsets, "q_causal_offsets", torch.int32, 1)
+    start = torch.empty(T, dtype=torch.int32, device=cu_seqlens_q.device)
+    length = torch.empty(T, dtype=torch.int32, device=cu_seqlens_q.device)
+    _check("dsa_thd_metadata_ratio",
+           lib().dsa_thd_metadata_ratio(_p(cu_seqlens_q), _p(cu_seqlens_k), _p(q_causal_offsets),
+                                        cu_seqlens_q.numel() - 1, T, int(ratio), _p(start), _p(length), _stream()))
+    return start, length
+
+
+def _ratio_inputs(qi, ki, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets):
+    _need(qi, "qi", torch.bfloat16, 3)
+    _need(ki, "ki", torch.bfloat16, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    if q_causal_offsets is not None:
+        _need(q_causal_offsets, "q_causal_offsets", torch.int32, 1)
+    if cu_seqlens_k.numel() != cu_seqlens_q.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    return qi.shape[0], ki.shape[0], qi.shape[1], qi.shape[2]
+
+
+def indexer_scores_ratio(qi, ki, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets, ratio: int, s_max: int,
+                         ld: int | None = None, out=None):
+    """Dense compressed-key indexer scores fp32 [Tq, ld] under the ratio-causal mask."""
+    Tq, Tk, Hi, d = _ratio_inputs(qi, ki, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets)
+    ld = ld or (s_max + 3) // 4 * 4
+    if out is None:
+        out = torch.empty((Tq, ld), dtype=torch.float32, device=qi.device)
+    _check("dsa_indexer_scores_ratio",
+           lib().dsa_indexer_scores_ratio(_p(qi), _p(ki), _p(w), _p(cu_seqlens_q), _p(cu_seqlens_k),
+                                          _p(q_causal_offsets), cu_seqlens_q.numel() - 1, Tq, Tk, Hi, d, int(ratio),
+                                          s_max, _p(out), ld, _stream()))
+    return out
+
+
+def indexer_topk_ratio(qi, ki, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets, ratio: int, k: int, s_max: int,
+                       want_logits: bool = False, want_softmax: bool = False, want_lse: bool = False, workspace=None):
+    """Combined compressed-key indexer + top-k: dict(idx [Tq, k] ascending
+    global key rows, topk_length[, logits][, softmax][, lse])."""
+    Tq, Tk, Hi, d = _ratio_inputs(qi, ki, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets)
+    dev = qi.device
+    if workspace is None:
+        workspace = torch.empty(indexer_topk_workspace_size(Tq, Hi, d, k, s_max), dtype=torch.uint8, device=dev)
+    want_logits = want_logits or want_softmax or want_lse
+    idx = torch.empty((Tq, k), dtype=torch.int32, device=dev)
+    tl = torch.empty(Tq, dtype=torch.int32, device=dev)
+    logits = torch.empty((Tq, k), dtype=torch.float32, device=dev) if want_logits else None
+    sm = torch.empty((Tq, k), dtype=torch.float32, device=dev) if want_softmax else None
+    lse = torch.empty(Tq, dtype=torch.float32, device=dev) if want_lse else None
+    _check("dsa_indexer_topk_ratio",
+           lib().dsa_indexer_topk_ratio(_p(qi), _p(ki), _p(w), _p(cu_seqlens_q), _p(cu_seqlens_k),
+                                        _p(q_causal_offsets), cu_seqlens_q.numel() - 1, Tq, Tk, Hi, d, int(ratio), k,
+                                        s_max, _p(idx), _p(tl), _p(logits), _p(sm), _p(lse), _p(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream()))
+    res = {"idx": idx, "topk_length": tl}
+    for name, t in (("logits", logits), ("softmax", sm), ("lse", lse)):
+        if t is not None:
+            res[name] = t
+    return res
 
 
 def indexer_scores(qi, ki, w, cu_seqlens, s_max: int, ld: int | None = None, out=None):

@@ -29,6 +29,13 @@ Recipe (every draw is reproducible and addressable by row):
   p's own block as a causal tail ``4*(p//4) .. p`` padded with -1, then
   groups of -1 up to the route width.  Row b uses its own generator
   ``SeedSequence([s, FIELD_ROUTES, b])`` and draws tokens in order.
+* Compressed-key indexer workloads: query segments as above; segment b's
+  causal offset (the global position of its first query, as for a later
+  chunk of a longer document) is 0 or uniform in [1, 16384], each with
+  probability 1/2, from ``SeedSequence([s, FIELD_OFFSETS, 0])``; the segment
+  holds ``ceil((offset + queries) / ratio)`` compressed key rows (every block
+  of ``ratio`` tokens up to its last query, the last one possibly partial).
+  Indexer q/k/w as for the bf16 workloads, ki with that many rows.
 """
 from __future__ import annotations
 
@@ -50,6 +57,7 @@ FIELD_KI = 6
 FIELD_W = 7
 FIELD_DOCS = 8
 FIELD_ROUTES = 9
+FIELD_OFFSETS = 10
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -104,6 +112,9 @@ class Workload:
     B: int = 0                        # GQA route workload: batch rows
     S: int = 0                        # GQA route workload: sequence length
     W: int = 0                        # GQA route workload: route width
+    ratio: int = 1                    # compressed-key indexer: tokens per key
+    cu_k: np.ndarray | None = None    # compressed-key indexer: key segment bounds
+    q_offsets: np.ndarray | None = None  # compressed-key indexer: causal offset per segment
 
     # ---- derived sizes -------------------------------------------------
     @property
@@ -112,7 +123,14 @@ class Workload:
 
     @property
     def s_max(self) -> int:
-        return int(np.max(np.diff(self.cu_seqlens)))
+        """Longest key segment (a row never sees more keys than its segment holds)."""
+        cu = self.cu_seqlens if self.cu_k is None else self.cu_k
+        return int(np.max(np.diff(cu)))
+
+    @property
+    def Tk(self) -> int:
+        """Indexer key rows."""
+        return self.T if self.cu_k is None else int(self.cu_k[-1])
 
     # ---- chunked generation ----------------------------------------------
     def _rows(self, fid: int, n_total: int, row_elems: int, make, rows=None, dtype=np.uint16):
@@ -185,9 +203,9 @@ class Workload:
         return a.reshape(-1, self.Hi, self.d)
 
     def ki_bits(self) -> np.ndarray:
-        """Indexer key, bf16 bits [T, d]."""
+        """Indexer key, bf16 bits [Tk, d]."""
         make = self._int_bf16(-4, 4) if self.indexer_kind == "int" else self._normal_bf16(self.sigma_index)
-        return self._rows(FIELD_KI, self.T, self.d, make)
+        return self._rows(FIELD_KI, self.Tk, self.d, make)
 
     def w(self, rows=None) -> np.ndarray:
         """Pre-scaled indexer head weights, fp32 [n, Hi]."""
@@ -266,4 +284,28 @@ def gqa_routes() -> Workload:
                     indexer_kind="none", B=B, S=S, W=256)
 
 
-ALL = {1: tiny, 2: single_doc_4k, 3: thd_16k, 4: long_64k, 5: gqa_routes}
+def _compressed(name: str, seed: int, lens, ratio: int, K: int, offsets=None) -> Workload:
+    lens = np.asarray(lens, np.int64)
+    if offsets is None:
+        rng = _rng(seed, FIELD_OFFSETS, 0)
+        offsets = np.where(rng.random(lens.size) < 0.5, 0, rng.integers(1, 16385, size=lens.size))
+    offsets = np.asarray(offsets, np.int64)
+    nk = (offsets + lens + ratio - 1) // ratio
+    return Workload(name=name, seed=seed, T=int(lens.sum()), H=64, Dqk=576, Dv=512, K=K,
+                    scale=1.0 / math.sqrt(576.0), Hi=64, d=128, cu_seqlens=_cu(lens), fused=True, ratio=ratio,
+                    cu_k=_cu(nk), q_offsets=offsets.astype(np.int32))
+
+
+def compressed_thd_8k() -> Workload:
+    """Compressed-key indexer: T=8192 packed query segments (lengths U[512,4096]),
+    causal offsets 0 or U[1,16384], ratio 4, Hi=64, d=128, top-k 512, seed 6."""
+    return _compressed("compressed_thd_T8192_r4_k512", 6, _doc_lengths(6, 8192, 512, 4096), 4, 512)
+
+
+def compressed_64k() -> Workload:
+    """Compressed-key indexer: T=65536 queries in one segment, offset 0, ratio 4
+    (16384 keys), Hi=64, d=128, top-k 2048, seed 7."""
+    return _compressed("compressed_T65536_r4_k2048", 7, [65536], 4, 2048, offsets=[0])
+
+
+ALL = {1: tiny, 2: single_doc_4k, 3: thd_16k, 4: long_64k, 5: gqa_routes, 6: compressed_thd_8k, 7: compressed_64k}

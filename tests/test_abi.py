@@ -21,7 +21,7 @@ def test_header_declares_the_hot_path():
     for must in ["dsa_thd_metadata", "dsa_indexer_scores", "dsa_topk", "dsa_compact_sort_indices",
                  "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_topk_ex", "dsa_topk_softmax",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex", "dsa_forward_host",
-                 "dsa_pack_routes",
+                 "dsa_pack_routes", "dsa_thd_metadata_ratio", "dsa_indexer_scores_ratio", "dsa_indexer_topk_ratio",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
 
@@ -80,6 +80,19 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, NULL, NULL, NULL),
     lambda L: L.dsa_select_candidates(NULL, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
     lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
+    lambda L: L.dsa_thd_metadata_ratio(FAKE, FAKE, NULL, 1, 10, 0, FAKE, FAKE, NULL),
+    lambda L: L.dsa_thd_metadata_ratio(FAKE, NULL, NULL, 1, 10, 4, FAKE, FAKE, NULL),
+    lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 0, 32, FAKE, 32, NULL),
+    lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 4, 33, FAKE, 36, NULL),
+    lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, NULL, NULL, 1, 128, 32, 64, 128, 4, 32, FAKE, 32, NULL),
+    lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 0, 64, 128, 4, 1, FAKE, 4, NULL),
+    lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 4, 32, FAKE, 30, NULL),
+    lambda L: L.dsa_indexer_topk_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 4, 0, 32, FAKE, NULL,
+                                       NULL, NULL, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_indexer_topk_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 4, 16, 32, FAKE, NULL,
+                                       NULL, FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_indexer_topk_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 4, 16, 32, NULL, NULL,
+                                       NULL, NULL, NULL, FAKE, 1 << 30, NULL),
 ])
 def test_invalid_arguments_are_rejected_before_launch(lib, call):
     assert call(lib) == ops.DSA_ERR_VALUE
@@ -94,6 +107,13 @@ def test_workspace_errors(lib):
     assert rc == ops.DSA_ERR_WORKSPACE
     rc = lib.dsa_indexer_topk(FAKE, FAKE, FAKE, FAKE, 1, 4096, 64, 128, 2048, 4096, FAKE, NULL,
                               ctypes.c_void_p(4096 + 16), need, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+
+
+def test_ratio_call_checks_the_workspace(lib):
+    need = lib.dsa_indexer_topk_workspace_size(4096, 64, 128, 512, 1024)
+    rc = lib.dsa_indexer_topk_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 4096, 1024, 64, 128, 4, 512, 1024, FAKE,
+                                    NULL, NULL, NULL, NULL, FAKE, need - 1, NULL)
     assert rc == ops.DSA_ERR_WORKSPACE
 
 

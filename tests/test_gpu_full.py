@@ -90,6 +90,48 @@ def _indexer_workload_check(wl, n_sample, seed):
     return idx, tl, rows
 
 
+def _ratio_workload_check(wl, n_sample, seed):
+    """Compressed-key workloads, at full size in the bench's launch
+    configuration: the combined call equals dense scores + top-k on every row
+    (bit-exact, logits included); sampled rows against the oracle."""
+    Tq, Tk, K = wl.T, wl.Tk, wl.K
+    qi, ki, w = wl.qi_bits(), wl.ki_bits(), wl.w()
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(wl.cu_seqlens), dev(wl.cu_k), dev(wl.q_offsets))
+    start, length = oracle.ratio_metadata(wl.cu_seqlens, wl.cu_k, wl.q_offsets, wl.ratio, Tq, Tk)
+    gs, gl = ops.thd_metadata_ratio(a[3], a[4], a[5], wl.ratio, Tq)
+    assert np.array_equal(gs.cpu().numpy(), start) and np.array_equal(gl.cpu().numpy(), length)
+    res = ops.indexer_topk_ratio(*a, wl.ratio, K, wl.s_max, want_logits=True)
+    idx, tl = res["idx"], res["topk_length"]
+    scores = ops.indexer_scores_ratio(*a, wl.ratio, wl.s_max)
+    ui, ut, _ = ops.topk(scores, gl, K, row_start=gs)
+    assert torch.equal(idx, ui) and torch.equal(tl, ut)
+    st = gs.long()
+    col = (idx.long() - st[:, None]).clamp(min=0)
+    want = torch.where(idx >= 0, torch.gather(scores, 1, col), torch.full_like(res["logits"], -math.inf))
+    assert torch.equal(res["logits"], want)
+    del st, col, want
+    bounds = np.concatenate([wl.cu_seqlens[:-1], wl.cu_seqlens[1:] - 1])
+    rows = np.unique(np.concatenate([_rows(Tq, K, n_sample, seed), bounds]))
+    sc_rows = scores[torch.from_numpy(rows).to(DEV)].cpu().numpy()[:, : wl.s_max]
+    ri, rt = oracle.topk(sc_rows.astype(np.float64), length[rows], K, start_rows=start[rows])
+    gi = idx[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    assert np.array_equal(gi, ri) and np.array_equal(tl.cpu().numpy()[rows], rt)
+    osc, mag = oracle.indexer_scores(f64(qi[rows]), f64(ki), w[rows], start[rows], length[rows], wl.s_max,
+                                     want_abs=True)
+    fin = np.isfinite(osc)
+    assert_scores_close(sc_rows, osc, mag, fin)
+    assert np.all(np.isneginf(sc_rows[~fin]))
+    _boundary_tolerant_topk(gi, osc, start[rows], length[rows], K)
+
+
+def test_compressed_thd_8k_workload():
+    _ratio_workload_check(W.compressed_thd_8k(), 64, 6)
+
+
+def test_compressed_64k_workload():
+    _ratio_workload_check(W.compressed_64k(), 32, 7)
+
+
 def _attention_check(wl, idx, tl, rows, v=None):
     q, kv, sk = wl.q_bits(), wl.kv_bits(), wl.sink()
     got = ops.sparse_attn_fwd(dev_bf16(q), dev_bf16(kv), idx, wl.scale, topk_length=tl,

@@ -113,6 +113,99 @@ def test_indexer_bf16_tolerance(Hi, d, lengths):
     assert np.all(np.isneginf(got[~fin]))
 
 
+# ------------------------------------------------- compressed-key (ratio) indexer
+# (query lengths, key lengths, offsets or None, ratio, s_max or None = longest key segment)
+RATIO_CASES = {
+    "one_segment_r4": ([700], [175], None, 4, None),
+    "segments_offsets_r4": ([300, 1, 513, 129], [200, 3, 300, 40], [500, 10, 683, 0], 4, None),
+    "clamped_rows_r2": ([600], [100], [150], 2, None),
+    "empty_key_segment": ([40, 300], [0, 90], [0, 60], 4, None),
+    "negative_offset_r3": ([400, 250], [130, 120], [-20, 100], 3, None),
+    "rows_cut_at_s_max_r4": ([1024], [300], [100], 4, 200),
+    "ratio_one": ([129, 1, 300], [129, 1, 300], None, 1, None),
+}
+
+
+def _ratio_inputs(name):
+    lq, lk, off, ratio, s_max = RATIO_CASES[name]
+    rng = np.random.default_rng(sum(lq) * 7 + ratio)
+    cq, ck = cu_from_lengths(lq), cu_from_lengths(lk)
+    Tq, Tk = int(cq[-1]), int(ck[-1])
+    qi = rand_bf16_bits(rng, (Tq, 64, 128))
+    ki = rand_bf16_bits(rng, (max(Tk, 1), 128))
+    w = (rng.random((Tq, 64), dtype=np.float32) / np.float32(8)).astype(np.float32)
+    off = None if off is None else np.asarray(off, np.int32)
+    s_max = s_max or int(max(max(lk), 1))
+    return cq, ck, off, ratio, s_max, Tq, Tk, qi, ki, w
+
+
+def _ratio_dev(cq, ck, off, qi, ki, w):
+    return (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cq), dev(ck), None if off is None else dev(off))
+
+
+@pytest.mark.parametrize("name", sorted(RATIO_CASES))
+def test_ratio_metadata(name):
+    cq, ck, off, ratio, _, Tq, Tk, *_ = _ratio_inputs(name)
+    s, l = ops.thd_metadata_ratio(dev(cq), dev(ck), None if off is None else dev(off), ratio, Tq)
+    rs, rl = oracle.ratio_metadata(cq, ck, off, ratio, Tq, max(Tk, 0))
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(l.cpu().numpy(), rl)
+
+
+@pytest.mark.parametrize("name", sorted(RATIO_CASES))
+def test_ratio_indexer_scores(name):
+    """Dense compressed-key scores against the oracle under its ratio-causal
+    mask (rows cut at s_max), -inf elsewhere."""
+    cq, ck, off, ratio, s_max, Tq, Tk, qi, ki, w = _ratio_inputs(name)
+    if Tk == 0:
+        pytest.skip("no keys")
+    a = _ratio_dev(cq, ck, off, qi, ki, w)
+    got = ops.indexer_scores_ratio(*a, ratio, s_max).cpu().numpy()[:, :s_max]
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    length = np.minimum(length, s_max)
+    sc, mag = oracle.indexer_scores(f64(qi), f64(ki), w, start, length, s_max, want_abs=True)
+    fin = np.isfinite(sc)
+    assert_scores_close(got, sc, mag, fin)
+    assert np.all(np.isneginf(got[~fin]))
+
+
+@pytest.mark.parametrize("name", sorted(RATIO_CASES))
+@pytest.mark.parametrize("k", [1, 64, 256])
+def test_ratio_fused_topk_equals_dense_then_topk(name, k):
+    """The combined compressed-key call equals dense scores + dsa_topk with
+    global ids, bit for bit, and the oracle's top-k of those scores."""
+    cq, ck, off, ratio, s_max, Tq, Tk, qi, ki, w = _ratio_inputs(name)
+    if Tk == 0:
+        pytest.skip("no keys")
+    a = _ratio_dev(cq, ck, off, qi, ki, w)
+    res = ops.indexer_topk_ratio(*a, ratio, k, s_max, want_logits=True, want_softmax=True, want_lse=True)
+    sc = ops.indexer_scores_ratio(*a, ratio, s_max)
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    length = np.minimum(length, s_max).astype(np.int32)
+    di, dt, _ = ops.topk(sc, dev(length), k, row_start=dev(start))
+    assert torch.equal(res["idx"], di) and torch.equal(res["topk_length"], dt)
+    scn = sc.cpu().numpy().astype(np.float64)
+    ri, rt = oracle.topk(scn, length, k, start_rows=start)
+    assert np.array_equal(res["idx"].cpu().numpy(), ri)
+    rl, rs, re = oracle.topk_softmax(scn, ri, rt, start_rows=start)
+    assert np.array_equal(res["logits"].cpu().numpy().astype(np.float64), rl)
+    assert_topk_softmax_close(res["softmax"], res["lse"], rs, re)
+
+
+def test_ratio_one_equals_plain_entry_points():
+    """ratio 1, no offsets, keys stored like the queries: the compressed-key
+    calls give the plain calls' results bit for bit."""
+    rng = np.random.default_rng(21)
+    cu, T, qi, ki, w = _indexer_inputs(rng, [129, 1, 300, 2049], 64, 128)
+    s_max = 2049
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    plain = ops.indexer_scores(*a, s_max)
+    ratio = ops.indexer_scores_ratio(*a[:3], dev(cu), dev(cu), None, 1, s_max)
+    assert torch.equal(plain[:, :s_max], ratio[:, :s_max])  # columns past s_max are not written
+    idx, tl = ops.indexer_topk(*a, 512, s_max)
+    res = ops.indexer_topk_ratio(*a[:3], dev(cu), dev(cu), None, 1, 512, s_max)
+    assert torch.equal(res["idx"], idx) and torch.equal(res["topk_length"], tl)
+
+
 # ---------------------------------------------------------------------- top-k
 def test_topk_on_gpu_scores_is_exact():
     rng = np.random.default_rng(5)
