@@ -273,6 +273,7 @@ def main():
     ap.add_argument("--no-topk-standalone", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional outputs")
+    ap.add_argument("--no-compressed", action="store_true", help="skip timing the compressed-key indexer")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="attention token ranges in the end-to-end leg")
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
                     help="2: single doc T=4096, 3: THD T=16384, 4: long T=65536 (the headline workload)")
@@ -476,6 +477,38 @@ def main():
                      "equals_fused_indices": same}
         del scores
 
+    # ---- compressed-key indexer (ratio-causal mask over a compressed key
+    # prefix): the combined call and the dense scores, timed on their own
+    comp = None
+    if not args.no_compressed:
+        cw = W.compressed_64k()
+        bfd = lambda bits: torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        c_in = (bfd(cw.qi_bits()), bfd(cw.ki_bits()), torch.from_numpy(cw.w()).to(dev),
+                torch.from_numpy(cw.cu_seqlens).to(dev), torch.from_numpy(cw.cu_k).to(dev),
+                torch.from_numpy(cw.q_offsets).to(dev))
+        _, c_len = ops.thd_metadata_ratio(c_in[3], c_in[4], c_in[5], cw.ratio, cw.T)
+        c_pairs = int(c_len.long().sum().item())
+        c_flops = c_pairs * cw.Hi * cw.d * 2
+        c_ws = torch.empty(ops.indexer_topk_workspace_size(cw.T, cw.Hi, cw.d, cw.K, cw.s_max), dtype=torch.uint8,
+                           device=dev)
+        fused = lambda: ops.indexer_topk_ratio(*c_in, cw.ratio, cw.K, cw.s_max, workspace=c_ws)
+        c_scores = torch.empty((cw.T, cw.s_max), dtype=torch.float32, device=dev)
+        dense = lambda: ops.indexer_scores_ratio(*c_in, cw.ratio, cw.s_max, out=c_scores)
+        for _ in range(2):
+            fused()
+            dense()
+        torch.cuda.synchronize()
+        f_ms, d_ms = timed(fused), timed(dense)
+        peak_t = pk["bf16_tflops_sustained"]
+        comp = {"workload": cw.name, "T": cw.T, "Tk": cw.Tk, "ratio": cw.ratio, "k": cw.K, "pairs": c_pairs,
+                "flops": c_flops, "indexer_topk_ms": f_ms, "indexer_topk_tflops": c_flops / (f_ms / 1e3) / 1e12,
+                "indexer_topk_frac_peak": c_flops / (f_ms / 1e3) / 1e12 / peak_t, "dense_scores_ms": d_ms,
+                "dense_tflops": c_flops / (d_ms / 1e3) / 1e12,
+                "dense_frac_peak": c_flops / (d_ms / 1e3) / 1e12 / peak_t}
+        del c_in, c_ws, c_scores, c_len
+        torch.cuda.empty_cache()
+        ops.device_status(clear=True)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.workload == 4:
         cpu = cpu_baseline(wl, args.cpu_rows, host["qi"], host["q"], host["w"], host["ki"], host["kv"])
@@ -513,6 +546,7 @@ def main():
             "device_status": status,
             "topk_standalone": topk_line,
             "optional_outputs": extras,
+            "compressed_indexer": comp,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

@@ -134,17 +134,38 @@ __device__ __forceinline__ int doc_index(const int32_t* __restrict__ cu, int n_d
   return lo;
 }
 
+// Keys that local row q of segment b sees in the general form (kept out of
+// line: inlined into every warp role it slowed the plain form measurably).
+// Returns (first key row, number of keys).
+__device__ __noinline__ int2 row_len_general(const int32_t* cu_q, const int32_t* cu_k, const int32_t* q_off, int ratio,
+                                             int s_max, int b, int t) {
+  const int k0 = __ldg(cu_k + b);
+  const int64_t nk = __ldg(cu_k + b + 1) - k0;
+  const int64_t num = (q_off ? static_cast<int64_t>(__ldg(q_off + b)) : 0) + (t - __ldg(cu_q + b)) + 1;
+  int64_t len = num > 0 ? num / ratio : 0;  // a non-positive bound clamps to 0 either way
+  len = len < nk ? len : nk;
+  len = len < s_max ? len : s_max;
+  return make_int2(k0, len > 0 ? static_cast<int>(len) : 0);
+}
+
 // Number of keys query row t sees; *start receives the row of its first key.
+// GEN = 0: the plain causal form (cu_k = cu_q, ratio 1, no offsets), with the
+// general form compiled out: kernels that only need the plain form keep the
+// plain form's code (measured: the general form compiled into the plain
+// kernels slowed the dense indexer by 4-8%).
+template <int GEN>
 __device__ __forceinline__ int row_geom(const Geom& g, int t, int* start) {
   const int b = doc_index(g.cu_q, g.n_docs, t);
-  const int k0 = __ldg(g.cu_k + b);
-  const int64_t nk = __ldg(g.cu_k + b + 1) - k0;
-  const int64_t num = (g.q_off ? static_cast<int64_t>(__ldg(g.q_off + b)) : 0) + (t - __ldg(g.cu_q + b)) + 1;
-  int64_t len = num > 0 ? num / g.ratio : 0;  // a non-positive bound clamps to 0 either way
-  len = len < nk ? len : nk;
-  len = len < g.s_max ? len : g.s_max;
-  *start = k0;
-  return len > 0 ? static_cast<int>(len) : 0;
+  if (!GEN) {
+    // the plain causal form: one load, len = q + 1 (at most the segment, so
+    // s_max only cuts rows a caller under-declared)
+    const int s = __ldg(g.cu_q + b);
+    *start = s;
+    return min(t - s + 1, g.s_max);
+  }
+  const int2 r = row_len_general(g.cu_q, g.cu_k, g.q_off, g.ratio, g.s_max, b, t);
+  *start = r.x;
+  return r.y;
 }
 
 struct BlockRange {
@@ -154,16 +175,21 @@ struct BlockRange {
 // Key tiles of a block of query rows: from the first row's first key to the
 // last row's last key (both ends grow with the row, within and across
 // segments); kt1 < kt0 when no row of the block sees a key.
+template <int GEN>
 __device__ __forceinline__ BlockRange block_range(const IndexerParams& p, int blk) {
   BlockRange r;
   r.t0 = blk * p.qb;
   r.t1 = min(r.t0 + p.qb, p.T);
   int s0, s1;
-  row_geom(p.g, r.t0, &s0);
-  const int l1 = row_geom(p.g, r.t1 - 1, &s1);
+  row_geom<GEN>(p.g, r.t0, &s0);
   r.kt0 = s0 / kKeyTile;
-  const int last = s1 + l1;  // one past the block's last key
-  r.kt1 = last > r.kt0 * kKeyTile ? (last - 1) / kKeyTile : r.kt0 - 1;
+  if (!GEN) {
+    r.kt1 = (r.t1 - 1) / kKeyTile;  // keys stored like the queries: the last row's own key
+    return r;
+  }
+  const int l1 = row_geom<GEN>(p.g, r.t1 - 1, &s1);
+  const int end = s1 + l1;  // one past the block's last key
+  r.kt1 = end > r.kt0 * kKeyTile ? (end - 1) / kKeyTile : r.kt0 - 1;
   return r;
 }
 
@@ -300,7 +326,7 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, 
   __syncwarp();
 }
 
-template <int FUSED, int HI>
+template <int FUSED, int HI, int GEN>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const IndexerParams p) {
@@ -367,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int iter = 0;
       bool ok = true;
       for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
-        const BlockRange br = block_range(p, blk);
+        const BlockRange br = block_range<GEN>(p, blk);
         if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
         for (int c = 0; c < nch; ++c)
@@ -394,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t q_addr = dsa::smem_u32(qbuf), k_addr = dsa::smem_u32(kbuf);
       for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
-        const BlockRange br = block_range(p, blk);
+        const BlockRange br = block_range<GEN>(p, blk);
         if (!dsa::mbar_wait(qfull, iter & 1, abort_flag, p.status)) break;
         dsa::tc_fence_after();
         for (int kt = br.kt0; kt <= br.kt1; ++kt) {
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = quarter;              // this warp writes segment `quarter` of its rows
     const int cap_seg = FUSED ? p.cap / 4 : 0;
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
-      const BlockRange br = block_range(p, blk);
+      const BlockRange br = block_range<GEN>(p, blk);
       uint32_t cmask = 0u;                 // bit q: this warp's segment of row q was compacted
       int wcnt[tok_per_half];              // candidates this warp wrote per row (warp-uniform)
 #pragma unroll
@@ -452,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = br.t0 + et;
         if (t < p.T) {
           int s;
-          tok_len[et] = row_geom(p.g, t, &s);
+          tok_len[et] = row_geom<GEN>(p.g, t, &s);
           tok_start[et] = s;
         } else {
           tok_start[et] = INT_MAX;
@@ -472,6 +498,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (FUSED)
         for (int i = et; i < kHistWords; i += kEpiThreads) hist[i] = 0u;
       named_bar(1, kEpiThreads);
+      // this thread's rows (tokens half*tok_per_half + q): key window
+      // [rs, rs + rl) in registers, so the per-token check needs no load
+      int rs[tok_per_half], rl[tok_per_half];
+#pragma unroll
+      for (int q = 0; q < tok_per_half; ++q) {
+        rs[q] = tok_start[half * tok_per_half + q];
+        rl[q] = tok_len[half * tok_per_half + q];
+      }
 
       for (int kt = br.kt0; kt <= br.kt1; ++kt) {
         if (!dsa::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) { ok = false; break; }
@@ -502,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float score = acc0 + acc1;
               const int r = half * tok_per_half + cl / HI;
               const int t = br.t0 + r;
-              const int st = tok_start[r];
-              const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(tok_len[r]);
+              const int st = rs[cl / HI];
+              const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(rl[cl / HI]);
               if (!FUSED) {
                 if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
@@ -642,6 +676,7 @@ struct SegmentedPairSrc {
 };
 
 // Stage 2 of the fused path: exact top-k of each row's candidates.
+template <int GEN>
 __global__ void __launch_bounds__(dsa::kTopkThreads)
     fused_select_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
                         const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
@@ -650,7 +685,7 @@ __global__ void __launch_bounds__(dsa::kTopkThreads)
   dsa::TopkShared& S = *reinterpret_cast<dsa::TopkShared*>(smem_raw2);
   const int t = blockIdx.x;
   int st;
-  const int len = row_geom(g, t, &st);
+  const int len = row_geom<GEN>(g, t, &st);
   int32_t* out = idx + static_cast<int64_t>(t) * k;
   if (len <= k) {
     for (int j = threadIdx.x; j < k; j += blockDim.x) out[j] = j < len ? st + j : -1;
@@ -746,6 +781,7 @@ __device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) 
   return before + incl - v;
 }
 
+template <int GEN>
 __global__ void __launch_bounds__(kSelThreads, 1)
     fused_select_fast_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
                              const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
@@ -775,7 +811,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   };
   auto row_len = [&](int r, int* st) {
     int s0;
-    const int len = row_geom(g, T - 1 - r, &s0);
+    const int len = row_geom<GEN>(g, T - 1 - r, &s0);
     if (st) *st = s0;
     return len;
   };
@@ -1086,29 +1122,38 @@ int make_maps(const void* qi, const void* ki, int Tq, int Tk, int Hi, int d, CUt
                                    kKeyTile, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int FUSED, int HI>
+bool is_plain(const Geom& g) { return g.cu_k == g.cu_q && g.ratio == 1 && !g.q_off; }
+
+template <int FUSED, int HI, int GEN>
 int launch_indexer_hi(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count,
                       cudaStream_t stream) {
   const int max_stages = FUSED ? 3 : 4;
   p.stages = p.d == 64 ? 6 : max_stages;
   const SmemLayout L = smem_layout(p.d, p.stages, p.qb, FUSED);
   const size_t smem = L.total + 1024;
-  if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("indexer_kernel smem attribute");
   const int grid = p.nblocks < sm_count ? p.nblocks : sm_count;
-  indexer_kernel<FUSED, HI><<<grid, kThreads, smem, stream>>>(mq, mk, p);
+  indexer_kernel<FUSED, HI, GEN><<<grid, kThreads, smem, stream>>>(mq, mk, p);
   return dsa::launch_error("indexer_kernel");
+}
+
+template <int FUSED, int GEN>
+int launch_indexer_gen(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count,
+                       cudaStream_t stream) {
+  switch (p.Hi) {
+    case 8: return launch_indexer_hi<FUSED, 8, GEN>(mq, mk, p, sm_count, stream);
+    case 16: return launch_indexer_hi<FUSED, 16, GEN>(mq, mk, p, sm_count, stream);
+    case 32: return launch_indexer_hi<FUSED, 32, GEN>(mq, mk, p, sm_count, stream);
+    default: return launch_indexer_hi<FUSED, 64, GEN>(mq, mk, p, sm_count, stream);
+  }
 }
 
 template <int FUSED>
 int launch_indexer(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count, cudaStream_t stream) {
-  switch (p.Hi) {
-    case 8: return launch_indexer_hi<FUSED, 8>(mq, mk, p, sm_count, stream);
-    case 16: return launch_indexer_hi<FUSED, 16>(mq, mk, p, sm_count, stream);
-    case 32: return launch_indexer_hi<FUSED, 32>(mq, mk, p, sm_count, stream);
-    default: return launch_indexer_hi<FUSED, 64>(mq, mk, p, sm_count, stream);
-  }
+  return is_plain(p.g) ? launch_indexer_gen<FUSED, 0>(mq, mk, p, sm_count, stream)
+                       : launch_indexer_gen<FUSED, 1>(mq, mk, p, sm_count, stream);
 }
 
 // Candidate capacity per row: four equal segments, one per key quarter of a
@@ -1231,8 +1276,9 @@ int run_candidates(const void* qi, const void* ki, const float* w, const Geom& g
 // True when stage 2 runs its fast form (the only form that can also write logits).
 bool select_is_fast(int s_max, int k) { return s_max <= kSelMaxLen && fused_cap(s_max, k) <= kSelMax; }
 
-int run_select(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32_t* topk_length, float* logits,
-               int sms, cudaStream_t stream) {
+template <int GEN>
+int run_select_gen(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32_t* topk_length, float* logits,
+                   int sms, cudaStream_t stream) {
   const int cap = fused_cap(g.s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
@@ -1240,20 +1286,27 @@ int run_select(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32
   uint32_t* status = dsa::device_status_ptr();
   if (select_is_fast(g.s_max, k)) {
     const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
-    if (cudaFuncSetAttribute(fused_select_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(fused_select_fast_kernel<GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return dsa::launch_error("fused_select_fast_kernel smem attribute");
     const int grid = T < sms ? T : sms;
-    fused_select_fast_kernel<<<grid, kSelThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length,
-                                                                  logits, status);
+    fused_select_fast_kernel<GEN><<<grid, kSelThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length,
+                                                                       logits, status);
     return dsa::launch_error("fused_select_fast_kernel");
   }
   const size_t smem = sizeof(dsa::TopkShared);
-  if (cudaFuncSetAttribute(fused_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(fused_select_kernel<GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("fused_select_kernel smem attribute");
-  fused_select_kernel<<<T, dsa::kTopkThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length, status);
+  fused_select_kernel<GEN><<<T, dsa::kTopkThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length,
+                                                                   status);
   return dsa::launch_error("fused_select_kernel");
+}
+
+int run_select(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32_t* topk_length, float* logits,
+               int sms, cudaStream_t stream) {
+  return is_plain(g) ? run_select_gen<0>(g, T, k, workspace, idx, topk_length, logits, sms, stream)
+                     : run_select_gen<1>(g, T, k, workspace, idx, topk_length, logits, sms, stream);
 }
 
 // Both stages plus the optional outputs of the pages' combined call (arguments
