@@ -56,6 +56,10 @@ def _load():
             lib.oracle_num_threads.restype = I
             lib.oracle_thd_metadata.argtypes = [P, I, I, P, P]
             lib.oracle_thd_metadata.restype = I
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_value.restype = D
+            lib.oracle_fp8_dequant.argtypes = [P, P, L, I, P]
+            lib.oracle_fp8_dequant.restype = None
             lib.oracle_ratio_metadata.argtypes = [P, P, P, I, I, I, I, P, P]
             lib.oracle_ratio_metadata.restype = I
             lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
@@ -116,6 +120,24 @@ def ratio_metadata(cu_q, cu_k, q_causal_offsets, ratio: int, Tq: int, Tk: int):
     if rc != 0:
         raise ValueError("cu_q / cu_k are not valid prefix arrays over [0, Tq) / [0, Tk), or ratio < 1")
     return start, length
+
+
+def e4m3_value(code: int) -> float:
+    """The value of one E4M3 code (see dsa_oracle.c)."""
+    return float(_load().oracle_e4m3_value(int(code) & 0xFF))
+
+
+def fp8_dequant(codes, scales):
+    """fp64 codes[..., len] decoded from E4M3 and multiplied by one fp32 descale
+    per row: scales has the shape of codes without its last axis."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.float32)
+    if c.shape[:-1] != s.shape:
+        raise ValueError("one descale per row of codes")
+    out = np.empty(c.shape, np.float64)
+    rows = int(np.prod(c.shape[:-1]))
+    _load().oracle_fp8_dequant(_ptr(c), _ptr(s), rows, int(c.shape[-1]), _ptr(out))
+    return out
 
 
 def indexer_scores(qi_rows, ki, w_rows, start_rows, len_rows, s_max: int, want_abs: bool = False):

@@ -107,6 +107,32 @@ int oracle_ratio_metadata(const int32_t* cu_q, const int32_t* cu_k,
 }
 
 /* ------------------------------------------------------------------------
+ * FP8 indexer inputs [P5 section 3, precision path "fp8": Q/K in E4M3 with
+ * fp32 descales, one per token (and head for Q)].  E4M3 is the 8-bit float
+ * with 1 sign, 4 exponent (bias 7) and 3 mantissa bits, no infinities, and
+ * NaN only for exponent and mantissa all ones:
+ *   e = 0:  (-1)^s * (m / 8) * 2^(1 - 7)      (zero and subnormals)
+ *   e > 0:  (-1)^s * (1 + m / 8) * 2^(e - 7)
+ * oracle_fp8_dequant writes out[r * len + i] = value(codes[r * len + i]) *
+ * scales[r]: each row of `len` codes has one descale.  The dequantized
+ * tensors then go through oracle_indexer_scores unchanged:
+ *   score = sum_h w * ReLU( sum_c (q_scale * q) * (k_scale * k) ).
+ * ------------------------------------------------------------------------ */
+double oracle_e4m3_value(uint8_t code) {
+  const int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, 1 - 7) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+void oracle_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows, int len, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int i = 0; i < len; ++i)
+      out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[r];
+}
+
+/* ------------------------------------------------------------------------
  * Lightning-indexer scores [P5 section 3; P1 cudnn_indexer_topk].
  * For one query row with inputs qi_row [Hi, d], w_row [Hi] and keys
  * ki [*, d]:

@@ -46,6 +46,11 @@ MUTANTS = {
     "compact_keeps_key_count": ("(int64_t)id < key_count", "(int64_t)id <= key_count"),
     "pack_wrong_batch_stride": ("v = b * S + id;", "v = b * W + id;"),
     "metadata_len_off_by_one": ("len[t] = t - cu[b] + 1;", "len[t] = t - cu[b];"),
+    "e4m3_bias_eight": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_as_normal": ("e == 0 ? ldexp((double)m / 8.0, 1 - 7)", "e == 0 ? ldexp(1.0 + (double)m / 8.0, -7)"),
+    "e4m3_no_nan": ("if (e == 15 && m == 7) return NAN;", ""),
+    "fp8_descale_wrong_row": ("out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[r];",
+                              "out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[0];"),
     "ratio_drop_plus_one": ("const int64_t num = off + (t - cu_q[b]) + 1;",
                             "const int64_t num = off + (t - cu_q[b]);"),
     "ratio_ceil_not_floor": ("int64_t bound = num >= 0 ? num / ratio : -((-num + ratio - 1) / ratio);",

@@ -95,6 +95,83 @@ def test_ratio_metadata_rejects_invalid(cu_q, cu_k, ratio, Tq, Tk):
         oracle.ratio_metadata(np.array(cu_q), np.array(cu_k), None, ratio, Tq, Tk)
 
 
+def test_e4m3_golden_values():
+    g = _gold("e4m3.json")
+    for code, v in g["values"].items():
+        got = oracle.e4m3_value(int(code))
+        assert got == v and np.signbit(got) == np.signbit(v), (code, got, v)
+    for code in g["nan"]:
+        assert np.isnan(oracle.e4m3_value(code))
+
+
+def test_e4m3_all_codes_match_torch_float8():
+    """Every one of the 256 codes against torch's float8_e4m3fn decoding (a
+    library implementation of the same format)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.fp8_dequant(codes[None, :], np.ones(1, np.float32))[0]
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin]) and np.array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))
+
+
+def _e4m3_code_of_int(v):
+    """E4M3 code of a small integer |v| <= 15 (exact): written out from the format."""
+    if v == 0:
+        return 0
+    s = 0x80 if v < 0 else 0
+    a = abs(v)
+    e = a.bit_length() - 1            # a = 2^e * (1 + m/8)
+    m = ((a << 3) >> e) & 7
+    return s | ((e + 7) << 3) | m
+
+
+def test_fp8_scores_reduce_to_integer_bf16_case():
+    """Codes of small integers with descales 1 are the integer inputs of the
+    exact bf16 case: the fp8 path's scores equal that case's scores exactly."""
+    rng = np.random.default_rng(31)
+    T, Hi, d = 9, 4, 16
+    qi = rng.integers(-4, 5, size=(T, Hi, d))
+    ki = rng.integers(-4, 5, size=(T, d))
+    w = rng.integers(1, 5, size=(T, Hi)).astype(np.float64)
+    enc = np.vectorize(_e4m3_code_of_int)
+    q8, k8 = enc(qi).astype(np.uint8), enc(ki).astype(np.uint8)
+    start, length = oracle.thd_metadata(np.array([0, 4, 9], np.int32), T)
+    ref = oracle.indexer_scores(qi.astype(np.float64), ki.astype(np.float64), w, start, length, 5)
+    got = oracle.indexer_scores(oracle.fp8_dequant(q8, np.ones((T, Hi), np.float32)),
+                                oracle.fp8_dequant(k8, np.ones(T, np.float32)), w, start, length, 5)
+    assert np.array_equal(got, ref)
+
+
+def test_fp8_descales_scale_rows_and_columns():
+    """score is positively homogeneous in each descale: doubling q_scale of
+    every head of row t doubles row t; doubling k_scale of key s doubles
+    column s - start of every row that sees it."""
+    rng = np.random.default_rng(32)
+    T, Hi, d = 12, 4, 32
+    q8 = rng.integers(0, 256, size=(T, Hi, d)).astype(np.uint8)
+    q8[(q8 & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    k8 = rng.integers(0, 256, size=(T, d)).astype(np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x38
+    qs = rng.uniform(0.5, 2.0, size=(T, Hi)).astype(np.float32)
+    ks = rng.uniform(0.5, 2.0, size=T).astype(np.float32)
+    w = rng.random((T, Hi))
+    start, length = oracle.thd_metadata(np.array([0, T], np.int32), T)
+    base = oracle.indexer_scores(oracle.fp8_dequant(q8, qs), oracle.fp8_dequant(k8, ks), w, start, length, T)
+    qs2 = qs.copy(); qs2[5] *= 2
+    r = oracle.indexer_scores(oracle.fp8_dequant(q8, qs2), oracle.fp8_dequant(k8, ks), w, start, length, T)
+    fin = np.isfinite(base)
+    assert np.allclose(r[5][fin[5]], 2 * base[5][fin[5]], rtol=1e-12)
+    assert np.array_equal(np.delete(r, 5, 0), np.delete(base, 5, 0))
+    ks2 = ks.copy(); ks2[3] *= 2
+    r = oracle.indexer_scores(oracle.fp8_dequant(q8, qs), oracle.fp8_dequant(k8, ks2), w, start, length, T)
+    assert np.allclose(r[3:, 3], 2 * base[3:, 3], rtol=1e-12)
+    assert np.array_equal(np.delete(r, 3, 1), np.delete(base, 3, 1))
+
+
 def _rand_bf16_like(rng, shape, lo=-4, hi=4):
     return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
 
