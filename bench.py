@@ -274,6 +274,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional outputs")
     ap.add_argument("--no-compressed", action="store_true", help="skip timing the compressed-key indexer")
+    ap.add_argument("--no-fp8", action="store_true", help="skip timing the fp8-input indexer")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="attention token ranges in the end-to-end leg")
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
                     help="2: single doc T=4096, 3: THD T=16384, 4: long T=65536 (the headline workload)")
@@ -509,6 +510,43 @@ def main():
         torch.cuda.empty_cache()
         ops.device_status(clear=True)
 
+    # ---- fp8 (E4M3 + fp32 descales) indexer inputs on the same workload: the
+    # combined call and the dense scores, timed on their own; the fp8 peak is
+    # the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+    fp8 = None
+    if not args.no_fp8:
+        q8, qs = wl.qi_fp8()
+        k8, ks = wl.ki_fp8()
+        f_in = (torch.from_numpy(q8).to(dev), torch.from_numpy(k8).to(dev), torch.from_numpy(qs).to(dev),
+                torch.from_numpy(ks).to(dev), d["w"], d["cu"], d["cu"], None)
+        del q8, k8
+        f_ws = torch.empty(ops.indexer_topk_workspace_size(T, wl.Hi, wl.d, K, wl.s_max), dtype=torch.uint8,
+                           device=dev)
+        f_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        f_tl = torch.empty(T, dtype=torch.int32, device=dev)
+        f_fused = lambda: ops.indexer_topk_fp8(*f_in, 1, K, wl.s_max, workspace=f_ws, idx=f_idx, topk_length=f_tl)
+        for _ in range(2):
+            f_fused()
+        torch.cuda.synchronize()
+        f_ms = timed(f_fused)
+        del f_ws, f_idx, f_tl
+        torch.cuda.empty_cache()
+        f_scores = torch.empty((T, wl.s_max), dtype=torch.float32, device=dev)
+        f_dense = lambda: ops.indexer_scores_fp8(*f_in, 1, wl.s_max, out=f_scores)
+        f_dense()
+        torch.cuda.synchronize()
+        fd_ms = timed(f_dense)
+        del f_scores, f_in
+        torch.cuda.empty_cache()
+        peak8 = pk["bf16_tflops_sustained"] * 2.0
+        fl = work["indexer_flops"]
+        fp8 = {"workload": wl.name, "inputs": "E4M3 qi/ki, fp32 descales per (token, head) / key row",
+               "indexer_topk_ms": f_ms, "indexer_topk_tflops": fl / (f_ms / 1e3) / 1e12,
+               "indexer_topk_frac_peak": fl / (f_ms / 1e3) / 1e12 / peak8, "dense_scores_ms": fd_ms,
+               "dense_tflops": fl / (fd_ms / 1e3) / 1e12, "dense_frac_peak": fl / (fd_ms / 1e3) / 1e12 / peak8,
+               "peak_tflops": peak8, "peak_source": f"{pk['source']} bf16 sustained x 2 (nominal fp8/bf16)"}
+        ops.device_status(clear=True)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.workload == 4:
         cpu = cpu_baseline(wl, args.cpu_rows, host["qi"], host["q"], host["w"], host["ki"], host["kv"])
@@ -547,6 +585,7 @@ def main():
             "topk_standalone": topk_line,
             "optional_outputs": extras,
             "compressed_indexer": comp,
+            "fp8_indexer": fp8,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

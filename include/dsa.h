@@ -233,6 +233,35 @@ int dsa_indexer_topk_ratio(const void* qi, const void* ki, const float* w,
                            float* logits, float* softmax, float* lse, void* workspace,
                            size_t ws_bytes, cudaStream_t stream);
 
+/* ---- FP8 indexer inputs ([cuDNN-DSA] 3, precision path "fp8": Q and K in
+ * E4M3 with fp32 descales, one per (token, head) for Q and one per key row
+ * for K).  With q = e4m3(qi8[t, h, :]) and k = e4m3(ki8[s, :]):
+ *   scores[t, j] = sum_h w[t, h] * ReLU( q_scale[t, h] * k_scale[s] * (q . k) ),
+ *   s = start[t] + j,
+ * over the row geometry of the compressed-key calls above (pass
+ * cu_seqlens_k = cu_seqlens_q, no offsets and ratio 1 for the plain causal
+ * form).  The products of E4M3 values are exact and accumulate in fp32 on the
+ * tensor cores; the descales are applied in fp32 after the dot product
+ * (q_scale folded into w, k_scale after the head sum), which is the formula
+ * above for positive descales -- descales must be positive and finite, codes
+ * must not be NaN (S.1111.111).
+ *   qi8 uint8 [Tq, Hi, d], ki8 uint8 [Tk, d] (16-byte aligned);
+ *   q_scale fp32 [Tq, Hi], k_scale fp32 [Tk]; other arguments and outputs as
+ *   dsa_indexer_scores_ratio / dsa_indexer_topk_ratio.
+ * Shapes: d = 128, Hi in {32, 64} (the pages' fp8 head counts).
+ * Errors: as the compressed-key calls, plus DSA_ERR_VALUE for NULL descales
+ * or other d / Hi. */
+int dsa_indexer_scores_fp8(const void* qi8, const void* ki8, const float* q_scale, const float* k_scale,
+                           const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                           int ratio, int s_max, float* scores, int64_t ld, cudaStream_t stream);
+
+int dsa_indexer_topk_fp8(const void* qi8, const void* ki8, const float* q_scale, const float* k_scale,
+                         const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                         const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                         int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length, float* logits,
+                         float* softmax, float* lse, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* The two stages of dsa_indexer_topk as separate calls, for callers that
  * schedule or time them apart ([cuDNN-DSA] "Limitations": the selection
  * over the candidate buffer is a stage of its own).  dsa_indexer_candidates

@@ -74,10 +74,14 @@ struct Geom {
 
 struct IndexerParams {
   const float* w;
+  const float* q_scale;  // fp8 inputs: descale per (token, head) [T, Hi]
+  const float* k_scale;  // fp8 inputs: descale per key row [Tk]
   Geom g;
   int T;
+  int Tk;
   int Hi;
   int d;
+  int nch;  // 128-byte chunks per row of qi / ki (d * element bytes / 128)
   int qb;        // tokens per block = 256 / Hi
   int nblocks;
   int stages;
@@ -99,9 +103,8 @@ struct SmemLayout {
   uint32_t q_off, k_off, w_off, tok_off, hist_off, row_off, cmp_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int d, int stages, int qb, int fused) {
+__host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, int fused) {
   SmemLayout L;
-  const uint32_t nch = d / 64;
   uint32_t o = 0;
   L.q_off = o;
   o += nch * kNRows * 128;
@@ -326,14 +329,19 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, 
   __syncwarp();
 }
 
-template <int FUSED, int HI, int GEN>
+// F8 = 1: qi / ki are E4M3 with fp32 descales (kind::f8f6f4 MMAs, K = 32
+// per instruction, so a 128-byte chunk is still four instructions); the
+// epilogue folds q_scale into the head weights and multiplies the head sum
+// by k_scale: w * ReLU(qs * ks * D) = ks * (w * qs) * ReLU(D) for positive
+// descales.
+template <int FUSED, int HI, int GEN, int F8>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dsa::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  const SmemLayout L = smem_layout(p.d, p.stages, p.qb, FUSED);
+  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED);
   uint8_t* qbuf = smem + L.q_off;
   uint8_t* kbuf = smem + L.k_off;
   float* w_s = reinterpret_cast<float*>(smem + L.w_off);
@@ -357,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = p.d / 64;
+  const int nch = p.nch;
+  constexpr int kChunkElems = F8 ? 128 : 64;  // elements per 128-byte chunk
   const int S = p.stages;
 
   if (threadIdx.x == 0) {
@@ -397,13 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
         for (int c = 0; c < nch; ++c)
-          dsa::tma_load_2d_hint(qbuf + c * kNRows * 128, &map_q, c * 64, br.t0 * p.Hi, qfull, stream);
+          dsa::tma_load_2d_hint(qbuf + c * kNRows * 128, &map_q, c * kChunkElems, br.t0 * p.Hi, qfull, stream);
         for (int kt = br.kt0; kt <= br.kt1; ++kt) {
           if (!dsa::mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           dsa::mbar_expect_tx(&full[stage], nch * kKeyTile * 128);
           uint8_t* dst = kbuf + stage * nch * kKeyTile * 128;
           for (int c = 0; c < nch; ++c)
-            dsa::tma_load_2d_hint(dst + c * kKeyTile * 128, &map_k, c * 64, kt * kKeyTile, &full[stage], keep);
+            dsa::tma_load_2d_hint(dst + c * kKeyTile * 128, &map_k, c * kChunkElems, kt * kKeyTile, &full[stage], keep);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -411,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = dsa::idesc_bf16(kKeyTile, kNRows, 0, 0);
+      constexpr uint32_t idesc = F8 ? dsa::idesc_e4m3(kKeyTile, kNRows) : dsa::idesc_bf16(kKeyTile, kNRows, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -434,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t ad = dsa::smem_desc(a0 + c * kKeyTile * 128 + kk * 32, 16, 1024, dsa::kSwizzle128B);
               const uint64_t bd = dsa::smem_desc(q_addr + c * kNRows * 128 + kk * 32, 16, 1024, dsa::kSwizzle128B);
-              dsa::umma_bf16(d_tmem, ad, bd, idesc, (c | kk) != 0);
+              if (F8) dsa::umma_f8(d_tmem, ad, bd, idesc, (c | kk) != 0);
+              else dsa::umma_bf16(d_tmem, ad, bd, idesc, (c | kk) != 0);
             }
           }
           dsa::umma_commit(&empty[stage]);
@@ -472,7 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = et; i < kNRows; i += kEpiThreads) {
         const int r = i / HI, h = i - r * HI;
         const int t = br.t0 + r;
-        w_s[i] = t < p.T ? __ldg(p.w + static_cast<int64_t>(t) * Hi + h) : 0.f;
+        float wv = t < p.T ? __ldg(p.w + static_cast<int64_t>(t) * Hi + h) : 0.f;
+        if (F8 && t < p.T) wv *= __ldg(p.q_scale + static_cast<int64_t>(t) * Hi + h);
+        w_s[i] = wv;
       }
       if (et < p.qb) {
         const int t = br.t0 + et;
@@ -507,7 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         rl[q] = tok_len[half * tok_per_half + q];
       }
 
+      // fp8: this thread's key descale, loaded one tile ahead
+      float ks_next = 1.f;
+      if (F8) {
+        const int s0 = br.kt0 * kKeyTile + key_lane;
+        ks_next = s0 < p.Tk ? __ldg(p.k_scale + s0) : 0.f;
+      }
       for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+        const float ks = ks_next;
+        if (F8) {
+          const int s1 = (kt + 1) * kKeyTile + key_lane;
+          ks_next = (kt < br.kt1 && s1 < p.Tk) ? __ldg(p.k_scale + s1) : 0.f;
+        }
         if (!dsa::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) { ok = false; break; }
         dsa::tc_fence_after();
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
@@ -533,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h & 1) acc1 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc1);
             else acc0 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc0);
             if (h == HI - 1) {
-              const float score = acc0 + acc1;
+              const float score = F8 ? (acc0 + acc1) * ks : acc0 + acc1;
               const int r = half * tok_per_half + cl / HI;
               const int t = br.t0 + r;
               const int st = rs[cl / HI];
@@ -1114,39 +1137,72 @@ int validate_ratio(const void* qi, const void* ki, const float* w, const int32_t
 
 Geom plain_geom(const int32_t* cu, int n_docs, int s_max) { return Geom{cu, cu, nullptr, n_docs, 1, s_max}; }
 
-int make_maps(const void* qi, const void* ki, int Tq, int Tk, int Hi, int d, CUtensorMap* mq, CUtensorMap* mk) {
-  int rc = dsa::encode_tensor_map_2d(mq, qi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, static_cast<uint64_t>(Tq) * Hi,
-                                     static_cast<uint64_t>(d) * 2, 64, kNRows, CU_TENSOR_MAP_SWIZZLE_128B);
+// The indexer's tensor inputs: bf16 qi / ki, or E4M3 with fp32 descales.
+struct Inputs {
+  const void* qi;
+  const void* ki;
+  const float* w;
+  const float* q_scale;  // non-NULL: qi / ki are E4M3 (one byte per element)
+  const float* k_scale;
+  int Tq, Tk, Hi, d;
+  int elem_bytes() const { return q_scale ? 1 : 2; }
+};
+
+int make_maps(const Inputs& in, CUtensorMap* mq, CUtensorMap* mk) {
+  const CUtensorMapDataType dt = in.q_scale ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t box = 128 / in.elem_bytes();  // one 128-byte swizzled chunk
+  const uint64_t row = static_cast<uint64_t>(in.d) * in.elem_bytes();
+  int rc = dsa::encode_tensor_map_2d(mq, in.qi, dt, in.d, static_cast<uint64_t>(in.Tq) * in.Hi, row, box, kNRows,
+                                     CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != DSA_OK) return rc;
-  return dsa::encode_tensor_map_2d(mk, ki, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d, Tk, static_cast<uint64_t>(d) * 2, 64,
-                                   kKeyTile, CU_TENSOR_MAP_SWIZZLE_128B);
+  return dsa::encode_tensor_map_2d(mk, in.ki, dt, in.d, in.Tk, row, box, kKeyTile, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+void fill_params(IndexerParams& p, const Inputs& in, const Geom& g) {
+  p.w = in.w;
+  p.q_scale = in.q_scale;
+  p.k_scale = in.k_scale;
+  p.g = g;
+  p.T = in.Tq;
+  p.Tk = in.Tk;
+  p.Hi = in.Hi;
+  p.d = in.d;
+  p.nch = in.d * in.elem_bytes() / 128;
+  p.qb = kNRows / in.Hi;
+  p.nblocks = (in.Tq + p.qb - 1) / p.qb;
+  p.s_max = g.s_max;
+  p.status = dsa::device_status_ptr();
 }
 
 bool is_plain(const Geom& g) { return g.cu_k == g.cu_q && g.ratio == 1 && !g.q_off; }
 
-template <int FUSED, int HI, int GEN>
+template <int FUSED, int HI, int GEN, int F8>
 int launch_indexer_hi(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count,
                       cudaStream_t stream) {
   const int max_stages = FUSED ? 3 : 4;
-  p.stages = p.d == 64 ? 6 : max_stages;
-  const SmemLayout L = smem_layout(p.d, p.stages, p.qb, FUSED);
+  p.stages = p.nch == 1 ? 6 : max_stages;
+  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED);
   const size_t smem = L.total + 1024;
-  if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI, GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI, GEN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("indexer_kernel smem attribute");
   const int grid = p.nblocks < sm_count ? p.nblocks : sm_count;
-  indexer_kernel<FUSED, HI, GEN><<<grid, kThreads, smem, stream>>>(mq, mk, p);
+  indexer_kernel<FUSED, HI, GEN, F8><<<grid, kThreads, smem, stream>>>(mq, mk, p);
   return dsa::launch_error("indexer_kernel");
 }
 
 template <int FUSED, int GEN>
 int launch_indexer_gen(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParams& p, int sm_count,
                        cudaStream_t stream) {
+  if (p.q_scale) {  // fp8 inputs: 32 or 64 heads (validated)
+    return p.Hi == 32 ? launch_indexer_hi<FUSED, 32, GEN, 1>(mq, mk, p, sm_count, stream)
+                      : launch_indexer_hi<FUSED, 64, GEN, 1>(mq, mk, p, sm_count, stream);
+  }
   switch (p.Hi) {
-    case 8: return launch_indexer_hi<FUSED, 8, GEN>(mq, mk, p, sm_count, stream);
-    case 16: return launch_indexer_hi<FUSED, 16, GEN>(mq, mk, p, sm_count, stream);
-    case 32: return launch_indexer_hi<FUSED, 32, GEN>(mq, mk, p, sm_count, stream);
-    default: return launch_indexer_hi<FUSED, 64, GEN>(mq, mk, p, sm_count, stream);
+    case 8: return launch_indexer_hi<FUSED, 8, GEN, 0>(mq, mk, p, sm_count, stream);
+    case 16: return launch_indexer_hi<FUSED, 16, GEN, 0>(mq, mk, p, sm_count, stream);
+    case 32: return launch_indexer_hi<FUSED, 32, GEN, 0>(mq, mk, p, sm_count, stream);
+    default: return launch_indexer_hi<FUSED, 64, GEN, 0>(mq, mk, p, sm_count, stream);
   }
 }
 
@@ -1173,23 +1229,14 @@ int fused_compact(int s_max, int k) { return fused_whole(s_max) > fused_bound(k)
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Dense scores (arguments already validated).
-int run_dense(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d,
-              float* scores, int64_t ld, int sms, cudaStream_t stream) {
+int run_dense(const Inputs& in, const Geom& g, float* scores, int64_t ld, int sms, cudaStream_t stream) {
   CUtensorMap mq, mk;
-  int rc = make_maps(qi, ki, Tq, Tk, Hi, d, &mq, &mk);
+  int rc = make_maps(in, &mq, &mk);
   if (rc != DSA_OK) return rc;
   IndexerParams p{};
-  p.w = w;
-  p.g = g;
-  p.T = Tq;
-  p.Hi = Hi;
-  p.d = d;
-  p.qb = kNRows / Hi;
-  p.nblocks = (Tq + p.qb - 1) / p.qb;
+  fill_params(p, in, g);
   p.scores = scores;
   p.ld = ld;
-  p.s_max = g.s_max;
-  p.status = dsa::device_status_ptr();
   return launch_indexer<0>(mq, mk, p, sms, stream);
 }
 
@@ -1206,7 +1253,8 @@ extern "C" int dsa_indexer_scores(const void* qi, const void* ki, const float* w
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_dense(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, scores, ld, sms, stream);
+  return run_dense(Inputs{qi, ki, w, nullptr, nullptr, T, T, Hi, d}, plain_geom(cu_seqlens, n_docs, s_max), scores, ld,
+                   sms, stream);
 }
 
 extern "C" int dsa_indexer_scores_ratio(const void* qi, const void* ki, const float* w, const int32_t* cu_seqlens_q,
@@ -1224,7 +1272,7 @@ extern "C" int dsa_indexer_scores_ratio(const void* qi, const void* ki, const fl
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
   const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
-  return run_dense(qi, ki, w, g, Tq, Tk, Hi, d, scores, ld, sms, stream);
+  return run_dense(Inputs{qi, ki, w, nullptr, nullptr, Tq, Tk, Hi, d}, g, scores, ld, sms, stream);
 }
 
 extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
@@ -1244,21 +1292,14 @@ int check_workspace(int T, int Hi, int d, int k, int s_max, const void* workspac
 }
 
 // Stage 1 launch (arguments already validated).
-int run_candidates(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d, int k,
-                   void* workspace, int sms, cudaStream_t stream) {
+int run_candidates(const Inputs& in, const Geom& g, int k, void* workspace, int sms, cudaStream_t stream) {
   CUtensorMap mq, mk;
-  int rc = make_maps(qi, ki, Tq, Tk, Hi, d, &mq, &mk);
+  int rc = make_maps(in, &mq, &mk);
   if (rc != DSA_OK) return rc;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int Tq = in.Tq;
   IndexerParams p{};
-  p.w = w;
-  p.g = g;
-  p.T = Tq;
-  p.Hi = Hi;
-  p.d = d;
-  p.qb = kNRows / Hi;
-  p.nblocks = (Tq + p.qb - 1) / p.qb;
-  p.s_max = g.s_max;
+  fill_params(p, in, g);
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
   p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(Tq) * 16));
   p.cap = fused_cap(g.s_max, k);
@@ -1268,7 +1309,6 @@ int run_candidates(const void* qi, const void* ki, const float* w, const Geom& g
   int bits = 0;
   while ((1 << bits) < bins) ++bits;
   p.hist_bits = bits;
-  p.status = dsa::device_status_ptr();
   return launch_indexer<1>(mq, mk, p, sms, stream);
 }
 
@@ -1311,14 +1351,13 @@ int run_select(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32
 
 // Both stages plus the optional outputs of the pages' combined call (arguments
 // already validated; logits may be NULL only when softmax and lse are).
-int run_fused(const void* qi, const void* ki, const float* w, const Geom& g, int Tq, int Tk, int Hi, int d, int k,
-              int32_t* idx, int32_t* topk_length, float* logits, float* softmax, float* lse, void* workspace,
-              int sms, cudaStream_t stream) {
-  int rc = run_candidates(qi, ki, w, g, Tq, Tk, Hi, d, k, workspace, sms, stream);
+int run_fused(const Inputs& in, const Geom& g, int k, int32_t* idx, int32_t* topk_length, float* logits,
+              float* softmax, float* lse, void* workspace, int sms, cudaStream_t stream) {
+  int rc = run_candidates(in, g, k, workspace, sms, stream);
   if (rc != DSA_OK) return rc;
-  rc = run_select(g, Tq, k, workspace, idx, topk_length, logits, sms, stream);
+  rc = run_select(g, in.Tq, k, workspace, idx, topk_length, logits, sms, stream);
   if (rc != DSA_OK || (!softmax && !lse)) return rc;
-  return dsa_topk_softmax(logits, idx, Tq, k, softmax, lse, stream);
+  return dsa_topk_softmax(logits, idx, in.Tq, k, softmax, lse, stream);
 }
 
 }  // namespace
@@ -1334,7 +1373,8 @@ extern "C" int dsa_indexer_candidates(const void* qi, const void* ki, const floa
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_candidates(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, workspace, sms, stream);
+  return run_candidates(Inputs{qi, ki, w, nullptr, nullptr, T, T, Hi, d}, plain_geom(cu_seqlens, n_docs, s_max), k,
+                        workspace, sms, stream);
 }
 
 extern "C" int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int T, int Hi, int d, int k, int s_max,
@@ -1366,8 +1406,8 @@ extern "C" int dsa_indexer_topk(const void* qi, const void* ki, const float* w, 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_fused(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, idx, topk_length, nullptr,
-                   nullptr, nullptr, workspace, sms, stream);
+  return run_fused(Inputs{qi, ki, w, nullptr, nullptr, T, T, Hi, d}, plain_geom(cu_seqlens, n_docs, s_max), k, idx,
+                   topk_length, nullptr, nullptr, nullptr, workspace, sms, stream);
 }
 
 // The fused call with the outputs that come with the indices on the pages'
@@ -1389,8 +1429,8 @@ extern "C" int dsa_indexer_topk_ex(const void* qi, const void* ki, const float* 
   int sms = 0;
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
-  return run_fused(qi, ki, w, plain_geom(cu_seqlens, n_docs, s_max), T, T, Hi, d, k, idx, topk_length, logits,
-                   softmax, lse, workspace, sms, stream);
+  return run_fused(Inputs{qi, ki, w, nullptr, nullptr, T, T, Hi, d}, plain_geom(cu_seqlens, n_docs, s_max), k, idx,
+                   topk_length, logits, softmax, lse, workspace, sms, stream);
 }
 
 // The combined call over a compressed key prefix with the ratio-causal mask
@@ -1417,7 +1457,68 @@ extern "C" int dsa_indexer_topk_ratio(const void* qi, const void* ki, const floa
   rc = dsa::check_device(&sms);
   if (rc != DSA_OK) return rc;
   const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
-  return run_fused(qi, ki, w, g, Tq, Tk, Hi, d, k, idx, topk_length, logits, softmax, lse, workspace, sms, stream);
+  return run_fused(Inputs{qi, ki, w, nullptr, nullptr, Tq, Tk, Hi, d}, g, k, idx, topk_length, logits, softmax, lse,
+                   workspace, sms, stream);
+}
+
+// ---- FP8 inputs (cuDNN DSA page, section 3 precision path "fp8": E4M3 Q/K
+// with fp32 descales, one per (token, head) for Q and per key row for K).
+namespace {
+int validate_fp8(const void* qi8, const void* ki8, const float* q_scale, const float* k_scale, const float* w,
+                 const int32_t* cu_q, const int32_t* cu_k, int n_docs, int Tq, int Tk, int Hi, int d, int ratio,
+                 int s_max, const char* fn) {
+  int rc = validate_ratio(qi8, ki8, w, cu_q, cu_k, n_docs, Tq, Tk, Hi, d, ratio, s_max, fn);
+  if (rc != DSA_OK) return rc;
+  if (!q_scale || !k_scale) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL q_scale or k_scale", fn);
+  if (d != 128 || (Hi != 32 && Hi != 64))
+    return dsa::set_error(DSA_ERR_VALUE, "%s: fp8 inputs need d = 128 and Hi in {32, 64} (got d %d, Hi %d)", fn, d, Hi);
+  return DSA_OK;
+}
+}  // namespace
+
+extern "C" int dsa_indexer_scores_fp8(const void* qi8, const void* ki8, const float* q_scale, const float* k_scale,
+                                      const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                      const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                                      int ratio, int s_max, float* scores, int64_t ld, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_fp8(qi8, ki8, q_scale, k_scale, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                        "dsa_indexer_scores_fp8");
+  if (rc != DSA_OK) return rc;
+  if (!scores) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_fp8: NULL scores");
+  if (ld < s_max || ld % 4 != 0)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_fp8: need ld >= s_max, ld % 4 == 0");
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_dense(Inputs{qi8, ki8, w, q_scale, k_scale, Tq, Tk, Hi, d}, g, scores, ld, sms, stream);
+}
+
+extern "C" int dsa_indexer_topk_fp8(const void* qi8, const void* ki8, const float* q_scale, const float* k_scale,
+                                    const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                    const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                                    int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length, float* logits,
+                                    float* softmax, float* lse, void* workspace, size_t ws_bytes,
+                                    cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_fp8(qi8, ki8, q_scale, k_scale, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                        "dsa_indexer_topk_fp8");
+  if (rc != DSA_OK) return rc;
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_fp8: NULL idx");
+  if ((softmax || lse) && !logits)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_fp8: softmax and lse need logits");
+  rc = check_workspace(Tq, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_topk_fp8");
+  if (rc != DSA_OK) return rc;
+  if (logits && !select_is_fast(s_max, k))
+    return dsa::set_error(DSA_ERR_UNSUPPORTED,
+                          "dsa_indexer_topk_fp8: logits need rows of at most %d columns (s_max = %d)", kSelMaxLen,
+                          s_max);
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_fused(Inputs{qi8, ki8, w, q_scale, k_scale, Tq, Tk, Hi, d}, g, k, idx, topk_length, logits, softmax, lse,
+                   workspace, sms, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -36,6 +36,11 @@ Recipe (every draw is reproducible and addressable by row):
   holds ``ceil((offset + queries) / ratio)`` compressed key rows (every block
   of ``ratio`` tokens up to its last query, the last one possibly partial).
   Indexer q/k/w as for the bf16 workloads, ki with that many rows.
+* FP8 indexer inputs (any workload): the bf16 qi / ki values, quantized per
+  row (a (token, head) row of qi, a key row of ki): descale =
+  float32(max |x| / 448) (1 for an all-zero row), code = E4M3 of x / descale
+  clipped to [-448, 448], rounded to nearest even (torch's float8_e4m3fn
+  conversion).
 """
 from __future__ import annotations
 
@@ -206,6 +211,26 @@ class Workload:
         """Indexer key, bf16 bits [Tk, d]."""
         make = self._int_bf16(-4, 4) if self.indexer_kind == "int" else self._normal_bf16(self.sigma_index)
         return self._rows(FIELD_KI, self.Tk, self.d, make)
+
+    @staticmethod
+    def _to_fp8(bits: np.ndarray):
+        """(E4M3 codes, fp32 descale per row) of bf16 bits [..., n]."""
+        import torch
+
+        x = bf16_bits_to_f32(bits)
+        amax = np.max(np.abs(x), axis=-1)
+        scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        y = np.clip(x / scale[..., None], -448.0, 448.0).astype(np.float32)
+        codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return codes, scale
+
+    def qi_fp8(self, rows=None):
+        """Indexer query as E4M3 codes [n, Hi, d] (uint8) and descales [n, Hi] (fp32)."""
+        return self._to_fp8(self.qi_bits(rows))
+
+    def ki_fp8(self):
+        """Indexer key as E4M3 codes [Tk, d] (uint8) and descales [Tk] (fp32)."""
+        return self._to_fp8(self.ki_bits())
 
     def w(self, rows=None) -> np.ndarray:
         """Pre-scaled indexer head weights, fp32 [n, Hi]."""

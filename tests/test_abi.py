@@ -22,6 +22,7 @@ def test_header_declares_the_hot_path():
                  "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_topk_ex", "dsa_topk_softmax",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex", "dsa_forward_host",
                  "dsa_pack_routes", "dsa_thd_metadata_ratio", "dsa_indexer_scores_ratio", "dsa_indexer_topk_ratio",
+                 "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
 
@@ -80,6 +81,14 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
     lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, NULL, NULL, NULL),
     lambda L: L.dsa_select_candidates(NULL, 1, 128, 64, 128, 64, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
     lambda L: L.dsa_select_candidates(FAKE, 1, 128, 64, 128, 0, 128, FAKE, 1 << 30, FAKE, NULL, NULL),
+    lambda L: L.dsa_indexer_scores_fp8(FAKE, FAKE, NULL, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 128, 64, 128, 1, 128,
+                                       FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 128, 64, 64, 1, 128,
+                                       FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_scores_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 128, 16, 128, 1, 128,
+                                       FAKE, 128, NULL),
+    lambda L: L.dsa_indexer_topk_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 128, 64, 128, 1, 64, 128,
+                                     NULL, NULL, NULL, NULL, NULL, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, FAKE, NULL, 1, 10, 0, FAKE, FAKE, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, NULL, NULL, 1, 10, 4, FAKE, FAKE, NULL),
     lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 0, 32, FAKE, 32, NULL),

@@ -206,6 +206,61 @@ def test_ratio_one_equals_plain_entry_points():
     assert torch.equal(res["idx"], idx) and torch.equal(res["topk_length"], tl)
 
 
+# ------------------------------------------------------------- fp8 indexer inputs
+FP8_CASES = {
+    "plain_one_doc": ([700], None, None, 1, 64),
+    "plain_thd": ([129, 1, 300, 257], None, None, 1, 32),
+    "compressed_offsets_r4": ([300, 1, 513, 129], [200, 3, 300, 40], [500, 10, 683, 0], 4, 64),
+}
+
+
+def _fp8_inputs(name):
+    lq, lk, off, ratio, Hi = FP8_CASES[name]
+    lk = lq if lk is None else lk
+    rng = np.random.default_rng(sum(lq) * 11 + Hi)
+    cq, ck = cu_from_lengths(lq), cu_from_lengths(lk)
+    Tq, Tk = int(cq[-1]), int(ck[-1])
+    q8, qs = W.Workload._to_fp8(rand_bf16_bits(rng, (Tq, Hi, 128)))
+    k8, ks = W.Workload._to_fp8(rand_bf16_bits(rng, (Tk, 128)))
+    w = (rng.random((Tq, Hi), dtype=np.float32) / np.float32(8)).astype(np.float32)
+    off = None if off is None else np.asarray(off, np.int32)
+    return cq, ck, off, ratio, int(max(lk)), Tq, Tk, q8, qs, k8, ks, w
+
+
+def _fp8_dev(cq, ck, off, q8, qs, k8, ks, w):
+    return (dev(q8), dev(k8), dev(qs), dev(ks), dev(w), dev(cq), dev(ck), None if off is None else dev(off))
+
+
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+def test_fp8_indexer_scores(name):
+    """E4M3 inputs with fp32 descales against the oracle's dequantized scores."""
+    cq, ck, off, ratio, s_max, Tq, Tk, q8, qs, k8, ks, w = _fp8_inputs(name)
+    got = ops.indexer_scores_fp8(*_fp8_dev(cq, ck, off, q8, qs, k8, ks, w), ratio, s_max).cpu().numpy()[:, :s_max]
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    sc, mag = oracle.indexer_scores(oracle.fp8_dequant(q8, qs), oracle.fp8_dequant(k8, ks), w, start, length, s_max,
+                                    want_abs=True)
+    fin = np.isfinite(sc)
+    assert_scores_close(got, sc, mag, fin)
+    assert np.all(np.isneginf(got[~fin]))
+
+
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+@pytest.mark.parametrize("k", [1, 64, 512])
+def test_fp8_fused_topk_equals_dense_then_topk(name, k):
+    cq, ck, off, ratio, s_max, Tq, Tk, q8, qs, k8, ks, w = _fp8_inputs(name)
+    a = _fp8_dev(cq, ck, off, q8, qs, k8, ks, w)
+    res = ops.indexer_topk_fp8(*a, ratio, k, s_max, want_logits=True)
+    sc = ops.indexer_scores_fp8(*a, ratio, s_max)
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    di, dt, _ = ops.topk(sc, dev(length), k, row_start=dev(start))
+    assert torch.equal(res["idx"], di) and torch.equal(res["topk_length"], dt)
+    scn = sc.cpu().numpy().astype(np.float64)
+    ri, rt = oracle.topk(scn, length, k, start_rows=start)
+    assert np.array_equal(res["idx"].cpu().numpy(), ri)
+    rl, _, _ = oracle.topk_softmax(scn, ri, rt, start_rows=start)
+    assert np.array_equal(res["logits"].cpu().numpy().astype(np.float64), rl)
+
+
 # ---------------------------------------------------------------------- top-k
 def test_topk_on_gpu_scores_is_exact():
     rng = np.random.default_rng(5)
