@@ -287,6 +287,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t start, uint32_t lbo, uint
 }
 constexpr uint32_t kSwizzle128B = 2;
 
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1): two fp32 fmas with round to
+// nearest in one packed instruction (fma.rn.f32x2); each lane is exactly
+// fmaf(a_i, b_i, d_i).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n mov.b64 z, {%0, %1};\n"
+      " fma.rn.f32x2 z, x, y, z;\n mov.b64 {%0, %1}, z;\n}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
 // a_mn / b_mn select MN-major (1) or K-major (0) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

@@ -545,16 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[64];
           dsa::tmem_ld64(t_addr + half * 128 + pair * 64, v);
           dsa::tmem_wait_ld();
+          const float2* w2 = reinterpret_cast<const float2*>(w_s + half * 128 + pair * 64);
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
+          for (int i = 1; i < 64; i += 2) {
+            // heads h-1 (even, chain acc0) and h (odd, chain acc1) in one
+            // packed fma: each lane is the fmaf of the two-chain sum
             const int cl = pair * 64 + i;             // column within this half (compile-time)
             const int h = cl % HI;                    // 128 % HI == 0, so the half offset drops out
-            if (h == 0) {
+            if (h == 1) {
               acc0 = 0.f;
               acc1 = 0.f;
             }
-            if (h & 1) acc1 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc1);
-            else acc0 = fmaf(w_s[half * 128 + cl], fmaxf(__uint_as_float(v[i]), 0.f), acc0);
+            const float2 wp = w2[i >> 1];
+            dsa::fma2(acc0, acc1, wp.x, wp.y, fmaxf(__uint_as_float(v[i - 1]), 0.f), fmaxf(__uint_as_float(v[i]), 0.f));
             if (h == HI - 1) {
               const float score = F8 ? (acc0 + acc1) * ks : acc0 + acc1;
               const int r = half * tok_per_half + cl / HI;
