@@ -74,6 +74,8 @@ def _load():
             lib.oracle_pack_routes.restype = None
             lib.oracle_sparse_attn.argtypes = [P, P, L, P, P, P, P, I, I, I, I, I, I, D, P, P, P, P, I, P]
             lib.oracle_sparse_attn.restype = None
+            lib.oracle_sparse_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, D, P, P, P]
+            lib.oracle_sparse_attn_bwd.restype = None
             _lib = lib
     return _lib
 
@@ -235,3 +237,29 @@ def sparse_attn(q_rows, kv, idx_rows, scale: float, topk_length=None, sink=None,
     if li is not None:
         res["lse_indexer"] = li
     return res
+
+
+def sparse_attn_bwd(q_rows, kv, idx_rows, scale: float, out_rows, dout_rows, lse_kv_rows, topk_length=None,
+                    sink=None, dv=None):
+    """(dq [n, H, Dqk], dkv [Tkv, Dqk], d_sink [H]) in fp64 (cuDNN DSA page,
+    section 2; formulas in dsa_oracle.c).  kv is the latent K = V tensor;
+    out / lse_kv are the forward's outputs for these rows."""
+    q = _f64(q_rows)
+    kvf = _f64(kv)
+    n, H, Dqk = q.shape
+    Tkv = kvf.shape[0]
+    if kvf.shape[1] != Dqk:
+        raise ValueError("kv rows must hold the Dqk query dims")
+    o = _f64(out_rows)
+    Dv = o.shape[2] if dv is None else dv
+    idx = _i32(idx_rows)
+    K = idx.shape[1]
+    tl = None if topk_length is None else _i32(topk_length)
+    sk = None if sink is None else _f64(sink)
+    dq = np.empty((n, H, Dqk), np.float64)
+    dkv = np.zeros((Tkv, Dqk), np.float64)
+    dsink = np.zeros(H, np.float64)
+    _load().oracle_sparse_attn_bwd(_ptr(q), _ptr(kvf), _ptr(idx), _ptr(tl), _ptr(sk), _ptr(o), _ptr(_f64(dout_rows)),
+                                   _ptr(_f64(lse_kv_rows)), n, Tkv, H, Dqk, Dv, K, float(scale), _ptr(dq), _ptr(dkv),
+                                   _ptr(dsink))
+    return dq, dkv, dsink

@@ -403,3 +403,69 @@ void oracle_sparse_attn(const double* q_rows, const double* kv, int64_t kv_ld,
     free(slot);
   }
 }
+
+/* ------------------------------------------------------------------------
+ * Sparse attention backward [P5 section 2 Sparse Attention Backward: inputs
+ * q, kv (K = V, MQA), out, dout, the KV-only lse, attn_sink, topk ids and
+ * lengths; outputs dq, dkv, d_sink].  With the forward of section 1 --
+ * s_j = scale * q . k_j over the valid slots j, the sink in the denominator
+ * only -- and L = logaddexp(lse_kv, sink) the full normaliser:
+ *     P_j     = exp(s_j - L),           P_sink = exp(sink - L)
+ *     dP_j    = dout . v_j,             delta  = dout . out
+ *     dS_j    = P_j * (dP_j - delta)
+ *     dq      = scale * sum_j dS_j k_j
+ *     dkv[id_j, 0:Dqk] += scale * dS_j q ;  dkv[id_j, 0:Dv] += P_j dout
+ *     d_sink  += -P_sink * delta          (summed over rows)
+ * (k_j = kv[id_j, 0:Dqk], v_j = kv[id_j, 0:Dv]).  Duplicate ids are separate
+ * slots and both contribute; invalid ids and slots past the length are
+ * absent; a row with no valid slot contributes nothing.  dq [n_rows, H,
+ * Dqk] is written; dkv [Tkv, Dqk] and dsink [H] are accumulated (the caller
+ * zeroes them), rows in order.
+ * ------------------------------------------------------------------------ */
+void oracle_sparse_attn_bwd(const double* q_rows, const double* kv, const int32_t* idx_rows, const int32_t* len_rows,
+                            const double* sink, const double* out_rows, const double* dout_rows,
+                            const double* lse_kv_rows, int n_rows, int Tkv, int H, int Dqk, int Dv, int K,
+                            double scale, double* dq_rows, double* dkv, double* dsink) {
+  for (int r = 0; r < n_rows; ++r) {
+    int lim = K;
+    if (len_rows) {
+      lim = len_rows[r];
+      if (lim < 0) lim = 0;
+      if (lim > K) lim = K;
+    }
+    for (int h = 0; h < H; ++h) {
+      const int64_t rh = (int64_t)r * H + h;
+      const double* qh = q_rows + rh * Dqk;
+      const double* o = out_rows + rh * Dv;
+      const double* dout = dout_rows + rh * Dv;
+      double* dq = dq_rows + rh * Dqk;
+      for (int c = 0; c < Dqk; ++c) dq[c] = 0.0;
+      int n = 0;
+      for (int j = 0; j < lim; ++j) {
+        const int32_t id = idx_rows[(int64_t)r * K + j];
+        if (id >= 0 && id < Tkv) ++n;
+      }
+      if (n == 0) continue;
+      const double sk = sink ? sink[h] : -INFINITY;
+      const double lkv = lse_kv_rows[rh];
+      const double L = lkv > sk ? lkv + log1p(exp(sk - lkv)) : sk + log1p(exp(lkv - sk));
+      double delta = 0.0;
+      for (int c = 0; c < Dv; ++c) delta += dout[c] * o[c];
+      for (int j = 0; j < lim; ++j) {
+        const int32_t id = idx_rows[(int64_t)r * K + j];
+        if (id < 0 || id >= Tkv) continue;
+        const double* k = kv + (int64_t)id * Dqk;
+        double dot = 0.0, dp = 0.0;
+        for (int c = 0; c < Dqk; ++c) dot += qh[c] * k[c];
+        for (int c = 0; c < Dv; ++c) dp += dout[c] * k[c];
+        const double p = exp(scale * dot - L);
+        const double ds = p * (dp - delta);
+        for (int c = 0; c < Dqk; ++c) dq[c] += scale * ds * k[c];
+        double* g = dkv + (int64_t)id * Dqk;
+        for (int c = 0; c < Dqk; ++c) g[c] += scale * ds * qh[c];
+        for (int c = 0; c < Dv; ++c) g[c] += p * dout[c];
+      }
+      if (dsink && sink) dsink[h] += -exp(sk - L) * delta;
+    }
+  }
+}

@@ -51,6 +51,12 @@ MUTANTS = {
     "e4m3_no_nan": ("if (e == 15 && m == 7) return NAN;", ""),
     "fp8_descale_wrong_row": ("out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[r];",
                               "out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[0];"),
+    "bwd_drop_delta": ("const double ds = p * (dp - delta);", "const double ds = p * dp;"),
+    "bwd_dq_without_scale": ("for (int c = 0; c < Dqk; ++c) dq[c] += scale * ds * k[c];",
+                             "for (int c = 0; c < Dqk; ++c) dq[c] += ds * k[c];"),
+    "bwd_drop_value_grad": ("for (int c = 0; c < Dv; ++c) g[c] += p * dout[c];", ""),
+    "bwd_sink_sign": ("dsink[h] += -exp(sk - L) * delta;", "dsink[h] += exp(sk - L) * delta;"),
+    "bwd_normaliser_without_sink": ("const double p = exp(scale * dot - L);", "const double p = exp(scale * dot - lkv);"),
     "ratio_drop_plus_one": ("const int64_t num = off + (t - cu_q[b]) + 1;",
                             "const int64_t num = off + (t - cu_q[b]);"),
     "ratio_ceil_not_floor": ("int64_t bound = num >= 0 ? num / ratio : -((-num + ratio - 1) / ratio);",

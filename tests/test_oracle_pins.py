@@ -619,3 +619,68 @@ def test_topk_softmax_invariants():
     np.testing.assert_allclose(s2, sm, rtol=1e-12, atol=1e-300)
     fin = np.isfinite(lse)
     np.testing.assert_allclose(e2[fin], lse[fin] + 2.5, rtol=1e-13)
+
+
+
+# ------------------------------------------------------- attention backward
+def _bwd_case(rng, n=3, H=3, Dqk=12, Dv=8, Tkv=10, K=7):
+    q = rng.standard_normal((n, H, Dqk))
+    kv = rng.standard_normal((Tkv, Dqk))
+    idx = rng.integers(-2, Tkv + 2, size=(n, K)).astype(np.int32)
+    idx[0, :3] = [4, 4, 7]            # a duplicate pair
+    tl = np.array([K, 4, 0][:n], np.int32)  # a truncated row and an empty one
+    sink = rng.standard_normal(H)
+    dout = rng.standard_normal((n, H, Dv))
+    return q, kv, idx, tl, sink, dout
+
+
+def _loss(q, kv, idx, tl, sink, dout, scale, Dv):
+    f = oracle.sparse_attn(q, kv, idx, scale, topk_length=tl, sink=sink, dv=Dv)
+    return float(np.sum(f["out"] * dout))
+
+
+def test_attn_bwd_matches_finite_differences():
+    """Every gradient against central differences of sum(dout * out) through
+    the (separately pinned) forward oracle, in fp64."""
+    rng = np.random.default_rng(41)
+    q, kv, idx, tl, sink, dout = _bwd_case(rng)
+    scale, Dv, eps = 0.37, dout.shape[2], 1e-6
+    f = oracle.sparse_attn(q, kv, idx, scale, topk_length=tl, sink=sink, dv=Dv)
+    dq, dkv, ds = oracle.sparse_attn_bwd(q, kv, idx, scale, f["out"], dout, f["lse_kv"], topk_length=tl, sink=sink)
+    for name, x, g in (("q", q, dq), ("kv", kv, dkv), ("sink", sink, ds)):
+        num = np.zeros_like(x)
+        for i in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[i] += eps
+            xm[i] -= eps
+            args = {"q": q, "kv": kv, "sink": sink}
+            lp = _loss(**{**args, name: xp}, idx=idx, tl=tl, dout=dout, scale=scale, Dv=Dv)
+            lm = _loss(**{**args, name: xm}, idx=idx, tl=tl, dout=dout, scale=scale, Dv=Dv)
+            num[i] = (lp - lm) / (2 * eps)
+        assert np.allclose(g, num, rtol=1e-6, atol=1e-8), (name, np.max(np.abs(g - num)))
+
+
+def test_attn_bwd_single_key_closed_form():
+    """One valid key, no sink: P = 1 and out = v, so delta = dP and dS = 0:
+    dq = 0 and the key row receives exactly dout on its value dims."""
+    rng = np.random.default_rng(42)
+    H, Dqk, Dv = 2, 6, 4
+    q = rng.standard_normal((1, H, Dqk))
+    kv = rng.standard_normal((5, Dqk))
+    idx = np.array([[3, -1]], np.int32)
+    dout = rng.standard_normal((1, H, Dv))
+    f = oracle.sparse_attn(q, kv, idx, 0.5, dv=Dv)
+    dq, dkv, ds = oracle.sparse_attn_bwd(q, kv, idx, 0.5, f["out"], dout, f["lse_kv"])
+    assert np.allclose(dq, 0.0, atol=1e-14)
+    want = np.zeros_like(kv)
+    want[3, :Dv] = dout[0].sum(axis=0)
+    assert np.allclose(dkv, want, atol=1e-14) and np.all(ds == 0.0)
+
+
+def test_attn_bwd_empty_row_contributes_nothing():
+    rng = np.random.default_rng(43)
+    q, kv, idx, tl, sink, dout = _bwd_case(rng)
+    tl = np.zeros_like(tl)
+    f = oracle.sparse_attn(q, kv, idx, 0.3, topk_length=tl, sink=sink, dv=dout.shape[2])
+    dq, dkv, ds = oracle.sparse_attn_bwd(q, kv, idx, 0.3, f["out"], dout, f["lse_kv"], topk_length=tl, sink=sink)
+    assert np.all(dq == 0.0) and np.all(dkv == 0.0) and np.all(ds == 0.0)
