@@ -340,6 +340,36 @@ int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int3
                         int Dqk, int Dv, int K, float scale, void* out, float* lse, float* lse_kv,
                         float* max_logits, cudaStream_t stream);
 
+/* Sparse attention backward ([cuDNN-DSA] 2 Sparse Attention Backward; the
+ * deterministic variant).  Inputs are the forward's: q bf16 [T, H, 576], the
+ * latent kv bf16 [Tkv, 576] (K = V = its first 512 dims), idx / topk_length
+ * as for dsa_sparse_attn_fwd, the forward's out bf16 [T, H, 512], its
+ * KV-only lse_kv fp32 [T, H] (+inf for an empty row), sink fp32 [H] or
+ * NULL, and dout bf16 [T, H, 512].  With s_j = scale * q . k_j over the
+ * valid slots and L = logaddexp(lse_kv, sink):
+ *   P_j = exp(s_j - L),  dS_j = P_j * (dout . v_j - dout . out),
+ *   dq = scale * sum_j dS_j k_j                  -> dq bf16 [T, H, 576] (out)
+ *   dkv[id_j] += scale * dS_j q (+ P_j dout on dims 0..511)
+ *                                                -> dkv fp32 [Tkv, 576] (out)
+ *   d_sink = -sum over rows of exp(sink - L) * (dout . out)
+ *                                                -> d_sink fp32 [H] or NULL
+ * Duplicate ids are separate slots; invalid ids and slots past topk_length
+ * are absent.  P and scale * dS are rounded to bf16 for the tensor-core
+ * products (as P is in the forward); every sum is fp32.  The result is
+ * bitwise reproducible: dkv is accumulated in 128 fp32 copies, each written
+ * by one CTA in a fixed order, and summed in a fixed order; d_sink likewise.
+ *   workspace: dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K) bytes,
+ *   256-byte aligned (it holds P and dS of every slot and the 128 copies).
+ * Shapes: Dqk = 576, Dv = 512, 1 <= H <= 128, K >= 1, scale finite > 0;
+ * q, kv, out, dout, dkv 16-byte aligned.
+ * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE. */
+size_t dsa_sparse_attn_bwd_workspace_size(int T, int Tkv, int H, int K);
+int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* out, const void* dout,
+                        const float* lse_kv, const float* sink, const int32_t* idx,
+                        const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K,
+                        float scale, void* dq, float* dkv, float* d_sink, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream);
+
 /* dsa_sparse_attn_fwd plus the indexer-prefix statistic ([cuDNN-DSA] 1,
  * outputs "lse_indexer" and compile-time "indexer_topk"):
  *   lse_indexer fp32 [T, H] (out): log sum exp(s_j) over the valid slots j <

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdsa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "small_ops.cu", "topk.cu", "indexer.cu", "attention.cu", "pipeline.cu"]
+SOURCES = ["api.cu", "small_ops.cu", "topk.cu", "indexer.cu", "attention.cu", "attention_bwd.cu", "pipeline.cu"]
 HEADERS = ["common.cuh", "block_sort.cuh", "topk_select.cuh"]
 
 

@@ -61,6 +61,8 @@ _SIGNATURES = {
     "dsa_indexer_topk_ratio": ([P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
     "dsa_indexer_scores_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, I64, P], I),
     "dsa_indexer_topk_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
+    "dsa_sparse_attn_bwd_workspace_size": ([I, I, I, I], SZ),
+    "dsa_sparse_attn_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P], I),
 }
 
 
@@ -492,3 +494,37 @@ def pack_routes(routes):
     out = torch.empty((B * S, Wp), dtype=torch.int32, device=routes.device)
     _check("dsa_pack_routes", lib().dsa_pack_routes(_p(routes), B, S, W, _p(out), _stream()))
     return out
+
+
+def sparse_attn_bwd_workspace_size(T: int, Tkv: int, H: int, K: int) -> int:
+    return int(lib().dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K))
+
+
+def sparse_attn_bwd(q, kv, out, dout, lse_kv, idx, scale: float, topk_length=None, sink=None, workspace=None):
+    """Sparse attention backward (latent K = V): dict(dq bf16 [T, H, 576],
+    dkv fp32 [Tkv, 576], d_sink fp32 [H] or None)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv, "kv", torch.bfloat16, 2)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(dout, "dout", torch.bfloat16, 3)
+    _need(lse_kv, "lse_kv", torch.float32, 2)
+    _need(idx, "idx", torch.int32, 2)
+    if topk_length is not None:
+        _need(topk_length, "topk_length", torch.int32, 1)
+    if sink is not None:
+        _need(sink, "sink", torch.float32, 1)
+    T, H, Dqk = q.shape
+    Tkv = kv.shape[0]
+    Dv = out.shape[2]
+    K = idx.shape[1]
+    dev = q.device
+    if workspace is None:
+        workspace = torch.empty(sparse_attn_bwd_workspace_size(T, Tkv, H, K), dtype=torch.uint8, device=dev)
+    dq = torch.empty((T, H, Dqk), dtype=torch.bfloat16, device=dev)
+    dkv = torch.empty((Tkv, Dqk), dtype=torch.float32, device=dev)
+    d_sink = torch.empty(H, dtype=torch.float32, device=dev) if sink is not None else None
+    _check("dsa_sparse_attn_bwd",
+           lib().dsa_sparse_attn_bwd(_p(q), _p(kv), _p(out), _p(dout), _p(lse_kv), _p(sink), _p(idx), _p(topk_length),
+                                     T, Tkv, H, Dqk, Dv, K, float(scale), _p(dq), _p(dkv), _p(d_sink), _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream()))
+    return {"dq": dq, "dkv": dkv, "d_sink": d_sink}

@@ -29,6 +29,26 @@ OUT_FRO_REL = 1e-2
 TOPK_SOFTMAX_REL = 1e-4
 
 
+# Derived (not stated): the backward rounds P and scale*dS to bf16 (2^-9
+# relative) before the tensor-core products and dq to bf16 on output; the
+# sums are fp32.  Normwise the error is a few 2^-9 of the result, so 1e-2
+# Frobenius-relative per output leaves a margin, and no element may be off by
+# more than 2e-2 of the output's largest magnitude.  d_sink involves no bf16
+# rounding beyond the inputs: 1e-3 of the sum of its terms' magnitudes.
+BWD_FRO_REL = 1e-2
+BWD_MAX_REL = 2e-2
+
+
+def assert_bwd_close(got, ref, name):
+    g = got.float().cpu().numpy().astype(np.float64) if hasattr(got, "cpu") else np.asarray(got, np.float64)
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    scale = max(np.max(np.abs(ref)), 1e-30)
+    err = np.abs(g - ref)
+    assert err.max() <= BWD_MAX_REL * scale, f"{name}: max err {err.max():.3g} vs max |ref| {scale:.3g}"
+    fro = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert fro <= BWD_FRO_REL, f"{name}: Frobenius-relative err {fro:.3g}"
+
+
 def assert_topk_softmax_close(sm, lse, ref_sm, ref_lse):
     sm = sm.cpu().numpy().astype(np.float64) if sm is not None else None
     lse = lse.cpu().numpy().astype(np.float64)

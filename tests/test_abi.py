@@ -22,7 +22,8 @@ def test_header_declares_the_hot_path():
                  "dsa_indexer_topk_workspace_size", "dsa_indexer_topk", "dsa_indexer_topk_ex", "dsa_topk_softmax",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex", "dsa_forward_host",
                  "dsa_pack_routes", "dsa_thd_metadata_ratio", "dsa_indexer_scores_ratio", "dsa_indexer_topk_ratio",
-                 "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8",
+                 "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8", "dsa_sparse_attn_bwd",
+                 "dsa_sparse_attn_bwd_workspace_size",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
 
@@ -89,6 +90,14 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
                                        FAKE, 128, NULL),
     lambda L: L.dsa_indexer_topk_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 128, 64, 128, 1, 64, 128,
                                      NULL, NULL, NULL, NULL, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 512, 512, 8, 0.1, FAKE,
+                                    FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 129, 576, 512, 8, 0.1, FAKE,
+                                    FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.0, FAKE,
+                                    FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.1, NULL,
+                                    FAKE, NULL, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, FAKE, NULL, 1, 10, 0, FAKE, FAKE, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, NULL, NULL, 1, 10, 4, FAKE, FAKE, NULL),
     lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 0, 32, FAKE, 32, NULL),

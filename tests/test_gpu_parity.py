@@ -9,8 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (DEV, assert_attention_close, assert_scores_close, assert_topk_softmax_close, cu_from_lengths,
-                      dev, dev_bf16, f64, rand_bf16_bits)
+from gpu_util import (DEV, assert_attention_close, assert_bwd_close, assert_scores_close, assert_topk_softmax_close,
+                      cu_from_lengths, dev, dev_bf16, f64, rand_bf16_bits)
 from sparse_attention_gemm_gb300 import ops
 from sparse_attention_gemm_gb300 import workloads as W
 
@@ -672,3 +672,63 @@ def test_attention_empty_inputs():
     got = _run_attn(q, kv, None, np.zeros((T, 0), np.int32), None, sk, 0.1)
     ref = _ref_attn(q, kv, None, np.zeros((T, 0), np.int32), None, sk, 0.1)
     assert_attention_close(got, ref)
+
+
+# ----------------------------------------------------------- attention backward
+def _bwd_inputs(T, Tkv, H, K, seed, sink=True, lengths="mixed"):
+    """Inputs of the backward, out / lse_kv from the oracle forward (rounded to
+    the storage types the GPU reads; the oracle backward sees the same values)."""
+    rng = np.random.default_rng(seed)
+    q = rand_bf16_bits(rng, (T, H, 576), 0.1)
+    kv = rand_bf16_bits(rng, (Tkv, 576), 0.1)
+    dout = rand_bf16_bits(rng, (T, H, 512), 1.0)
+    idx = rng.integers(-3, Tkv + 3, size=(T, K)).astype(np.int32)
+    idx[0, 1] = idx[0, 0]                 # duplicates inside a tile
+    if K > 70:
+        idx[1, 70] = idx[1, 3]            # and across tiles
+    if lengths == "mixed":
+        tl = rng.integers(0, K + 1, size=T).astype(np.int32)
+        fixed = [K, 0, 1, min(K, 65)][:T]
+        tl[: len(fixed)] = fixed
+    else:
+        tl = np.full(T, K, np.int32)
+    sk = rng.standard_normal(H).astype(np.float32) if sink else None
+    scale = 1.0 / math.sqrt(576.0)
+    f = oracle.sparse_attn(f64(q), f64(kv), idx, scale, topk_length=tl, sink=sk, dv=512)
+    out_bits = W.f32_to_bf16_bits(f["out"].astype(np.float32))
+    lse_kv = f["lse_kv"].astype(np.float32)
+    return q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv
+
+
+@pytest.mark.parametrize("T,Tkv,H,K,sink", [(40, 300, 64, 256, True), (9, 100, 12, 100, True),
+                                            (6, 500, 128, 130, False), (3, 64, 64, 64, True)])
+def test_attention_bwd_against_oracle(T, Tkv, H, K, sink):
+    q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv = _bwd_inputs(T, Tkv, H, K, T * 7 + H, sink)
+    res = ops.sparse_attn_bwd(dev_bf16(q), dev_bf16(kv), dev_bf16(out_bits), dev_bf16(dout), dev(lse_kv), dev(idx),
+                              scale, topk_length=dev(tl), sink=None if sk is None else dev(sk))
+    dq, dkv, ds = oracle.sparse_attn_bwd(f64(q), f64(kv), idx, scale, f64(out_bits), f64(dout),
+                                         lse_kv.astype(np.float64), topk_length=tl, sink=sk)
+    assert_bwd_close(res["dq"], dq, "dq")
+    assert_bwd_close(res["dkv"], dkv, "dkv")
+    if sk is not None:
+        g = res["d_sink"].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(g - ds) <= 1e-3 * np.maximum(np.abs(ds), 1e-3) + 1e-5), (g, ds)
+
+
+def test_attention_bwd_is_deterministic():
+    q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv = _bwd_inputs(64, 200, 64, 192, 5, True, lengths="full")
+    a = (dev_bf16(q), dev_bf16(kv), dev_bf16(out_bits), dev_bf16(dout), dev(lse_kv), dev(idx), scale)
+    r1 = ops.sparse_attn_bwd(*a, topk_length=dev(tl), sink=dev(sk))
+    r2 = ops.sparse_attn_bwd(*a, topk_length=dev(tl), sink=dev(sk))
+    for key in ("dq", "dkv", "d_sink"):
+        assert torch.equal(r1[key].view(torch.int32) if r1[key].dtype == torch.float32 else r1[key].view(torch.int16),
+                           r2[key].view(torch.int32) if r2[key].dtype == torch.float32 else r2[key].view(torch.int16)), key
+
+
+def test_attention_bwd_all_rows_empty():
+    q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv = _bwd_inputs(5, 80, 64, 64, 6, True)
+    tl[:] = 0
+    lse_kv[:] = np.inf
+    res = ops.sparse_attn_bwd(dev_bf16(q), dev_bf16(kv), dev_bf16(out_bits), dev_bf16(dout), dev(lse_kv), dev(idx),
+                              scale, topk_length=dev(tl), sink=dev(sk))
+    assert torch.all(res["dq"].float() == 0) and torch.all(res["dkv"] == 0) and torch.all(res["d_sink"] == 0)
