@@ -275,6 +275,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional outputs")
     ap.add_argument("--no-compressed", action="store_true", help="skip timing the compressed-key indexer")
     ap.add_argument("--no-fp8", action="store_true", help="skip timing the fp8-input indexer")
+    ap.add_argument("--no-bwd", action="store_true", help="skip timing the attention backward")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="attention token ranges in the end-to-end leg")
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
                     help="2: single doc T=4096, 3: THD T=16384, 4: long T=65536 (the headline workload)")
@@ -547,6 +548,29 @@ def main():
                "peak_tflops": peak8, "peak_source": f"{pk['source']} bf16 sustained x 2 (nominal fp8/bf16)"}
         ops.device_status(clear=True)
 
+    # ---- sparse attention backward (deterministic) on the step's own ids,
+    # with a synthetic dout; timed on its own
+    bwd = None
+    if not args.no_bwd:
+        fwd = ops.sparse_attn_fwd(d["q"], d["kv"], idx, wl.scale, topk_length=tl, sink=d["sink"], want_lse_kv=True)
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        dout_t = (torch.randn((T, H, wl.Dv), generator=g, device=dev) * 0.1).to(torch.bfloat16)
+        b_ws = torch.empty(ops.sparse_attn_bwd_workspace_size(T, T, H, K), dtype=torch.uint8, device=dev)
+        b_run = lambda: ops.sparse_attn_bwd(d["q"], d["kv"], fwd["out"], dout_t, fwd["lse_kv"], idx, wl.scale,
+                                            topk_length=tl, sink=d["sink"], workspace=b_ws)
+        b_run()
+        torch.cuda.synchronize()
+        b_ms = timed(b_run)
+        b_flops = work["attn_pairs"] * H * 2 * (3 * wl.Dqk + 2 * wl.Dv)
+        bwd = {"call": "dsa_sparse_attn_bwd (deterministic)", "ms": b_ms, "flops": b_flops,
+               "tflops": b_flops / (b_ms / 1e3) / 1e12,
+               "frac_peak": b_flops / (b_ms / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+               "workspace_gb": b_ws.numel() / 1e9}
+        del fwd, dout_t, b_ws
+        torch.cuda.empty_cache()
+        ops.device_status(clear=True)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and args.workload == 4:
         cpu = cpu_baseline(wl, args.cpu_rows, host["qi"], host["q"], host["w"], host["ki"], host["kv"])
@@ -586,6 +610,7 @@ def main():
             "optional_outputs": extras,
             "compressed_indexer": comp,
             "fp8_indexer": fp8,
+            "attention_backward": bwd,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

@@ -523,6 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -------------------------------------------------------------- 3. dkv
 constexpr int kDkvThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 drain + shard update
 constexpr int kDrainThreads = 128;
+// staging row stride (floats): 4 floats of padding put the eight keys a warp
+// writes at once in different banks (unpadded rows 512 bytes apart collide)
+constexpr int kStageLd = 132;
 
 struct DkvLayout {
   uint32_t qd, a, stage, ids, bars, misc, total;
@@ -534,8 +537,8 @@ __host__ __device__ inline DkvLayout dkv_layout() {
   o += kNv * 2 * kChunkBytes + kChunkBytes;
   L.a = o;  // two buffers of [scale dS chunk | P chunk] (64 slots x 64 heads each)
   o += 2 * 2 * kChunkBytes;
-  L.stage = o;  // 64 keys x 128 dims fp32
-  o += kKeys * 128 * 4;
+  L.stage = o;  // 64 keys x 128 dims fp32, rows padded to kStageLd
+  o += kKeys * kStageLd * 4;
   L.ids = o;  // ids of the tile, first slot of each id in the tile
   o += 2 * kKeys * 4;
   L.bars = o;
@@ -580,6 +583,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   int32_t* tids = reinterpret_cast<int32_t*>(smem + L.ids);
   int32_t* first = tids + kKeys;
+  volatile int* dupflag = reinterpret_cast<volatile int*>(smem + L.misc + 8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* qd_full = bars;
   uint64_t* qd_empty = bars + 1;
@@ -710,6 +714,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           int id = j < len ? __ldg(p.idx + static_cast<int64_t>(t) * p.K + j) : -1;
           tids[dt] = (id >= 0 && id < p.Tkv) ? id : -1;
         }
+        if (dt == 0) *dupflag = 0;
         named_bar(1, kDrainThreads);
         if (dt < kKeys) {
           const int id = tids[dt];
@@ -721,45 +726,69 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
                 break;
               }
           first[dt] = f;
+          if (f != dt) *dupflag = 1;
         }
+        named_bar(1, kDrainThreads);  // first[] of the tile complete
         for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
           const int db = blk_ctr & 1;
           const int nd = nb < 4 ? 128 : 64;
+          // the shard values this thread will update, read while the block's
+          // products finish: thread (key group kg, 4-dim column c4) owns rows
+          // kg + 4k; unique ids never alias, and earlier updates of the same
+          // values are ordered before this by the barrier that ended the
+          // previous block
+          const int kg = dt >> 5, c4 = dt & 31;
+          const bool col_on = 4 * c4 < nd;
+          float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
+          float4 acc[kKeys / 4];
+#pragma unroll
+          for (int k = 0; k < kKeys / 4; ++k) {
+            const int r = kg + 4 * k;
+            const int id = tids[r];
+            acc[k] = (col_on && id >= 0 && first[r] == r) ? base[static_cast<int64_t>(id) * (kDqk / 4)]
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
           if (!dsa::mbar_wait(&d_full[db], (blk_ctr >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
           dsa::tc_fence_after();
-          for (int c0 = 0; c0 < nd; c0 += 32) {
-            uint32_t v[16];
-            dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + c0, v);
+          {
+            uint32_t v[4][16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
             dsa::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int col = c0 + 8 * j + 2 * (lane & 3);
-              *reinterpret_cast<float2*>(stage + kA * 128 + col) =
-                  make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
-              *reinterpret_cast<float2*>(stage + kB * 128 + col) =
-                  make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            for (int q4 = 0; q4 < 4; ++q4) {
+              if (32 * q4 >= nd) continue;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
+                *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                    make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
+                *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                    make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+              }
             }
           }
           dsa::tc_fence_before();
           named_bar(1, kDrainThreads);  // stage and first[] complete
           if (lane == 0) dsa::mbar_arrive(&d_empty[db]);
-          if (dt < nd) {
+          if (*dupflag) {
             // repeated ids: later slots fold into the first one, in slot order
-            for (int r = 1; r < kKeys; ++r)
-              if (first[r] != r) stage[first[r] * 128 + dt] += stage[r * 128 + dt];
-            // read every unique row's shard value first, then write: unique
-            // ids never alias, so the loads need not wait for the stores
-            float* base = shard + nb * 128 + dt;
-            float acc[kKeys];
+            if (dt < nd)
+              for (int r = 1; r < kKeys; ++r)
+                if (first[r] != r) stage[first[r] * kStageLd + dt] += stage[r * kStageLd + dt];
+            named_bar(1, kDrainThreads);
+          }
+          if (col_on) {
 #pragma unroll
-            for (int r = 0; r < kKeys; ++r) {
+            for (int k = 0; k < kKeys / 4; ++k) {
+              const int r = kg + 4 * k;
               const int id = tids[r];
-              acc[r] = (id >= 0 && first[r] == r) ? base[static_cast<int64_t>(id) * kDqk] : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < kKeys; ++r) {
-              const int id = tids[r];
-              if (id >= 0 && first[r] == r) base[static_cast<int64_t>(id) * kDqk] = acc[r] + stage[r * 128 + dt];
+              if (id >= 0 && first[r] == r) {
+                const float4 s = *reinterpret_cast<const float4*>(stage + r * kStageLd + 4 * c4);
+                base[static_cast<int64_t>(id) * (kDqk / 4)] =
+                    make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
+              }
             }
           }
           named_bar(1, kDrainThreads);  // stage is read before the next block overwrites it
