@@ -15,9 +15,12 @@
 // TMEM (2 x 256 fp32 columns, double-buffered) so that the epilogue of one key
 // tile overlaps the MMAs of the next.  Each epilogue thread owns one key (a
 // TMEM lane) and reduces over the heads of its tokens with fma(w[h],
-// max(D, 0), acc) in two interleaved chains over even and odd heads, added
-// at the end; both modes run this same instruction sequence, so the fused
-// mode sees exactly the scores that the dense mode writes.
+// max(D, 0), acc) in four independent chains (head pair i in chain i % 4,
+// two heads per packed fma), summed as a tree at the token's last head; its
+// 128 columns arrive in four 32-column TMEM loads, each issued before the
+// previous chunk is processed.  Both modes run this same instruction
+// sequence, so the fused mode sees exactly the scores that the dense mode
+// writes.
 //
 // Warp roles (320 threads): warp 0 issues TMA loads (qi block once per block,
 // ki tiles through a multi-stage ring), warp 1 allocates TMEM and issues the
@@ -46,6 +49,7 @@
 // this exists for.
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "topk_select.cuh"
@@ -54,9 +58,13 @@ namespace {
 
 constexpr int kKeyTile = 128;
 constexpr int kNRows = 256;
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreads = 64 + kEpiThreads;     // TMA warp, MMA warp, epilogue
+constexpr int kSlices = kEpiWarps / 4;          // column slices of the 256 accumulator columns
+constexpr int kSliceCols = kNRows / kSlices;    // columns one epilogue warp reduces per tile
+constexpr int kSliceChunks = kSliceCols / 32;   // 32-column TMEM loads per tile
+static_assert(kSliceChunks == 2 || kSliceChunks == 4, "a slice is 64 or 128 columns");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kHistWords = 8192;   // 16384 16-bit bin counters shared by the block's rows
 constexpr int kTauUpdateEvery = 512;
@@ -458,13 +466,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------- epilogue
-    const int ew = warp - 2;                  // 0..7
+    const int ew = warp - 2;                  // 0 .. kEpiWarps-1
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
-    const int half = ew >> 2;                 // column half: 0 or 1
+    const int slice = ew >> 2;                // column slice: 0 .. kSlices-1
     const int et = threadIdx.x - 64;          // 0..255
     const int key_lane = quarter * 32 + lane; // key within the tile
     constexpr int QB = kNRows / HI;
-    constexpr int tok_per_half = QB / 2;
+    constexpr int tok_per_slice = QB / kSlices;  // tokens of one column slice
     const int Hi = HI;
     const int hist_words_row = FUSED ? (kHistWords / QB) : 0;
     int acc = 0;
@@ -475,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
       const BlockRange br = block_range<GEN>(p, blk);
       uint32_t cmask = 0u;                 // bit q: this warp's segment of row q was compacted
-      int wcnt[tok_per_half];              // candidates this warp wrote per row (warp-uniform)
+      int wcnt[tok_per_slice];              // candidates this warp wrote per row (warp-uniform)
 #pragma unroll
-      for (int q = 0; q < tok_per_half; ++q) wcnt[q] = 0;
+      for (int q = 0; q < tok_per_slice; ++q) wcnt[q] = 0;
       named_bar(1, kEpiThreads);  // previous block's readers of w_s / tok_* are done
       for (int i = et; i < kNRows; i += kEpiThreads) {
         const int r = i / HI, h = i - r * HI;
@@ -510,13 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (FUSED)
         for (int i = et; i < kHistWords; i += kEpiThreads) hist[i] = 0u;
       named_bar(1, kEpiThreads);
-      // this thread's rows (tokens half*tok_per_half + q): key window
+      // this thread's rows (tokens slice*tok_per_slice + q): key window
       // [rs, rs + rl) in registers, so the per-token check needs no load
-      int rs[tok_per_half], rl[tok_per_half];
+      int rs[tok_per_slice], rl[tok_per_slice];
 #pragma unroll
-      for (int q = 0; q < tok_per_half; ++q) {
-        rs[q] = tok_start[half * tok_per_half + q];
-        rl[q] = tok_len[half * tok_per_half + q];
+      for (int q = 0; q < tok_per_slice; ++q) {
+        rs[q] = tok_start[slice * tok_per_slice + q];
+        rl[q] = tok_len[slice * tok_per_slice + q];
       }
 
       // fp8: this thread's key descale, loaded one tile ahead
@@ -534,47 +542,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!dsa::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) { ok = false; break; }
         dsa::tc_fence_after();
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
-        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows;
-        // columns [half*128, half*128+128) = tokens [half*tok_per_half, ...)
-        // score = sum_h w[h] * max(D[h], 0), as two interleaved fma chains
-        // (even and odd heads) added at the end; fused and dense modes run
-        // this same sequence, so their scores are identical
-        float acc0 = 0.f, acc1 = 0.f;
+        // this warp's columns [slice*kSliceCols, (slice+1)*kSliceCols) = tokens [slice*tok_per_slice, ...)
+        const uint32_t t_addr =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows + slice * kSliceCols;
+        // fused: a row's entry bound for this tile, read once (tau only rises
+        // and a compacted segment's floor only rises, so a value read early
+        // can only admit more candidates)
+        uint32_t thr[tok_per_slice];
+        if (FUSED) {
 #pragma unroll
-        for (int pair = 0; pair < 2; ++pair) {
-          uint32_t v[64];
-          dsa::tmem_ld64(t_addr + half * 128 + pair * 64, v);
-          dsa::tmem_wait_ld();
-          const float2* w2 = reinterpret_cast<const float2*>(w_s + half * 128 + pair * 64);
+          for (int q = 0; q < tok_per_slice; ++q) {
+            const int r = slice * tok_per_slice + q;
+            const uint32_t tau = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
+            const uint32_t fl =
+                ((cmask >> q) & 1u) ? reinterpret_cast<volatile uint32_t*>(seg_floor)[r * 4 + seg] : 0u;
+            thr[q] = max(tau, fl);
+          }
+        }
+        // score = sum_h w[h] * max(D[h], 0).  Head pair (2i, 2i+1) goes to
+        // chain i % 4 (one packed fma per pair), and the four chains are
+        // summed as a tree at the token's last head: four independent
+        // dependency chains instead of one.  Fused and dense modes run this
+        // same sequence, so their scores are identical.
+        float ch[8];
+        auto process = [&](const uint32_t(&v)[32], auto chunk) {
+          constexpr int c = decltype(chunk)::value;  // 32-column chunk of this slice
+          const float4* w4 = reinterpret_cast<const float4*>(w_s + slice * kSliceCols + c * 32);
 #pragma unroll
-          for (int i = 1; i < 64; i += 2) {
-            // heads h-1 (even, chain acc0) and h (odd, chain acc1) in one
-            // packed fma: each lane is the fmaf of the two-chain sum
-            const int cl = pair * 64 + i;             // column within this half (compile-time)
-            const int h = cl % HI;                    // 128 % HI == 0, so the half offset drops out
-            if (h == 1) {
-              acc0 = 0.f;
-              acc1 = 0.f;
+          for (int g = 0; g < 8; ++g) {
+            const int cl = c * 32 + 4 * g;  // first of four columns (compile-time)
+            const int h = cl % HI;          // a multiple of 4 (kSliceCols % HI == 0, HI % 8 == 0)
+            if (h == 0) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) ch[j] = 0.f;
             }
-            const float2 wp = w2[i >> 1];
-            dsa::fma2(acc0, acc1, wp.x, wp.y, fmaxf(__uint_as_float(v[i - 1]), 0.f), fmaxf(__uint_as_float(v[i]), 0.f));
-            if (h == HI - 1) {
-              const float score = F8 ? (acc0 + acc1) * ks : acc0 + acc1;
-              const int r = half * tok_per_half + cl / HI;
+            const float4 wv = w4[g];
+            const int j0 = (h >> 1) & 3;  // 0 or 2; the next pair takes j0 + 1
+            dsa::fma2(ch[2 * j0], ch[2 * j0 + 1], wv.x, wv.y, fmaxf(__uint_as_float(v[4 * g]), 0.f),
+                      fmaxf(__uint_as_float(v[4 * g + 1]), 0.f));
+            dsa::fma2(ch[2 * j0 + 2], ch[2 * j0 + 3], wv.z, wv.w, fmaxf(__uint_as_float(v[4 * g + 2]), 0.f),
+                      fmaxf(__uint_as_float(v[4 * g + 3]), 0.f));
+            if (h + 3 == HI - 1) {
+              const float sum = ((ch[0] + ch[1]) + (ch[2] + ch[3])) + ((ch[4] + ch[5]) + (ch[6] + ch[7]));
+              const float score = F8 ? sum * ks : sum;
+              const int q = cl / HI;  // token within this slice (compile-time)
+              const int r = slice * tok_per_slice + q;
               const int t = br.t0 + r;
-              const int st = rs[cl / HI];
-              const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(rl[cl / HI]);
+              const int st = rs[q];
+              const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(rl[q]);
               if (!FUSED) {
                 if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
                 const uint32_t key = dsa::f32_key(score);
-                const uint32_t fl = ((cmask >> (cl / HI)) & 1u) ? reinterpret_cast<volatile uint32_t*>(seg_floor)[r * 4 + seg] : 0u;
-                const bool emit = valid && key >= *reinterpret_cast<volatile uint32_t*>(&row_tau[r]) && key >= fl;
+                const bool emit = valid && key >= thr[q];
                 // append to this warp's own segment of row t: no atomics, the
                 // warp-uniform counter lives in a register; the segment has
                 // room for a whole tile (compaction below)
                 const uint32_t em = __ballot_sync(0xffffffffu, emit);
-                const int q = cl / HI;  // row index within this half (compile-time)
                 const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
                 if (emit) {
                   __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
@@ -587,6 +611,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+        };
+        // four 32-column TMEM loads, each issued before the previous chunk is
+        // processed, so only the first load's latency is exposed
+        uint32_t va[32], vb[32];
+        dsa::tmem_ld32(t_addr, va);
+        dsa::tmem_wait_ld_pin(va);
+        dsa::tmem_ld32(t_addr + 32, vb);
+        process(va, std::integral_constant<int, 0>{});
+        dsa::tmem_wait_ld_pin(vb);
+        if constexpr (kSliceChunks == 4) {
+          dsa::tmem_ld32(t_addr + 64, va);
+          process(vb, std::integral_constant<int, 1>{});
+          dsa::tmem_wait_ld_pin(va);
+          dsa::tmem_ld32(t_addr + 96, vb);
+          process(va, std::integral_constant<int, 2>{});
+          dsa::tmem_wait_ld_pin(vb);
+          process(vb, std::integral_constant<int, 3>{});
+        } else {
+          process(vb, std::integral_constant<int, 1>{});
         }
         dsa::tc_fence_before();
         __syncwarp();
@@ -596,9 +639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (FUSED && p.compact) {
           // a segment that might not hold the next tile's 32 keys is cut to its top-k
 #pragma unroll
-          for (int q = 0; q < tok_per_half; ++q) {
+          for (int q = 0; q < tok_per_slice; ++q) {
             if (wcnt[q] > cap_seg - 32) {
-              const int r = half * tok_per_half + q;
+              const int r = slice * tok_per_slice + q;
               const int64_t t = br.t0 + r;
               const uint32_t fl = compact_segment(p.cand + (t * 4 + seg) * cap_seg, wcnt[q], p.k, cmp_hist + ew * 256);
               if (lane == 0) {
@@ -616,13 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // new candidates arrived.  No barrier: tau only has to stay a lower
           // bound of the row's k-th largest key, and a histogram read while
           // other warps still add to it can only undercount, which lowers it.
-          const int r0 = half * tok_per_half;
+          const int r0 = slice * tok_per_slice;
           if (lane == 0) {
 #pragma unroll
-            for (int q = 0; q < tok_per_half; ++q)
+            for (int q = 0; q < tok_per_slice; ++q)
               reinterpret_cast<volatile int32_t*>(seg_cnt)[(r0 + q) * 4 + seg] = wcnt[q] + seg_drop[(r0 + q) * 4 + seg];
           }
-          for (int r = r0 + (ew & 3); r < r0 + tok_per_half; r += 4) {
+          for (int r = r0 + (ew & 3); r < r0 + tok_per_slice; r += 4) {
             int cnt = 0;  // candidates emitted so far (stored or since dropped)
             if (lane == 0) {
               const volatile int32_t* sc = reinterpret_cast<volatile int32_t*>(seg_cnt) + r * 4;
@@ -649,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if (lane == 0) {
 #pragma unroll
-        for (int q = 0; q < tok_per_half; ++q) {
-          const int t = br.t0 + half * tok_per_half + q;
+        for (int q = 0; q < tok_per_slice; ++q) {
+          const int t = br.t0 + slice * tok_per_slice + q;
           if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
         }
       }
