@@ -14,7 +14,9 @@
 //      lower bound of the k-th key by construction;
 //   2. one streaming pass (eight 16-byte loads per thread in flight, no block
 //      barrier) appends every (key, column) with key >= tau0 to a shared
-//      candidate buffer, one atomic per warp;
+//      candidate buffer, one atomic per warp; when it starts, the row's next
+//      two rounds are requested into L2, and when it ends, the sampled runs
+//      and first round of the row one resident wave later;
 //   3. the exact k-th key follows from radix passes over the candidates' key
 //      range, the last few keys ranked by one warp;
 //   4. the selected columns are set in a bitmap over the row, which one block
@@ -114,6 +116,19 @@ __device__ __forceinline__ void find_bin(Shared& S, int r, int par) {
   __syncthreads();
 }
 
+// L2 prefetches: fire-and-forget, no registers or shared memory held.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes));
+}
+__device__ __forceinline__ void prefetch_l2_line(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
+// Bytes of columns [c0, min(c0 + cols, n)) of a 16-byte aligned row that a
+// bulk prefetch may cover (a multiple of 16; 0 when nothing is left).
+__device__ __forceinline__ uint32_t prefetch_bytes(int c0, int cols, int n) {
+  const int c1 = c0 + cols < n ? c0 + cols : n;
+  return c1 > c0 ? (static_cast<uint32_t>(c1 - c0) * 4u) & ~15u : 0u;
+}
+
 __device__ __forceinline__ uint32_t block_max(uint32_t v, Shared& S) {
   v = __reduce_max_sync(0xffffffffu, v);
   if ((threadIdx.x & 31) == 0) S.whi[threadIdx.x >> 5] = v;
@@ -198,7 +213,7 @@ __device__ __forceinline__ void mark(Shared& S, const Src& src) {
 __global__ void __launch_bounds__(kThreads, 4)
     topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ len,
                        const int32_t* __restrict__ row_start, int T, int k, int32_t* __restrict__ idx,
-                       int32_t* __restrict__ topk_length, float* __restrict__ vals) {
+                       int32_t* __restrict__ topk_length, float* __restrict__ vals, int ahead) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -314,7 +329,14 @@ __global__ void __launch_bounds__(kThreads, 4)
     tau0 += static_cast<uint32_t>(S.bin) << sshift2;
   }
 
-  // ---- 2. one pass over the row: keys >= tau0 into the candidate buffer
+  // ---- 2. one pass over the row: keys >= tau0 into the candidate buffer.
+  // One thread asks L2 for the next two rounds (a bulk prefetch) while the
+  // first is loaded (measured: 3% faster; prefetching further rounds from
+  // inside the loop cost registers and was slower).
+  if (threadIdx.x == 0) {
+    const uint32_t b = prefetch_bytes(kRound, 2 * kRound, n);
+    if (b) prefetch_l2_bulk(r + kRound, b);
+  }
   for (int b0 = 0; b0 < n; b0 += kRound) {
     float4 v[kU];
 #pragma unroll
@@ -363,6 +385,28 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
   __syncthreads();
   const int nc = S.nc;
+  if (ahead > 0 && static_cast<int64_t>(blockIdx.x) + ahead < T) {
+    // The block `ahead` places later (one resident wave) starts on an SM
+    // about when this row ends: bring its sampled runs and first round into
+    // L2 now, so that its sample phase does not wait on DRAM.
+    const int64_t prow = T - 1 - (static_cast<int64_t>(blockIdx.x) + ahead);
+    int pn = __ldg(len + prow);
+    if (pn > ld) pn = static_cast<int>(ld);
+    if (pn > k) {
+      const float* pr = scores + prow * ld;
+      if (pn > kSample) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int run = 2 * threadIdx.x + h;
+          prefetch_l2_line(pr + (static_cast<int>((static_cast<int64_t>(run) * pn) / kRuns) & ~3));
+        }
+      }
+      if (threadIdx.x == 0) {
+        const uint32_t b = prefetch_bytes(0, kRound, pn);
+        if (b) prefetch_l2_bulk(pr, b);
+      }
+    }
+  }
 
   // ---- 3. exact k-th key
   if (!S.fail && nc >= k) {
@@ -492,12 +536,14 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* len, const int32
 }
 
 int launch_topk_stream(const float* scores, int64_t ld, const int32_t* len, const int32_t* row_start, int T, int k,
-                       int32_t* idx, int32_t* topk_length, float* vals, cudaStream_t stream) {
+                       int32_t* idx, int32_t* topk_length, float* vals, int sm_count, cudaStream_t stream) {
   const size_t smem = sizeof(st::Shared);
   if (cudaFuncSetAttribute(st::topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("topk_stream_kernel smem attribute");
-  st::topk_stream_kernel<<<T, st::kThreads, smem, stream>>>(scores, ld, len, row_start, T, k, idx, topk_length, vals);
+  // four CTAs are resident per SM: the block one wave later is 4 * SMs ahead
+  st::topk_stream_kernel<<<T, st::kThreads, smem, stream>>>(scores, ld, len, row_start, T, k, idx, topk_length, vals,
+                                                            4 * sm_count);
   return dsa::launch_error("topk_stream_kernel");
 }
 
@@ -510,12 +556,13 @@ extern "C" int dsa_topk(const float* scores, int64_t ld, const int32_t* len, con
     return dsa::set_error(DSA_ERR_VALUE, "dsa_topk: need T >= 0, ld >= 1, 1 <= k <= %d", DSA_MAX_TOPK);
   if (ld > INT32_MAX) return dsa::set_error(DSA_ERR_VALUE, "dsa_topk: ld exceeds the int32 column range");
   if (T > 0 && (!scores || !len || !idx)) return dsa::set_error(DSA_ERR_VALUE, "dsa_topk: NULL pointer");
-  int rc = dsa::check_device(nullptr);
+  int sm_count = 0;
+  int rc = dsa::check_device(&sm_count);
   if (rc != DSA_OK) return rc;
   if (T == 0) return DSA_OK;
   const bool vec4 = ld % 4 == 0 && dsa::aligned(scores, 16);
   if (vec4 && ld <= st::kMaxLen)
-    return launch_topk_stream(scores, ld, len, row_start, T, k, idx, topk_length, vals, stream);
+    return launch_topk_stream(scores, ld, len, row_start, T, k, idx, topk_length, vals, sm_count, stream);
   if (vec4) return launch_topk<true>(scores, ld, len, row_start, T, k, idx, topk_length, vals, stream);
   return launch_topk<false>(scores, ld, len, row_start, T, k, idx, topk_length, vals, stream);
 }
