@@ -66,7 +66,7 @@ constexpr int kSliceCols = kNRows / kSlices;    // columns one epilogue warp red
 constexpr int kSliceChunks = kSliceCols / 32;   // 32-column TMEM loads per tile
 static_assert(kSliceChunks == 2 || kSliceChunks == 4, "a slice is 64 or 128 columns");
 constexpr uint32_t kTmemCols = 512;
-constexpr int kHistWords = 8192;   // 16384 16-bit bin counters shared by the block's rows
+constexpr int kHistWords = 8192;   // 32-bit bin counters shared by the block's rows
 constexpr int kTauUpdateEvery = 512;
 
 // Which keys each query row sees (see the file comment).  Row lengths are
@@ -281,21 +281,43 @@ __device__ __noinline__ uint32_t compact_segment(uint2* seg, int n, int k, uint3
   return prefix == 0xFFFFFFFFu ? prefix : prefix + 1u;
 }
 
-// Raise tau of one row from its packed 16-bit histogram (one warp): find the
-// highest bin b at which the counts of bins >= b reach k and set tau to b's
-// lower edge (only ever raised).  Two warp scans: first over 32 contiguous
-// groups of words (lane 0 = highest), then over the words of the crossing
-// group spread across the lanes.
-__device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, int hist_bits, int k, uint32_t* tau) {
+// Row histogram bins: a window of 64 octaves of positive scores, [2^-32,
+// 2^32), at 2^(bits-6) bins per octave (32 for 2048 bins); keys below the
+// window (negative, zero and tiny scores) share bin 0 and keys above it the
+// top bin.  The map is monotone in the key and hist_edge(b) is the smallest
+// key that bin b holds, so the edge of a bin is a lower bound of every key
+// counted at or above it.  (The leading key bits alone would give 8 bins per
+// octave, and index scores typically span an octave or two.)
+constexpr uint32_t kHistWindowLo = 0xAF800000u;  // the key of 2^-32
+__device__ __forceinline__ uint32_t hist_bin(uint32_t key, int bits) {
+  const int shift = 29 - bits;  // keeps bits - 6 mantissa bits
+  const int b = static_cast<int>(key >> shift) - static_cast<int>(kHistWindowLo >> shift);
+  return static_cast<uint32_t>(min(max(b, 0), (1 << bits) - 1));
+}
+__device__ __forceinline__ uint32_t hist_edge(int bin, int bits) {
+  const int shift = 29 - bits;
+  return bin == 0 ? 0u : (static_cast<uint32_t>(bin) + (kHistWindowLo >> shift)) << shift;
+}
+
+// Raise tau of one row from its histogram (one warp, one 32-bit counter per
+// bin): find the highest bin b at which the counts of bins >= b reach k and
+// set tau to b's lower edge (only ever raised).  Bins below the current
+// tau's bin cannot give a higher edge, so only bins from that one up are
+// read.  Two warp scans: first over 32 contiguous groups of those bins
+// (lane 0 = highest), then over the bins of the crossing group spread across
+// the lanes.
+__device__ __forceinline__ void update_tau(const uint32_t* hist_row, int bins, int hist_bits, int k, uint32_t* tau) {
   const int lane = threadIdx.x & 31;
-  const int per = words / 32;  // words per group; group 0 holds the highest bins
-  const int w_hi = words - lane * per;
+  const int b_lo = static_cast<int>(hist_bin(*reinterpret_cast<volatile uint32_t*>(tau), hist_bits));
+  int per = 1;  // bins per group, a power of two; group 0 holds the highest bins
+  while (per * 32 < bins - b_lo) per <<= 1;
+  const int b_hi = bins - lane * per;
   int s = 0;
   // the sum does not depend on order: start each lane at a different offset so
-  // that the 32 lanes read 32 different banks (per is a multiple of 32)
+  // that the lanes spread over the banks
   for (int j = 0; j < per; ++j) {
-    const uint32_t v = hist_row[w_hi - 1 - ((j + lane) & (per - 1))];
-    s += static_cast<int>((v & 0xFFFFu) + (v >> 16));
+    const int bi = b_hi - 1 - ((j + lane) & (per - 1));
+    if (bi >= b_lo) s += static_cast<int>(hist_row[bi]);
   }
   int incl = s;
 #pragma unroll
@@ -304,16 +326,14 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, 
     if (lane >= o) incl += y;
   }
   const uint32_t hit = __ballot_sync(0xffffffffu, incl >= k);
-  if (hit == 0u) return;               // fewer than k candidates so far
+  if (hit == 0u) return;               // fewer than k candidates at or above tau's bin so far
   const int g = __ffs(hit) - 1;        // crossing group
   int before = __shfl_sync(0xffffffffu, incl - s, g);
-  // words of group g, top down, spread over the lanes in rounds of 32
-  const int g_hi = words - g * per;
+  // bins of group g, top down, spread over the lanes in rounds of 32
+  const int g_hi = bins - g * per;
   for (int r0 = 0; r0 < per; r0 += 32) {
-    const int wi = g_hi - 1 - r0 - lane;  // lane 0 takes the highest word of the round
-    const uint32_t v = (r0 + lane < per) ? hist_row[wi] : 0u;  // groups narrower than 32 words
-    const int hi_c = static_cast<int>(v >> 16), lo_c = static_cast<int>(v & 0xFFFFu);
-    const int c = hi_c + lo_c;
+    const int bi = g_hi - 1 - r0 - lane;  // lane 0 takes the highest bin of the round
+    const int c = (r0 + lane < per && bi >= b_lo) ? static_cast<int>(hist_row[bi]) : 0;  // groups narrower than 32
     int inc = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -322,11 +342,8 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int words, 
     }
     const uint32_t h2 = __ballot_sync(0xffffffffu, before + inc >= k);
     if (h2 != 0u) {
-      const int l2 = __ffs(h2) - 1;
-      if (lane == l2) {
-        const int ex = before + inc - c;     // count of bins above this word
-        const int bin = (ex + hi_c >= k) ? 2 * wi + 1 : 2 * wi;
-        const uint32_t t = static_cast<uint32_t>(bin) << (32 - hist_bits);
+      if (lane == __ffs(h2) - 1) {
+        const uint32_t t = hist_edge(bi, hist_bits);
         volatile uint32_t* vt = tau;
         if (t > *vt) *vt = t;
       }
@@ -602,10 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
                 if (emit) {
                   __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
-                  // histogram of stored keys; bin b lives in 16-bit half (b & 1) of word (b >> 1);
-                  // the result is unused, so this is a fire-and-forget reduction
-                  const uint32_t bin = key >> (32 - p.hist_bits);
-                  atomicAdd(&hist[r * hist_words_row + (bin >> 1)], 1u << (16 * (bin & 1)));
+                  // histogram of stored keys, one 32-bit counter per bin; the
+                  // result is unused, so this is a fire-and-forget reduction
+                  atomicAdd(&hist[r * hist_words_row + hist_bin(key, p.hist_bits)], 1u);
                 }
                 wcnt[q] += __popc(em);
               }
@@ -1351,7 +1367,7 @@ int run_candidates(const Inputs& in, const Geom& g, int k, void* workspace, int 
   p.cap = fused_cap(g.s_max, k);
   p.compact = fused_compact(g.s_max, k);
   p.k = k;
-  int bins = 2 * kHistWords / p.qb;
+  int bins = kHistWords / p.qb;
   int bits = 0;
   while ((1 << bits) < bins) ++bits;
   p.hist_bits = bits;

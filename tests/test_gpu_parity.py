@@ -524,6 +524,44 @@ def test_fused_topk_exact_when_every_key_beats_the_running_threshold(pattern, k)
     assert np.array_equal(got[rows], oi)
 
 
+def _long_rising_inputs(T, Hi=8, d=64):
+    """Integer inputs whose scores are 2^21 + j along the key axis, strictly
+    rising within one narrow band (2^21 .. 2^21 + T, under 4% wide), exact in
+    bf16 and in fp32 accumulation: q = (2^21, 65536, 256, 1) against
+    k[j] = (1, c, a, b) with j = 65536 c + 256 a + b."""
+    j = np.arange(T)
+    qi = np.zeros((T, Hi, d), np.float32)
+    qi[:, 0, :4] = (2.0 ** 21, 65536.0, 256.0, 1.0)
+    ki = np.zeros((T, d), np.float32)
+    ki[:, 0], ki[:, 1], ki[:, 2], ki[:, 3] = 1.0, j >> 16, (j >> 8) & 255, j & 255
+    w = np.zeros((T, Hi), np.float32)
+    w[:, 0] = 1.0
+    return W.f32_to_bf16_bits(qi), W.f32_to_bf16_bits(ki), w
+
+
+@pytest.mark.parametrize("k", [1, 16])
+def test_fused_topk_long_rising_rows_in_one_narrow_band(k):
+    """Rows of up to 70001 keys whose scores rise inside a band a few percent
+    wide: every key beats the running threshold, so more than 65535 keys of a
+    row land in the same histogram bin.  The threshold must stay a lower bound
+    of the k-th key (a bin count that wrapped into its neighbour would push it
+    above the row's maximum); the top-k are the last k keys of each row."""
+    T = 70001
+    qi, ki, w = _long_rising_inputs(T)
+    cu = np.array([0, T], np.int32)
+    a = (dev_bf16(qi), dev_bf16(ki), dev(w), dev(cu))
+    ops.device_status(clear=True)
+    idx, tl = ops.indexer_topk(*a, k, T)
+    torch.cuda.synchronize()
+    assert ops.device_status(clear=True) == 0
+    got = idx.cpu().numpy()
+    t = np.arange(T)
+    long_rows = t + 1 > k
+    want = (t[long_rows, None] - k + 1) + np.arange(k)[None, :]
+    assert np.array_equal(got[long_rows], want)
+    assert np.array_equal(tl.cpu().numpy(), np.minimum(t + 1, k))
+
+
 def test_fused_topk_rows_longer_than_65536_columns():
     """Rows past 65536 columns take the other stage-2 selection (its column
     bitmap has no 16-bit limit); the result must still equal the unfused path."""
