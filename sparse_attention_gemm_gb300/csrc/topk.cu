@@ -337,6 +337,14 @@ __global__ void __launch_bounds__(kThreads, 4)
     const uint32_t b = prefetch_bytes(kRound, 2 * kRound, n);
     if (b) prefetch_l2_bulk(r + kRound, b);
   }
+  // The pass compares floats: for every non-NaN x, key(x) >= tau0 exactly
+  // when x >= tau0f (the key order is the float order with -0 == +0; a
+  // threshold at or below the key of -inf admits every x).  NaN scores have
+  // no defined order; they are never candidates here.  Columns past the row
+  // (the tail of the last float4, which is still inside the ld-wide row) are
+  // dropped by one mask per round, not by a test per element (measured:
+  // 4.28 -> 3.81 ms for both changes on 65536 rows of 65536 columns).
+  const float tau0f = tau0 <= 0x007FFFFFu ? -INFINITY : dsa::key_f32(tau0);
   for (int b0 = 0; b0 < n; b0 += kRound) {
     float4 v[kU];
 #pragma unroll
@@ -347,11 +355,19 @@ __global__ void __launch_bounds__(kThreads, 4)
     uint32_t pass = 0u;
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int j = b0 + u * (kThreads * 4) + 4 * threadIdx.x;
-      pass |= (j < n && dsa::f32_key(v[u].x) >= tau0) ? 1u << (4 * u) : 0u;
-      pass |= (j + 1 < n && dsa::f32_key(v[u].y) >= tau0) ? 1u << (4 * u + 1) : 0u;
-      pass |= (j + 2 < n && dsa::f32_key(v[u].z) >= tau0) ? 1u << (4 * u + 2) : 0u;
-      pass |= (j + 3 < n && dsa::f32_key(v[u].w) >= tau0) ? 1u << (4 * u + 3) : 0u;
+      pass |= v[u].x >= tau0f ? 1u << (4 * u) : 0u;
+      pass |= v[u].y >= tau0f ? 1u << (4 * u + 1) : 0u;
+      pass |= v[u].z >= tau0f ? 1u << (4 * u + 2) : 0u;
+      pass |= v[u].w >= tau0f ? 1u << (4 * u + 3) : 0u;
+    }
+    if (b0 + kRound > n) {  // the last round: drop the columns past the row
+      uint32_t in_row = 0u;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = n - (b0 + u * (kThreads * 4) + 4 * static_cast<int>(threadIdx.x));
+        in_row |= (c >= 4 ? 15u : c > 0 ? (1u << c) - 1u : 0u) << (4 * u);
+      }
+      pass &= in_row;
     }
     const int cnt = __popc(pass);
     int incl = cnt;
