@@ -54,12 +54,18 @@ def _load():
             L = ctypes.c_int64
             D = ctypes.c_double
             lib.oracle_num_threads.restype = I
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_set_num_threads.restype = I
             lib.oracle_thd_metadata.argtypes = [P, I, I, P, P]
             lib.oracle_thd_metadata.restype = I
             lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_value.restype = D
             lib.oracle_fp8_dequant.argtypes = [P, P, L, I, P]
             lib.oracle_fp8_dequant.restype = None
+            lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_value.restype = D
+            lib.oracle_mxfp8_dequant.argtypes = [P, P, L, I, P]
+            lib.oracle_mxfp8_dequant.restype = None
             lib.oracle_ratio_metadata.argtypes = [P, P, P, I, I, I, I, P, P]
             lib.oracle_ratio_metadata.restype = I
             lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
@@ -94,6 +100,11 @@ def _i32(a):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads of the oracle's row loops from now on; returns the previous count."""
+    return int(_load().oracle_set_num_threads(int(n)))
 
 
 def thd_metadata(cu_seqlens, T: int):
@@ -139,6 +150,25 @@ def fp8_dequant(codes, scales):
     out = np.empty(c.shape, np.float64)
     rows = int(np.prod(c.shape[:-1]))
     _load().oracle_fp8_dequant(_ptr(c), _ptr(s), rows, int(c.shape[-1]), _ptr(out))
+    return out
+
+
+def e8m0_value(code: int) -> float:
+    """The value of one E8M0 scale byte (see dsa_oracle.c)."""
+    return float(_load().oracle_e8m0_value(int(code) & 0xFF))
+
+
+def mxfp8_dequant(codes, scales):
+    """fp64 codes[..., len] decoded from E4M3, each block of 32 consecutive
+    elements multiplied by its E8M0 scale: scales has the shape of codes with
+    the last axis len / 32 (uint8 biased exponents)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    if c.shape[-1] % 32 != 0 or s.shape != c.shape[:-1] + (c.shape[-1] // 32,):
+        raise ValueError("one E8M0 scale per 32 elements of each row of codes")
+    out = np.empty(c.shape, np.float64)
+    rows = int(np.prod(c.shape[:-1]))
+    _load().oracle_mxfp8_dequant(_ptr(c), _ptr(s), rows, int(c.shape[-1]), _ptr(out))
     return out
 
 

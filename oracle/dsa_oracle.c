@@ -47,6 +47,19 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads the row loops below use from now on (n >= 1); for timing the
+ * oracle on one core and on all of them.  Returns the previous count. */
+int oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  const int prev = omp_get_max_threads();
+  if (n >= 1) omp_set_num_threads(n);
+  return prev;
+#else
+  (void)n;
+  return 1;
+#endif
+}
+
 /* ------------------------------------------------------------------------
  * THD metadata [P1 prepare_cudnn_dsa_packed_metadata, "Returns": per-query
  * storage starts and real causal lengths].  Tokens of document b occupy
@@ -130,6 +143,32 @@ void oracle_fp8_dequant(const uint8_t* codes, const float* scales, int64_t rows,
   for (int64_t r = 0; r < rows; ++r)
     for (int i = 0; i < len; ++i)
       out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[r];
+}
+
+/* ------------------------------------------------------------------------
+ * MXFP8 indexer inputs [P5 section 3, precision path "mxfp8": Q/K in E4M3
+ * with block-scaled E8M0 scales, sf_vec_size 32].  An E8M0 scale is an
+ * exponent alone: byte e stands for 2^(e - 127) (e = 0 .. 254); e = 255 is
+ * NaN.  A row of `len` codes carries len / 32 scales, scale b applying to
+ * elements 32 b .. 32 b + 31:
+ *   x[i] = value(codes[i]) * 2^(scales[i / 32] - 127).
+ * The dequantized tensors then go through oracle_indexer_scores unchanged,
+ * so each dot product is the block-scaled sum
+ *   sum_b 2^(eq_b - 127) * 2^(ek_b - 127) * sum_{i in block b} q[i] * k[i].
+ * The page leaves the packed storage of the scales to its library; here they
+ * are plain [rows, len / 32] bytes.
+ * ------------------------------------------------------------------------ */
+double oracle_e8m0_value(uint8_t e) {
+  if (e == 255) return NAN;
+  return ldexp(1.0, (int)e - 127);
+}
+
+void oracle_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int64_t rows, int len, double* out) {
+  const int nb = len / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int i = 0; i < len; ++i)
+      out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * oracle_e8m0_value(scales[r * nb + i / 32]);
 }
 
 /* ------------------------------------------------------------------------

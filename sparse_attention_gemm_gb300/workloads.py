@@ -36,6 +36,12 @@ Recipe (every draw is reproducible and addressable by row):
   holds ``ceil((offset + queries) / ratio)`` compressed key rows (every block
   of ``ratio`` tokens up to its last query, the last one possibly partial).
   Indexer q/k/w as for the bf16 workloads, ki with that many rows.
+* MXFP8 indexer inputs (any workload): the bf16 qi / ki values, quantized per
+  block of 32 consecutive elements of a row (OCP MX recipe): the block's
+  E8M0 scale byte is floor(log2(max |x|)) - 8 + 127 (E4M3's largest power of
+  two is 2^8), clamped to [0, 254] (127 for an all-zero block), and the codes
+  are E4M3 of x / 2^(byte - 127) clipped to [-448, 448], rounded to nearest
+  even (torch's float8_e4m3fn conversion).
 * FP8 indexer inputs (any workload): the bf16 qi / ki values, quantized per
   row (a (token, head) row of qi, a key row of ki): descale =
   float32(max |x| / 448) (1 for an all-zero row), code = E4M3 of x / descale
@@ -223,6 +229,29 @@ class Workload:
         y = np.clip(x / scale[..., None], -448.0, 448.0).astype(np.float32)
         codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         return codes, scale
+
+    @staticmethod
+    def _to_mxfp8(bits: np.ndarray):
+        """(E4M3 codes, E8M0 scale bytes per 32 elements) of bf16 bits [..., n]."""
+        import torch
+
+        x = bf16_bits_to_f32(bits)
+        blk = x.reshape(x.shape[:-1] + (x.shape[-1] // 32, 32))
+        amax = np.max(np.abs(blk), axis=-1)
+        with np.errstate(divide="ignore"):
+            e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, 0).astype(np.int32)
+        byte = np.clip(e + 127, 0, 254)
+        y = np.clip(blk / np.ldexp(np.float32(1.0), byte - 127)[..., None], -448.0, 448.0).astype(np.float32)
+        codes = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return codes.reshape(x.shape), byte.astype(np.uint8)
+
+    def qi_mxfp8(self, rows=None):
+        """Indexer query as E4M3 codes [n, Hi, d] (uint8) and E8M0 block scales [n, Hi, d/32] (uint8)."""
+        return self._to_mxfp8(self.qi_bits(rows))
+
+    def ki_mxfp8(self):
+        """Indexer key as E4M3 codes [Tk, d] (uint8) and E8M0 block scales [Tk, d/32] (uint8)."""
+        return self._to_mxfp8(self.ki_bits())
 
     def qi_fp8(self, rows=None):
         """Indexer query as E4M3 codes [n, Hi, d] (uint8) and descales [n, Hi] (fp32)."""

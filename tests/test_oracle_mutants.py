@@ -51,6 +51,10 @@ MUTANTS = {
     "e4m3_no_nan": ("if (e == 15 && m == 7) return NAN;", ""),
     "fp8_descale_wrong_row": ("out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[r];",
                               "out[r * len + i] = oracle_e4m3_value(codes[r * len + i]) * (double)scales[0];"),
+    "e8m0_bias_126": ("return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
+    "e8m0_no_nan": ("  if (e == 255) return NAN;\n  return ldexp", "  return ldexp"),
+    "mxfp8_block_of_16": ("oracle_e8m0_value(scales[r * nb + i / 32])", "oracle_e8m0_value(scales[r * nb + i / 16])"),
+    "mxfp8_scale_row_ignored": ("oracle_e8m0_value(scales[r * nb + i / 32])", "oracle_e8m0_value(scales[i / 32])"),
     "bwd_drop_delta": ("const double ds = p * (dp - delta);", "const double ds = p * dp;"),
     "bwd_dq_without_scale": ("for (int c = 0; c < Dqk; ++c) dq[c] += scale * ds * k[c];",
                              "for (int c = 0; c < Dqk; ++c) dq[c] += ds * k[c];"),

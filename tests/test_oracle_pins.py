@@ -172,6 +172,66 @@ def test_fp8_descales_scale_rows_and_columns():
     assert np.array_equal(np.delete(r, 3, 1), np.delete(base, 3, 1))
 
 
+def test_e8m0_golden_values():
+    g = _gold("e8m0.json")
+    for code, v in g["values"].items():
+        assert oracle.e8m0_value(int(code)) == v, code
+    for code in g["nan"]:
+        assert np.isnan(oracle.e8m0_value(code))
+
+
+def test_mxfp8_unit_scales_reduce_to_e4m3():
+    """With every E8M0 scale 127 (the power 1) the block-scaled decoding is
+    the plain E4M3 decoding of the per-row-descale path with descale 1."""
+    rng = np.random.default_rng(41)
+    codes = rng.integers(0, 256, size=(6, 128)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38
+    got = oracle.mxfp8_dequant(codes, np.full((6, 4), 127, np.uint8))
+    ref = oracle.fp8_dequant(codes, np.ones(6, np.float32))
+    assert np.array_equal(got, ref)
+
+
+def test_mxfp8_block_scaled_score_closed_form():
+    """One query head and one key of 128 elements, every code 1.0 (0x38),
+    scales 2^b on the query's block b: the score is 32 * (1 + 2 + 4 + 8) =
+    480.  With the key's scales 2^(3-b) every block contributes 32 * 8: 1024.
+    A block of -1.0 codes (0xB8) subtracts its share, and a negative total is
+    cut by the ReLU."""
+    q = np.full((1, 1, 128), 0x38, np.uint8)
+    k = np.full((1, 128), 0x38, np.uint8)
+    w = np.ones((1, 1))
+    st, ln = np.zeros(1, np.int32), np.ones(1, np.int32)
+    qs = np.array([[[127, 128, 129, 130]]], np.uint8)
+
+    def score(qc, qsc, kc, ksc):
+        return oracle.indexer_scores(oracle.mxfp8_dequant(qc, qsc), oracle.mxfp8_dequant(kc, ksc), w, st, ln, 1)[0, 0]
+
+    assert score(q, qs, k, np.full((1, 4), 127, np.uint8)) == 480.0
+    assert score(q, qs, k, np.array([[130, 129, 128, 127]], np.uint8)) == 1024.0
+    qn = q.copy()
+    qn[0, 0, 64:96] = 0xB8  # block 2 (scale 4) negated: 32 * (1 + 2 - 4 + 8)
+    assert score(qn, qs, k, np.full((1, 4), 127, np.uint8)) == 224.0
+    qn[0, 0, 96:128] = 0xB8  # blocks 2 and 3 negated: 32 * (1 + 2 - 4 - 8) < 0
+    assert score(qn, qs, k, np.full((1, 4), 127, np.uint8)) == 0.0
+
+
+def test_mxfp8_scale_moves_only_its_block():
+    """Raising one scale byte of one row by 1 doubles exactly the 32 elements
+    of that block of that row; every other element is unchanged."""
+    rng = np.random.default_rng(42)
+    codes = rng.integers(0, 256, size=(5, 3, 64)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38
+    sc = rng.integers(110, 140, size=(5, 3, 2)).astype(np.uint8)
+    base = oracle.mxfp8_dequant(codes, sc)
+    sc2 = sc.copy()
+    sc2[3, 1, 1] += 1
+    r = oracle.mxfp8_dequant(codes, sc2)
+    assert np.array_equal(r[3, 1, 32:], 2 * base[3, 1, 32:])
+    mask = np.ones(base.shape, bool)
+    mask[3, 1, 32:] = False
+    assert np.array_equal(r[mask], base[mask])
+
+
 def _rand_bf16_like(rng, shape, lo=-4, hi=4):
     return rng.integers(lo, hi + 1, size=shape).astype(np.float64)
 
