@@ -57,6 +57,8 @@ extern "C" {
 /* Bits of the device status word (see dsa_device_status). */
 #define DSA_STATUS_WAIT_TIMEOUT 0x1u   /* a bounded device wait gave up */
 #define DSA_STATUS_CAND_OVERFLOW 0x2u  /* fused top-k candidate buffer overflowed */
+#define DSA_STATUS_DRAIN_TIMEOUT 0x4u  /* an aborting CTA gave up waiting for its own copies / MMAs */
+#define DSA_STATUS_CHECK_FAILED 0x8u   /* checked build only: an in-kernel range check failed (access skipped) */
 
 /* Limits ([NeMo-GLM] _MAX_TOPK = 2048, _INDEX_HEAD_DIM = 128,
  * _ATTENTION_HEAD_DIM = 576, _VALUE_HEAD_DIM = 512; [cuDNN-DSA] 5: top_k <= 2048). */
@@ -72,6 +74,22 @@ const char* dsa_last_error(void);
  * This call synchronises the device (it is a diagnostic, not part of the
  * hot path).  Returns DSA_OK or DSA_ERR_CUDA / DSA_ERR_UNSUPPORTED. */
 int dsa_device_status(uint32_t* flags, int clear);
+
+/* Failure-detection hook (no counterpart on the pages, which only describe
+ * request-or-fail validation).  Every wait of a tcgen05 / TMA kernel on an
+ * mbarrier gives up after a limit, raises DSA_STATUS_WAIT_TIMEOUT, and the
+ * kernel then leaves in order: the CTA's roles agree to stop at their
+ * barriers, each waits (bounded by 2 s regardless of this setting) for the
+ * copies and MMAs it issued, TMEM is freed and the kernel returns, so the
+ * context stays usable.  This call sets that limit for kernels launched
+ * afterwards on the current device: 0 restores the default (2 s, far above
+ * any legitimate wait); a tiny value (e.g. 1 ns) makes the first wait that is
+ * not already satisfied give up, which is how the abort path is exercised
+ * without a real hang.  Outputs of a call whose kernels aborted are
+ * unspecified.  Synchronises the device; call it with none of this
+ * library's kernels in flight.  Returns DSA_OK or DSA_ERR_CUDA /
+ * DSA_ERR_UNSUPPORTED. */
+int dsa_set_wait_limit_ns(uint64_t limit_ns);
 
 /* THD metadata ([NeMo-GLM] prepare_cudnn_dsa_packed_metadata, "Returns":
  * per-query storage starts and real causal lengths).

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -13,8 +14,9 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
-// Status word of this library on each device (OR of DSA_STATUS_* bits).
-__device__ uint32_t g_status_word;
+// Control block of this library on each device: the status word (OR of
+// DSA_STATUS_* bits) and the wait-limit override (0: the default).
+__device__ dsa::DeviceControl g_ctl;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -62,7 +64,7 @@ int check_device(int* sm_count) {
       g_dev_sm_count[dev] = major * 10 + minor;
     } else {
       void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+      if (cudaGetSymbolAddress(&p, g_ctl) != cudaSuccess) {
         cudaGetLastError();
         return set_error(DSA_ERR_CUDA, "cannot resolve the device status word");
       }
@@ -144,13 +146,25 @@ extern "C" int dsa_device_status(uint32_t* flags, int clear) {
   int rc = dsa::check_device(nullptr);
   if (rc != DSA_OK) return rc;
   uint32_t v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(&v, g_ctl, sizeof(v), offsetof(dsa::DeviceControl, status)) != cudaSuccess)
     return dsa::launch_error("dsa_device_status read");
   if (clear) {
     uint32_t z = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &z, sizeof(z)) != cudaSuccess)
+    if (cudaMemcpyToSymbol(g_ctl, &z, sizeof(z), offsetof(dsa::DeviceControl, status)) != cudaSuccess)
       return dsa::launch_error("dsa_device_status clear");
   }
   *flags = v;
+  return DSA_OK;
+}
+
+extern "C" int dsa_set_wait_limit_ns(uint64_t limit_ns) {
+  dsa::clear_error();
+  int rc = dsa::check_device(nullptr);
+  if (rc != DSA_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return dsa::launch_error("dsa_set_wait_limit_ns synchronize");
+  if (cudaMemcpyToSymbol(g_ctl, &limit_ns, sizeof(limit_ns), offsetof(dsa::DeviceControl, wait_limit_ns)) !=
+      cudaSuccess)
+    return dsa::launch_error("dsa_set_wait_limit_ns write");
+  if (cudaDeviceSynchronize() != cudaSuccess) return dsa::launch_error("dsa_set_wait_limit_ns synchronize");
   return DSA_OK;
 }

@@ -192,6 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 10;
   uint64_t* q_empty = bars + 11;
   uint64_t* o_done = bars + 12;
+  uint64_t* drain = bars + 13;     // [2]: the MMA issuers' exit commits
+  // Completes once per unit, after the unit's last MMA2.  The epilogue waits
+  // on it rather than on o_done: o_done completes once per tile, and a parity
+  // wait for the last tile's phase would also pass while the tile before it
+  // is still running (its phase has the other parity).  Nothing orders that
+  // tile's MMA2 before the softmax of the last tile; for the rescale, which
+  // waits on o_done for tile i-1 while processing tile i, MMA2 of tile i-2 has
+  // completed (it released the buffer that tile i was gathered into).
+  uint64_t* o_unit = bars + 15;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -209,6 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     dsa::mbar_init(q_full, 1);
     dsa::mbar_init(q_empty, 1);
     dsa::mbar_init(o_done, 1);
+    dsa::mbar_init(&drain[0], 1);
+    dsa::mbar_init(&drain[1], 1);
+    dsa::mbar_init(o_unit, 1);
     *abort_flag = 0;
     dsa::fence_barrier_init();
   }
@@ -217,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   dsa::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
 
   if (warp < kGatherWarps) {
     // ------------------------------------------------------------ gather
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = (i + 1) * kKeys + jk;
           nxt[kg] = (i + 1 < nt && jk < kKeys && j < len) ? __ldcs(irow + j) : -1;
         }
-        if (!dsa::mbar_wait(&kv_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        if (!dsa::mbar_wait(&kv_empty[b], ((tile_ctr >> 1) & 1) ^ 1, wt)) { ok = false; break; }
         dsa::fence_proxy_async_smem();
         const uint32_t buf = dsa::smem_u32(kvbuf) + b * L.buf_bytes;
 #pragma unroll
@@ -263,6 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key >= kKeys) continue;
           const uint32_t nbytes = id[kg] >= 0 ? 16u : 0u;
           const int64_t row = id[kg] >= 0 ? id[kg] : 0;
+          // checked build: the row is inside kv (and v), the slot inside the tile buffer
+          if (!dsa::check(row < p.Tkv && (p.n_qk + (p.v ? p.n_v : 0)) * kChunkBytes <= L.buf_bytes, p.status))
+            continue;
           const uint8_t* krow = p.kv + row * p.kv_row_bytes + piece * 16;
           for (int c = 0; c < p.n_qk; ++c)
             cp_async16(buf + c * kChunkBytes + dsa::sw128_offset(key, piece * 16), krow + c * 128, nbytes, keep);
@@ -321,17 +337,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t tile_ctr = 0, unit_ctr = 0;
       bool ok = true;
+      bool q_pending = false;  // a query load is in flight that no wait has consumed
       int u = next_unit(blockIdx.x);
-      if (u < n_units) load_q(u);
+      if (u < n_units) {
+        load_q(u);
+        q_pending = true;
+      }
       while (u < n_units && ok) {
         const int nt = unit_tiles(u);
         const int u_next = next_unit(u + gridDim.x);
-        if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
+        if (!dsa::mbar_wait_warp(q_full, unit_ctr & 1, wt)) break;
+        q_pending = false;
         // MMA1(tc): S^T[tc&1] = KV(tile tc) . Q^T; needs the tile and a free S buffer
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
           const int b = tile_ctr & 1;
-          if (!dsa::mbar_wait(&s_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status) ||
-              !dsa::mbar_wait(&kv_full[b], (tile_ctr >> 1) & 1, abort_flag, p.status)) {
+          if (!dsa::mbar_wait_warp(&s_empty[b], ((tile_ctr >> 1) & 1) ^ 1, wt) ||
+              !dsa::mbar_wait_warp(&kv_full[b], (tile_ctr >> 1) & 1, wt)) {
             ok = false;
             break;
           }
@@ -339,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dsa::tc_fence_after();
           const uint64_t a0 = kv_desc + b * buf16;
           const uint32_t d = tmem_base + kSCol + b * 64;
+          dsa::check(kSCol + b * 64 + kKeys <= static_cast<int>(kOCol), p.status);  // S^T stays clear of O^T
           for (int c = 0; c < p.n_qk; ++c) {
             const uint64_t ac = a0 + c * (kChunkBytes >> 4), bc = q_desc + c * (kQChunkBytes >> 4);
 #pragma unroll
@@ -353,12 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) dsa::umma_commit(q_empty);
         __syncwarp();
         if (u_next < n_units) {
-          if (!dsa::mbar_wait(q_empty, unit_ctr & 1, abort_flag, p.status)) break;
+          if (!dsa::mbar_wait_warp(q_empty, unit_ctr & 1, wt)) break;
           load_q(u_next);
+          q_pending = true;
         }
         ++unit_ctr;
         u = u_next;
       }
+      // leave nothing in flight: the query load no wait consumed (only after
+      // an abort), then every MMA1 this warp issued
+      if (leader) {
+        if (q_pending) dsa::mbar_drain(q_full, unit_ctr & 1, p.status);
+        dsa::umma_drain(&drain[0], p.status);
+      }
+      __syncwarp();
     } else {
       constexpr uint32_t idesc2 = dsa::idesc_bf16(128, kHG, 1, 1);
       const uint64_t v_desc = dsa::smem_desc(kv_addr + p.v_first * kChunkBytes, kChunkBytes, 1024, dsa::kSwizzle128B);
@@ -373,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA2(tc): O^T += V^T(tile tc) . P^T(tile tc); releases the tile buffer
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
           const int b = tile_ctr & 1;
-          if (!dsa::mbar_wait(&p_full[b], (tile_ctr >> 1) & 1, abort_flag, p.status)) {
+          if (!dsa::mbar_wait_warp(&p_full[b], (tile_ctr >> 1) & 1, wt)) {
             ok = false;
             break;
           }
@@ -382,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int mb = 0; mb < p.n_v / 2; ++mb) {
             const uint64_t am = a0 + mb * (2 * kChunkBytes >> 4);
             const uint32_t d = tmem_base + kOCol + mb * kHG;
+            if (!dsa::check(kOCol + (mb + 1) * kHG <= static_cast<int>(kTmemCols), p.status)) break;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
               if (leader)
@@ -393,7 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
+        if (ok && leader) dsa::umma_commit(o_unit);  // the unit's O^T is complete
+        __syncwarp();
       }
+      if (leader) dsa::umma_drain(&drain[1], p.status);  // every MMA2 issued has completed
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
@@ -411,6 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool want_max = p.max_logits != nullptr;
     uint32_t tile_ctr = 0;
     bool ok = true;
+    // A wait of this warp gave up (warp-uniform).  The eight warps only leave
+    // together, at a barrier that carries the flag (the per-tile exflag
+    // barrier or the unit's last barrier); until then a failed warp skips its
+    // TMEM accesses but keeps arriving at every named barrier.
+    bool failed = false;
+    uint32_t unit_ctr = 0;  // units with at least one tile so far (phases of o_unit)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int uu = n_units - 1 - u;
       const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
@@ -446,19 +487,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           nA = jA + kKeys < len ? __ldcs(irow + jA + kKeys) : -1;
           nB = jB + kKeys < len ? __ldcs(irow + jB + kKeys) : -1;
         }
-        if (!dsa::mbar_wait(&s_full[b], ph, abort_flag, p.status)) { ok = false; break; }
-        dsa::tc_fence_after();
+        if (!failed) failed = !dsa::mbar_wait_warp(&s_full[b], ph, wt);
         float x[16];
-        {
+        if (!failed) {
+          dsa::tc_fence_after();
           uint32_t v[16];
           dsa::tmem_ld16x256b_x4(tmem_base + lane_off + kSCol + b * 64 + hh * 32, v);
           dsa::tmem_wait_ld();
 #pragma unroll
           for (int r = 0; r < 16; ++r) x[r] = __uint_as_float(v[r]);
+          dsa::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
+        } else {
+#pragma unroll
+          for (int r = 0; r < 16; ++r) x[r] = 0.f;
         }
-        dsa::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
         // y = s*log2(e) - m for the current reference m of each head; a tile
         // whose scores pass m + theta anywhere moves the reference first
         float y[16];
@@ -475,14 +519,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const bool ex_warp = __any_sync(0xffffffffu, ex);
-        if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = ex_warp ? 1 : 0;
+        if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = (ex_warp ? 1 : 0) | (failed ? 2 : 0);
         named_bar(1, kSoftThreads);
         // the first tile of a unit always sets the reference (mref still holds
         // the previous unit's, so its y above are discarded)
         bool reduce = want_max || i == 0;
         bool need_rescale = false;
+        int any_failed = 0;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) reduce |= exflag[(tile_ctr & 1) * 8 + w] != 0;
+        for (int w = 0; w < 8; ++w) {
+          const int f = exflag[(tile_ctr & 1) * 8 + w];
+          reduce |= (f & 1) != 0;
+          any_failed |= f & 2;
+        }
+        if (any_failed) {  // every softmax thread read the same flags: the group leaves together
+          ok = false;
+          break;
+        }
         if (reduce) {
           // tile maximum per head: this thread's two keys, then the 8 threads
           // that share its heads (lane bits 2..4)
@@ -524,7 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               y[4 * j + 2 + e] = vB ? fmaf(x[4 * j + 2 + e], p.scale_log2, -m) : -INFINITY;
             }
           }
-          need_rescale = rescale && i > 0;
+          // warp-uniform: the rescale below loads the warp's 32 heads from TMEM
+          // (heads whose reference did not move have alpha = 1)
+          need_rescale = __any_sync(0xffffffffu, rescale) && i > 0;
         }
         // P^T rows kA and kB: heads hbase + 8j + {0, 1} are 4 bytes at 16-byte
         // unit hh*4 + j of the row (128-byte swizzle: unit ^ (key & 7))
@@ -543,9 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // O^T columns of heads whose reference moved get alpha[h]; this runs after
         // P is written so that the scores are no longer live.
-        if (need_rescale) {
+        if (need_rescale && !failed) {
           // MMA2 of the previous tile must have landed before O^T is scaled
-          if (!dsa::mbar_wait(o_done, ((tile_ctr - 1) & 1), abort_flag, p.status)) { ok = false; break; }
+          failed = !dsa::mbar_wait_warp(o_done, ((tile_ctr - 1) & 1), wt);
+        }
+        if (need_rescale && !failed) {
           dsa::tc_fence_after();
           const float* a32 = alpha + hh * 32;
           for (int mb = 0; mb < p.n_v / 2; ++mb) {
@@ -589,7 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      if (!dsa::mbar_wait(o_done, (tile_ctr - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!failed) failed = !dsa::mbar_wait_warp(o_unit, unit_ctr & 1, wt);
+      ++unit_ctr;
       dsa::tc_fence_after();
       // per-head sums over the quarter's 16 keys: the 8 threads sharing a head
 #pragma unroll
@@ -629,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_bar(1, kSoftThreads);
-      {
+      if (!failed) {
         const float* f32 = fac + hh * 32;
         const int hcount = min(32, hv - hh * 32);  // real heads in this warp's half
         for (int mb = 0; mb < p.n_v / 2; ++mb) {
@@ -637,15 +695,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           dsa::tmem_ld32(tmem_base + lane_off + kOCol + mb * kHG + hh * 32, v);
           dsa::tmem_wait_ld();
           __nv_bfloat16* o = p.out + (orow + hh * 32) * p.Dv + mb * 128 + quarter * 32 + lane;
+          // checked build: the head rows written are inside out [T, H, Dv]
+          const bool in_out =
+              dsa::check(hcount <= 0 || (orow + hh * 32 + hcount) * p.Dv <= static_cast<int64_t>(p.T) * p.H * p.Dv,
+                         p.status);
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            if (c < hcount) __stcs(o, __float2bfloat16_rn(__uint_as_float(v[c]) * f32[c]));
+            if (c < hcount && in_out) __stcs(o, __float2bfloat16_rn(__uint_as_float(v[c]) * f32[c]));
             o += p.Dv;
           }
         }
       }
       dsa::tc_fence_before();
-      named_bar(1, kSoftThreads);
+      // the unit's last barrier: the group leaves together if any warp's wait gave up
+      if (dsa::named_bar_any(1, kSoftThreads, failed)) {
+        ok = false;
+        break;
+      }
     }
   }
 

@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 5;
   uint64_t* q_empty = bars + 6;
   uint64_t* o_done = bars + 7;
+  uint64_t* drain = bars + 8;  // [2]: the MMA issuers' exit commits
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
 
@@ -204,6 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = p.T * p.G;
 
   if (threadIdx.x == 0) {
+    dsa::mbar_init(&drain[0], 1);
+    dsa::mbar_init(&drain[1], 1);
     dsa::mbar_init(kv_full, kGatherThreads);
     dsa::mbar_init(kv_empty, 1);
     dsa::mbar_init(s_full, 1);
@@ -220,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   dsa::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
 
   if (warp < kGatherWarps) {
     // ------------------------------------------------------------ gather
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = (i + 1) * kKeys + jk;
           nxt[kg] = (i + 1 < nt && jk < kKeys && j < len) ? __ldcs(irow + j) : -1;
         }
-        if (!dsa::mbar_wait(kv_empty, (tile_ctr & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        if (!dsa::mbar_wait(kv_empty, (tile_ctr & 1) ^ 1, wt)) { ok = false; break; }
         dsa::fence_proxy_async_smem();
         const uint32_t buf = dsa::smem_u32(kvbuf);
 #pragma unroll
@@ -303,15 +307,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t tile_ctr = 0, unit_ctr = 0;
       bool ok = true;
+      bool q_pending = false;  // a query + dout load is in flight that no wait has consumed
       int u = next_unit(blockIdx.x);
-      if (u < n_units) load_qd(u);
+      if (u < n_units) {
+        load_qd(u);
+        q_pending = true;
+      }
       while (u < n_units && ok) {
         const int nt = unit_tiles(u);
         const int u_next = next_unit(u + gridDim.x);
-        if (!dsa::mbar_wait(q_full, unit_ctr & 1, abort_flag, p.status)) break;
+        if (!dsa::mbar_wait_warp(q_full, unit_ctr & 1, wt)) break;
+        q_pending = false;
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
-          if (!dsa::mbar_wait(s_empty, (tile_ctr & 1) ^ 1, abort_flag, p.status) ||
-              !dsa::mbar_wait(kv_full, tile_ctr & 1, abort_flag, p.status)) {
+          if (!dsa::mbar_wait_warp(s_empty, (tile_ctr & 1) ^ 1, wt) ||
+              !dsa::mbar_wait_warp(kv_full, tile_ctr & 1, wt)) {
             ok = false;
             break;
           }
@@ -331,12 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) dsa::umma_commit(q_empty);
         __syncwarp();
         if (u_next < n_units) {
-          if (!dsa::mbar_wait(q_empty, unit_ctr & 1, abort_flag, p.status)) break;
+          if (!dsa::mbar_wait_warp(q_empty, unit_ctr & 1, wt)) break;
           load_qd(u_next);
+          q_pending = true;
         }
         ++unit_ctr;
         u = u_next;
       }
+      // leave nothing in flight: the unconsumed query + dout load (only after
+      // an abort), then every MMA this warp issued
+      if (leader) {
+        if (q_pending) dsa::mbar_drain(q_full, unit_ctr & 1, p.status);
+        dsa::umma_drain(&drain[0], p.status);
+      }
+      __syncwarp();
     } else {
       // dq^T[dim, head] += kv^T[dim, key] . dS^T[key, head]: four M = 128
       // blocks over dims 0..511 and one M = 64 block over dims 512..575
@@ -349,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = next_unit(blockIdx.x); u < n_units && ok; u = next_unit(u + gridDim.x)) {
         const int nt = unit_tiles(u);
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
-          if (!dsa::mbar_wait(p_full, tile_ctr & 1, abort_flag, p.status)) {
+          if (!dsa::mbar_wait_warp(p_full, tile_ctr & 1, wt)) {
             ok = false;
             break;
           }
@@ -370,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
+      if (leader) dsa::umma_drain(&drain[1], p.status);  // every dq MMA issued has completed
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------ P, dS and dq out
@@ -384,6 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hbase = hh * 32 + 2 * (lane & 3);
     uint32_t tile_ctr = 0;
     bool ok = true;
+    // a wait of this warp gave up (warp-uniform): the warp skips the rest of
+    // the unit's TMEM work, and the eight warps leave together at the unit's
+    // last barrier, which carries the flag
+    bool failed = false;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int uu = n_units - 1 - u;
       const int t = uu / p.G, g = uu - (uu / p.G) * p.G;
@@ -415,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           nA = jA + kKeys < len ? __ldcs(irow + jA + kKeys) : -1;
           nB = jB + kKeys < len ? __ldcs(irow + jB + kKeys) : -1;
         }
-        if (!dsa::mbar_wait(s_full, ph, abort_flag, p.status)) { ok = false; break; }
+        if (!dsa::mbar_wait_warp(s_full, ph, wt)) {
+          failed = true;
+          break;
+        }
         dsa::tc_fence_after();
         uint32_t xs[16], dps[16];
         dsa::tmem_ld16x256b_x4(tmem_base + lane_off + kSCol + hh * 32, xs);
@@ -473,12 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) dsa::mbar_arrive(p_full);
       }
-      if (!ok) break;
       // ---- dq of the unit: dq^T blocks from TMEM (scale already in dS)
-      if (!dsa::mbar_wait(o_done, (tile_ctr - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!failed) failed = !dsa::mbar_wait_warp(o_done, (tile_ctr - 1) & 1, wt);
       dsa::tc_fence_after();
       const int hcount = min(32, hv - hh * 32);
-      for (int mb = 0; mb < 4; ++mb) {
+      for (int mb = 0; mb < 4 && !failed; ++mb) {
         uint32_t v[32];
         dsa::tmem_ld32(tmem_base + lane_off + kQCol + mb * kHG + hh * 32, v);
         dsa::tmem_wait_ld();
@@ -489,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           o += kDqk;
         }
       }
-      {
+      if (!failed) {
         // dims 512..575: an M = 64 accumulator (dim 512 + r in lane
         // 32*(r/16) + r%16), read like S^T
         uint32_t v[16];
@@ -509,7 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       dsa::tc_fence_before();
-      named_bar(1, kSoftThreads);
+      if (dsa::named_bar_any(1, kSoftThreads, failed)) {
+        ok = false;
+        break;
+      }
     }
   }
 
@@ -591,6 +619,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   uint64_t* a_empty = bars + 4;  // [2]
   uint64_t* d_full = bars + 6;   // [2]
   uint64_t* d_empty = bars + 8;  // [2]
+  uint64_t* drain = bars + 10;   // the MMA issuer's exit commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -606,6 +635,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       dsa::mbar_init(&d_full[b], 1);
       dsa::mbar_init(&d_empty[b], 4);
     }
+    dsa::mbar_init(drain, 1);
     *abort_flag = 0;
     dsa::fence_barrier_init();
   }
@@ -614,6 +644,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
   __syncthreads();
   dsa::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
   // units of this lane, in order: u = lane_id + kLanes * k over (t, g), t-major
   auto unit_tiles = [&](int u) { return (dkv_len(p, u / p.G) + kKeys - 1) / kKeys; };
 
@@ -625,11 +656,13 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       dsa::tma_prefetch_desc(&map_ds);
       dsa::tma_prefetch_desc(&map_p);
       uint32_t tile_ctr = 0, unit_ctr = 0;
+      uint32_t qd_issued = 0;  // query + dout loads issued: load m completes phase m of qd_full
       for (int u = lane_id; u < n_units; u += kLanes) {
         const int nt = unit_tiles(u);
         if (nt == 0) continue;
         const int t = u / p.G, g = u - (u / p.G) * p.G;
-        if (!dsa::mbar_wait(qd_empty, (unit_ctr & 1) ^ 1, abort_flag, p.status)) break;
+        if (!dsa::mbar_wait(qd_empty, (unit_ctr & 1) ^ 1, wt)) break;
+        ++qd_issued;
         dsa::mbar_expect_tx(qd_full, (kNqk + kNv) * kChunkBytes);
         for (int c = 0; c < kNqk; ++c)
           dsa::tma_load_3d_hint(qd + c * 2 * kChunkBytes, &map_q, c * 64, g * kHG, t, qd_full, policy);
@@ -638,7 +671,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         bool ok = true;
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
           const int b = tile_ctr & 1;
-          if (!dsa::mbar_wait(&a_empty[b], ((tile_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!dsa::mbar_wait(&a_empty[b], ((tile_ctr >> 1) & 1) ^ 1, wt)) { ok = false; break; }
           dsa::mbar_expect_tx(&a_full[b], 2 * kChunkBytes);
           const int row = t * p.K + i * kKeys;
           uint8_t* dst = abuf + b * 2 * kChunkBytes;
@@ -647,6 +680,15 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         }
         if (!ok) break;
         ++unit_ctr;
+      }
+      // every copy issued has landed before the CTA leaves (all were consumed
+      // unless the kernel aborted): the newest query + dout load and the newest
+      // load of each of the two [scale dS | P] buffers (tile i went to buffer
+      // i & 1, phase (i >> 1) & 1; a buffer is reloaded only once consumed)
+      if (qd_issued > 0) dsa::mbar_drain(qd_full, (qd_issued - 1) & 1, p.status);
+      for (uint32_t j = 1; j <= tile_ctr && j <= 2; ++j) {
+        const uint32_t i = tile_ctr - j;
+        dsa::mbar_drain(&a_full[i & 1], (i >> 1) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -659,15 +701,18 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     for (int u = lane_id; u < n_units && ok; u += kLanes) {
       const int nt = unit_tiles(u);
       if (nt == 0) continue;
-      if (!dsa::mbar_wait(qd_full, unit_ctr & 1, abort_flag, p.status)) break;
+      if (!dsa::mbar_wait_warp(qd_full, unit_ctr & 1, wt)) break;
       for (int i = 0; i < nt; ++i, ++tile_ctr) {
         const int b = tile_ctr & 1;
-        if (!dsa::mbar_wait(&a_full[b], (tile_ctr >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!dsa::mbar_wait_warp(&a_full[b], (tile_ctr >> 1) & 1, wt)) { ok = false; break; }
         dsa::tc_fence_after();
         const uint32_t a0 = a_addr + b * 2 * kChunkBytes;
         for (int nb = 0; nb < 5 && ok; ++nb, ++blk_ctr) {
           const int db = blk_ctr & 1;
-          if (!dsa::mbar_wait(&d_empty[db], ((blk_ctr >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!dsa::mbar_wait_warp(&d_empty[db], ((blk_ctr >> 1) & 1) ^ 1, wt)) {
+            ok = false;
+            break;
+          }
           dsa::tc_fence_after();
           const uint32_t d = tmem_base + db * 128;
           const uint32_t bq = qd_addr + nb * 2 * (2 * kChunkBytes);  // query chunk 2nb
@@ -692,6 +737,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       __syncwarp();
       ++unit_ctr;
     }
+    if (leader) dsa::umma_drain(drain, p.status);  // every MMA issued has completed
+    __syncwarp();
   } else {
     // ------------------------------------------- drain + shard update
     const int dt = threadIdx.x - 64;       // 0..127
@@ -701,6 +748,10 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     float* shard = p.shards + static_cast<int64_t>(lane_id) * p.Tkv * kDqk;
     uint32_t blk_ctr = 0;
     bool ok = true;
+    // a wait of this warp gave up (warp-uniform): it skips its TMEM reads and
+    // shard writes, and the four warps leave together at the block's last
+    // barrier, which carries the flag
+    bool failed = false;
     for (int u = lane_id; u < n_units && ok; u += kLanes) {
       const int len = dkv_len(p, u / p.G);
       const int nt = (len + kKeys - 1) / kKeys;
@@ -748,9 +799,9 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             acc[k] = (col_on && id >= 0 && first[r] == r) ? base[static_cast<int64_t>(id) * (kDqk / 4)]
                                                           : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          if (!dsa::mbar_wait(&d_full[db], (blk_ctr >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
           dsa::tc_fence_after();
-          {
+          if (!failed) {
             uint32_t v[4][16];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
@@ -779,7 +830,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
                 if (first[r] != r) stage[first[r] * kStageLd + dt] += stage[r * kStageLd + dt];
             named_bar(1, kDrainThreads);
           }
-          if (col_on) {
+          if (col_on && !failed) {
 #pragma unroll
             for (int k = 0; k < kKeys / 4; ++k) {
               const int r = kg + 4 * k;
@@ -791,7 +842,12 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
               }
             }
           }
-          named_bar(1, kDrainThreads);  // stage is read before the next block overwrites it
+          // stage is read before the next block overwrites it; the group
+          // leaves together if any warp's wait gave up
+          if (dsa::named_bar_any(1, kDrainThreads, failed)) {
+            ok = false;
+            break;
+          }
         }
       }
     }

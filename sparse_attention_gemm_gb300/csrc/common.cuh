@@ -9,12 +9,24 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/dsa.h"
 
 #ifndef DSA_WAIT_TIMEOUT_NS
 #define DSA_WAIT_TIMEOUT_NS 2000000000ull  // 2 s: no legitimate wait comes close
+#endif
+
+// The checked build (-DDSA_CHECKED) range-checks the indices and offsets of
+// the kernels' shared-memory, TMEM and global accesses before using them: a
+// failed check ORs DSA_STATUS_CHECK_FAILED into the status word and the
+// access is skipped (never a trap).  In the normal build every check is the
+// constant true and compiles away.
+#ifdef DSA_CHECKED
+#define DSA_CHECKED_BUILD 1
+#else
+#define DSA_CHECKED_BUILD 0
 #endif
 
 namespace dsa {
@@ -87,22 +99,105 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The library's control block on each device.  Kernels receive the address
+// of `status` (the word they OR their DSA_STATUS_* bits into); the limit of
+// the bounded waits sits 8 bytes after it: 0 means DSA_WAIT_TIMEOUT_NS, any
+// other value (set by dsa_set_wait_limit_ns) replaces it.
+struct DeviceControl {
+  uint32_t status;
+  uint32_t reserved;
+  uint64_t wait_limit_ns;
+};
+
+static_assert(offsetof(DeviceControl, wait_limit_ns) == 2 * sizeof(uint32_t), "limit 8 bytes after status");
+
+__device__ __forceinline__ uint64_t wait_limit(const uint32_t* status) {
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return v ? v : DSA_WAIT_TIMEOUT_NS;
+}
+
+// What a bounded wait needs: the CTA's abort flag (shared memory), the
+// device status word, and whether the wait-limit hook shortened the limit
+// below the default (read once per thread when its role starts).
+struct Waiter {
+  volatile int* abort;
+  uint32_t* status;
+  bool poll;
+};
+__device__ __forceinline__ Waiter make_waiter(volatile int* abort, uint32_t* status) {
+  const uint64_t v = *reinterpret_cast<const volatile uint64_t*>(status + 2);
+  return Waiter{abort, status, v != 0 && v < DSA_WAIT_TIMEOUT_NS};
+}
+
 // Bounded wait.  Returns false when the kernel is aborting: either another
-// thread already raised *abort, or this wait exceeded DSA_WAIT_TIMEOUT_NS, in
+// thread already raised *abort, or this wait exceeded the wait limit, in
 // which case DSA_STATUS_WAIT_TIMEOUT is OR-ed into the status word first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// try_wait suspends the thread until the phase completes or a hardware time
+// slice ends; under a limit shortened by the failure-detection hook the wait
+// polls without suspending instead, so that any wait not satisfied at its
+// first probe gives up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waiter& w) {
+  if (w.poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = wait_limit(w.status);
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > DSA_WAIT_TIMEOUT_NS) {
-      atomicOr(status, DSA_STATUS_WAIT_TIMEOUT);
-      *abort = 1;
+    if (w.poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (globaltimer() - t0 > limit) {
+      atomicOr(w.status, DSA_STATUS_WAIT_TIMEOUT);
+      *w.abort = 1;
       return false;
     }
   }
+}
+
+// The same wait taken by a whole converged warp: every lane waits and the
+// lanes agree on the outcome, so that what follows (tcgen05.ld, which all 32
+// lanes must execute, __syncwarp, an elected issuer) sees one decision.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Waiter& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Before a CTA that is aborting leaves, each thread waits for the
+// asynchronous work it issued and nobody consumed (a TMA copy landing in
+// shared memory, MMAs reading shared memory and writing TMEM), so that none
+// of it outlives the CTA's shared memory and TMEM.  Bounded by
+// DSA_WAIT_TIMEOUT_NS whatever the wait-limit override and the abort flag
+// say; DSA_STATUS_DRAIN_TIMEOUT if it gave up.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > DSA_WAIT_TIMEOUT_NS) {
+      atomicOr(status, DSA_STATUS_DRAIN_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Named barrier `id` over `n` threads (whole warps, converged) that also
+// returns, to every participant, whether `pred` held for any of them: the one
+// point where a group whose members may have seen different waits give up
+// takes a single decision to leave.
+__device__ __forceinline__ bool named_bar_any(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// In-kernel range check of the checked build: true when `ok`; otherwise the
+// failure is recorded and the caller skips the access.
+__device__ __forceinline__ bool check(bool ok, uint32_t* status) {
+  if (DSA_CHECKED_BUILD && !ok) {
+    atomicOr(status, DSA_STATUS_CHECK_FAILED);
+    return false;
+  }
+  return true;
 }
 
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma, TMA).
@@ -212,6 +307,12 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+// An issuing thread's last step before its CTA leaves: every tcgen05.mma it
+// issued has completed (commit to `bar`, fresh at phase 0, and a bounded wait).
+__device__ __forceinline__ void umma_drain(uint64_t* bar, uint32_t* status) {
+  umma_commit(bar);
+  mbar_drain(bar, 0, status);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 // tcgen05.wait::ld with the 32 destination registers of an earlier

@@ -129,7 +129,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, i
   L.cmp_off = o;
   if (fused) o += kEpiWarps * 256 * 4;  // one 256-bin histogram per epilogue warp (segment compaction)
   L.bar_off = o;
-  o += (2 * 8 + 6) * 8;
+  o += (2 * 8 + 7) * 8;
   L.misc_off = o;
   o += 16;
   L.total = o;
@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qempty = bars + 17;
   uint64_t* tfull = bars + 18;   // [2]
   uint64_t* tempty = bars + 20;  // [2]
+  uint64_t* drain = bars + 22;   // the MMA issuer's exit commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
@@ -405,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dsa::mbar_init(&tfull[b], 1);
       dsa::mbar_init(&tempty[b], kEpiWarps);
     }
+    dsa::mbar_init(drain, 1);
     *abort_flag = 0;
     dsa::fence_barrier_init();
   }
@@ -413,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   dsa::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -426,20 +429,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
+      int n_issued = 0;  // key-tile loads issued: load i went to stage i % S, phase (i / S) & 1
+      int q_issued = 0;  // query-block loads issued: load m completes phase m of qfull
       for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
         const BlockRange br = block_range<GEN>(p, blk);
-        if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (iter > 0 && !dsa::mbar_wait(qempty, (iter - 1) & 1, wt)) { ok = false; break; }
         dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
         for (int c = 0; c < nch; ++c)
           dsa::tma_load_2d_hint(qbuf + c * kNRows * 128, &map_q, c * kChunkElems, br.t0 * p.Hi, qfull, stream);
+        ++q_issued;
         for (int kt = br.kt0; kt <= br.kt1; ++kt) {
-          if (!dsa::mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!dsa::mbar_wait(&empty[stage], phase ^ 1, wt)) { ok = false; break; }
           dsa::mbar_expect_tx(&full[stage], nch * kKeyTile * 128);
           uint8_t* dst = kbuf + stage * nch * kKeyTile * 128;
           for (int c = 0; c < nch; ++c)
             dsa::tma_load_2d_hint(dst + c * kKeyTile * 128, &map_k, c * kChunkElems, kt * kKeyTile, &full[stage], keep);
+          ++n_issued;
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
+      }
+      // Every copy this thread issued has landed before the CTA leaves (all of
+      // them were consumed unless the kernel aborted): the newest query block
+      // and the newest load of each ring stage (a stage or the query buffer is
+      // reloaded only after its previous load was consumed).
+      if (q_issued > 0) dsa::mbar_drain(qfull, (q_issued - 1) & 1, p.status);
+      for (int j = 1; j <= n_issued && j <= S; ++j) {
+        const int i = n_issued - j;
+        dsa::mbar_drain(&full[i % S], (i / S) & 1, p.status);
       }
     }
   } else if (warp == 1) {
@@ -455,11 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = dsa::smem_u32(qbuf), k_addr = dsa::smem_u32(kbuf);
       for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
         const BlockRange br = block_range<GEN>(p, blk);
-        if (!dsa::mbar_wait(qfull, iter & 1, abort_flag, p.status)) break;
+        if (!dsa::mbar_wait(qfull, iter & 1, wt)) break;
         dsa::tc_fence_after();
         for (int kt = br.kt0; kt <= br.kt1; ++kt) {
-          if (!dsa::mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (!dsa::mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          if (!dsa::mbar_wait(&tempty[acc], acc_phase ^ 1, wt)) { ok = false; break; }
+          if (!dsa::mbar_wait(&full[stage], phase, wt)) { ok = false; break; }
           dsa::tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kNRows;
           const uint32_t a0 = k_addr + stage * nch * kKeyTile * 128;
@@ -480,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         dsa::umma_commit(qempty);
       }
+      dsa::umma_drain(drain, p.status);  // every MMA issued has completed
     }
   } else {
     // -------------------------------------------------------- epilogue
@@ -495,6 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
+    // a wait of this warp gave up (warp-uniform); the eight warps leave
+    // together at the block's last barrier, which carries the flag
+    bool failed = false;
     const int seg = quarter;              // this warp writes segment `quarter` of its rows
     const int cap_seg = FUSED ? p.cap / 4 : 0;
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
@@ -556,12 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s1 = (kt + 1) * kKeyTile + key_lane;
           ks_next = (kt < br.kt1 && s1 < p.Tk) ? __ldg(p.k_scale + s1) : 0.f;
         }
-        if (!dsa::mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status)) { ok = false; break; }
+        if (!dsa::mbar_wait_warp(&tfull[acc], acc_phase, wt)) {
+          failed = true;
+          break;
+        }
         dsa::tc_fence_after();
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
         // this warp's columns [slice*kSliceCols, (slice+1)*kSliceCols) = tokens [slice*tok_per_slice, ...)
         const uint32_t t_addr =
             tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows + slice * kSliceCols;
+        dsa::check(acc * kNRows + (slice + 1) * kSliceCols <= static_cast<int>(kTmemCols), p.status);
         // fused: a row's entry bound for this tile, read once (tau only rises
         // and a compacted segment's floor only rises, so a value read early
         // can only admit more candidates)
@@ -608,7 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int st = rs[q];
               const bool valid = static_cast<uint32_t>(s_key - st) < static_cast<uint32_t>(rl[q]);
               if (!FUSED) {
-                if (valid) __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
+                // checked build: row and column inside scores [T, ld]
+                if (valid && dsa::check(t < p.T && s_key - st < p.ld, p.status))
+                  __stcs(p.scores + static_cast<int64_t>(t) * p.ld + (s_key - st), score);
               } else {
                 const uint32_t key = dsa::f32_key(score);
                 const bool emit = valid && key >= thr[q];
@@ -617,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // room for a whole tile (compaction below)
                 const uint32_t em = __ballot_sync(0xffffffffu, emit);
                 const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
-                if (emit) {
+                if (emit && dsa::check(slot < cap_seg && t < p.T, p.status)) {
                   __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
                   // histogram of stored keys, one 32-bit counter per bin; the
                   // result is unused, so this is a fire-and-forget reduction
@@ -696,8 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) break;
-      named_bar(1, kEpiThreads);
+      if (dsa::named_bar_any(1, kEpiThreads, failed)) {
+        ok = false;
+        break;
+      }
       if (!FUSED) {
         // columns len[t] .. s_max-1 of the block's rows are -inf
         for (int r = 0; r < p.qb; ++r) {
@@ -930,6 +958,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     dsa::fence_barrier_init();
   }
   __syncthreads();
+  const dsa::Waiter wt = dsa::make_waiter(&S.abort, status);
   if (threadIdx.x == 0) {
     const int r0 = row_len(blockIdx.x, nullptr) > k ? blockIdx.x : next_row(blockIdx.x);
     if (r0 < T) issue(r0);
@@ -964,8 +993,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     const bool overflow = seg_counts(t, c);
     if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
     const int n = c[0] + c[1] + c[2] + c[3];
-    if (!dsa::mbar_wait(&S.full, phase, &S.abort, status)) break;
-    phase ^= 1;
+    // every thread waits for the row's copy; the block agrees on the outcome
+    // at the barrier below, before anyone depends on the staged candidates
+    const bool staged = dsa::mbar_wait(&S.full, phase, wt);
     // ---- staging buffer -> registers: element e = i*1024 + thread of the concatenated segments
     const int e1 = c[0], e2 = e1 + c[1], e3 = e2 + c[2];
     uint32_t key[kSelPer];
@@ -995,7 +1025,14 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       S.whi[warp] = hi;
     }
     if (threadIdx.x == 0) S.lcnt = 0;
-    __syncthreads();  // every thread has its candidates: the staging buffer is free
+    // every thread has its candidates: the staging buffer is free
+    if (!__syncthreads_and(staged)) {
+      // a wait gave up: the copy that did not arrive must land before the CTA
+      // leaves (thread 0 issued it; later rows were never requested)
+      if (threadIdx.x == 0) dsa::mbar_drain(&S.full, phase, status);
+      break;
+    }
+    phase ^= 1;
     if (threadIdx.x == 0) {
       const int rn = next_row(r);
       if (rn < T) {
@@ -1089,6 +1126,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     for (int i = 0; i < kSelPer; ++i) {
       if (!valid(i)) continue;
       const int col = column(i);
+      if (!dsa::check(col < len, status)) continue;  // checked build: a candidate's column lies in its row
       if (key[i] > tau) atomicOr(&S.sel[col >> 5], 1u << (col & 31));
       else if (key[i] == tau) atomicOr(&S.tie[col >> 5], 1u << (col & 31));
     }
@@ -1134,12 +1172,14 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     while (m0) {
       const int b = __ffs(m0) - 1;
       m0 &= m0 - 1;
-      out[pos++] = st + (w0 << 5) + b;
+      if (dsa::check(pos < k, status)) out[pos] = st + (w0 << 5) + b;  // checked build: k ids at most
+      ++pos;
     }
     while (m1) {
       const int b = __ffs(m1) - 1;
       m1 &= m1 - 1;
-      out[pos++] = st + ((w0 + 1) << 5) + b;
+      if (dsa::check(pos < k, status)) out[pos] = st + ((w0 + 1) << 5) + b;
+      ++pos;
     }
     if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
     if (lout) {

@@ -213,7 +213,8 @@ __device__ __forceinline__ void mark(Shared& S, const Src& src) {
 __global__ void __launch_bounds__(kThreads, 4)
     topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ len,
                        const int32_t* __restrict__ row_start, int T, int k, int32_t* __restrict__ idx,
-                       int32_t* __restrict__ topk_length, float* __restrict__ vals, int ahead) {
+                       int32_t* __restrict__ topk_length, float* __restrict__ vals, int ahead,
+                       uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& S = *reinterpret_cast<Shared*>(smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -482,7 +483,9 @@ __global__ void __launch_bounds__(kThreads, 4)
     while (b) {
       const int bit = __ffs(b) - 1;
       b &= b - 1;
-      staged[pos++] = base + ((w0 + i) << 5) + bit;
+      // checked build: at most k ids, staged inside the candidate buffer
+      if (dsa::check(pos < k && pos < 2 * kCap, status)) staged[pos] = base + ((w0 + i) << 5) + bit;
+      ++pos;
     }
   }
   __syncthreads();
@@ -559,7 +562,7 @@ int launch_topk_stream(const float* scores, int64_t ld, const int32_t* len, cons
     return dsa::launch_error("topk_stream_kernel smem attribute");
   // four CTAs are resident per SM: the block one wave later is 4 * SMs ahead
   st::topk_stream_kernel<<<T, st::kThreads, smem, stream>>>(scores, ld, len, row_start, T, k, idx, topk_length, vals,
-                                                            4 * sm_count);
+                                                            4 * sm_count, dsa::device_status_ptr());
   return dsa::launch_error("topk_stream_kernel");
 }
 

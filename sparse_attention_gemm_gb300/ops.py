@@ -17,7 +17,9 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libdsa.so")
+# DSA_LIB_PATH selects another build of this library (the range-checked one
+# under _build_checked/, for its tests); by default the optimised build.
+LIB_PATH = os.environ.get("DSA_LIB_PATH") or os.path.join(_HERE, "_build", "libdsa.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "dsa.h")
 
 DSA_OK = 0
@@ -27,6 +29,8 @@ DSA_ERR_CUDA = 3
 DSA_ERR_WORKSPACE = 4
 DSA_STATUS_WAIT_TIMEOUT = 0x1
 DSA_STATUS_CAND_OVERFLOW = 0x2
+DSA_STATUS_DRAIN_TIMEOUT = 0x4
+DSA_STATUS_CHECK_FAILED = 0x8
 MAX_TOPK = 2048
 
 _lock = threading.Lock()
@@ -41,6 +45,7 @@ SZ = ctypes.c_size_t
 _SIGNATURES = {
     "dsa_last_error": ([], ctypes.c_char_p),
     "dsa_device_status": ([P, I], I),
+    "dsa_set_wait_limit_ns": ([ctypes.c_uint64], I),
     "dsa_thd_metadata": ([P, I, I, P, P, P], I),
     "dsa_indexer_scores": ([P, P, P, P, I, I, I, I, I, P, I64, P], I),
     "dsa_topk": ([P, I64, P, P, I, I, P, P, P, P], I),
@@ -128,6 +133,12 @@ def device_status(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check("dsa_device_status", lib().dsa_device_status(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """Bounded-wait limit of the kernels launched afterwards on the current
+    device (0: the library default).  Failure-detection hook; synchronises."""
+    _check("dsa_set_wait_limit_ns", lib().dsa_set_wait_limit_ns(int(limit_ns)))
 
 
 def thd_metadata(cu_seqlens: torch.Tensor, T: int):
