@@ -314,6 +314,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip timing the optional outputs")
     ap.add_argument("--no-compressed", action="store_true", help="skip timing the compressed-key indexer")
     ap.add_argument("--no-fp8", action="store_true", help="skip timing the fp8-input indexer")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip timing the MXFP8-input indexer")
     ap.add_argument("--no-bwd", action="store_true", help="skip timing the attention backward")
     ap.add_argument("--e2e-chunks", type=int, default=8, help="attention token ranges in the end-to-end leg")
     ap.add_argument("--workload", type=int, default=4, choices=[2, 3, 4],
@@ -587,6 +588,43 @@ def main():
                "peak_tflops": peak8, "peak_source": f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16)"}
         ops.device_status(clear=True)
 
+    # ---- MXFP8 indexer inputs (E4M3 codes, E8M0 scales per 32 elements) on
+    # the same workload: the combined call and the dense scores, timed on
+    # their own against the same fp8 peak
+    mx = None
+    if not args.no_mxfp8:
+        q8, qs = wl.qi_mxfp8()
+        k8, ks = wl.ki_mxfp8()
+        m_in = (torch.from_numpy(q8).to(dev), torch.from_numpy(k8).to(dev), torch.from_numpy(qs).to(dev),
+                torch.from_numpy(ks).to(dev), d["w"], d["cu"], d["cu"], None)
+        del q8, k8, qs, ks
+        m_ws = torch.empty(ops.indexer_topk_workspace_size(T, wl.Hi, wl.d, K, wl.s_max), dtype=torch.uint8,
+                           device=dev)
+        m_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+        m_tl = torch.empty(T, dtype=torch.int32, device=dev)
+        m_fused = lambda: ops.indexer_topk_mxfp8(*m_in, 1, K, wl.s_max, workspace=m_ws, idx=m_idx, topk_length=m_tl)
+        for _ in range(2):
+            m_fused()
+        torch.cuda.synchronize()
+        mf_ms = timed(m_fused)
+        del m_ws, m_idx, m_tl
+        torch.cuda.empty_cache()
+        m_scores = torch.empty((T, wl.s_max), dtype=torch.float32, device=dev)
+        m_dense = lambda: ops.indexer_scores_mxfp8(*m_in, 1, wl.s_max, out=m_scores)
+        m_dense()
+        torch.cuda.synchronize()
+        md_ms = timed(m_dense)
+        del m_scores, m_in
+        torch.cuda.empty_cache()
+        peak8 = pk["bf16_tflops"] * 2.0
+        fl = work["indexer_flops"]
+        mx = {"workload": wl.name, "inputs": "E4M3 qi/ki, E8M0 scales per 32 elements of d (block-scaled MMA)",
+              "indexer_topk_ms": mf_ms, "indexer_topk_tflops": fl / (mf_ms / 1e3) / 1e12,
+              "indexer_topk_frac_peak": fl / (mf_ms / 1e3) / 1e12 / peak8, "dense_scores_ms": md_ms,
+              "dense_tflops": fl / (md_ms / 1e3) / 1e12, "dense_frac_peak": fl / (md_ms / 1e3) / 1e12 / peak8,
+              "peak_tflops": peak8, "peak_source": f"{pk['source']} bf16 burst x 2 (nominal fp8/bf16)"}
+        ops.device_status(clear=True)
+
     # ---- sparse attention backward (deterministic) on the step's own ids,
     # with a synthetic dout; timed on its own
     bwd = None
@@ -730,6 +768,7 @@ def main():
             "optional_outputs": extras,
             "compressed_indexer": comp,
             "fp8_indexer": fp8,
+            "mxfp8_indexer": mx,
             "attention_backward": bwd,
             "other_workloads": others,
         }

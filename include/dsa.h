@@ -280,6 +280,39 @@ int dsa_indexer_topk_fp8(const void* qi8, const void* ki8, const float* q_scale,
                          int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length, float* logits,
                          float* softmax, float* lse, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
+/* ---- MXFP8 indexer inputs ([cuDNN-DSA] 3, precision path "mxfp8": Q and K
+ * in E4M3 with block-scaled E8M0 scales, sf_vec_size 32).  Each row of 128
+ * codes (a (token, head) row of qi8, a key row of ki8) carries 4 scale bytes,
+ * byte b = e standing for 2^(e - 127) on elements 32 b .. 32 b + 31:
+ *   q[c] = e4m3(qi8[t, h, c]) * 2^(q_sf[t, h, c / 32] - 127),
+ *   k[c] = e4m3(ki8[s, c])    * 2^(k_sf[s, c / 32] - 127),
+ *   scores[t, j] = sum_h w[t, h] * ReLU(q . k),  s = start[t] + j,
+ * over the row geometry of the compressed-key calls (plain causal form:
+ * cu_seqlens_k = cu_seqlens_q, no offsets, ratio 1).  The tensor cores apply
+ * the scales per 32-element block (block-scaled MMA) and accumulate in fp32;
+ * products of scaled E4M3 values are exact.  Codes must not be NaN
+ * (S.1111.111) and scale bytes must not be 255 (NaN).
+ *   qi8 uint8 [Tq, Hi, d], ki8 uint8 [Tk, d] (16-byte aligned);
+ *   q_sf uint8 [Tq, Hi, d / 32], k_sf uint8 [Tk, d / 32] (4-byte aligned):
+ *   plain row-major bytes; the page's packed scale layout is its library's
+ *   own and is not needed here (the kernel stages the scales itself).
+ *   Other arguments and outputs as dsa_indexer_scores_ratio /
+ *   dsa_indexer_topk_ratio.
+ * Shapes: d = 128, Hi in {32, 64} (the pages' MXFP8 head counts).
+ * Errors: as the compressed-key calls, plus DSA_ERR_VALUE for NULL or
+ * misaligned scales or other d / Hi. */
+int dsa_indexer_scores_mxfp8(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf,
+                             const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                             int ratio, int s_max, float* scores, int64_t ld, cudaStream_t stream);
+
+int dsa_indexer_topk_mxfp8(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf,
+                           const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                           int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length,
+                           float* logits, float* softmax, float* lse, void* workspace,
+                           size_t ws_bytes, cudaStream_t stream);
+
 /* The two stages of dsa_indexer_topk as separate calls, for callers that
  * schedule or time them apart ([cuDNN-DSA] "Limitations": the selection
  * over the candidate buffer is a stage of its own).  dsa_indexer_candidates

@@ -351,11 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA1(tc): S^T[tc&1] = KV(tile tc) . Q^T; needs the tile and a free S buffer
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
           const int b = tile_ctr & 1;
-          if (!dsa::mbar_wait_warp(&s_empty[b], ((tile_ctr >> 1) & 1) ^ 1, wt) ||
-              !dsa::mbar_wait_warp(&kv_full[b], (tile_ctr >> 1) & 1, wt)) {
-            ok = false;
-            break;
-          }
+          // every lane waits on its own (as fast as one elected lane would);
+          // only a leader whose waits succeeded issues, and the lanes agree
+          // on leaving at the end of the tile, where they sync anyway
+          const bool got = dsa::mbar_wait(&s_empty[b], ((tile_ctr >> 1) & 1) ^ 1, wt) &&
+                           dsa::mbar_wait(&kv_full[b], (tile_ctr >> 1) & 1, wt);
           dsa::fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05 reads
           dsa::tc_fence_after();
           const uint64_t a0 = kv_desc + b * buf16;
@@ -365,10 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ac = a0 + c * (kChunkBytes >> 4), bc = q_desc + c * (kQChunkBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              if (leader) dsa::umma_bf16(d, ac + kk * 2, bc + kk * 2, idesc1, (c | kk) != 0);
+              if (leader && got) dsa::umma_bf16(d, ac + kk * 2, bc + kk * 2, idesc1, (c | kk) != 0);
           }
-          if (leader) dsa::umma_commit(&s_full[b]);
-          __syncwarp();
+          if (leader && got) dsa::umma_commit(&s_full[b]);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
         }
         if (!ok) break;
         // the query buffer is free once this unit's MMA1 have run
@@ -403,10 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMA2(tc): O^T += V^T(tile tc) . P^T(tile tc); releases the tile buffer
         for (int i = 0; i < nt; ++i, ++tile_ctr) {
           const int b = tile_ctr & 1;
-          if (!dsa::mbar_wait_warp(&p_full[b], (tile_ctr >> 1) & 1, wt)) {
-            ok = false;
-            break;
-          }
+          const bool got = dsa::mbar_wait(&p_full[b], (tile_ctr >> 1) & 1, wt);  // as MMA1: agreed at the tile end
           dsa::tc_fence_after();
           const uint64_t a0 = v_desc + b * buf16, b0 = p_desc + b * pbuf16;
           for (int mb = 0; mb < p.n_v / 2; ++mb) {
@@ -415,14 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!dsa::check(kOCol + (mb + 1) * kHG <= static_cast<int>(kTmemCols), p.status)) break;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
-              if (leader)
+              if (leader && got)
                 dsa::umma_bf16(d, am + kk * (2048 >> 4), b0 + kk * (2048 >> 4), idesc2, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          if (leader) {
+          if (leader && got) {
             dsa::umma_commit(o_done);
             dsa::umma_commit(&kv_empty[b]);
           }
-          __syncwarp();
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
         }
         if (ok && leader) dsa::umma_commit(o_unit);  // the unit's O^T is complete
         __syncwarp();
@@ -446,10 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool want_max = p.max_logits != nullptr;
     uint32_t tile_ctr = 0;
     bool ok = true;
-    // A wait of this warp gave up (warp-uniform).  The eight warps only leave
-    // together, at a barrier that carries the flag (the per-tile exflag
-    // barrier or the unit's last barrier); until then a failed warp skips its
-    // TMEM accesses but keeps arriving at every named barrier.
+    // A wait of this thread gave up.  The eight warps only leave together,
+    // at a point that reduces the flag over the group (the per-tile exflag
+    // word, or the unit's last barrier); until then a thread whose wait
+    // failed carries on with the tile: its TMEM loads and stores stay in the
+    // allocation and its global stores in the outputs, so the garbage it may
+    // compute is harmless in a kernel that is aborting, and no collective
+    // instruction ever sees a diverged warp.
     bool failed = false;
     uint32_t unit_ctr = 0;  // units with at least one tile so far (phases of o_unit)
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -487,22 +493,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           nA = jA + kKeys < len ? __ldcs(irow + jA + kKeys) : -1;
           nB = jB + kKeys < len ? __ldcs(irow + jB + kKeys) : -1;
         }
-        if (!failed) failed = !dsa::mbar_wait_warp(&s_full[b], ph, wt);
+        if (!failed) failed = !dsa::mbar_wait(&s_full[b], ph, wt);
+        dsa::tc_fence_after();
         float x[16];
-        if (!failed) {
-          dsa::tc_fence_after();
+        {
           uint32_t v[16];
           dsa::tmem_ld16x256b_x4(tmem_base + lane_off + kSCol + b * 64 + hh * 32, v);
           dsa::tmem_wait_ld();
 #pragma unroll
           for (int r = 0; r < 16; ++r) x[r] = __uint_as_float(v[r]);
-          dsa::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
-        } else {
-#pragma unroll
-          for (int r = 0; r < 16; ++r) x[r] = 0.f;
         }
+        dsa::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) dsa::mbar_arrive(&s_empty[b]);
         // y = s*log2(e) - m for the current reference m of each head; a tile
         // whose scores pass m + theta anywhere moves the reference first
         float y[16];
@@ -518,8 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ex |= (y[4 * j + e] > kTheta) || (y[4 * j + 2 + e] > kTheta);
           }
         }
-        const bool ex_warp = __any_sync(0xffffffffu, ex);
-        if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = (ex_warp ? 1 : 0) | (failed ? 2 : 0);
+        // bit 0: some thread of the warp passes the reference; bit 1: some
+        // thread's wait gave up (one reduction, where a vote was due anyway)
+        const uint32_t wflags = __reduce_or_sync(0xffffffffu, (ex ? 1u : 0u) | (failed ? 2u : 0u));
+        if (lane == 0) exflag[(tile_ctr & 1) * 8 + sw] = static_cast<int>(wflags);
         named_bar(1, kSoftThreads);
         // the first tile of a unit always sets the reference (mref still holds
         // the previous unit's, so its y above are discarded)
@@ -598,11 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // O^T columns of heads whose reference moved get alpha[h]; this runs after
         // P is written so that the scores are no longer live.
-        if (need_rescale && !failed) {
+        if (need_rescale) {
           // MMA2 of the previous tile must have landed before O^T is scaled
-          failed = !dsa::mbar_wait_warp(o_done, ((tile_ctr - 1) & 1), wt);
-        }
-        if (need_rescale && !failed) {
+          if (!failed) failed = !dsa::mbar_wait(o_done, ((tile_ctr - 1) & 1), wt);
           dsa::tc_fence_after();
           const float* a32 = alpha + hh * 32;
           for (int mb = 0; mb < p.n_v / 2; ++mb) {
@@ -646,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ---------------------------------------------------------- epilogue
-      if (!failed) failed = !dsa::mbar_wait_warp(o_unit, unit_ctr & 1, wt);
+      if (!failed) failed = !dsa::mbar_wait(o_unit, unit_ctr & 1, wt);
       ++unit_ctr;
       dsa::tc_fence_after();
       // per-head sums over the quarter's 16 keys: the 8 threads sharing a head
@@ -687,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_bar(1, kSoftThreads);
-      if (!failed) {
+      {
         const float* f32 = fac + hh * 32;
         const int hcount = min(32, hv - hh * 32);  // real heads in this warp's half
         for (int mb = 0; mb < p.n_v / 2; ++mb) {

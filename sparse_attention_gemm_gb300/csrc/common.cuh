@@ -303,6 +303,25 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t a_desc, uint64
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= (A * 2^(sfa - 127)) * (B * 2^(sfb - 127))^T, kind::mxf8f6f4
+// with E8M0 block scales (scale_vec::1X: one scale per row of A and of B for
+// the instruction's 32 elements of K).  The scales are read from TMEM (see
+// idesc_mxf8 for which byte of which column).
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], "
+      "%1, %2, %3, [%4], [%5], p; }" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared memory -> TMEM copy of 32 rows of 16 bytes, written to lanes r,
+// r + 32, r + 64 and r + 96 (row r) at 4 consecutive columns.  Issued, like
+// the MMAs, by one thread; it executes in order with the MMAs that thread
+// issues afterwards.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
 // Arrive on *bar once all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -417,6 +436,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scales: E4M3 A and B,
+// K-major, UE8M0 scales (bit 23), and which byte of the 32-bit scale word the
+// MMA uses for A (bits 29-30) and for B (bits 4-5).  Measured placement of
+// the scales (M = 128, N = 256): the scale of A-row m is read from TMEM lane
+// m, column sfa + m / 32; the scale of B-row n, for the output rows of lane
+// quarter q, from lane 32 q + n % 32, column sfb + n / 32.  One
+// tcgen05.cp.32x128b.warpx4 of a 128-row block laid out [r][m / 32][byte]
+// (16 bytes per r = m % 32) puts every scale where it is read.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_sf_id, int b_sf_id) {
+  return (static_cast<uint32_t>(b_sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(a_sf_id) << 29);
 }
 
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0

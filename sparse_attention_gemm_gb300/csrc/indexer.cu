@@ -84,6 +84,8 @@ struct IndexerParams {
   const float* w;
   const float* q_scale;  // fp8 inputs: descale per (token, head) [T, Hi]
   const float* k_scale;  // fp8 inputs: descale per key row [Tk]
+  const uint32_t* q_sf;  // mxfp8 inputs: E8M0 scales [T * Hi] rows of 4 bytes (one per 32 elements of d)
+  const uint32_t* k_sf;  // mxfp8 inputs: E8M0 scales [Tk] rows of 4 bytes
   Geom g;
   int T;
   int Tk;
@@ -108,16 +110,23 @@ struct IndexerParams {
 };
 
 struct SmemLayout {
-  uint32_t q_off, k_off, w_off, tok_off, hist_off, row_off, cmp_off, bar_off, misc_off, total;
+  uint32_t q_off, k_off, sf_off, w_off, tok_off, hist_off, row_off, cmp_off, bar_off, misc_off, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, int fused) {
+// MXFP8 block scales staged for tcgen05.cp: 512 bytes per 128-row block
+// ([row % 32][row / 32][4 scale bytes]), one block per key tile of each ring
+// stage, then the query block's two.
+constexpr uint32_t kSfBlockBytes = 512;
+
+__host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, int fused, int mx = 0) {
   SmemLayout L;
   uint32_t o = 0;
   L.q_off = o;
   o += nch * kNRows * 128;
   L.k_off = o;
   o += stages * nch * kKeyTile * 128;
+  L.sf_off = o;
+  if (mx) o += (stages + kNRows / 128) * kSfBlockBytes;
   L.w_off = o;
   o += kNRows * 4;
   L.tok_off = o;
@@ -359,6 +368,13 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int bins, i
 // epilogue folds q_scale into the head weights and multiplies the head sum
 // by k_scale: w * ReLU(qs * ks * D) = ks * (w * qs) * ReLU(D) for positive
 // descales.
+// F8 = 2: qi / ki are E4M3 with E8M0 scales per 32 elements of d (MXFP8).
+// The block-scaled MMA (kind::mxf8f6f4, one instruction per 32-element block)
+// applies them: the whole TMA warp stages each key tile's and query block's
+// scale bytes in shared memory in the layout tcgen05.cp expects, the MMA
+// thread copies them to TMEM before the tile's MMAs (in issue order), and the
+// epilogue is the bf16 one.  The scale columns take the TMEM room of the second
+// accumulator, so the accumulator is single-buffered.
 template <int FUSED, int HI, int GEN, int F8>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -366,9 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dsa::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED);
+  constexpr bool MX = F8 == 2;
+  constexpr int kAccBufs = MX ? 1 : 2;  // TMEM accumulators
+  constexpr uint32_t kSfaCol = 256, kSfbCol = 264;  // MX: scale columns (A: 4, B: 8)
+  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED, MX);
   uint8_t* qbuf = smem + L.q_off;
   uint8_t* kbuf = smem + L.k_off;
+  uint8_t* sfbuf = smem + L.sf_off;  // MX: [stage] key-tile scales, then the query block's
   float* w_s = reinterpret_cast<float*>(smem + L.w_off);
   int32_t* tok_start = reinterpret_cast<int32_t*>(smem + L.tok_off);
   int32_t* tok_len = tok_start + 32;
@@ -396,11 +416,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.stages;
 
   if (threadIdx.x == 0) {
+    // MX: a tile (query block) is ready when its TMA bytes landed and the
+    // producer warp staged its scales: two arrivals
     for (int s = 0; s < S; ++s) {
-      dsa::mbar_init(&full[s], 1);
+      dsa::mbar_init(&full[s], MX ? 2 : 1);
       dsa::mbar_init(&empty[s], 1);
     }
-    dsa::mbar_init(qfull, 1);
+    dsa::mbar_init(qfull, MX ? 2 : 1);
     dsa::mbar_init(qempty, 1);
     for (int b = 0; b < 2; ++b) {
       dsa::mbar_init(&tfull[b], 1);
@@ -418,7 +440,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
 
   if (warp == 0) {
-    if (lane == 0) {
+    if constexpr (MX) {
+      // ------------------------------------------ TMA producer (MX: whole warp)
+      // Lane 0 issues the TMA loads; all 32 lanes stage the scale bytes of
+      // each query block and key tile, and lane 0 then arrives a second time.
+      if (lane == 0) {
+        dsa::tma_prefetch_desc(&map_q);
+        dsa::tma_prefetch_desc(&map_k);
+      }
+      const uint64_t keep = dsa::l2_policy_evict_last();
+      const uint64_t stream = dsa::l2_policy_evict_first();
+      // scale rows [row0, row0 + 128 nblk) -> nblk staged blocks at dst: lane r
+      // writes the 16 bytes of rows r, r + 32, r + 64, r + 96 of each block
+      auto stage_scales = [&](uint8_t* dst, const uint32_t* src, int64_t row0, int nblk, int64_t rows) {
+        dsa::fence_proxy_async_smem();  // the slot's last reader was tcgen05.cp (async proxy)
+        for (int h = 0; h < nblk; ++h) {
+          uint32_t v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t r = row0 + 128 * h + 32 * q + lane;
+            v[q] = r < rows ? __ldg(src + r) : 0x7F7F7F7Fu;  // past the end: scale 1 on zero-filled codes
+          }
+          *reinterpret_cast<uint4*>(dst + h * kSfBlockBytes + lane * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        dsa::fence_proxy_async_smem();  // generic writes -> tcgen05.cp (async proxy)
+        __syncwarp();
+      };
+      int stage = 0;
+      uint32_t phase = 0;
+      int iter = 0;
+      bool ok = true;
+      int n_issued = 0;  // key-tile loads issued: load i went to stage i % S, phase (i / S) & 1
+      int q_issued = 0;  // query-block loads issued: load m completes phase m of qfull
+      for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
+        const BlockRange br = block_range<GEN>(p, blk);
+        if (iter > 0 && !dsa::mbar_wait_warp(qempty, (iter - 1) & 1, wt)) { ok = false; break; }
+        if (lane == 0) {
+          dsa::mbar_expect_tx(qfull, nch * kNRows * 128);
+          for (int c = 0; c < nch; ++c)
+            dsa::tma_load_2d_hint(qbuf + c * kNRows * 128, &map_q, c * kChunkElems, br.t0 * p.Hi, qfull, stream);
+        }
+        ++q_issued;
+        stage_scales(sfbuf + S * kSfBlockBytes, p.q_sf, static_cast<int64_t>(br.t0) * p.Hi, kNRows / 128,
+                     static_cast<int64_t>(p.T) * p.Hi);
+        if (lane == 0) dsa::mbar_arrive(qfull);
+        for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+          if (!dsa::mbar_wait_warp(&empty[stage], phase ^ 1, wt)) { ok = false; break; }
+          if (lane == 0) {
+            dsa::mbar_expect_tx(&full[stage], nch * kKeyTile * 128);
+            uint8_t* dst = kbuf + stage * nch * kKeyTile * 128;
+            for (int c = 0; c < nch; ++c)
+              dsa::tma_load_2d_hint(dst + c * kKeyTile * 128, &map_k, c * kChunkElems, kt * kKeyTile, &full[stage],
+                                    keep);
+          }
+          stage_scales(sfbuf + stage * kSfBlockBytes, p.k_sf, static_cast<int64_t>(kt) * kKeyTile, 1, p.Tk);
+          if (lane == 0) dsa::mbar_arrive(&full[stage]);
+          ++n_issued;
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (lane == 0) {  // drain, as below
+        if (q_issued > 0) dsa::mbar_drain(qfull, (q_issued - 1) & 1, p.status);
+        for (int j = 1; j <= n_issued && j <= S; ++j) {
+          const int i = n_issued - j;
+          dsa::mbar_drain(&full[i % S], (i / S) & 1, p.status);
+        }
+      }
+      __syncwarp();
+    } else if (lane == 0) {
       // ------------------------------------------------------ TMA producer
       dsa::tma_prefetch_desc(&map_q);
       dsa::tma_prefetch_desc(&map_k);
@@ -459,7 +548,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (MX && lane == 0) {
+      // ------------------------------------------- MMA issuer (MX: block scales)
+      const uint32_t q_addr = dsa::smem_u32(qbuf), k_addr = dsa::smem_u32(kbuf), sf_addr = dsa::smem_u32(sfbuf);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      int iter = 0;
+      bool ok = true;
+      for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
+        const BlockRange br = block_range<GEN>(p, blk);
+        if (!dsa::mbar_wait(qfull, iter & 1, wt)) break;
+        dsa::tc_fence_after();
+        for (int kt = br.kt0; kt <= br.kt1; ++kt) {
+          // the single accumulator is free once the epilogue drained the last tile
+          // (so the previous MMAs, and the copies before them, are complete)
+          if (!dsa::mbar_wait(&tempty[0], acc_phase ^ 1, wt)) { ok = false; break; }
+          if (!dsa::mbar_wait(&full[stage], phase, wt)) { ok = false; break; }
+          dsa::tc_fence_after();
+          if (kt == br.kt0) {  // the query block's scales, 2 x 128 rows, to columns kSfbCol ..
+            dsa::tmem_cp_32x128b_x4(tmem_base + kSfbCol, dsa::smem_desc(sf_addr + S * kSfBlockBytes, 128, 128, 0));
+            dsa::tmem_cp_32x128b_x4(tmem_base + kSfbCol + 4,
+                                    dsa::smem_desc(sf_addr + (S + 1) * kSfBlockBytes, 128, 128, 0));
+          }
+          dsa::tmem_cp_32x128b_x4(tmem_base + kSfaCol, dsa::smem_desc(sf_addr + stage * kSfBlockBytes, 128, 128, 0));
+          const uint32_t a0 = k_addr + stage * nch * kKeyTile * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {  // one instruction per 32-element scale block of d = 128
+            const uint64_t ad = dsa::smem_desc(a0 + kk * 32, 16, 1024, dsa::kSwizzle128B);
+            const uint64_t bd = dsa::smem_desc(q_addr + kk * 32, 16, 1024, dsa::kSwizzle128B);
+            dsa::umma_mxf8(tmem_base, ad, bd, dsa::idesc_mxf8(kKeyTile, kNRows, kk, kk), tmem_base + kSfaCol,
+                           tmem_base + kSfbCol, kk != 0);
+          }
+          dsa::umma_commit(&empty[stage]);
+          dsa::umma_commit(&tfull[0]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+          acc_phase ^= 1;
+        }
+        dsa::umma_commit(qempty);
+      }
+      dsa::umma_drain(drain, p.status);  // every MMA and copy issued has completed
+    } else if (lane == 0) {
       // ------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = F8 ? dsa::idesc_e4m3(kKeyTile, kNRows) : dsa::idesc_bf16(kKeyTile, kNRows, 0, 0);
       int stage = 0;
@@ -512,8 +641,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    // a wait of this warp gave up (warp-uniform); the eight warps leave
-    // together at the block's last barrier, which carries the flag
+    // A wait of this thread gave up.  The thread carries on through the
+    // block's tiles (its TMEM loads stay in the allocation, its stores in the
+    // outputs and candidate segments, so the garbage it may compute is
+    // harmless in a kernel that is aborting, and no collective instruction
+    // sees a diverged warp); the eight warps leave together at the block's
+    // last barrier, which reduces the flag over the group.
     bool failed = false;
     const int seg = quarter;              // this warp writes segment `quarter` of its rows
     const int cap_seg = FUSED ? p.cap / 4 : 0;
@@ -528,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = i / HI, h = i - r * HI;
         const int t = br.t0 + r;
         float wv = t < p.T ? __ldg(p.w + static_cast<int64_t>(t) * Hi + h) : 0.f;
-        if (F8 && t < p.T) wv *= __ldg(p.q_scale + static_cast<int64_t>(t) * Hi + h);
+        if (F8 == 1 && t < p.T) wv *= __ldg(p.q_scale + static_cast<int64_t>(t) * Hi + h);
         w_s[i] = wv;
       }
       if (et < p.qb) {
@@ -566,20 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // fp8: this thread's key descale, loaded one tile ahead
       float ks_next = 1.f;
-      if (F8) {
+      if (F8 == 1) {
         const int s0 = br.kt0 * kKeyTile + key_lane;
         ks_next = s0 < p.Tk ? __ldg(p.k_scale + s0) : 0.f;
       }
       for (int kt = br.kt0; kt <= br.kt1; ++kt) {
         const float ks = ks_next;
-        if (F8) {
+        if (F8 == 1) {
           const int s1 = (kt + 1) * kKeyTile + key_lane;
           ks_next = (kt < br.kt1 && s1 < p.Tk) ? __ldg(p.k_scale + s1) : 0.f;
         }
-        if (!dsa::mbar_wait_warp(&tfull[acc], acc_phase, wt)) {
-          failed = true;
-          break;
-        }
+        if (!failed) failed = !dsa::mbar_wait(&tfull[acc], acc_phase, wt);
         dsa::tc_fence_after();
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
         // this warp's columns [slice*kSliceCols, (slice+1)*kSliceCols) = tokens [slice*tok_per_slice, ...)
@@ -625,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       fmaxf(__uint_as_float(v[4 * g + 3]), 0.f));
             if (h + 3 == HI - 1) {
               const float sum = ((ch[0] + ch[1]) + (ch[2] + ch[3])) + ((ch[4] + ch[5]) + (ch[6] + ch[7]));
-              const float score = F8 ? sum * ks : sum;
+              const float score = F8 == 1 ? sum * ks : sum;
               const int q = cl / HI;  // token within this slice (compile-time)
               const int r = slice * tok_per_slice + q;
               const int t = br.t0 + r;
@@ -676,8 +806,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsa::tc_fence_before();
         __syncwarp();
         if (lane == 0) dsa::mbar_arrive(&tempty[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
         if (FUSED && p.compact) {
           // a segment that might not hold the next tile's 32 keys is cut to its top-k
 #pragma unroll
@@ -1247,11 +1379,13 @@ struct Inputs {
   const float* q_scale;  // non-NULL: qi / ki are E4M3 (one byte per element)
   const float* k_scale;
   int Tq, Tk, Hi, d;
-  int elem_bytes() const { return q_scale ? 1 : 2; }
+  const uint32_t* q_sf = nullptr;  // non-NULL: qi / ki are E4M3 with E8M0 block scales (MXFP8)
+  const uint32_t* k_sf = nullptr;
+  int elem_bytes() const { return (q_scale || q_sf) ? 1 : 2; }
 };
 
 int make_maps(const Inputs& in, CUtensorMap* mq, CUtensorMap* mk) {
-  const CUtensorMapDataType dt = in.q_scale ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = in.elem_bytes() == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t box = 128 / in.elem_bytes();  // one 128-byte swizzled chunk
   const uint64_t row = static_cast<uint64_t>(in.d) * in.elem_bytes();
   int rc = dsa::encode_tensor_map_2d(mq, in.qi, dt, in.d, static_cast<uint64_t>(in.Tq) * in.Hi, row, box, kNRows,
@@ -1264,6 +1398,8 @@ void fill_params(IndexerParams& p, const Inputs& in, const Geom& g) {
   p.w = in.w;
   p.q_scale = in.q_scale;
   p.k_scale = in.k_scale;
+  p.q_sf = in.q_sf;
+  p.k_sf = in.k_sf;
   p.g = g;
   p.T = in.Tq;
   p.Tk = in.Tk;
@@ -1283,7 +1419,7 @@ int launch_indexer_hi(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParam
                       cudaStream_t stream) {
   const int max_stages = FUSED ? 3 : 4;
   p.stages = p.nch == 1 ? 6 : max_stages;
-  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED);
+  const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED, F8 == 2);
   const size_t smem = L.total + 1024;
   if (cudaFuncSetAttribute(indexer_kernel<FUSED, HI, GEN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -1299,6 +1435,10 @@ int launch_indexer_gen(const CUtensorMap& mq, const CUtensorMap& mk, IndexerPara
   if (p.q_scale) {  // fp8 inputs: 32 or 64 heads (validated)
     return p.Hi == 32 ? launch_indexer_hi<FUSED, 32, GEN, 1>(mq, mk, p, sm_count, stream)
                       : launch_indexer_hi<FUSED, 64, GEN, 1>(mq, mk, p, sm_count, stream);
+  }
+  if (p.q_sf) {  // mxfp8 inputs: 32 or 64 heads (validated)
+    return p.Hi == 32 ? launch_indexer_hi<FUSED, 32, GEN, 2>(mq, mk, p, sm_count, stream)
+                      : launch_indexer_hi<FUSED, 64, GEN, 2>(mq, mk, p, sm_count, stream);
   }
   switch (p.Hi) {
     case 8: return launch_indexer_hi<FUSED, 8, GEN, 0>(mq, mk, p, sm_count, stream);
@@ -1620,6 +1760,76 @@ extern "C" int dsa_indexer_topk_fp8(const void* qi8, const void* ki8, const floa
   if (rc != DSA_OK) return rc;
   const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
   return run_fused(Inputs{qi8, ki8, w, q_scale, k_scale, Tq, Tk, Hi, d}, g, k, idx, topk_length, logits, softmax, lse,
+                   workspace, sms, stream);
+}
+
+// ---- MXFP8 inputs (cuDNN DSA page, section 3 precision path "mxfp8": E4M3
+// Q/K with block-scaled E8M0 scales, one per 32 elements of d).
+namespace {
+int validate_mxfp8(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf, const float* w,
+                   const int32_t* cu_q, const int32_t* cu_k, int n_docs, int Tq, int Tk, int Hi, int d, int ratio,
+                   int s_max, const char* fn) {
+  int rc = validate_ratio(qi8, ki8, w, cu_q, cu_k, n_docs, Tq, Tk, Hi, d, ratio, s_max, fn);
+  if (rc != DSA_OK) return rc;
+  if (!q_sf || !k_sf) return dsa::set_error(DSA_ERR_VALUE, "%s: NULL q_sf or k_sf", fn);
+  if (!dsa::aligned(q_sf, 4) || !dsa::aligned(k_sf, 4))
+    return dsa::set_error(DSA_ERR_VALUE, "%s: q_sf and k_sf must be 4-byte aligned", fn);
+  if (d != 128 || (Hi != 32 && Hi != 64))
+    return dsa::set_error(DSA_ERR_VALUE, "%s: mxfp8 inputs need d = 128 and Hi in {32, 64} (got d %d, Hi %d)", fn, d,
+                          Hi);
+  return DSA_OK;
+}
+Inputs mx_inputs(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf, const float* w, int Tq,
+                 int Tk, int Hi, int d) {
+  Inputs in{qi8, ki8, w, nullptr, nullptr, Tq, Tk, Hi, d};
+  in.q_sf = reinterpret_cast<const uint32_t*>(q_sf);
+  in.k_sf = reinterpret_cast<const uint32_t*>(k_sf);
+  return in;
+}
+}  // namespace
+
+extern "C" int dsa_indexer_scores_mxfp8(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf,
+                                        const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                        const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                                        int ratio, int s_max, float* scores, int64_t ld, cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_mxfp8(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                          "dsa_indexer_scores_mxfp8");
+  if (rc != DSA_OK) return rc;
+  if (!scores) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_mxfp8: NULL scores");
+  if (ld < s_max || ld % 4 != 0)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_scores_mxfp8: need ld >= s_max, ld % 4 == 0");
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_dense(mx_inputs(qi8, ki8, q_sf, k_sf, w, Tq, Tk, Hi, d), g, scores, ld, sms, stream);
+}
+
+extern "C" int dsa_indexer_topk_mxfp8(const void* qi8, const void* ki8, const uint8_t* q_sf, const uint8_t* k_sf,
+                                      const float* w, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                      const int32_t* q_causal_offsets, int n_docs, int Tq, int Tk, int Hi, int d,
+                                      int ratio, int k, int s_max, int32_t* idx, int32_t* topk_length, float* logits,
+                                      float* softmax, float* lse, void* workspace, size_t ws_bytes,
+                                      cudaStream_t stream) {
+  dsa::clear_error();
+  int rc = validate_mxfp8(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, n_docs, Tq, Tk, Hi, d, ratio, s_max,
+                          "dsa_indexer_topk_mxfp8");
+  if (rc != DSA_OK) return rc;
+  if (!idx) return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_mxfp8: NULL idx");
+  if ((softmax || lse) && !logits)
+    return dsa::set_error(DSA_ERR_VALUE, "dsa_indexer_topk_mxfp8: softmax and lse need logits");
+  rc = check_workspace(Tq, Hi, d, k, s_max, workspace, ws_bytes, "dsa_indexer_topk_mxfp8");
+  if (rc != DSA_OK) return rc;
+  if (logits && !select_is_fast(s_max, k))
+    return dsa::set_error(DSA_ERR_UNSUPPORTED,
+                          "dsa_indexer_topk_mxfp8: logits need rows of at most %d columns (s_max = %d)", kSelMaxLen,
+                          s_max);
+  int sms = 0;
+  rc = dsa::check_device(&sms);
+  if (rc != DSA_OK) return rc;
+  const Geom g{cu_seqlens_q, cu_seqlens_k, q_causal_offsets, n_docs, ratio, s_max};
+  return run_fused(mx_inputs(qi8, ki8, q_sf, k_sf, w, Tq, Tk, Hi, d), g, k, idx, topk_length, logits, softmax, lse,
                    workspace, sms, stream);
 }
 

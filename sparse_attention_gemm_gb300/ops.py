@@ -66,6 +66,8 @@ _SIGNATURES = {
     "dsa_indexer_topk_ratio": ([P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
     "dsa_indexer_scores_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, I64, P], I),
     "dsa_indexer_topk_fp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
+    "dsa_indexer_scores_mxfp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, I64, P], I),
+    "dsa_indexer_topk_mxfp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
     "dsa_sparse_attn_bwd_workspace_size": ([I, I, I, I], SZ),
     "dsa_sparse_attn_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P], I),
 }
@@ -263,6 +265,61 @@ def indexer_topk_fp8(qi8, ki8, q_scale, k_scale, w, cu_seqlens_q, cu_seqlens_k, 
                                       _p(cu_seqlens_k), _p(q_causal_offsets), cu_seqlens_q.numel() - 1, Tq, Tk, Hi, d,
                                       int(ratio), k, s_max, _p(idx), _p(tl), _p(logits), _p(sm), _p(lse),
                                       _p(workspace), workspace.numel() * workspace.element_size(), _stream()))
+    res = {"idx": idx, "topk_length": tl}
+    for name, t in (("logits", logits), ("softmax", sm), ("lse", lse)):
+        if t is not None:
+            res[name] = t
+    return res
+
+
+def _mxfp8_inputs(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets):
+    _need(qi8, "qi8", torch.uint8, 3)
+    _need(ki8, "ki8", torch.uint8, 2)
+    _need(q_sf, "q_sf", torch.uint8, 3)
+    _need(k_sf, "k_sf", torch.uint8, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    if q_causal_offsets is not None:
+        _need(q_causal_offsets, "q_causal_offsets", torch.int32, 1)
+    if q_sf.shape != (qi8.shape[0], qi8.shape[1], qi8.shape[2] // 32) or k_sf.shape != (ki8.shape[0], ki8.shape[1] // 32):
+        raise ValueError("q_sf / k_sf must hold one scale byte per 32 elements of qi8 / ki8")
+    return qi8.shape[0], ki8.shape[0], qi8.shape[1], qi8.shape[2]
+
+
+def indexer_scores_mxfp8(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets, ratio: int,
+                         s_max: int, ld: int | None = None, out=None):
+    """Dense indexer scores fp32 [Tq, ld] from E4M3 qi8 / ki8 with E8M0 block scales q_sf / k_sf (uint8)."""
+    Tq, Tk, Hi, d = _mxfp8_inputs(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets)
+    ld = ld or (s_max + 3) // 4 * 4
+    if out is None:
+        out = torch.empty((Tq, ld), dtype=torch.float32, device=qi8.device)
+    _check("dsa_indexer_scores_mxfp8",
+           lib().dsa_indexer_scores_mxfp8(_p(qi8), _p(ki8), _p(q_sf), _p(k_sf), _p(w), _p(cu_seqlens_q),
+                                          _p(cu_seqlens_k), _p(q_causal_offsets), cu_seqlens_q.numel() - 1, Tq, Tk,
+                                          Hi, d, int(ratio), s_max, _p(out), ld, _stream()))
+    return out
+
+
+def indexer_topk_mxfp8(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets, ratio: int, k: int,
+                       s_max: int, want_logits: bool = False, want_softmax: bool = False, want_lse: bool = False,
+                       workspace=None, idx=None, topk_length=None):
+    """Combined indexer + top-k on MXFP8 inputs: dict(idx, topk_length[, logits][, softmax][, lse])."""
+    Tq, Tk, Hi, d = _mxfp8_inputs(qi8, ki8, q_sf, k_sf, w, cu_seqlens_q, cu_seqlens_k, q_causal_offsets)
+    dev = qi8.device
+    if workspace is None:
+        workspace = torch.empty(indexer_topk_workspace_size(Tq, Hi, d, k, s_max), dtype=torch.uint8, device=dev)
+    want_logits = want_logits or want_softmax or want_lse
+    idx = torch.empty((Tq, k), dtype=torch.int32, device=dev) if idx is None else idx
+    tl = torch.empty(Tq, dtype=torch.int32, device=dev) if topk_length is None else topk_length
+    logits = torch.empty((Tq, k), dtype=torch.float32, device=dev) if want_logits else None
+    sm = torch.empty((Tq, k), dtype=torch.float32, device=dev) if want_softmax else None
+    lse = torch.empty(Tq, dtype=torch.float32, device=dev) if want_lse else None
+    _check("dsa_indexer_topk_mxfp8",
+           lib().dsa_indexer_topk_mxfp8(_p(qi8), _p(ki8), _p(q_sf), _p(k_sf), _p(w), _p(cu_seqlens_q),
+                                        _p(cu_seqlens_k), _p(q_causal_offsets), cu_seqlens_q.numel() - 1, Tq, Tk, Hi,
+                                        d, int(ratio), k, s_max, _p(idx), _p(tl), _p(logits), _p(sm), _p(lse),
+                                        _p(workspace), workspace.numel() * workspace.element_size(), _stream()))
     res = {"idx": idx, "topk_length": tl}
     for name, t in (("logits", logits), ("softmax", sm), ("lse", lse)):
         if t is not None:

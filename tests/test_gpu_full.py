@@ -150,6 +150,32 @@ def test_long_64k_fp8_inputs():
     assert np.array_equal(res["idx"][torch.from_numpy(rows).to(DEV)].cpu().numpy(), ri)
 
 
+def test_long_64k_mxfp8_inputs():
+    """The long-context workload with MXFP8 indexer inputs (E4M3 codes, E8M0
+    scales per 32 elements): combined call == dense + top-k on every row;
+    sampled rows against the oracle's dequantized scores."""
+    wl = W.long_64k()
+    T, K = wl.T, wl.K
+    q8, qs = wl.qi_mxfp8()
+    k8, ks = wl.ki_mxfp8()
+    w = wl.w()
+    cu = dev(wl.cu_seqlens)
+    a = (dev(q8), dev(k8), dev(qs), dev(ks), dev(w), cu, cu, None)
+    res = ops.indexer_topk_mxfp8(*a, 1, K, wl.s_max)
+    scores = ops.indexer_scores_mxfp8(*a, 1, wl.s_max)
+    start, length = oracle.thd_metadata(wl.cu_seqlens, T)
+    ui, ut, _ = ops.topk(scores, dev(length), K, row_start=dev(start))
+    assert torch.equal(res["idx"], ui) and torch.equal(res["topk_length"], ut)
+    rows = _rows(T, K, 24, 19)
+    sc_rows = scores[torch.from_numpy(rows).to(DEV)].cpu().numpy()[:, : wl.s_max]
+    osc, mag = oracle.indexer_scores(oracle.mxfp8_dequant(q8[rows], qs[rows]), oracle.mxfp8_dequant(k8, ks), w[rows],
+                                     start[rows], length[rows], wl.s_max, want_abs=True)
+    fin = np.isfinite(osc)
+    assert_scores_close(sc_rows, osc, mag, fin)
+    ri, rt = oracle.topk(sc_rows.astype(np.float64), length[rows], K, start_rows=start[rows])
+    assert np.array_equal(res["idx"][torch.from_numpy(rows).to(DEV)].cpu().numpy(), ri)
+
+
 def test_compressed_thd_8k_workload():
     _ratio_workload_check(W.compressed_thd_8k(), 64, 6)
 

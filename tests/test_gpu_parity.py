@@ -261,6 +261,91 @@ def test_fp8_fused_topk_equals_dense_then_topk(name, k):
     assert np.array_equal(res["logits"].cpu().numpy().astype(np.float64), rl)
 
 
+# ---------------------------------------------------------- mxfp8 indexer inputs
+def _mx_inputs(name, jitter=True):
+    """MXFP8 inputs of an FP8_CASES geometry: E4M3 codes with per-32-element
+    E8M0 scales (the workload quantiser), then each scale byte moved by a
+    random -3..3 and the codes kept, so that every block of every row carries
+    its own power of two and a scale applied to the wrong block, row or
+    operand changes the scores."""
+    lq, lk, off, ratio, Hi = FP8_CASES[name]
+    lk = lq if lk is None else lk
+    rng = np.random.default_rng(sum(lq) * 13 + Hi)
+    cq, ck = cu_from_lengths(lq), cu_from_lengths(lk)
+    Tq, Tk = int(cq[-1]), int(ck[-1])
+    q8, qs = W.Workload._to_mxfp8(rand_bf16_bits(rng, (Tq, Hi, 128)))
+    k8, ks = W.Workload._to_mxfp8(rand_bf16_bits(rng, (Tk, 128)))
+    if jitter:
+        qs = np.clip(qs.astype(np.int32) + rng.integers(-3, 4, size=qs.shape), 1, 254).astype(np.uint8)
+        ks = np.clip(ks.astype(np.int32) + rng.integers(-3, 4, size=ks.shape), 1, 254).astype(np.uint8)
+    w = (rng.random((Tq, Hi), dtype=np.float32) / np.float32(8)).astype(np.float32)
+    off = None if off is None else np.asarray(off, np.int32)
+    return cq, ck, off, ratio, int(max(lk)), Tq, Tk, q8, qs, k8, ks, w
+
+
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+def test_mxfp8_indexer_scores(name):
+    """E4M3 inputs with E8M0 block scales against the oracle's dequantized scores."""
+    cq, ck, off, ratio, s_max, Tq, Tk, q8, qs, k8, ks, w = _mx_inputs(name)
+    got = ops.indexer_scores_mxfp8(*_fp8_dev(cq, ck, off, q8, qs, k8, ks, w), ratio, s_max).cpu().numpy()[:, :s_max]
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    sc, mag = oracle.indexer_scores(oracle.mxfp8_dequant(q8, qs), oracle.mxfp8_dequant(k8, ks), w, start, length,
+                                    s_max, want_abs=True)
+    fin = np.isfinite(sc)
+    assert_scores_close(got, sc, mag, fin)
+    assert np.all(np.isneginf(got[~fin]))
+
+
+def test_mxfp8_integer_scores_exact():
+    """Codes of integers in [-3, 3], power-of-two scales 2^-1 .. 2^1 per block
+    and weights 1 or 2: a dot product is a multiple of 2^-2 below 128 * 9 * 4,
+    the score below 64 * 2 times that, so every product and partial sum has
+    at most 22 significant bits and is exact in fp32: the GPU scores equal the
+    oracle's bit for bit, whatever the summation order."""
+    rng = np.random.default_rng(77)
+    T, Hi = 300, 64
+    enc = np.vectorize(_e4m3_code_int)
+    q8 = enc(rng.integers(-3, 4, size=(T, Hi, 128))).astype(np.uint8)
+    k8 = enc(rng.integers(-3, 4, size=(T, 128))).astype(np.uint8)
+    qs = rng.integers(126, 129, size=(T, Hi, 4)).astype(np.uint8)
+    ks = rng.integers(126, 129, size=(T, 4)).astype(np.uint8)
+    w = rng.integers(1, 3, size=(T, Hi)).astype(np.float32)
+    cu = cu_from_lengths([T])
+    got = ops.indexer_scores_mxfp8(dev(q8), dev(k8), dev(qs), dev(ks), dev(w), dev(cu), dev(cu), None, 1,
+                                   T).cpu().numpy()
+    start, length = oracle.thd_metadata(cu, T)
+    ref = oracle.indexer_scores(oracle.mxfp8_dequant(q8, qs), oracle.mxfp8_dequant(k8, ks), w.astype(np.float64),
+                                start, length, T)
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin].astype(np.float64), ref[fin])
+
+
+def _e4m3_code_int(v):
+    v = int(v)
+    if v == 0:
+        return 0
+    a = abs(v)
+    e = a.bit_length() - 1
+    return (0x80 if v < 0 else 0) | ((e + 7) << 3) | (((a << 3) >> e) & 7)
+
+
+@pytest.mark.parametrize("name", sorted(FP8_CASES))
+@pytest.mark.parametrize("k", [1, 64, 512])
+def test_mxfp8_fused_topk_equals_dense_then_topk(name, k):
+    cq, ck, off, ratio, s_max, Tq, Tk, q8, qs, k8, ks, w = _mx_inputs(name)
+    a = _fp8_dev(cq, ck, off, q8, qs, k8, ks, w)
+    res = ops.indexer_topk_mxfp8(*a, ratio, k, s_max, want_logits=True)
+    sc = ops.indexer_scores_mxfp8(*a, ratio, s_max)
+    start, length = oracle.ratio_metadata(cq, ck, off, ratio, Tq, Tk)
+    di, dt, _ = ops.topk(sc, dev(length), k, row_start=dev(start))
+    assert torch.equal(res["idx"], di) and torch.equal(res["topk_length"], dt)
+    scn = sc.cpu().numpy().astype(np.float64)
+    ri, rt = oracle.topk(scn, length, k, start_rows=start)
+    assert np.array_equal(res["idx"].cpu().numpy(), ri)
+    rl, _, _ = oracle.topk_softmax(scn, ri, rt, start_rows=start)
+    assert np.array_equal(res["logits"].cpu().numpy().astype(np.float64), rl)
+
+
 # ---------------------------------------------------------------------- top-k
 def test_topk_on_gpu_scores_is_exact():
     rng = np.random.default_rng(5)
