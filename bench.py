@@ -35,13 +35,14 @@ L2_BYTES = 129 * 1024 * 1024
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# long-context workload's two large kernels, each from one ncu capture of this
-# bench (command and figures in profiles/).  A figure only stands for the
-# kernel sources it measured: when their hash differs it is reported as null.
+# long-context workload's two large kernels, each from one single-pass ncu
+# capture of one launch at the full T=65536 shapes (command and figures in
+# profiles/).  A figure only stands for the kernel sources it measured: when
+# their hash differs it is reported as null.
 TRAFFIC = {
-    "indexer_kernel": (5392211712, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
-                       "c53cbf9863f56ab0"),
-    "sparse_attn_kernel": (11375263488, ("attention.cu", "common.cuh"), "e2b4e7239cc9f413"),
+    "indexer_kernel": (5380000000, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
+                       "892a00219dde9e14"),
+    "sparse_attn_kernel": (11330000000, ("attention.cu", "common.cuh"), "ecd829e5b4e9c800"),
 }
 
 
@@ -496,7 +497,7 @@ def main():
         del ws
         torch.cuda.empty_cache()
         scores = torch.empty((T, wl.s_max), dtype=torch.float32, device=dev)
-        ops.indexer_scores(d["qi"], d["ki"], d["w"], d["cu"], wl.s_max, out=scores)
+        dense_ms = timed(lambda: ops.indexer_scores(d["qi"], d["ki"], d["w"], d["cu"], wl.s_max, out=scores))
         tk_idx = torch.empty((T, K), dtype=torch.int32, device=dev)
         tk_tl = torch.empty(T, dtype=torch.int32, device=dev)
         for _ in range(2):
@@ -516,7 +517,9 @@ def main():
         tavg = sum(tms) / len(tms)
         topk_line = {"ms": tavg, "algorithmic_bytes": tbytes, "achieved_gbs": tbytes / (tavg / 1e3) / 1e9,
                      "peak_gbs": pk["hbm_gbs"], "frac": tbytes / (tavg / 1e3) / 1e9 / pk["hbm_gbs"],
-                     "equals_fused_indices": same}
+                     "equals_fused_indices": same,
+                     "dense_indexer_ms": dense_ms,
+                     "dense_indexer_frac_peak": work["indexer_flops"] / (dense_ms / 1e3) / 1e12 / pk["bf16_tflops"]}
         del scores
 
     # ---- compressed-key indexer (ratio-causal mask over a compressed key

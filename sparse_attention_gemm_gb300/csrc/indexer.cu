@@ -138,7 +138,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, i
   L.cmp_off = o;
   if (fused) o += kEpiWarps * 256 * 4;  // one 256-bin histogram per epilogue warp (segment compaction)
   L.bar_off = o;
-  o += (2 * 8 + 7) * 8;
+  o += (2 * 8 + 9) * 8;
   L.misc_off = o;
   o += 16;
   L.total = o;
@@ -383,8 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = dsa::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   constexpr bool MX = F8 == 2;
-  constexpr int kAccBufs = MX ? 1 : 2;  // TMEM accumulators
-  constexpr uint32_t kSfaCol = 256, kSfbCol = 264;  // MX: scale columns (A: 4, B: 8)
+  // MX: the accumulator is a ring of three 128-column half-tiles (half s of
+  // tile g is half-tile j = 2g + s, slot j % 3, read by the epilogue warps of
+  // column slice s), and the block scales take the columns after it, two
+  // buffers each (key tile by tile parity, query block by block parity).
+  constexpr int kMxSlots = 3;
+  constexpr uint32_t kSfaCol = 3 * 128, kSfbCol = kSfaCol + 8;  // MX: A 2 x 4, B 2 x 8 columns
   const SmemLayout L = smem_layout(p.nch, p.stages, p.qb, FUSED, MX);
   uint8_t* qbuf = smem + L.q_off;
   uint8_t* kbuf = smem + L.k_off;
@@ -404,9 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = bars + 8;
   uint64_t* qfull = bars + 16;
   uint64_t* qempty = bars + 17;
-  uint64_t* tfull = bars + 18;   // [2]
-  uint64_t* tempty = bars + 20;  // [2]
-  uint64_t* drain = bars + 22;   // the MMA issuer's exit commit
+  uint64_t* tfull = bars + 18;   // [2] ([3] for MX)
+  uint64_t* tempty = bars + 21;  // [2] ([3] for MX)
+  uint64_t* drain = bars + 24;   // the MMA issuer's exit commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
@@ -424,9 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     dsa::mbar_init(qfull, MX ? 2 : 1);
     dsa::mbar_init(qempty, 1);
-    for (int b = 0; b < 2; ++b) {
+    // an accumulator is drained by every epilogue warp; an MX half-tile slot
+    // by the four warps of its column slice
+    for (int b = 0; b < (MX ? kMxSlots : 2); ++b) {
       dsa::mbar_init(&tfull[b], 1);
-      dsa::mbar_init(&tempty[b], kEpiWarps);
+      dsa::mbar_init(&tempty[b], MX ? kEpiWarps / kSlices : kEpiWarps);
     }
     dsa::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -553,37 +559,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = dsa::smem_u32(qbuf), k_addr = dsa::smem_u32(kbuf), sf_addr = dsa::smem_u32(sfbuf);
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase = 0;
+      uint32_t j = 0;  // half-tiles issued
+      uint32_t g = 0;  // tiles issued
       int iter = 0;
       bool ok = true;
       for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x, ++iter) {
         const BlockRange br = block_range<GEN>(p, blk);
         if (!dsa::mbar_wait(qfull, iter & 1, wt)) break;
         dsa::tc_fence_after();
-        for (int kt = br.kt0; kt <= br.kt1; ++kt) {
-          // the single accumulator is free once the epilogue drained the last tile
-          // (so the previous MMAs, and the copies before them, are complete)
-          if (!dsa::mbar_wait(&tempty[0], acc_phase ^ 1, wt)) { ok = false; break; }
+        const uint32_t sfb = kSfbCol + 8 * (iter & 1);
+        for (int kt = br.kt0; kt <= br.kt1 && ok; ++kt, ++g) {
           if (!dsa::mbar_wait(&full[stage], phase, wt)) { ok = false; break; }
-          dsa::tc_fence_after();
-          if (kt == br.kt0) {  // the query block's scales, 2 x 128 rows, to columns kSfbCol ..
-            dsa::tmem_cp_32x128b_x4(tmem_base + kSfbCol, dsa::smem_desc(sf_addr + S * kSfBlockBytes, 128, 128, 0));
-            dsa::tmem_cp_32x128b_x4(tmem_base + kSfbCol + 4,
-                                    dsa::smem_desc(sf_addr + (S + 1) * kSfBlockBytes, 128, 128, 0));
-          }
-          dsa::tmem_cp_32x128b_x4(tmem_base + kSfaCol, dsa::smem_desc(sf_addr + stage * kSfBlockBytes, 128, 128, 0));
+          const uint32_t sfa = kSfaCol + 4 * (g & 1);
           const uint32_t a0 = k_addr + stage * nch * kKeyTile * 128;
+          for (int h = 0; h < kSlices; ++h, ++j) {
+            const uint32_t slot = j % kMxSlots;
+            // the slot's last reader (three half-tiles back) is done: so is every
+            // MMA before it, hence the scale buffers two tiles / one block back
+            if (!dsa::mbar_wait(&tempty[slot], ((j / kMxSlots) & 1) ^ 1, wt)) { ok = false; break; }
+            dsa::tc_fence_after();
+            if (h == 0) {
+              if (kt == br.kt0) {  // the query block's scales, 2 x 128 rows
+                dsa::tmem_cp_32x128b_x4(tmem_base + sfb, dsa::smem_desc(sf_addr + S * kSfBlockBytes, 128, 128, 0));
+                dsa::tmem_cp_32x128b_x4(tmem_base + sfb + 4,
+                                        dsa::smem_desc(sf_addr + (S + 1) * kSfBlockBytes, 128, 128, 0));
+              }
+              dsa::tmem_cp_32x128b_x4(tmem_base + sfa, dsa::smem_desc(sf_addr + stage * kSfBlockBytes, 128, 128, 0));
+            }
+            // half h: the 128 query rows of column slice h against the 128 keys
+            const uint32_t b0 = q_addr + h * (kNRows / kSlices) * 128;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {  // one instruction per 32-element scale block of d = 128
-            const uint64_t ad = dsa::smem_desc(a0 + kk * 32, 16, 1024, dsa::kSwizzle128B);
-            const uint64_t bd = dsa::smem_desc(q_addr + kk * 32, 16, 1024, dsa::kSwizzle128B);
-            dsa::umma_mxf8(tmem_base, ad, bd, dsa::idesc_mxf8(kKeyTile, kNRows, kk, kk), tmem_base + kSfaCol,
-                           tmem_base + kSfbCol, kk != 0);
+            for (int kk = 0; kk < 4; ++kk) {  // one instruction per 32-element scale block of d = 128
+              const uint64_t ad = dsa::smem_desc(a0 + kk * 32, 16, 1024, dsa::kSwizzle128B);
+              const uint64_t bd = dsa::smem_desc(b0 + kk * 32, 16, 1024, dsa::kSwizzle128B);
+              dsa::umma_mxf8(tmem_base + slot * 128, ad, bd, dsa::idesc_mxf8(kKeyTile, kNRows / kSlices, kk, kk),
+                             tmem_base + sfa, tmem_base + sfb + 4 * h, kk != 0);
+            }
+            dsa::umma_commit(&tfull[slot]);
           }
+          if (!ok) break;
           dsa::umma_commit(&empty[stage]);
-          dsa::umma_commit(&tfull[0]);
           if (++stage == S) { stage = 0; phase ^= 1; }
-          acc_phase ^= 1;
         }
         dsa::umma_commit(qempty);
       }
@@ -640,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hist_words_row = FUSED ? (kHistWords / QB) : 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t jh = static_cast<uint32_t>(slice);  // MX: this warp's half-tiles are 2g + slice
     bool ok = true;
     // A wait of this thread gave up.  The thread carries on through the
     // block's tiles (its TMEM loads stay in the allocation, its stores in the
@@ -709,12 +726,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s1 = (kt + 1) * kKeyTile + key_lane;
           ks_next = (kt < br.kt1 && s1 < p.Tk) ? __ldg(p.k_scale + s1) : 0.f;
         }
-        if (!failed) failed = !dsa::mbar_wait(&tfull[acc], acc_phase, wt);
+        // the accumulator (or, MX, this slice's half-tile slot) of this tile
+        uint32_t slot = static_cast<uint32_t>(acc), slot_phase = acc_phase;
+        if constexpr (MX) {
+          slot = jh % kMxSlots;
+          slot_phase = (jh / kMxSlots) & 1;
+        }
+        if (!failed) failed = !dsa::mbar_wait(&tfull[slot], slot_phase, wt);
         dsa::tc_fence_after();
         const int s_key = kt * kKeyTile + key_lane;  // absolute key row
         // this warp's columns [slice*kSliceCols, (slice+1)*kSliceCols) = tokens [slice*tok_per_slice, ...)
-        const uint32_t t_addr =
-            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kNRows + slice * kSliceCols;
+        const uint32_t t_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                (MX ? slot * 128 : acc * kNRows + slice * kSliceCols);
+        dsa::check((MX ? (slot + 1) * 128 : acc * kNRows + (slice + 1) * kSliceCols) <= kSfaCol || !MX, p.status);
         dsa::check(acc * kNRows + (slice + 1) * kSliceCols <= static_cast<int>(kTmemCols), p.status);
         // fused: a row's entry bound for this tile, read once (tau only rises
         // and a compacted segment's floor only rises, so a value read early
@@ -805,10 +829,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         dsa::tc_fence_before();
         __syncwarp();
-        if (lane == 0) dsa::mbar_arrive(&tempty[acc]);
-        if (++acc == kAccBufs) {
-          acc = 0;
-          acc_phase ^= 1;
+        if (lane == 0) dsa::mbar_arrive(&tempty[slot]);
+        if constexpr (MX) {
+          jh += kSlices;
+        } else {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
         }
         if (FUSED && p.compact) {
           // a segment that might not hold the next tile's 32 keys is cut to its top-k

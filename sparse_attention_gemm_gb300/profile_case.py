@@ -13,6 +13,9 @@ holds a few GB on the device and its inputs exceed the 129 MB L2.
 Cases (kernel to select with -k in parentheses):
   indexer_dense   dsa_indexer_scores, scores [T, T] fp32       (indexer_kernel)
   indexer_fused   stage 1 of dsa_indexer_topk                   (indexer_kernel)
+  indexer_mxfp8   dsa_indexer_scores_mxfp8 on E4M3 codes with E8M0 scales per 32
+                  elements (drawn codes and scales), scores [T, T] fp32
+                                                                (indexer_kernel)
   select          stage 2 of dsa_indexer_topk                   (fused_select_fast_kernel)
   topk            dsa_topk on the dense causal scores           (topk_stream_kernel)
   attention       dsa_sparse_attn_fwd on the fused top-k ids    (sparse_attn_kernel)
@@ -29,7 +32,7 @@ import sys
 import numpy as np
 import torch
 
-CASES = ("indexer_dense", "indexer_fused", "select", "topk", "attention", "gqa")
+CASES = ("indexer_dense", "indexer_fused", "indexer_mxfp8", "select", "topk", "attention", "gqa")
 
 
 def _bf16(shape, sigma, g, dev):
@@ -76,6 +79,17 @@ def main(argv=None) -> int:
         print(f"gqa: B={B} S={S} Hq={Hq} D={D} width={idx.shape[1]}")
         return 0
 
+    if args.case == "indexer_mxfp8":
+        # E4M3 codes of N(0,1) draws with scale bytes around 2^-2 (no NaN codes)
+        q8 = torch.randn((T, Hi, d), generator=g, device=dev).to(torch.float8_e4m3fn).view(torch.uint8)
+        k8 = torch.randn((T, d), generator=g, device=dev).to(torch.float8_e4m3fn).view(torch.uint8)
+        qs = torch.randint(123, 128, (T, Hi, d // 32), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        ks = torch.randint(123, 128, (T, d // 32), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+        w = torch.rand((T, Hi), generator=g, device=dev, dtype=torch.float32) / 8.0
+        scores = torch.empty((T, T), dtype=torch.float32, device=dev)
+        twice(lambda: ops.indexer_scores_mxfp8(q8, k8, qs, ks, w, cu, cu, None, 1, T, out=scores))
+        print(f"{args.case}: T={T} status={ops.device_status(clear=True):#x}")
+        return 0
     qi = _bf16((T, Hi, d), 1.0, g, dev)
     ki = _bf16((T, d), 1.0, g, dev)
     w = torch.rand((T, Hi), generator=g, device=dev, dtype=torch.float32) / 8.0
