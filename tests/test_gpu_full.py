@@ -176,6 +176,53 @@ def test_long_64k_mxfp8_inputs():
     assert np.array_equal(res["idx"][torch.from_numpy(rows).to(DEV)].cpu().numpy(), ri)
 
 
+def test_long_64k_backward_key_shared_by_every_row():
+    """dkv of keys referenced by many rows, at the 64K-token shapes.  Key 0
+    sits in every row (at slot t % k), key 1 in every other row: dkv[0] sums
+    65534 x 64 contributions through the 128 fp32 copies and their
+    fixed-order reduction, dkv[1] half as many.  The backward's inputs out,
+    dout and lse_kv are drawn (any finite values are valid inputs of its
+    formula; none comes from the CUDA path), so one key's dkv depends only on
+    that key's slot of each row: the oracle computes it from one-slot id
+    lists, a few GFLOP instead of the whole backward."""
+    wl = W.long_64k()
+    T, H, K = wl.T, wl.H, wl.K
+    rng = np.random.default_rng(78)
+    q, kv, sk = wl.q_bits(), wl.kv_bits(), wl.sink()
+    # causal ids drawn in [2, t] for rows t >= 2 (rows 0 and 1 are empty), then
+    # key 0 at slot t % k of every row and key 1 at another slot of odd rows
+    tl = np.full(T, K, np.int32)
+    tl[:2] = 0
+    idx = np.floor(rng.random((T, K)) * (np.arange(T)[:, None] + 1)).astype(np.int32)
+    idx = np.where(idx <= 1, 2, idx).astype(np.int32)
+    idx[:2] = -1
+    rows = np.arange(2, T)
+    slot0 = rows % K
+    idx[rows, slot0] = 0
+    odd = rows[rows % 2 == 1]
+    slot1 = (odd * 7 + 3) % K
+    slot1 = np.where(slot1 == odd % K, (slot1 + 1) % K, slot1)
+    idx[odd, slot1] = 1
+    out = W.f32_to_bf16_bits(rng.standard_normal((T, H, wl.Dv), dtype=np.float32) * np.float32(0.1))
+    dout = W.f32_to_bf16_bits(rng.standard_normal((T, H, wl.Dv), dtype=np.float32) * np.float32(0.1))
+    lse_kv = np.full((T, H), np.log(np.float32(K)), np.float32)
+    res = ops.sparse_attn_bwd(dev_bf16(q), dev_bf16(kv), dev_bf16(out), dev_bf16(dout), dev(lse_kv), dev(idx),
+                              wl.scale, topk_length=dev(tl), sink=dev(sk))
+    got = res["dkv"][:2].cpu().numpy().astype(np.float64)
+    del res
+    kv2 = f64(kv[:2])
+    for key, krows in ((0, rows), (1, odd)):
+        ref = np.zeros(kv.shape[1], np.float64)
+        for c in range(0, krows.size, 4096):  # chunks keep the fp64 copies of q, out, dout small
+            r = krows[c:c + 4096]
+            one = np.full((r.size, 1), key, np.int32)
+            _, dkv, _ = oracle.sparse_attn_bwd(f64(q[r]), kv2, one, wl.scale, f64(out[r]), f64(dout[r]),
+                                               lse_kv[r].astype(np.float64), topk_length=np.ones(r.size, np.int32),
+                                               sink=sk)
+            ref += dkv[key]
+        assert_bwd_close(got[key], ref, f"dkv[{key}] ({krows.size} referencing rows)")
+
+
 def test_compressed_thd_8k_workload():
     _ratio_workload_check(W.compressed_thd_8k(), 64, 6)
 
