@@ -353,7 +353,9 @@ int dsa_select_candidates(const int32_t* cu_seqlens, int n_docs, int T, int Hi, 
  *    does not).
  *  - The first call on a device looks up the array's device address (with
  *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    stream capture.  The cache is not keyed on the CUDA context: after a
+ *    cudaDeviceReset the array may live at another address, so a process
+ *    that resets a device must not call this entry point on it again.
  *  - Every call on a device shares the one array and it keeps whatever the
  *    last call left there.  Nothing needs clearing: each word the kernels read
  *    is written earlier in the same call.  Calls that overlap on the GPU
