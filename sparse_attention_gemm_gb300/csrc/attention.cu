@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ac = a0 + c * (kChunkBytes >> 4), bc = q_desc + c * (kQChunkBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              if (leader && got) dsa::umma_bf16(d, ac + kk * 2, bc + kk * 2, idesc1, (c | kk) != 0);
+              dsa::umma_bf16_if(leader && got, d, ac + kk * 2, bc + kk * 2, idesc1, (c | kk) != 0);
           }
           if (leader && got) dsa::umma_commit(&s_full[b]);
           if (!__all_sync(0xffffffffu, got)) {
@@ -415,8 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!dsa::check(kOCol + (mb + 1) * kHG <= static_cast<int>(kTmemCols), p.status)) break;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
-              if (leader && got)
-                dsa::umma_bf16(d, am + kk * (2048 >> 4), b0 + kk * (2048 >> 4), idesc2, (i > 0 || kk > 0) ? 1u : 0u);
+              dsa::umma_bf16_if(leader && got, d, am + kk * (2048 >> 4), b0 + kk * (2048 >> 4), idesc2, (i > 0 || kk > 0) ? 1u : 0u);
           }
           if (leader && got) {
             dsa::umma_commit(o_done);

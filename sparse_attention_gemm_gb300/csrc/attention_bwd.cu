@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t ac = kv_desc + c * (kChunkBytes >> 4), bc = qd_desc + c * (2 * kChunkBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              if (leader) dsa::umma_bf16(d, ac + kk * 2, bc + kk * 2, c < kNv ? idesc_qd : idesc_q, (c | kk) != 0);
+              dsa::umma_bf16_if(leader, d, ac + kk * 2, bc + kk * 2, c < kNv ? idesc_qd : idesc_q, (c | kk) != 0);
           }
           if (leader) dsa::umma_commit(s_full);
           __syncwarp();
@@ -376,9 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t d = tmem_base + kQCol + mb * kHG;
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk)
-              if (leader)
-                dsa::umma_bf16(d, am + kk * (2048 >> 4), ds_desc + kk * (2048 >> 4), mb < 4 ? idesc_m128 : idesc_m64,
-                               (i > 0 || kk > 0) ? 1u : 0u);
+              dsa::umma_bf16_if(leader, d, am + kk * (2048 >> 4), ds_desc + kk * (2048 >> 4),
+                                mb < 4 ? idesc_m128 : idesc_m64, (i > 0 || kk > 0) ? 1u : 0u);
           }
           if (leader) {
             dsa::umma_commit(o_done);
@@ -723,7 +722,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             const uint32_t bs = bq + (kk < 4 ? 0u : kChunkBytes) + (kk & 3) * 2048;
             const uint64_t ad = dsa::smem_desc(as, 16, 1024, dsa::kSwizzle128B);
             const uint64_t bd = dsa::smem_desc(bs, 2 * kChunkBytes, 1024, dsa::kSwizzle128B);
-            if (leader) dsa::umma_bf16(d, ad, bd, nb < 4 ? idesc_n128 : idesc_n64, kk > 0 ? 1u : 0u);
+            dsa::umma_bf16_if(leader, d, ad, bd, nb < 4 ? idesc_n128 : idesc_n64, kk > 0 ? 1u : 0u);
           }
           if (leader) dsa::umma_commit(&d_full[db]);
           __syncwarp();
