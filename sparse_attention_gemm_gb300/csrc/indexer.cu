@@ -102,6 +102,7 @@ struct IndexerParams {
   // fused
   uint2* cand;        // [T][4 segments][cap/4] (key, column) pairs
   int32_t* cand_cnt;  // [T][4] candidates written per segment
+  uint32_t* cand_tau; // [T] the row's threshold at its end: at least k stored candidates reach it
   int cap;            // per row, a multiple of 16
   int compact;        // segments may fill up (cap below the longest row's keys per segment)
   int k;
@@ -892,11 +893,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* row = p.scores + static_cast<int64_t>(t) * p.ld;
           for (int j = tok_len[r] + et; j < p.s_max; j += kEpiThreads) row[j] = -INFINITY;
         }
-      } else if (lane == 0) {
+      } else {
+        if (lane == 0) {
 #pragma unroll
-        for (int q = 0; q < tok_per_slice; ++q) {
-          const int t = br.t0 + slice * tok_per_slice + q;
-          if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
+          for (int q = 0; q < tok_per_slice; ++q) {
+            const int t = br.t0 + slice * tok_per_slice + q;
+            if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
+          }
+        }
+        // Each row's threshold from its complete histogram (the running one
+        // lags by up to kTauUpdateEvery candidates): the lower edge of the
+        // highest bin at which the row's emitted candidates number >= k.  A
+        // candidate a compacted segment dropped is beaten by k stored keys of
+        // its segment, so at least k stored candidates reach this edge, and
+        // stage 2 may discard every candidate below it.  (The block's last
+        // barrier above ordered every histogram update before these reads;
+        // the next block clears the histograms only after its first barrier.)
+        for (int r = ew; r < p.qb; r += kEpiWarps) {
+          update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
+          __syncwarp();
+          const int t = br.t0 + r;
+          if (lane == 0 && t < p.T) p.cand_tau[t] = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
         }
       }
     }
@@ -1019,6 +1036,7 @@ struct SelShared {
   uint32_t tie[kSelWords];
   int wsum[2][kSelWarps];
   uint32_t wlo[kSelWarps], whi[kSelWarps];
+  int wcnt[kSelWarps];
   uint32_t lkey[32];  // keys of the bin that holds the k-th key
   int lcnt;
   int bin, above, n_eq, need;
@@ -1055,8 +1073,8 @@ __device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) 
 template <int GEN>
 __global__ void __launch_bounds__(kSelThreads, 1)
     fused_select_fast_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
-                             const int32_t* __restrict__ cand_cnt, int cap, int32_t* idx, int32_t* topk_length,
-                             float* logits, uint32_t* status) {
+                             const int32_t* __restrict__ cand_cnt, const uint32_t* __restrict__ cand_tau, int cap,
+                             int32_t* idx, int32_t* topk_length, float* logits, uint32_t* status) {
   extern __shared__ __align__(128) uint8_t smem_sel[];
   SelShared& S = *reinterpret_cast<SelShared*>(smem_sel);
   uint2* stage = reinterpret_cast<uint2*>(smem_sel + sel_stage_offset());
@@ -1151,6 +1169,9 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     const bool overflow = seg_counts(t, c);
     if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
     const int n = c[0] + c[1] + c[2] + c[3];
+    // candidates below stage 1's final threshold cannot be selected (at least
+    // k stored ones reach it); after an overflow nothing is discarded
+    const uint32_t tau_f = overflow ? 0u : __ldg(cand_tau + t);
     // every thread waits for the row's copy; the block agrees on the outcome
     // at the barrier below, before anyone depends on the staged candidates
     const bool staged = dsa::mbar_wait(&S.full, phase, wt);
@@ -1158,6 +1179,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     const int e1 = c[0], e2 = e1 + c[1], e3 = e2 + c[2];
     uint32_t key[kSelPer];
     uint32_t colp[kSelPer / 2];  // two 16-bit columns per word
+    uint32_t vmask = 0u;         // bit i: slot i holds a candidate that reaches tau_f
     uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
     for (int i = 0; i < kSelPer; ++i) {
@@ -1167,20 +1189,25 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         const int sg = (e >= e1) + (e >= e2) + (e >= e3);
         const int off = e - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
         v = stage[sg * cap_seg + off];
-        lo = min(lo, v.x);
-        hi = max(hi, v.x);
+        if (v.x >= tau_f) {
+          lo = min(lo, v.x);
+          hi = max(hi, v.x);
+          vmask |= 1u << i;
+        }
       }
       key[i] = v.x;
       if (i & 1) colp[i >> 1] |= v.y << 16;
       else colp[i >> 1] = v.y & 0xFFFFu;
     }
-    auto valid = [&](int i) { return i * kSelThreads + static_cast<int>(threadIdx.x) < n; };
+    auto valid = [&](int i) { return ((vmask >> i) & 1u) != 0u; };
     auto column = [&](int i) { return static_cast<int>((colp[i >> 1] >> (16 * (i & 1))) & 0xFFFFu); };
     lo = __reduce_min_sync(0xffffffffu, lo);
     hi = __reduce_max_sync(0xffffffffu, hi);
+    const int wc = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(__popc(vmask))));
     if (lane == 0) {
       S.wlo[warp] = lo;
       S.whi[warp] = hi;
+      S.wcnt[warp] = wc;
     }
     if (threadIdx.x == 0) S.lcnt = 0;
     // every thread has its candidates: the staging buffer is free
@@ -1209,10 +1236,36 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     }
     lo = __reduce_min_sync(0xffffffffu, S.wlo[lane]);
     hi = __reduce_max_sync(0xffffffffu, S.whi[lane]);
+    int n_surv = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(S.wcnt[lane])));
+    if (n_surv < k) {
+      // not reachable (stage 1 leaves at least k stored candidates at or
+      // above tau_f); kept so that a row is never selected from fewer than k
+      vmask = 0u;
+      lo = 0xFFFFFFFFu;
+      hi = 0u;
+#pragma unroll
+      for (int i = 0; i < kSelPer; ++i)
+        if (i * kSelThreads + static_cast<int>(threadIdx.x) < n) {
+          vmask |= 1u << i;
+          lo = min(lo, key[i]);
+          hi = max(hi, key[i]);
+        }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      __syncthreads();  // every thread has read the per-warp words above
+      if (lane == 0) {
+        S.wlo[warp] = lo;
+        S.whi[warp] = hi;
+      }
+      __syncthreads();
+      lo = __reduce_min_sync(0xffffffffu, S.wlo[lane]);
+      hi = __reduce_max_sync(0xffffffffu, S.whi[lane]);
+      n_surv = n;
+    }
     const int nbits = hi > lo ? 32 - __clz(hi - lo) : 0;
-    // ---- radix passes over v = key - lo, at most 11 bits each, top down
+    // ---- radix passes over v = key - lo (surviving candidates only), at most 11 bits each, top down
     uint32_t prefix = 0u, mask = 0u;
-    int k_rem = k, n_eq = n, shift = nbits, par = 0;
+    int k_rem = k, n_eq = n_surv, shift = nbits, par = 0;
     auto run_pass = [&](int db) {
       shift -= db;
       const int nb = 1 << db;
@@ -1356,6 +1409,358 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       S.sel[w0 + 1] = 0u;
       S.tie[w0] = 0u;
       S.tie[w0 + 1] = 0u;
+    }
+    __syncthreads();  // the next row reuses the shared words above
+  }
+}
+
+// Stage 2, multi-row form: four persistent 256-thread CTAs per SM, one row
+// each at a time, so that the rows' phases overlap.  Per row:
+//  1. one streaming pass over the row's candidate segments (16-byte loads)
+//     keeps those at or above stage 1's final threshold tau_f (at least k
+//     stored candidates reach it, so nothing else can be selected) in shared
+//     memory: about k plus the keys of tau_f's histogram bin.  A row with more
+//     survivors than the list holds is selected from the segments themselves
+//     (the same steps, each a pass over global memory).
+//  2. radix passes (11 bits at most) over v = key - lo of the survivors, with
+//     lo / hi their smallest / largest key, find the exact k-th key tau and
+//     how many keys equal to it are still needed;
+//  3. keys above tau and keys equal to it are set in two column bitmaps; the
+//     block takes the needed tied columns from the smallest up, and one scan
+//     of the bitmap turns it into ascending ids (and, when asked for, the
+//     logits of the selected candidates at their slots).
+constexpr int kMThreads = 256;
+constexpr int kMWarps = kMThreads / 32;
+constexpr int kMSurv = 3072;                  // survivors kept in shared memory
+constexpr int kMBins = 2048;
+constexpr int kMWords = kSelMaxLen / 32;       // column bitmaps for rows of up to 65536 columns
+constexpr int kMWordsPer = kMWords / kMThreads;  // bitmap words owned by one thread
+constexpr int kMCtasPerSm = 4;
+
+struct MultiShared {
+  uint32_t skey[kMSurv];
+  uint32_t scol[kMSurv];
+  uint32_t hist[kMBins];
+  uint32_t sel[kMWords];
+  uint32_t tie[kMWords];
+  int wsum[2][kMWarps];
+  uint32_t wlo[kMWarps], whi[kMWarps];
+  int ns;  // survivors of the row (may exceed kMSurv)
+  int bin, above, n_eq;
+};
+
+// Exclusive prefix of v over the block (one barrier); wsum buffer `par`
+// must not be in use by another scan between two barriers.
+__device__ __forceinline__ int multi_scan(int v, int (*wsum)[kMWarps], int par) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[par][warp] = incl;
+  __syncthreads();
+  int before = 0;
+#pragma unroll
+  for (int w = 0; w < kMWarps; ++w)
+    if (w < warp) before += wsum[par][w];
+  return before + incl - v;
+}
+
+template <int GEN>
+__global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
+    fused_select_multi_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
+                              const int32_t* __restrict__ cand_cnt, const uint32_t* __restrict__ cand_tau, int cap,
+                              int32_t* idx, int32_t* topk_length, float* logits, uint32_t* status) {
+  extern __shared__ __align__(16) uint8_t smem_multi[];
+  MultiShared& S = *reinterpret_cast<MultiShared*>(smem_multi);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cap_seg = cap / 4;
+  for (int i = threadIdx.x; i < kMBins; i += kMThreads) S.hist[i] = 0u;
+  for (int i = threadIdx.x; i < kMWords; i += kMThreads) {
+    S.sel[i] = 0u;
+    S.tie[i] = 0u;
+  }
+  __syncthreads();
+  // the candidate segments of row r into L2 (the streaming pass then waits
+  // on L2 rather than DRAM latency)
+  auto prefetch_row = [&](int r) {
+    if (r >= T) return;
+    const int t = T - 1 - r;
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) {
+      const int cnt = min(__ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg), cap_seg);
+      const uint32_t bytes = static_cast<uint32_t>((cnt + 1) & ~1) * 8u;  // whole 16-byte pairs
+      if (bytes) dsa::l2_prefetch_bulk(cand + static_cast<int64_t>(t) * cap + sg * cap_seg, bytes);
+    }
+  };
+  if (threadIdx.x == 0) prefetch_row(blockIdx.x);
+  // longest rows first
+  for (int r = blockIdx.x; r < T; r += gridDim.x) {
+    if (threadIdx.x == 0) prefetch_row(r + gridDim.x);
+    const int t = T - 1 - r;
+    int st = 0;
+    const int len = row_geom<GEN>(g, t, &st);
+    int32_t* out = idx + static_cast<int64_t>(t) * k;
+    float* lout = logits ? logits + static_cast<int64_t>(t) * k : nullptr;
+    int c[4];
+    bool overflow = false;
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) {
+      c[sg] = __ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg);
+      if (c[sg] > cap_seg) {
+        overflow = true;
+        c[sg] = cap_seg;
+      }
+    }
+    const uint2* seg0 = cand + static_cast<int64_t>(t) * cap;
+    if (len <= k) {
+      for (int j = threadIdx.x; j < k; j += kMThreads) out[j] = j < len ? st + j : -1;
+      if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
+      if (lout) {
+        // every key of a row this short is a candidate: its value goes to the
+        // slot of its column
+        for (int j = len + threadIdx.x; j < k; j += kMThreads) lout[j] = -INFINITY;
+#pragma unroll
+        for (int sg = 0; sg < 4; ++sg)
+          for (int i = threadIdx.x; i < c[sg]; i += kMThreads) {
+            const uint2 v = seg0[sg * cap_seg + i];
+            if (static_cast<int>(v.y) < len) lout[v.y] = dsa::key_f32(v.x);
+          }
+      }
+      continue;
+    }
+    if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
+    const int n = c[0] + c[1] + c[2] + c[3];
+    if (n < k) {  // only reachable after an overflow: keep the output well-formed
+      for (int j = threadIdx.x; j < k; j += kMThreads) {
+        out[j] = -1;
+        if (lout) lout[j] = -INFINITY;
+      }
+      if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
+      continue;
+    }
+    // ---- 1. survivors (key >= tau_f) into the shared list; their count and range
+    uint32_t tau_f = overflow ? 0u : __ldg(cand_tau + t);
+    uint32_t lo, hi;
+    int n_surv;
+    for (;;) {
+      if (threadIdx.x == 0) S.ns = 0;
+      __syncthreads();
+      lo = 0xFFFFFFFFu;
+      hi = 0u;
+#pragma unroll
+      for (int sg = 0; sg < 4; ++sg) {
+        const uint4* b4 = reinterpret_cast<const uint4*>(seg0 + sg * cap_seg);  // 16-byte aligned: cap_seg % 4 == 0
+        const int cnt = c[sg];
+        const int n4 = (cnt + 1) >> 1;
+        for (int j0 = 0; j0 < n4; j0 += 4 * kMThreads) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kMThreads + static_cast<int>(threadIdx.x);
+            v[u] = j < n4 ? __ldcs(b4 + j) : make_uint4(0u, 0u, 0u, 0u);
+          }
+          // this thread's keepers of the 8 pairs, then one shared-counter add per warp
+          uint32_t kmask = 0u;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * (j0 + u * kMThreads + static_cast<int>(threadIdx.x)) + h;
+              const uint32_t key = h ? v[u].z : v[u].x;
+              if (e < cnt && key >= tau_f) {
+                lo = min(lo, key);
+                hi = max(hi, key);
+                kmask |= 1u << (2 * u + h);
+              }
+            }
+          }
+          const int mine = __popc(kmask);
+          int incl = mine;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          int base = 0;
+          if (lane == 31 && incl > 0) base = atomicAdd(&S.ns, incl);
+          base = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if ((kmask >> (2 * u + h)) & 1u) {
+                if (base < kMSurv) {
+                  S.skey[base] = h ? v[u].z : v[u].x;
+                  S.scol[base] = h ? v[u].w : v[u].y;
+                }
+                ++base;
+              }
+            }
+          }
+        }
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      if (lane == 0) {
+        S.wlo[warp] = lo;
+        S.whi[warp] = hi;
+      }
+      __syncthreads();
+      n_surv = S.ns;
+      lo = 0xFFFFFFFFu;
+      hi = 0u;
+#pragma unroll
+      for (int w = 0; w < kMWarps; ++w) {
+        lo = min(lo, S.wlo[w]);
+        hi = max(hi, S.whi[w]);
+      }
+      // not reachable (stage 1 leaves at least k stored candidates at or above
+      // tau_f); kept so that a row is never selected from fewer than k
+      if (n_surv >= k || tau_f == 0u) break;
+      tau_f = 0u;
+      __syncthreads();  // every thread has read S.ns and the per-warp words
+    }
+    const bool in_smem = n_surv <= kMSurv;
+    // f(key, column) for every survivor: from the shared list, or from the
+    // segments when the list overflowed (no warp-collective inside f)
+    auto for_each = [&](auto&& f) {
+      if (in_smem) {
+        for (int i = threadIdx.x; i < n_surv; i += kMThreads) f(S.skey[i], S.scol[i]);
+      } else {
+#pragma unroll 1
+        for (int sg = 0; sg < 4; ++sg)
+          for (int i = threadIdx.x; i < c[sg]; i += kMThreads) {
+            const uint2 v = seg0[sg * cap_seg + i];
+            if (v.x >= tau_f) f(v.x, v.y);
+          }
+      }
+    };
+    // ---- 2. radix passes over v = key - lo, at most 11 bits each, top down
+    const int nbits = hi > lo ? 32 - __clz(hi - lo) : 0;
+    uint32_t prefix = 0u, mask = 0u;
+    int k_rem = k, n_eq = n_surv, shift = nbits, par = 0;
+    while (shift > 0) {
+      const int db = shift < 11 ? shift : 11;
+      shift -= db;
+      const int nb = 1 << db;
+      for_each([&](uint32_t key, uint32_t) {
+        const uint32_t v = key - lo;
+        if ((v & mask) == prefix) atomicAdd(&S.hist[(v >> shift) & (nb - 1)], 1u);
+      });
+      __syncthreads();
+      // thread i holds bins nb-1-8i .. nb-8-8i (the top bins first)
+      int cb[8];
+      int sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int b = nb - 1 - 8 * static_cast<int>(threadIdx.x) - j;
+        cb[j] = b >= 0 ? static_cast<int>(S.hist[b]) : 0;
+        if (b >= 0) S.hist[b] = 0u;  // ready for the next pass
+        sum += cb[j];
+      }
+      const int excl = multi_scan(sum, S.wsum, par);
+      par ^= 1;
+      if (excl < k_rem && excl + sum >= k_rem) {
+        int acc = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (acc + cb[j] >= k_rem) {
+            S.bin = nb - 1 - 8 * static_cast<int>(threadIdx.x) - j;
+            S.above = acc;
+            S.n_eq = cb[j];
+            break;
+          }
+          acc += cb[j];
+        }
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(S.bin) << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
+      k_rem -= S.above;
+      n_eq = S.n_eq;
+    }
+    const uint32_t tau = lo + prefix;
+    const int need = k_rem;
+    // ---- 3. bitmaps of the selected and the tied columns
+    for_each([&](uint32_t key, uint32_t col) {
+      if (!dsa::check(static_cast<int>(col) < len, status)) return;  // checked build: the column lies in the row
+      if (key > tau) atomicOr(&S.sel[col >> 5], 1u << (col & 31));
+      else if (key == tau) atomicOr(&S.tie[col >> 5], 1u << (col & 31));
+    });
+    __syncthreads();
+    const int w0 = kMWordsPer * static_cast<int>(threadIdx.x);  // this thread's words, in column order
+    uint32_t m[kMWordsPer], tb[kMWordsPer];
+    int pm = 0, pt = 0;
+#pragma unroll
+    for (int j = 0; j < kMWordsPer; ++j) {
+      m[j] = S.sel[w0 + j];
+      tb[j] = S.tie[w0 + j];
+      S.sel[w0 + j] = 0u;  // ready for the next row
+      S.tie[w0 + j] = 0u;
+      pt += __popc(tb[j]);
+    }
+    if (n_eq != need) {
+      // only the `need` tied columns with the smallest indices
+      int taken = multi_scan(pt, S.wsum, par);
+      par ^= 1;
+#pragma unroll
+      for (int j = 0; j < kMWordsPer; ++j) {
+        uint32_t keep = 0u, rest = tb[j];
+        while (rest && taken < need) {
+          const uint32_t low = rest & (0u - rest);
+          keep |= low;
+          rest ^= low;
+          ++taken;
+        }
+        tb[j] = keep;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMWordsPer; ++j) {
+      m[j] |= tb[j];
+      pm += __popc(m[j]);
+    }
+    int pos = multi_scan(pm, S.wsum, par);
+    par ^= 1;
+    if (lout) {
+      // the final bitmap and each word's first output slot, for the logits
+      int p2 = pos;
+#pragma unroll
+      for (int j = 0; j < kMWordsPer; ++j) {
+        S.sel[w0 + j] = m[j];
+        S.tie[w0 + j] = static_cast<uint32_t>(p2);
+        p2 += __popc(m[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMWordsPer; ++j) {
+      uint32_t w = m[j];
+      while (w) {
+        const int b = __ffs(w) - 1;
+        w &= w - 1;
+        if (dsa::check(pos < k, status)) out[pos] = st + ((w0 + j) << 5) + b;  // checked build: k ids at most
+        ++pos;
+      }
+    }
+    if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
+    if (lout) {
+      // each selected candidate's value at the slot of its column: the slot is
+      // its word's first slot plus the selected columns below it in the word
+      __syncthreads();
+      for_each([&](uint32_t key, uint32_t col) {
+        if (static_cast<int>(col) >= len) return;
+        const uint32_t word = S.sel[col >> 5], below = (1u << (col & 31)) - 1u;
+        if ((word >> (col & 31)) & 1u) lout[S.tie[col >> 5] + __popc(word & below)] = dsa::key_f32(key);
+      });
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kMWordsPer; ++j) {
+        S.sel[w0 + j] = 0u;
+        S.tie[w0 + j] = 0u;
+      }
     }
     __syncthreads();  // the next row reuses the shared words above
   }
@@ -1543,10 +1948,15 @@ extern "C" int dsa_indexer_scores_ratio(const void* qi, const void* ki, const fl
   return run_dense(Inputs{qi, ki, w, nullptr, nullptr, Tq, Tk, Hi, d}, g, scores, ld, sms, stream);
 }
 
+// Workspace of the fused path: per-row segment counts [T][4], per-row final
+// thresholds [T], then the candidate segments [T][cap].
+size_t ws_tau_offset(int T) { return align256(static_cast<size_t>(T) * 16); }
+size_t ws_cand_offset(int T) { return ws_tau_offset(T) + align256(static_cast<size_t>(T) * 4); }
+
 extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
   if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1) return 0;
   const size_t cap = static_cast<size_t>(fused_cap(s_max, k));
-  return align256(static_cast<size_t>(T) * 16) + align256(static_cast<size_t>(T) * cap * 8);
+  return ws_cand_offset(T) + align256(static_cast<size_t>(T) * cap * 8);
 }
 
 namespace {
@@ -1569,7 +1979,8 @@ int run_candidates(const Inputs& in, const Geom& g, int k, void* workspace, int 
   IndexerParams p{};
   fill_params(p, in, g);
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
-  p.cand = reinterpret_cast<uint2*>(ws + align256(static_cast<size_t>(Tq) * 16));
+  p.cand_tau = reinterpret_cast<uint32_t*>(ws + ws_tau_offset(Tq));
+  p.cand = reinterpret_cast<uint2*>(ws + ws_cand_offset(Tq));
   p.cap = fused_cap(g.s_max, k);
   p.compact = fused_compact(g.s_max, k);
   p.k = k;
@@ -1590,17 +2001,18 @@ int run_select_gen(const Geom& g, int T, int k, void* workspace, int32_t* idx, i
   const int cap = fused_cap(g.s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
-  const uint2* cand = reinterpret_cast<const uint2*>(ws + align256(static_cast<size_t>(T) * 16));
+  const uint32_t* cand_tau = reinterpret_cast<const uint32_t*>(ws + ws_tau_offset(T));
+  const uint2* cand = reinterpret_cast<const uint2*>(ws + ws_cand_offset(T));
   uint32_t* status = dsa::device_status_ptr();
   if (select_is_fast(g.s_max, k)) {
-    const size_t smem = sel_stage_offset() + static_cast<size_t>(cap) * 8;
-    if (cudaFuncSetAttribute(fused_select_fast_kernel<GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = sizeof(MultiShared);
+    if (cudaFuncSetAttribute(fused_select_multi_kernel<GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
-      return dsa::launch_error("fused_select_fast_kernel smem attribute");
-    const int grid = T < sms ? T : sms;
-    fused_select_fast_kernel<GEN><<<grid, kSelThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cap, idx, topk_length,
-                                                                       logits, status);
-    return dsa::launch_error("fused_select_fast_kernel");
+      return dsa::launch_error("fused_select_multi_kernel smem attribute");
+    const int grid = T < kMCtasPerSm * sms ? T : kMCtasPerSm * sms;
+    fused_select_multi_kernel<GEN><<<grid, kMThreads, smem, stream>>>(g, T, k, cand, cand_cnt, cand_tau, cap, idx,
+                                                                      topk_length, logits, status);
+    return dsa::launch_error("fused_select_multi_kernel");
   }
   const size_t smem = sizeof(dsa::TopkShared);
   if (cudaFuncSetAttribute(fused_select_kernel<GEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -154,12 +154,14 @@ def test_workspace_size_depends_on_shapes_only(lib):
                                        (16384, 512, 4096), (70001, 256, 70001)])
 def test_fused_workspace_layout(lib, T, k, s_max):
     """The fused indexer + top-k workspace: per row four int32 segment counts,
-    then four segments of (key, column) pairs, 8 bytes each.  A row holds
-    cap = 4 * min(32 * (ceil(s_max / 128) + 1), max(2k, 4096)) pairs: room for
-    every key a tile quarter can add to a segment, else a bound at which a
-    segment is cut to its top-k.  Both parts start on 256-byte boundaries."""
+    then per row one uint32 final threshold, then four segments of (key,
+    column) pairs, 8 bytes each.  A row holds cap = 4 * min(32 * (ceil(s_max
+    / 128) + 1), max(2k, 4096)) pairs: room for every key a tile quarter can
+    add to a segment, else a bound at which a segment is cut to its top-k.
+    Every part starts on a 256-byte boundary."""
     def a256(x):
         return (x + 255) // 256 * 256
 
     cap = 4 * min(32 * ((s_max + 127) // 128 + 1), max(2 * k, 4096))
-    assert lib.dsa_indexer_topk_workspace_size(T, 64, 128, k, s_max) == a256(T * 16) + a256(T * cap * 8)
+    want = a256(T * 16) + a256(T * 4) + a256(T * cap * 8)
+    assert lib.dsa_indexer_topk_workspace_size(T, 64, 128, k, s_max) == want
