@@ -102,7 +102,8 @@ struct IndexerParams {
   // fused
   uint2* cand;        // [T][4 segments][cap/4] (key, column) pairs
   int32_t* cand_cnt;  // [T][4] candidates written per segment
-  uint32_t* cand_tau; // [T] the row's threshold at its end: at least k stored candidates reach it
+  uint2* cand_tau;    // [T] the row's final threshold bin [x, y): at least k stored candidates reach x,
+                      // fewer than k reach y (y = 0: x's bin is the top one)
   int cap;            // per row, a multiple of 16
   int compact;        // segments may fill up (cap below the longest row's keys per segment)
   int k;
@@ -901,19 +902,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
           }
         }
-        // Each row's threshold from its complete histogram (the running one
-        // lags by up to kTauUpdateEvery candidates): the lower edge of the
-        // highest bin at which the row's emitted candidates number >= k.  A
-        // candidate a compacted segment dropped is beaten by k stored keys of
-        // its segment, so at least k stored candidates reach this edge, and
-        // stage 2 may discard every candidate below it.  (The block's last
-        // barrier above ordered every histogram update before these reads;
-        // the next block clears the histograms only after its first barrier.)
+        // Each row's threshold bin from its complete histogram (the running
+        // threshold lags by up to kTauUpdateEvery candidates): b = the highest
+        // bin at which the row's emitted candidates number >= k, [x, y) its
+        // key range.  A candidate that a compacted segment dropped (or never
+        // admitted, below its floor) is beaten by k stored keys of its
+        // segment, so at least k stored candidates reach x; fewer than k keys
+        // of the row reach y, all of them stored, so all of them are in the
+        // row's top-k.  Stage 2 takes those outright and ranks only the
+        // stored keys in [x, y).  (The block's last barrier above ordered
+        // every histogram update before these reads; the next block clears
+        // the histograms only after its first barrier.)
         for (int r = ew; r < p.qb; r += kEpiWarps) {
           update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
           __syncwarp();
           const int t = br.t0 + r;
-          if (lane == 0 && t < p.T) p.cand_tau[t] = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
+          if (lane == 0 && t < p.T) {
+            const uint32_t x = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
+            const int b = static_cast<int>(hist_bin(x, p.hist_bits));
+            const uint32_t y = b + 1 < (1 << p.hist_bits) ? hist_edge(b + 1, p.hist_bits) : 0u;
+            p.cand_tau[t] = make_uint2(x, y);
+          }
         }
       }
     }
@@ -1415,37 +1424,44 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 }
 
 // Stage 2, multi-row form: four persistent 256-thread CTAs per SM, one row
-// each at a time, so that the rows' phases overlap.  Per row:
-//  1. one streaming pass over the row's candidate segments (16-byte loads)
-//     keeps those at or above stage 1's final threshold tau_f (at least k
-//     stored candidates reach it, so nothing else can be selected) in shared
-//     memory: about k plus the keys of tau_f's histogram bin.  A row with more
-//     survivors than the list holds is selected from the segments themselves
-//     (the same steps, each a pass over global memory).
-//  2. radix passes (11 bits at most) over v = key - lo of the survivors, with
-//     lo / hi their smallest / largest key, find the exact k-th key tau and
-//     how many keys equal to it are still needed;
-//  3. keys above tau and keys equal to it are set in two column bitmaps; the
-//     block takes the needed tied columns from the smallest up, and one scan
-//     of the bitmap turns it into ascending ids (and, when asked for, the
+// each at a time, so that the rows' phases overlap.  Stage 1 hands over each
+// row's final threshold bin [x, y) (see the fused epilogue): fewer than k of
+// the row's keys reach y and all of them are stored, so all of them are
+// selected; at least k stored keys reach x, so nothing below x is.  Per row:
+//  1. one streaming pass over the candidate segments (16-byte loads, the
+//     segments prefetched into L2 one row ahead) sets the columns of keys
+//     >= y in the selection bitmap and keeps the keys in [x, y) -- typically
+//     a few hundred -- in a shared-memory list (a row with more than the list
+//     holds is ranked from the segments themselves, the same steps as passes
+//     over global memory);
+//  2. radix passes (11 bits at most) over v = key - lo of the kept keys, with
+//     lo / hi their smallest / largest key, find the exact key tau of rank
+//     need = k - (keys >= y) among them and how many keys equal to tau are
+//     still needed;
+//  3. kept keys above tau go to the selection bitmap and keys equal to it to
+//     a tie bitmap; the block takes the needed tied columns from the smallest
+//     up, and one scan of the bitmap turns it into ascending ids, staged in
+//     shared memory and stored with 16-byte writes (and, when asked for, the
 //     logits of the selected candidates at their slots).
 constexpr int kMThreads = 256;
 constexpr int kMWarps = kMThreads / 32;
-constexpr int kMSurv = 3072;                  // survivors kept in shared memory
+constexpr int kMKeep = 2048;                  // kept keys ([x, y)) held in shared memory
 constexpr int kMBins = 2048;
 constexpr int kMWords = kSelMaxLen / 32;       // column bitmaps for rows of up to 65536 columns
 constexpr int kMWordsPer = kMWords / kMThreads;  // bitmap words owned by one thread
 constexpr int kMCtasPerSm = 4;
+static_assert(kMKeep >= DSA_MAX_TOPK, "the id staging buffer aliases the kept keys");
 
 struct MultiShared {
-  uint32_t skey[kMSurv];
-  uint32_t scol[kMSurv];
+  uint32_t skey[kMKeep];  // kept keys; after step 2, the row's ids (staged for the store)
+  uint32_t scol[kMKeep];
   uint32_t hist[kMBins];
   uint32_t sel[kMWords];
   uint32_t tie[kMWords];
   int wsum[2][kMWarps];
   uint32_t wlo[kMWarps], whi[kMWarps];
-  int ns;  // survivors of the row (may exceed kMSurv)
+  int wtop[kMWarps];
+  int ns;  // kept keys of the row (may exceed kMKeep)
   int bin, above, n_eq;
 };
 
@@ -1471,7 +1487,7 @@ __device__ __forceinline__ int multi_scan(int v, int (*wsum)[kMWarps], int par) 
 template <int GEN>
 __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
     fused_select_multi_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
-                              const int32_t* __restrict__ cand_cnt, const uint32_t* __restrict__ cand_tau, int cap,
+                              const int32_t* __restrict__ cand_cnt, const uint2* __restrict__ cand_tau, int cap,
                               int32_t* idx, int32_t* topk_length, float* logits, uint32_t* status) {
   extern __shared__ __align__(16) uint8_t smem_multi[];
   MultiShared& S = *reinterpret_cast<MultiShared*>(smem_multi);
@@ -1496,6 +1512,7 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
     }
   };
   if (threadIdx.x == 0) prefetch_row(blockIdx.x);
+  const int w0 = kMWordsPer * static_cast<int>(threadIdx.x);  // this thread's bitmap words, in column order
   // longest rows first
   for (int r = blockIdx.x; r < T; r += gridDim.x) {
     if (threadIdx.x == 0) prefetch_row(r + gridDim.x);
@@ -1541,15 +1558,17 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
       continue;
     }
-    // ---- 1. survivors (key >= tau_f) into the shared list; their count and range
-    uint32_t tau_f = overflow ? 0u : __ldg(cand_tau + t);
+    // ---- 1. keys >= y into the bitmap, keys in [x, y) into the kept list
+    const uint2 xy = __ldg(cand_tau + t);
+    uint32_t tx = overflow ? 0u : xy.x, ty = overflow ? 0u : xy.y;  // ty == 0: no outright keys
     uint32_t lo, hi;
-    int n_surv;
+    int n_keep, n_top;
     for (;;) {
       if (threadIdx.x == 0) S.ns = 0;
       __syncthreads();
       lo = 0xFFFFFFFFu;
       hi = 0u;
+      int top = 0;
 #pragma unroll
       for (int sg = 0; sg < 4; ++sg) {
         const uint4* b4 = reinterpret_cast<const uint4*>(seg0 + sg * cap_seg);  // 16-byte aligned: cap_seg % 4 == 0
@@ -1562,18 +1581,25 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
             const int j = j0 + u * kMThreads + static_cast<int>(threadIdx.x);
             v[u] = j < n4 ? __ldcs(b4 + j) : make_uint4(0u, 0u, 0u, 0u);
           }
-          // this thread's keepers of the 8 pairs, then one shared-counter add per warp
+          // this thread's kept keys of the 8 pairs, then one shared-counter add per warp
           uint32_t kmask = 0u;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int e = 2 * (j0 + u * kMThreads + static_cast<int>(threadIdx.x)) + h;
-              const uint32_t key = h ? v[u].z : v[u].x;
-              if (e < cnt && key >= tau_f) {
-                lo = min(lo, key);
-                hi = max(hi, key);
-                kmask |= 1u << (2 * u + h);
+              const uint32_t key = h ? v[u].z : v[u].x, col = h ? v[u].w : v[u].y;
+              if (e < cnt && key >= tx) {
+                if (ty != 0u && key >= ty) {
+                  if (dsa::check(static_cast<int>(col) < len, status)) {  // checked build: the column lies in the row
+                    atomicOr(&S.sel[col >> 5], 1u << (col & 31));
+                    ++top;
+                  }
+                } else {
+                  lo = min(lo, key);
+                  hi = max(hi, key);
+                  kmask |= 1u << (2 * u + h);
+                }
               }
             }
           }
@@ -1592,7 +1618,7 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if ((kmask >> (2 * u + h)) & 1u) {
-                if (base < kMSurv) {
+                if (base < kMKeep) {
                   S.skey[base] = h ? v[u].z : v[u].x;
                   S.scol[base] = h ? v[u].w : v[u].y;
                 }
@@ -1604,44 +1630,51 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       }
       lo = __reduce_min_sync(0xffffffffu, lo);
       hi = __reduce_max_sync(0xffffffffu, hi);
+      top = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(top)));
       if (lane == 0) {
         S.wlo[warp] = lo;
         S.whi[warp] = hi;
+        S.wtop[warp] = top;
       }
       __syncthreads();
-      n_surv = S.ns;
+      n_keep = S.ns;
       lo = 0xFFFFFFFFu;
       hi = 0u;
+      n_top = 0;
 #pragma unroll
       for (int w = 0; w < kMWarps; ++w) {
         lo = min(lo, S.wlo[w]);
         hi = max(hi, S.whi[w]);
+        n_top += S.wtop[w];
       }
-      // not reachable (stage 1 leaves at least k stored candidates at or above
-      // tau_f); kept so that a row is never selected from fewer than k
-      if (n_surv >= k || tau_f == 0u) break;
-      tau_f = 0u;
+      // not reachable (see the stage 1 epilogue): fewer than k keys reach y and
+      // at least k reach x; kept so that a row is never selected wrongly
+      if ((n_top < k && n_top + n_keep >= k) || (tx == 0u && ty == 0u)) break;
+      tx = 0u;
+      ty = 0u;
+#pragma unroll
+      for (int j = 0; j < kMWordsPer; ++j) S.sel[w0 + j] = 0u;
       __syncthreads();  // every thread has read S.ns and the per-warp words
     }
-    const bool in_smem = n_surv <= kMSurv;
-    // f(key, column) for every survivor: from the shared list, or from the
+    const bool in_smem = n_keep <= kMKeep;
+    // f(key, column) for every kept key: from the shared list, or from the
     // segments when the list overflowed (no warp-collective inside f)
     auto for_each = [&](auto&& f) {
       if (in_smem) {
-        for (int i = threadIdx.x; i < n_surv; i += kMThreads) f(S.skey[i], S.scol[i]);
+        for (int i = threadIdx.x; i < n_keep; i += kMThreads) f(S.skey[i], S.scol[i]);
       } else {
 #pragma unroll 1
         for (int sg = 0; sg < 4; ++sg)
           for (int i = threadIdx.x; i < c[sg]; i += kMThreads) {
             const uint2 v = seg0[sg * cap_seg + i];
-            if (v.x >= tau_f) f(v.x, v.y);
+            if (v.x >= tx && (ty == 0u || v.x < ty)) f(v.x, v.y);
           }
       }
     };
     // ---- 2. radix passes over v = key - lo, at most 11 bits each, top down
     const int nbits = hi > lo ? 32 - __clz(hi - lo) : 0;
     uint32_t prefix = 0u, mask = 0u;
-    int k_rem = k, n_eq = n_surv, shift = nbits, par = 0;
+    int k_rem = k - n_top, n_eq = n_keep, shift = nbits, par = 0;
     while (shift > 0) {
       const int db = shift < 11 ? shift : 11;
       shift -= db;
@@ -1691,7 +1724,6 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       else if (key == tau) atomicOr(&S.tie[col >> 5], 1u << (col & 31));
     });
     __syncthreads();
-    const int w0 = kMWordsPer * static_cast<int>(threadIdx.x);  // this thread's words, in column order
     uint32_t m[kMWordsPer], tb[kMWordsPer];
     int pm = 0, pt = 0;
 #pragma unroll
@@ -1723,38 +1755,55 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       m[j] |= tb[j];
       pm += __popc(m[j]);
     }
-    int pos = multi_scan(pm, S.wsum, par);
+    // the ids in ascending order, staged in shared memory (the kept list is
+    // no longer read unless logits are asked for: then they go to global memory
+    // directly), then stored with 16-byte writes where the row allows
+    const int pos0 = multi_scan(pm, S.wsum, par);
     par ^= 1;
-    if (lout) {
-      // the final bitmap and each word's first output slot, for the logits
-      int p2 = pos;
-#pragma unroll
-      for (int j = 0; j < kMWordsPer; ++j) {
-        S.sel[w0 + j] = m[j];
-        S.tie[w0 + j] = static_cast<uint32_t>(p2);
-        p2 += __popc(m[j]);
-      }
-    }
+    const bool stage_ids = lout == nullptr && (reinterpret_cast<uintptr_t>(out) & 15u) == 0u;
+    int pos = pos0;
 #pragma unroll
     for (int j = 0; j < kMWordsPer; ++j) {
       uint32_t w = m[j];
       while (w) {
         const int b = __ffs(w) - 1;
         w &= w - 1;
-        if (dsa::check(pos < k, status)) out[pos] = st + ((w0 + j) << 5) + b;  // checked build: k ids at most
+        if (dsa::check(pos < k, status)) {  // checked build: k ids at most
+          const int id = st + ((w0 + j) << 5) + b;
+          if (stage_ids) S.skey[pos] = static_cast<uint32_t>(id);
+          else out[pos] = id;
+        }
         ++pos;
       }
     }
     if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
+    if (stage_ids) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < k / 4; i += kMThreads)
+        reinterpret_cast<int4*>(out)[i] = reinterpret_cast<const int4*>(S.skey)[i];
+      for (int i = (k & ~3) + static_cast<int>(threadIdx.x); i < k; i += kMThreads)
+        out[i] = static_cast<int32_t>(S.skey[i]);
+    }
     if (lout) {
       // each selected candidate's value at the slot of its column: the slot is
       // its word's first slot plus the selected columns below it in the word
+      int p2 = pos0;
+#pragma unroll
+      for (int j = 0; j < kMWordsPer; ++j) {
+        S.sel[w0 + j] = m[j];
+        S.tie[w0 + j] = static_cast<uint32_t>(p2);
+        p2 += __popc(m[j]);
+      }
       __syncthreads();
-      for_each([&](uint32_t key, uint32_t col) {
-        if (static_cast<int>(col) >= len) return;
-        const uint32_t word = S.sel[col >> 5], below = (1u << (col & 31)) - 1u;
-        if ((word >> (col & 31)) & 1u) lout[S.tie[col >> 5] + __popc(word & below)] = dsa::key_f32(key);
-      });
+#pragma unroll 1
+      for (int sg = 0; sg < 4; ++sg)
+        for (int i = threadIdx.x; i < c[sg]; i += kMThreads) {
+          const uint2 v = seg0[sg * cap_seg + i];
+          const int col = static_cast<int>(v.y);
+          if (v.x < tx || col >= len) continue;
+          const uint32_t word = S.sel[col >> 5], below = (1u << (col & 31)) - 1u;
+          if ((word >> (col & 31)) & 1u) lout[S.tie[col >> 5] + __popc(word & below)] = dsa::key_f32(v.x);
+        }
       __syncthreads();
 #pragma unroll
       for (int j = 0; j < kMWordsPer; ++j) {
@@ -1949,9 +1998,9 @@ extern "C" int dsa_indexer_scores_ratio(const void* qi, const void* ki, const fl
 }
 
 // Workspace of the fused path: per-row segment counts [T][4], per-row final
-// thresholds [T], then the candidate segments [T][cap].
+// threshold bins [T] (two keys), then the candidate segments [T][cap].
 size_t ws_tau_offset(int T) { return align256(static_cast<size_t>(T) * 16); }
-size_t ws_cand_offset(int T) { return ws_tau_offset(T) + align256(static_cast<size_t>(T) * 4); }
+size_t ws_cand_offset(int T) { return ws_tau_offset(T) + align256(static_cast<size_t>(T) * 8); }
 
 extern "C" size_t dsa_indexer_topk_workspace_size(int T, int Hi, int d, int k, int s_max) {
   if (T < 1 || Hi < 1 || d < 1 || k < 1 || k > DSA_MAX_TOPK || s_max < 1) return 0;
@@ -1979,7 +2028,7 @@ int run_candidates(const Inputs& in, const Geom& g, int k, void* workspace, int 
   IndexerParams p{};
   fill_params(p, in, g);
   p.cand_cnt = reinterpret_cast<int32_t*>(ws);
-  p.cand_tau = reinterpret_cast<uint32_t*>(ws + ws_tau_offset(Tq));
+  p.cand_tau = reinterpret_cast<uint2*>(ws + ws_tau_offset(Tq));
   p.cand = reinterpret_cast<uint2*>(ws + ws_cand_offset(Tq));
   p.cap = fused_cap(g.s_max, k);
   p.compact = fused_compact(g.s_max, k);
@@ -2001,7 +2050,7 @@ int run_select_gen(const Geom& g, int T, int k, void* workspace, int32_t* idx, i
   const int cap = fused_cap(g.s_max, k);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int32_t* cand_cnt = reinterpret_cast<const int32_t*>(ws);
-  const uint32_t* cand_tau = reinterpret_cast<const uint32_t*>(ws + ws_tau_offset(T));
+  const uint2* cand_tau = reinterpret_cast<const uint2*>(ws + ws_tau_offset(T));
   const uint2* cand = reinterpret_cast<const uint2*>(ws + ws_cand_offset(T));
   uint32_t* status = dsa::device_status_ptr();
   if (select_is_fast(g.s_max, k)) {

@@ -154,8 +154,8 @@ def test_workspace_size_depends_on_shapes_only(lib):
                                        (16384, 512, 4096), (70001, 256, 70001)])
 def test_fused_workspace_layout(lib, T, k, s_max):
     """The fused indexer + top-k workspace: per row four int32 segment counts,
-    then per row one uint32 final threshold, then four segments of (key,
-    column) pairs, 8 bytes each.  A row holds cap = 4 * min(32 * (ceil(s_max
+    then per row its final threshold bin (two uint32 keys), then four
+    segments of (key, column) pairs, 8 bytes each.  A row holds cap = 4 * min(32 * (ceil(s_max
     / 128) + 1), max(2k, 4096)) pairs: room for every key a tile quarter can
     add to a segment, else a bound at which a segment is cut to its top-k.
     Every part starts on a 256-byte boundary."""
@@ -163,5 +163,5 @@ def test_fused_workspace_layout(lib, T, k, s_max):
         return (x + 255) // 256 * 256
 
     cap = 4 * min(32 * ((s_max + 127) // 128 + 1), max(2 * k, 4096))
-    want = a256(T * 16) + a256(T * 4) + a256(T * cap * 8)
+    want = a256(T * 16) + a256(T * 8) + a256(T * cap * 8)
     assert lib.dsa_indexer_topk_workspace_size(T, 64, 128, k, s_max) == want
