@@ -1017,411 +1017,9 @@ __global__ void __launch_bounds__(dsa::kTopkThreads)
   if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
 }
 
-// Stage 2, fast form: one persistent 1024-thread CTA per SM, one row at a
-// time.  While a row is being selected, the TMA unit copies the next row's
-// candidate segments into shared memory, from where they are moved into
-// registers (16 per thread, columns packed in 16 bits; the per-row capacity
-// is at most 16384).  The exact k-th key tau comes from a radix pass over the
-// key range the row actually spans (its minimum to its maximum, at most 11
-// bits), which spreads the histogram over its bins instead of piling onto the
-// few bins that the top bits of similar scores share.  The few keys of the
-// bin that holds the k-th key are then ranked by one warp; when that bin
-// holds more than 32 keys, further radix passes resolve the remaining bits.
-// The selected columns are set in a shared-memory bitmap over the row, which
-// one block scan turns into ascending ids; among keys equal to tau the
-// smallest columns are taken.  Histogram bins and bitmap words are zeroed by
-// the thread that reads them.
-constexpr int kSelThreads = 1024;
-constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelPer = 16;
-constexpr int kSelMax = kSelThreads * kSelPer;  // >= the per-row candidate capacity
-constexpr int kSelBins = 2048;
-constexpr int kSelMaxLen = 65536;  // columns must fit 16 bits; longer rows use fused_select_kernel
-constexpr int kSelWords = kSelMaxLen / 32;
-
-struct SelShared {
-  uint32_t hist[kSelBins];
-  uint32_t sel[kSelWords];
-  uint32_t tie[kSelWords];
-  int wsum[2][kSelWarps];
-  uint32_t wlo[kSelWarps], whi[kSelWarps];
-  int wcnt[kSelWarps];
-  uint32_t lkey[32];  // keys of the bin that holds the k-th key
-  int lcnt;
-  int bin, above, n_eq, need;
-  uint32_t tau;
-  int abort;
-  uint64_t full;  // staging buffer filled
-};
-
-__host__ __device__ inline size_t sel_stage_offset() { return (sizeof(SelShared) + 127) / 128 * 128; }
-
-// Exclusive prefix of v over the block (one barrier); wsum buffer `par`
-// must not be in use by another scan between two barriers.
-__device__ __forceinline__ int sel_scan(int v, int (*wsum)[kSelWarps], int par) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) wsum[par][warp] = incl;
-  __syncthreads();
-  const int x = lane < kSelWarps ? wsum[par][lane] : 0;
-  int wincl = x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, wincl, o);
-    if (lane >= o) wincl += y;
-  }
-  const int before = __shfl_sync(0xffffffffu, wincl - x, warp);
-  return before + incl - v;
-}
-
-template <int GEN>
-__global__ void __launch_bounds__(kSelThreads, 1)
-    fused_select_fast_kernel(const __grid_constant__ Geom g, int T, int k, const uint2* cand,
-                             const int32_t* __restrict__ cand_cnt, const uint32_t* __restrict__ cand_tau, int cap,
-                             int32_t* idx, int32_t* topk_length, float* logits, uint32_t* status) {
-  extern __shared__ __align__(128) uint8_t smem_sel[];
-  SelShared& S = *reinterpret_cast<SelShared*>(smem_sel);
-  uint2* stage = reinterpret_cast<uint2*>(smem_sel + sel_stage_offset());
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int cap_seg = cap / 4;
-  for (int i = threadIdx.x; i < kSelBins; i += kSelThreads) S.hist[i] = 0u;
-  for (int i = threadIdx.x; i < kSelWords; i += kSelThreads) {
-    S.sel[i] = 0u;
-    S.tie[i] = 0u;
-  }
-  // counts of a row's segments, clamped to the capacity
-  auto seg_counts = [&](int t, int (&c)[4]) {
-    bool over = false;
-#pragma unroll
-    for (int sg = 0; sg < 4; ++sg) {
-      c[sg] = __ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg);
-      if (c[sg] > cap_seg) {
-        over = true;
-        c[sg] = cap_seg;
-      }
-    }
-    return over;
-  };
-  auto row_len = [&](int r, int* st) {
-    int s0;
-    const int len = row_geom<GEN>(g, T - 1 - r, &s0);
-    if (st) *st = s0;
-    return len;
-  };
-  // thread 0: the copy of row r's segments into the staging buffer
-  const uint64_t once = dsa::l2_policy_evict_first();
-  auto issue = [&](int r) {
-    const int t = T - 1 - r;
-    int c[4];
-    seg_counts(t, c);
-    uint32_t total = 0;
-#pragma unroll
-    for (int sg = 0; sg < 4; ++sg) total += static_cast<uint32_t>((c[sg] + 1) & ~1) * 8u;
-    dsa::mbar_expect_tx(&S.full, total);
-#pragma unroll
-    for (int sg = 0; sg < 4; ++sg) {
-      const uint32_t bytes = static_cast<uint32_t>((c[sg] + 1) & ~1) * 8u;
-      if (bytes)
-        dsa::bulk_load_hint(stage + sg * cap_seg, cand + (static_cast<int64_t>(t) * 4 + sg) * cap_seg, bytes, &S.full,
-                            once);
-    }
-  };
-  // next row of this CTA after r that needs its candidates (T if none)
-  auto next_row = [&](int r) {
-    for (r += gridDim.x; r < T; r += gridDim.x)
-      if (row_len(r, nullptr) > k) return r;
-    return T;
-  };
-  if (threadIdx.x == 0) {
-    dsa::mbar_init(&S.full, 1);
-    S.abort = 0;
-    dsa::fence_barrier_init();
-  }
-  __syncthreads();
-  const dsa::Waiter wt = dsa::make_waiter(&S.abort, status);
-  if (threadIdx.x == 0) {
-    const int r0 = row_len(blockIdx.x, nullptr) > k ? blockIdx.x : next_row(blockIdx.x);
-    if (r0 < T) issue(r0);
-  }
-  uint32_t phase = 0;
-  // longest rows first
-  for (int r = blockIdx.x; r < T; r += gridDim.x) {
-    const int t = T - 1 - r;
-    int st = 0;
-    const int len = row_len(r, &st);
-    int32_t* out = idx + static_cast<int64_t>(t) * k;
-    float* lout = logits ? logits + static_cast<int64_t>(t) * k : nullptr;
-    if (len <= k) {
-      for (int j = threadIdx.x; j < k; j += kSelThreads) out[j] = j < len ? st + j : -1;
-      if (threadIdx.x == 0 && topk_length) topk_length[t] = len;
-      if (lout) {
-        // every key of a row this short is a candidate: its value goes to the
-        // slot of its column
-        int c[4];
-        seg_counts(t, c);
-        for (int j = len + threadIdx.x; j < k; j += kSelThreads) lout[j] = -INFINITY;
-#pragma unroll
-        for (int sg = 0; sg < 4; ++sg)
-          for (int i = threadIdx.x; i < c[sg]; i += kSelThreads) {
-            const uint2 v = cand[(static_cast<int64_t>(t) * 4 + sg) * cap_seg + i];
-            if (static_cast<int>(v.y) < len) lout[v.y] = dsa::key_f32(v.x);
-          }
-      }
-      continue;
-    }
-    int c[4];
-    const bool overflow = seg_counts(t, c);
-    if (overflow && threadIdx.x == 0) atomicOr(status, DSA_STATUS_CAND_OVERFLOW);
-    const int n = c[0] + c[1] + c[2] + c[3];
-    // candidates below stage 1's final threshold cannot be selected (at least
-    // k stored ones reach it); after an overflow nothing is discarded
-    const uint32_t tau_f = overflow ? 0u : __ldg(cand_tau + t);
-    // every thread waits for the row's copy; the block agrees on the outcome
-    // at the barrier below, before anyone depends on the staged candidates
-    const bool staged = dsa::mbar_wait(&S.full, phase, wt);
-    // ---- staging buffer -> registers: element e = i*1024 + thread of the concatenated segments
-    const int e1 = c[0], e2 = e1 + c[1], e3 = e2 + c[2];
-    uint32_t key[kSelPer];
-    uint32_t colp[kSelPer / 2];  // two 16-bit columns per word
-    uint32_t vmask = 0u;         // bit i: slot i holds a candidate that reaches tau_f
-    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
-#pragma unroll
-    for (int i = 0; i < kSelPer; ++i) {
-      const int e = i * kSelThreads + threadIdx.x;
-      uint2 v = make_uint2(0u, 0u);
-      if (e < n) {
-        const int sg = (e >= e1) + (e >= e2) + (e >= e3);
-        const int off = e - (sg == 0 ? 0 : sg == 1 ? e1 : sg == 2 ? e2 : e3);
-        v = stage[sg * cap_seg + off];
-        if (v.x >= tau_f) {
-          lo = min(lo, v.x);
-          hi = max(hi, v.x);
-          vmask |= 1u << i;
-        }
-      }
-      key[i] = v.x;
-      if (i & 1) colp[i >> 1] |= v.y << 16;
-      else colp[i >> 1] = v.y & 0xFFFFu;
-    }
-    auto valid = [&](int i) { return ((vmask >> i) & 1u) != 0u; };
-    auto column = [&](int i) { return static_cast<int>((colp[i >> 1] >> (16 * (i & 1))) & 0xFFFFu); };
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    const int wc = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(__popc(vmask))));
-    if (lane == 0) {
-      S.wlo[warp] = lo;
-      S.whi[warp] = hi;
-      S.wcnt[warp] = wc;
-    }
-    if (threadIdx.x == 0) S.lcnt = 0;
-    // every thread has its candidates: the staging buffer is free
-    if (!__syncthreads_and(staged)) {
-      // a wait gave up: the copy that did not arrive must land before the CTA
-      // leaves (thread 0 issued it; later rows were never requested)
-      if (threadIdx.x == 0) dsa::mbar_drain(&S.full, phase, status);
-      break;
-    }
-    phase ^= 1;
-    if (threadIdx.x == 0) {
-      const int rn = next_row(r);
-      if (rn < T) {
-        dsa::fence_proxy_async_smem();  // the generic reads above before the async overwrite
-        issue(rn);
-      }
-    }
-    if (n < k) {  // only reachable after an overflow: keep the output well-formed
-      for (int j = threadIdx.x; j < k; j += kSelThreads) {
-        out[j] = -1;
-        if (lout) lout[j] = -INFINITY;
-      }
-      if (threadIdx.x == 0 && topk_length) topk_length[t] = 0;
-      __syncthreads();
-      continue;
-    }
-    lo = __reduce_min_sync(0xffffffffu, S.wlo[lane]);
-    hi = __reduce_max_sync(0xffffffffu, S.whi[lane]);
-    int n_surv = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(S.wcnt[lane])));
-    if (n_surv < k) {
-      // not reachable (stage 1 leaves at least k stored candidates at or
-      // above tau_f); kept so that a row is never selected from fewer than k
-      vmask = 0u;
-      lo = 0xFFFFFFFFu;
-      hi = 0u;
-#pragma unroll
-      for (int i = 0; i < kSelPer; ++i)
-        if (i * kSelThreads + static_cast<int>(threadIdx.x) < n) {
-          vmask |= 1u << i;
-          lo = min(lo, key[i]);
-          hi = max(hi, key[i]);
-        }
-      lo = __reduce_min_sync(0xffffffffu, lo);
-      hi = __reduce_max_sync(0xffffffffu, hi);
-      __syncthreads();  // every thread has read the per-warp words above
-      if (lane == 0) {
-        S.wlo[warp] = lo;
-        S.whi[warp] = hi;
-      }
-      __syncthreads();
-      lo = __reduce_min_sync(0xffffffffu, S.wlo[lane]);
-      hi = __reduce_max_sync(0xffffffffu, S.whi[lane]);
-      n_surv = n;
-    }
-    const int nbits = hi > lo ? 32 - __clz(hi - lo) : 0;
-    // ---- radix passes over v = key - lo (surviving candidates only), at most 11 bits each, top down
-    uint32_t prefix = 0u, mask = 0u;
-    int k_rem = k, n_eq = n_surv, shift = nbits, par = 0;
-    auto run_pass = [&](int db) {
-      shift -= db;
-      const int nb = 1 << db;
-#pragma unroll
-      for (int i = 0; i < kSelPer; ++i) {
-        const uint32_t v = key[i] - lo;
-        if (valid(i) && (v & mask) == prefix) atomicAdd(&S.hist[(v >> shift) & (nb - 1)], 1u);
-      }
-      __syncthreads();
-      // thread i holds bins nb-1-2i and nb-2-2i (the top bins first)
-      const int b0 = nb - 1 - 2 * static_cast<int>(threadIdx.x);
-      const uint32_t c0 = b0 >= 0 ? S.hist[b0] : 0u;
-      const uint32_t c1 = b0 >= 1 ? S.hist[b0 - 1] : 0u;
-      if (b0 >= 0) S.hist[b0] = 0u;  // ready for the next pass
-      if (b0 >= 1) S.hist[b0 - 1] = 0u;
-      const int sum = static_cast<int>(c0 + c1);
-      const int excl = sel_scan(sum, S.wsum, par);
-      if (excl < k_rem && excl + sum >= k_rem) {
-        const bool first = excl + static_cast<int>(c0) >= k_rem;
-        S.bin = first ? b0 : b0 - 1;
-        S.above = first ? excl : excl + static_cast<int>(c0);
-        S.n_eq = static_cast<int>(first ? c0 : c1);
-      }
-      __syncthreads();
-      prefix |= static_cast<uint32_t>(S.bin) << shift;
-      mask |= static_cast<uint32_t>(nb - 1) << shift;
-      k_rem -= S.above;
-      n_eq = S.n_eq;
-      par ^= 1;
-    };
-    if (shift > 0) run_pass(shift < 11 ? shift : 11);
-    uint32_t tau;
-    int need;
-    if (shift > 0 && n_eq <= 32) {
-      // rank the keys of the bin that holds the k-th key within one warp
-#pragma unroll
-      for (int i = 0; i < kSelPer; ++i) {
-        const uint32_t v = key[i] - lo;
-        if (valid(i) && (v & mask) == prefix) S.lkey[atomicAdd(&S.lcnt, 1)] = key[i];
-      }
-      __syncthreads();
-      if (warp == 0) {
-        const uint32_t mine = lane < n_eq ? S.lkey[lane] : 0u;
-        int greater = 0, equal = 0;
-        for (int j = 0; j < n_eq; ++j) {
-          const uint32_t o = S.lkey[j];
-          greater += o > mine;
-          equal += o == mine;
-        }
-        const bool hit = lane < n_eq && greater < k_rem && k_rem <= greater + equal;
-        const uint32_t hits = __ballot_sync(0xffffffffu, hit);
-        if (hits && lane == __ffs(hits) - 1) {
-          S.tau = mine;
-          S.need = k_rem - greater;
-          S.n_eq = equal;
-        }
-      }
-      __syncthreads();
-      tau = S.tau;
-      need = S.need;
-      n_eq = S.n_eq;
-    } else {
-      while (shift > 0) run_pass(shift < 11 ? shift : 11);
-      tau = lo + prefix;
-      need = k_rem;
-    }
-    // ---- bitmap of the selected columns
-#pragma unroll
-    for (int i = 0; i < kSelPer; ++i) {
-      if (!valid(i)) continue;
-      const int col = column(i);
-      if (!dsa::check(col < len, status)) continue;  // checked build: a candidate's column lies in its row
-      if (key[i] > tau) atomicOr(&S.sel[col >> 5], 1u << (col & 31));
-      else if (key[i] == tau) atomicOr(&S.tie[col >> 5], 1u << (col & 31));
-    }
-    __syncthreads();
-    // this thread's two words, in column order
-    const int w0 = 2 * threadIdx.x;
-    uint32_t m0 = S.sel[w0], m1 = S.sel[w0 + 1];
-    uint32_t t0 = S.tie[w0], t1 = S.tie[w0 + 1];
-    S.sel[w0] = 0u;  // ready for the next row
-    S.sel[w0 + 1] = 0u;
-    S.tie[w0] = 0u;
-    S.tie[w0 + 1] = 0u;
-    if (n_eq != need) {
-      // only the `need` tied columns with the smallest indices
-      int taken = sel_scan(__popc(t0) + __popc(t1), S.wsum, par);
-      par ^= 1;
-      uint32_t keep0 = 0u, keep1 = 0u;
-      while (t0 && taken < need) {
-        const uint32_t low = t0 & (0u - t0);
-        keep0 |= low;
-        t0 ^= low;
-        ++taken;
-      }
-      while (t1 && taken < need) {
-        const uint32_t low = t1 & (0u - t1);
-        keep1 |= low;
-        t1 ^= low;
-        ++taken;
-      }
-      t0 = keep0;
-      t1 = keep1;
-    }
-    m0 |= t0;
-    m1 |= t1;
-    int pos = sel_scan(__popc(m0) + __popc(m1), S.wsum, par);
-    if (lout) {
-      // the final bitmap and each word's first output slot, for the logits
-      S.sel[w0] = m0;
-      S.sel[w0 + 1] = m1;
-      S.tie[w0] = static_cast<uint32_t>(pos);
-      S.tie[w0 + 1] = static_cast<uint32_t>(pos + __popc(m0));
-    }
-    while (m0) {
-      const int b = __ffs(m0) - 1;
-      m0 &= m0 - 1;
-      if (dsa::check(pos < k, status)) out[pos] = st + (w0 << 5) + b;  // checked build: k ids at most
-      ++pos;
-    }
-    while (m1) {
-      const int b = __ffs(m1) - 1;
-      m1 &= m1 - 1;
-      if (dsa::check(pos < k, status)) out[pos] = st + ((w0 + 1) << 5) + b;
-      ++pos;
-    }
-    if (threadIdx.x == 0 && topk_length) topk_length[t] = k;
-    if (lout) {
-      // each selected candidate's value at the slot of its column: the slot is
-      // its word's first slot plus the selected columns below it in the word
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < kSelPer; ++i) {
-        if (!valid(i)) continue;
-        const int col = column(i);
-        const uint32_t word = S.sel[col >> 5], below = (1u << (col & 31)) - 1u;
-        if ((word >> (col & 31)) & 1u) lout[S.tie[col >> 5] + __popc(word & below)] = dsa::key_f32(key[i]);
-      }
-      __syncthreads();
-      S.sel[w0] = 0u;
-      S.sel[w0 + 1] = 0u;
-      S.tie[w0] = 0u;
-      S.tie[w0 + 1] = 0u;
-    }
-    __syncthreads();  // the next row reuses the shared words above
-  }
-}
+// Stage 2's multi-row form (below) serves rows of up to kSelMaxLen columns
+// (its column bitmaps); longer rows use fused_select_kernel.
+constexpr int kSelMaxLen = 65536;
 
 // Stage 2, multi-row form: four persistent 256-thread CTAs per SM, one row
 // each at a time, so that the rows' phases overlap.  Stage 1 hands over each
@@ -1445,15 +1043,27 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 //     logits of the selected candidates at their slots).
 constexpr int kMThreads = 256;
 constexpr int kMWarps = kMThreads / 32;
-constexpr int kMKeep = 2048;                  // kept keys ([x, y)) held in shared memory
-constexpr int kMBins = 2048;
+constexpr int kMKeep = 1024;                  // kept keys ([x, y)) held in shared memory
+constexpr int kMBits = 10;                     // radix digit
+constexpr int kMBins = 1 << kMBits;
+constexpr int kMBinsPer = kMBins / kMThreads;  // histogram bins one thread scans
+constexpr int kMStageU = 6;                    // 16-byte loads in flight per thread
+constexpr int kMStage = kMStageU * kMThreads;  // staged 16-byte slots of one batch
 constexpr int kMWords = kSelMaxLen / 32;       // column bitmaps for rows of up to 65536 columns
 constexpr int kMWordsPer = kMWords / kMThreads;  // bitmap words owned by one thread
 constexpr int kMCtasPerSm = 4;
-static_assert(kMKeep >= DSA_MAX_TOPK, "the id staging buffer aliases the kept keys");
+static_assert(kMStage * 4 >= DSA_MAX_TOPK, "the id staging buffer aliases the load staging buffer");
+
+// 16-byte global -> shared copy that the L2 may evict first (read once).
+__device__ __forceinline__ void cp_async16_cs(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "l"(dsa::l2_policy_evict_first())
+               : "memory");
+}
 
 struct MultiShared {
-  uint32_t skey[kMKeep];  // kept keys; after step 2, the row's ids (staged for the store)
+  uint4 stage[kMStage];   // each thread's in-flight 16-byte loads; after step 2, the row's ids
+  uint32_t skey[kMKeep];  // kept keys
   uint32_t scol[kMKeep];
   uint32_t hist[kMBins];
   uint32_t sel[kMWords];
@@ -1499,33 +1109,45 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
     S.tie[i] = 0u;
   }
   __syncthreads();
-  // the candidate segments of row r into L2 (the streaming pass then waits
-  // on L2 rather than DRAM latency)
-  auto prefetch_row = [&](int r) {
+  // A row's segment counts and threshold bin are loaded one row ahead (their
+  // latency hides behind the row before), and its candidate segments are
+  // prefetched into L2 then.
+  int4 cnt_next = make_int4(0, 0, 0, 0);
+  uint2 xy_next = make_uint2(0u, 0u);
+  auto load_meta = [&](int r) {
     if (r >= T) return;
     const int t = T - 1 - r;
+    cnt_next = __ldg(reinterpret_cast<const int4*>(cand_cnt) + t);  // [T][4] int32: 16-byte rows
+    xy_next = __ldg(cand_tau + t);
+  };
+  auto prefetch_row = [&](int r, const int4& cn) {
+    if (r >= T) return;
+    const int t = T - 1 - r;
+    const int cs[4] = {cn.x, cn.y, cn.z, cn.w};
 #pragma unroll
     for (int sg = 0; sg < 4; ++sg) {
-      const int cnt = min(__ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg), cap_seg);
+      const int cnt = min(cs[sg], cap_seg);
       const uint32_t bytes = static_cast<uint32_t>((cnt + 1) & ~1) * 8u;  // whole 16-byte pairs
       if (bytes) dsa::l2_prefetch_bulk(cand + static_cast<int64_t>(t) * cap + sg * cap_seg, bytes);
     }
   };
-  if (threadIdx.x == 0) prefetch_row(blockIdx.x);
+  load_meta(blockIdx.x);
   const int w0 = kMWordsPer * static_cast<int>(threadIdx.x);  // this thread's bitmap words, in column order
   // longest rows first
   for (int r = blockIdx.x; r < T; r += gridDim.x) {
-    if (threadIdx.x == 0) prefetch_row(r + gridDim.x);
+    const int4 cn = cnt_next;
+    const uint2 xy = xy_next;
+    load_meta(r + gridDim.x);
+    if (threadIdx.x == 0) prefetch_row(r + gridDim.x, cnt_next);
     const int t = T - 1 - r;
     int st = 0;
     const int len = row_geom<GEN>(g, t, &st);
     int32_t* out = idx + static_cast<int64_t>(t) * k;
     float* lout = logits ? logits + static_cast<int64_t>(t) * k : nullptr;
-    int c[4];
+    int c[4] = {cn.x, cn.y, cn.z, cn.w};
     bool overflow = false;
 #pragma unroll
     for (int sg = 0; sg < 4; ++sg) {
-      c[sg] = __ldg(cand_cnt + static_cast<int64_t>(t) * 4 + sg);
       if (c[sg] > cap_seg) {
         overflow = true;
         c[sg] = cap_seg;
@@ -1559,7 +1181,6 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       continue;
     }
     // ---- 1. keys >= y into the bitmap, keys in [x, y) into the kept list
-    const uint2 xy = __ldg(cand_tau + t);
     uint32_t tx = overflow ? 0u : xy.x, ty = overflow ? 0u : xy.y;  // ty == 0: no outright keys
     uint32_t lo, hi;
     int n_keep, n_top;
@@ -1569,25 +1190,37 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       lo = 0xFFFFFFFFu;
       hi = 0u;
       int top = 0;
+      // the row's 16-byte slots (two pairs each) as one flat range over the
+      // four segments: segment sg holds slots [o[sg], o[sg + 1])
+      const int o1 = (c[0] + 1) >> 1, o2 = o1 + ((c[1] + 1) >> 1), o3 = o2 + ((c[2] + 1) >> 1);
+      const int n4 = o3 + ((c[3] + 1) >> 1);
+      for (int j0 = 0; j0 < n4; j0 += kMStage) {
+        // kMStageU copies per thread into its own staging slots (read back
+        // only by this thread, after its own wait: no barrier needed)
 #pragma unroll
-      for (int sg = 0; sg < 4; ++sg) {
-        const uint4* b4 = reinterpret_cast<const uint4*>(seg0 + sg * cap_seg);  // 16-byte aligned: cap_seg % 4 == 0
-        const int cnt = c[sg];
-        const int n4 = (cnt + 1) >> 1;
-        for (int j0 = 0; j0 < n4; j0 += 4 * kMThreads) {
-          uint4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j0 + u * kMThreads + static_cast<int>(threadIdx.x);
-            v[u] = j < n4 ? __ldcs(b4 + j) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < kMStageU; ++u) {
+          const int f = j0 + u * kMThreads + static_cast<int>(threadIdx.x);
+          if (f < n4) {
+            const int sg = (f >= o1) + (f >= o2) + (f >= o3);
+            const int local = f - (sg == 0 ? 0 : sg == 1 ? o1 : sg == 2 ? o2 : o3);
+            cp_async16_cs(dsa::smem_u32(&S.stage[u * kMThreads + threadIdx.x]),
+                          reinterpret_cast<const uint4*>(seg0 + sg * cap_seg) + local);
           }
-          // this thread's kept keys of the 8 pairs, then one shared-counter add per warp
-          uint32_t kmask = 0u;
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        // this thread's kept keys of its pairs, then one shared-counter add per warp
+        uint32_t kmask = 0u;
+        uint4 v[kMStageU];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMStageU; ++u) {
+          const int f = j0 + u * kMThreads + static_cast<int>(threadIdx.x);
+          v[u] = S.stage[u * kMThreads + threadIdx.x];
+          const int sg = (f >= o1) + (f >= o2) + (f >= o3);
+          const int local = f - (sg == 0 ? 0 : sg == 1 ? o1 : sg == 2 ? o2 : o3);
+          const int cnt = f < n4 ? (sg == 0 ? c[0] : sg == 1 ? c[1] : sg == 2 ? c[2] : c[3]) : 0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int e = 2 * (j0 + u * kMThreads + static_cast<int>(threadIdx.x)) + h;
+          for (int h = 0; h < 2; ++h) {
+              const int e = 2 * local + h;
               const uint32_t key = h ? v[u].z : v[u].x, col = h ? v[u].w : v[u].y;
               if (e < cnt && key >= tx) {
                 if (ty != 0u && key >= ty) {
@@ -1601,8 +1234,8 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
                   kmask |= 1u << (2 * u + h);
                 }
               }
-            }
           }
+        }
           const int mine = __popc(kmask);
           int incl = mine;
 #pragma unroll
@@ -1614,7 +1247,7 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
           if (lane == 31 && incl > 0) base = atomicAdd(&S.ns, incl);
           base = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < kMStageU; ++u) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if ((kmask >> (2 * u + h)) & 1u) {
@@ -1626,7 +1259,6 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
               }
             }
           }
-        }
       }
       lo = __reduce_min_sync(0xffffffffu, lo);
       hi = __reduce_max_sync(0xffffffffu, hi);
@@ -1676,7 +1308,7 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
     uint32_t prefix = 0u, mask = 0u;
     int k_rem = k - n_top, n_eq = n_keep, shift = nbits, par = 0;
     while (shift > 0) {
-      const int db = shift < 11 ? shift : 11;
+      const int db = shift < kMBits ? shift : kMBits;
       shift -= db;
       const int nb = 1 << db;
       for_each([&](uint32_t key, uint32_t) {
@@ -1684,12 +1316,12 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
         if ((v & mask) == prefix) atomicAdd(&S.hist[(v >> shift) & (nb - 1)], 1u);
       });
       __syncthreads();
-      // thread i holds bins nb-1-8i .. nb-8-8i (the top bins first)
-      int cb[8];
+      // thread i holds bins nb-1-kMBinsPer*i .. (the top bins first)
+      int cb[kMBinsPer];
       int sum = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int b = nb - 1 - 8 * static_cast<int>(threadIdx.x) - j;
+      for (int j = 0; j < kMBinsPer; ++j) {
+        const int b = nb - 1 - kMBinsPer * static_cast<int>(threadIdx.x) - j;
         cb[j] = b >= 0 ? static_cast<int>(S.hist[b]) : 0;
         if (b >= 0) S.hist[b] = 0u;  // ready for the next pass
         sum += cb[j];
@@ -1699,9 +1331,9 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       if (excl < k_rem && excl + sum >= k_rem) {
         int acc = excl;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kMBinsPer; ++j) {
           if (acc + cb[j] >= k_rem) {
-            S.bin = nb - 1 - 8 * static_cast<int>(threadIdx.x) - j;
+            S.bin = nb - 1 - kMBinsPer * static_cast<int>(threadIdx.x) - j;
             S.above = acc;
             S.n_eq = cb[j];
             break;
@@ -1755,9 +1387,10 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
       m[j] |= tb[j];
       pm += __popc(m[j]);
     }
-    // the ids in ascending order, staged in shared memory (the kept list is
-    // no longer read unless logits are asked for: then they go to global memory
-    // directly), then stored with 16-byte writes where the row allows
+    // the ids in ascending order, staged in shared memory (in the load
+    // staging buffer, free since step 1), then stored with 16-byte writes
+    // where the row allows (with logits asked for they go to global memory
+    // directly)
     const int pos0 = multi_scan(pm, S.wsum, par);
     par ^= 1;
     const bool stage_ids = lout == nullptr && (reinterpret_cast<uintptr_t>(out) & 15u) == 0u;
@@ -1770,7 +1403,7 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
         w &= w - 1;
         if (dsa::check(pos < k, status)) {  // checked build: k ids at most
           const int id = st + ((w0 + j) << 5) + b;
-          if (stage_ids) S.skey[pos] = static_cast<uint32_t>(id);
+          if (stage_ids) reinterpret_cast<int32_t*>(S.stage)[pos] = id;
           else out[pos] = id;
         }
         ++pos;
@@ -1780,9 +1413,9 @@ __global__ void __launch_bounds__(kMThreads, kMCtasPerSm)
     if (stage_ids) {
       __syncthreads();
       for (int i = threadIdx.x; i < k / 4; i += kMThreads)
-        reinterpret_cast<int4*>(out)[i] = reinterpret_cast<const int4*>(S.skey)[i];
+        reinterpret_cast<int4*>(out)[i] = reinterpret_cast<const int4*>(S.stage)[i];
       for (int i = (k & ~3) + static_cast<int>(threadIdx.x); i < k; i += kMThreads)
-        out[i] = static_cast<int32_t>(S.skey[i]);
+        out[i] = reinterpret_cast<const int32_t*>(S.stage)[i];
     }
     if (lout) {
       // each selected candidate's value at the slot of its column: the slot is
@@ -2041,8 +1674,8 @@ int run_candidates(const Inputs& in, const Geom& g, int k, void* workspace, int 
 }
 
 // Stage 2 launch (arguments already validated).
-// True when stage 2 runs its fast form (the only form that can also write logits).
-bool select_is_fast(int s_max, int k) { return s_max <= kSelMaxLen && fused_cap(s_max, k) <= kSelMax; }
+// True when stage 2 runs its multi-row form (the only form that can also write logits).
+bool select_is_fast(int s_max, int) { return s_max <= kSelMaxLen; }
 
 template <int GEN>
 int run_select_gen(const Geom& g, int T, int k, void* workspace, int32_t* idx, int32_t* topk_length, float* logits,

@@ -16,7 +16,7 @@ Cases (kernel to select with -k in parentheses):
   indexer_mxfp8   dsa_indexer_scores_mxfp8 on E4M3 codes with E8M0 scales per 32
                   elements (drawn codes and scales), scores [T, T] fp32
                                                                 (indexer_kernel)
-  select          stage 2 of dsa_indexer_topk                   (fused_select_fast_kernel)
+  select          stage 2 of dsa_indexer_topk                   (fused_select_multi_kernel)
   topk            dsa_topk on the dense causal scores           (topk_stream_kernel)
   attention       dsa_sparse_attn_fwd on the fused top-k ids    (sparse_attn_kernel)
   gqa             dsa_sparse_attn_fwd, block-routed GQA, B = 8 x S = T / 8 packed
