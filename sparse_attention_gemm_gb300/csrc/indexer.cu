@@ -61,6 +61,10 @@ constexpr int kNRows = 256;
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = 64 + kEpiThreads;     // TMA warp, MMA warp, epilogue
+constexpr int kCmpWarps = 2;                   // fused mode: warps compacting the previous block's candidates
+constexpr int kCmpWarp0 = 2 + kEpiWarps;
+constexpr int kCompactU = 8;                   // 16-byte loads per lane per compaction round
+__host__ __device__ constexpr int indexer_threads(int fused) { return kThreads + (fused ? kCmpWarps * 32 : 0); }
 constexpr int kSlices = kEpiWarps / 4;          // column slices of the 256 accumulator columns
 constexpr int kSliceCols = kNRows / kSlices;    // columns one epilogue warp reduces per tile
 constexpr int kSliceChunks = kSliceCols / 32;   // 32-column TMEM loads per tile
@@ -137,10 +141,11 @@ __host__ __device__ inline SmemLayout smem_layout(int nch, int stages, int qb, i
   if (fused) o += kHistWords * 4;
   L.row_off = o;
   o += (32 + 128 + 32 + 128 + 128) * 4;  // tau, segment counts, since, segment floors, segment drops
+  o += 2 * (32 + 128) * 4;               // two slots of a block's final thresholds and segment counts
   L.cmp_off = o;
   if (fused) o += kEpiWarps * 256 * 4;  // one 256-bin histogram per epilogue warp (segment compaction)
   L.bar_off = o;
-  o += (2 * 8 + 9) * 8;
+  o += (2 * 8 + 9 + 4) * 8;
   L.misc_off = o;
   o += 16;
   L.total = o;
@@ -378,7 +383,7 @@ __device__ __forceinline__ void update_tau(const uint32_t* hist_row, int bins, i
 // epilogue is the bf16 one.  The scale columns take the TMEM room of the second
 // accumulator, so the accumulator is single-buffered.
 template <int FUSED, int HI, int GEN, int F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(indexer_threads(FUSED), 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                    const IndexerParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -404,6 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* row_since = seg_cnt + 128;  // candidate count at the row's last tau update (owner warp only)
   uint32_t* seg_floor = reinterpret_cast<uint32_t*>(row_since + 32);  // [32][4] entry floor after a compaction
   int32_t* seg_drop = reinterpret_cast<int32_t*>(seg_floor + 128);    // [32][4] candidates dropped by compactions
+  // [2 slots]: a finished block's final threshold per row [32] and stored
+  // candidates per (row, segment) [32][4], handed from the epilogue to the
+  // compaction warps (slot = the block's parity within this CTA)
+  uint32_t* pend_x = reinterpret_cast<uint32_t*>(seg_drop + 128);
+  int32_t* pend_n = reinterpret_cast<int32_t*>(pend_x + 2 * 32);
   uint32_t* cmp_hist = reinterpret_cast<uint32_t*>(smem + L.cmp_off);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* full = bars;
@@ -413,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 18;   // [2] ([3] for MX)
   uint64_t* tempty = bars + 21;  // [2] ([3] for MX)
   uint64_t* drain = bars + 24;   // the MMA issuer's exit commit
+  uint64_t* pend_full = bars + 25;   // [2] a slot holds a finished block (all epilogue warps)
+  uint64_t* pend_empty = bars + 27;  // [2] the compaction warps are done with a slot
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
 
@@ -437,6 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       dsa::mbar_init(&tempty[b], MX ? kEpiWarps / kSlices : kEpiWarps);
     }
     dsa::mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      dsa::mbar_init(&pend_full[b], kEpiWarps);
+      dsa::mbar_init(&pend_empty[b], kCmpWarps);
+    }
     *abort_flag = 0;
     dsa::fence_barrier_init();
   }
@@ -645,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       dsa::umma_drain(drain, p.status);  // every MMA issued has completed
     }
-  } else {
+  } else if (warp < kCmpWarp0) {
     // -------------------------------------------------------- epilogue
     const int ew = warp - 2;                  // 0 .. kEpiWarps-1
     const int quarter = warp & 3;             // TMEM lane quarter of this warp
@@ -669,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
     const int seg = quarter;              // this warp writes segment `quarter` of its rows
     const int cap_seg = FUSED ? p.cap / 4 : 0;
+    uint32_t blk_i = 0;                   // blocks finished by this CTA (slot of the hand-over)
     for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0 && ok; blk -= gridDim.x) {
       const BlockRange br = block_range<GEN>(p, blk);
       uint32_t cmask = 0u;                 // bit q: this warp's segment of row q was compacted
@@ -895,11 +912,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = tok_len[r] + et; j < p.s_max; j += kEpiThreads) row[j] = -INFINITY;
         }
       } else {
+        // this block goes to slot blk_i & 1 once the compaction warps are done
+        // with the block that used it before
+        const int slot = static_cast<int>(blk_i & 1u);
+        if (!failed) failed = !dsa::mbar_wait(&pend_empty[slot], ((blk_i >> 1) & 1u) ^ 1u, wt);
         if (lane == 0) {
 #pragma unroll
           for (int q = 0; q < tok_per_slice; ++q) {
-            const int t = br.t0 + slice * tok_per_slice + q;
-            if (t < p.T) p.cand_cnt[static_cast<int64_t>(t) * 4 + seg] = wcnt[q];
+            const int r = slice * tok_per_slice + q;
+            pend_n[slot * 128 + r * 4 + seg] = wcnt[q];
           }
         }
         // Each row's threshold bin from its complete histogram (the running
@@ -917,14 +938,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           update_tau(hist + r * hist_words_row, hist_words_row, p.hist_bits, p.k, &row_tau[r]);
           __syncwarp();
           const int t = br.t0 + r;
+          const uint32_t x = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
+          if (lane == 0) pend_x[slot * 32 + r] = x;
           if (lane == 0 && t < p.T) {
-            const uint32_t x = reinterpret_cast<volatile uint32_t*>(row_tau)[r];
             const int b = static_cast<int>(hist_bin(x, p.hist_bits));
             const uint32_t y = b + 1 < (1 << p.hist_bits) ? hist_edge(b + 1, p.hist_bits) : 0u;
             p.cand_tau[t] = make_uint2(x, y);
           }
         }
+        __syncwarp();
+        if (lane == 0) dsa::mbar_arrive(&pend_full[slot]);
       }
+      ++blk_i;
+    }
+  } else if (FUSED) {
+    // -------------------------------------------------- segment compaction
+    // One block behind the epilogue: each finished block's candidate
+    // segments are compacted in place to the candidates at or above the
+    // row's final threshold x (nothing below it can be selected), so that
+    // stage 2 reads about k candidates per row instead of all that were
+    // emitted.  A kept candidate moves to index kept + (kept ones before it
+    // in the round), never past its own index, and a round's stores follow
+    // all its loads, so nothing is read after it was overwritten.  These
+    // warps only touch global memory and the handed-over slot.
+    const int cw = warp - kCmpWarp0;  // 0 .. kCmpWarps-1
+    const int cap_seg = p.cap / 4;
+    uint32_t i = 0;
+    for (int blk = p.nblocks - 1 - blockIdx.x; blk >= 0; blk -= gridDim.x, ++i) {
+      const BlockRange br = block_range<GEN>(p, blk);
+      const int slot = static_cast<int>(i & 1u);
+      if (!dsa::mbar_wait_warp(&pend_full[slot], (i >> 1) & 1u, wt)) break;
+      for (int pr = cw; pr < p.qb * 4; pr += kCmpWarps) {
+        const int r = pr >> 2, sg = pr & 3;
+        const int t = br.t0 + r;
+        if (t >= p.T) break;
+        const uint32_t x = pend_x[slot * 32 + r];
+        const int n = pend_n[slot * 128 + pr];
+        int kept = n;
+        if (x != 0u) {  // x == 0: every candidate stays
+          uint2* segp = p.cand + (static_cast<int64_t>(t) * 4 + sg) * cap_seg;  // 16-byte aligned: cap_seg % 4 == 0
+          const uint4* seg4 = reinterpret_cast<const uint4*>(segp);
+          const uint32_t below = (1u << lane) - 1u;
+          kept = 0;
+          for (int i0 = 0; i0 < n; i0 += 64 * kCompactU) {
+            uint4 v[kCompactU];
+#pragma unroll
+            for (int u = 0; u < kCompactU; ++u) {
+              const int e = i0 + 64 * u + 2 * lane;  // the pair's first candidate
+              v[u] = e < n ? seg4[e >> 1] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < kCompactU; ++u) {
+              const int e = i0 + 64 * u + 2 * lane;
+              const uint32_t m0 = __ballot_sync(0xffffffffu, e < n && v[u].x >= x);
+              const uint32_t m1 = __ballot_sync(0xffffffffu, e + 1 < n && v[u].z >= x);
+              const bool k0 = (m0 >> lane) & 1u, k1 = (m1 >> lane) & 1u;
+              const int at = kept + __popc(m0 & below) + __popc(m1 & below);
+              if (k0) segp[at] = make_uint2(v[u].x, v[u].y);
+              if (k1) segp[at + (k0 ? 1 : 0)] = make_uint2(v[u].z, v[u].w);
+              kept += __popc(m0) + __popc(m1);
+            }
+          }
+        }
+        if (lane == 0) p.cand_cnt[static_cast<int64_t>(t) * 4 + sg] = kept;
+      }
+      __syncwarp();
+      if (lane == 0) dsa::mbar_arrive(&pend_empty[slot]);
     }
   }
 
@@ -1538,7 +1617,7 @@ int launch_indexer_hi(const CUtensorMap& mq, const CUtensorMap& mk, IndexerParam
                            static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("indexer_kernel smem attribute");
   const int grid = p.nblocks < sm_count ? p.nblocks : sm_count;
-  indexer_kernel<FUSED, HI, GEN, F8><<<grid, kThreads, smem, stream>>>(mq, mk, p);
+  indexer_kernel<FUSED, HI, GEN, F8><<<grid, indexer_threads(FUSED), smem, stream>>>(mq, mk, p);
   return dsa::launch_error("indexer_kernel");
 }
 
