@@ -22,11 +22,14 @@
 // sequence, so the fused mode sees exactly the scores that the dense mode
 // writes.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (qi block once per block,
-// ki tiles through a multi-stage ring), warp 1 allocates TMEM and issues the
-// MMAs, warps 2..9 run the epilogue (two warps per TMEM lane quarter, each on
-// half of the 256 columns).  The kernel is persistent: CTA c handles query
-// blocks nblocks-1-c, nblocks-1-c-grid, ... (the longest causal rows first).
+// Warp roles (320 threads; 384 in fused mode): warp 0 issues TMA loads (qi
+// block once per block, ki tiles through a multi-stage ring), warp 1
+// allocates TMEM and issues the MMAs, warps 2..9 run the epilogue (two warps
+// per TMEM lane quarter, each on half of the 256 columns), and in fused mode
+// warps 10..11 compact each finished block's candidate segments to the rows'
+// final thresholds while the next block runs.  The kernel is persistent: CTA
+// c handles query blocks nblocks-1-c, nblocks-1-c-grid, ... (the longest
+// causal rows first).
 //
 // Dense mode writes scores[t, j] for j < len[t] and -inf up to s_max.
 // Fused mode (cuDNN DSA section 4: no dense score matrix, caller-owned
@@ -1104,7 +1107,8 @@ constexpr int kSelMaxLen = 65536;
 // each at a time, so that the rows' phases overlap.  Stage 1 hands over each
 // row's final threshold bin [x, y) (see the fused epilogue): fewer than k of
 // the row's keys reach y and all of them are stored, so all of them are
-// selected; at least k stored keys reach x, so nothing below x is.  Per row:
+// selected; at least k stored keys reach x, so nothing below x is (stage 1's
+// compaction warps have already removed those).  Per row:
 //  1. one streaming pass over the candidate segments (16-byte loads, the
 //     segments prefetched into L2 one row ahead) sets the columns of keys
 //     >= y in the selection bitmap and keeps the keys in [x, y) -- typically
