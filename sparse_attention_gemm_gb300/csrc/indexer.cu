@@ -164,6 +164,12 @@ __device__ __forceinline__ int doc_index(const int32_t* __restrict__ cu, int n_d
   return lo;
 }
 
+// Drops the 128-byte L2 line at `a` (128-byte aligned) without writing it
+// back; its contents become undefined.
+__device__ __forceinline__ void l2_discard_line(uintptr_t a) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
+}
+
 // Keys that local row q of segment b sees in the general form (kept out of
 // line: inlined into every warp role it slowed the plain form measurably).
 // Returns (first key row, number of keys).
@@ -820,7 +826,8 @@ __global__ void __launch_bounds__(indexer_threads(FUSED), 1)
                 const uint32_t em = __ballot_sync(0xffffffffu, emit);
                 const int slot = wcnt[q] + __popc(em & dsa::lanemask_lt());
                 if (emit && dsa::check(slot < cap_seg && t < p.T, p.status)) {
-                  __stcs(p.cand + (static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot, make_uint2(key, s_key - st));
+                  // default L2 policy: the compaction warps read the segment back one block later
+                  p.cand[(static_cast<int64_t>(t) * 4 + seg) * cap_seg + slot] = make_uint2(key, s_key - st);
                   // histogram of stored keys, one 32-bit counter per bin; the
                   // result is unused, so this is a fire-and-forget reduction
                   atomicAdd(&hist[r * hist_words_row + hist_bin(key, p.hist_bits)], 1u);
@@ -1004,6 +1011,16 @@ __global__ void __launch_bounds__(indexer_threads(FUSED), 1)
           }
         }
         if (lane == 0) p.cand_cnt[static_cast<int64_t>(t) * 4 + sg] = kept;
+        if (kept < n) {
+          // The candidates past `kept` are dead: drop their L2 lines without
+          // writing them back (only lines wholly inside the dead range of
+          // this segment; the line holding the last live or the last emitted
+          // candidate stays)
+          const uintptr_t seg0 = reinterpret_cast<uintptr_t>(p.cand + (static_cast<int64_t>(t) * 4 + sg) * cap_seg);
+          const uintptr_t lo = (seg0 + static_cast<uintptr_t>(kept) * 8u + 127u) & ~static_cast<uintptr_t>(127);
+          const uintptr_t hi = (seg0 + static_cast<uintptr_t>(n) * 8u) & ~static_cast<uintptr_t>(127);
+          for (uintptr_t a = lo + 128u * lane; a < hi; a += 128u * 32u) l2_discard_line(a);
+        }
       }
       __syncwarp();
       if (lane == 0) dsa::mbar_arrive(&pend_empty[slot]);
