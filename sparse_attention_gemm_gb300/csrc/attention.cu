@@ -13,7 +13,7 @@
 // (MQA).  At 64 heads the step needs ~120 FLOP per gathered byte, so the
 // kernel is organised around keeping the gather streaming: two 64-key tile
 // buffers alternate (a 128-key tile would not fit twice next to the resident
-// query), and four warps gather with cp.async, each warp instruction moving
+// query), and eight warps gather with cp.async, each warp instruction moving
 // four 128-byte row segments into their 128-byte-swizzled slots (rows of
 // invalid slots are zero-filled without reading memory).
 //
@@ -37,9 +37,10 @@
 // denominator and writes out (bf16), lse (sink included) and optionally
 // lse_kv and max_logits.
 //
-// Warps: 0..3 gather, 4 = TMEM allocation, MMA1 issue and query loads (TMA),
-// 5..12 softmax and epilogue, 13 = MMA2 issue.  Persistent CTAs take units
-// from the longest rows down.
+// Warps: 0..7 gather, 8..15 softmax and epilogue, 16 = TMEM allocation,
+// MMA1 issue and query loads (TMA), 17 = MMA2 issue, 18..19 idle (they fill
+// the fifth warpgroup, whose registers go to the softmax).  Persistent CTAs
+// take units from the longest rows down.
 #include <climits>
 
 #include "common.cuh"
@@ -50,18 +51,24 @@ constexpr int kKeys = 64;                       // keys per tile
 constexpr int kHG = 64;                         // heads per group
 // cp.async gather bandwidth grows with the warps issuing it (measured on
 // GB300, random 1152-byte rows into 64-key tiles: 4 warps 30 B/clk/SM,
-// 6 warps 36, 8 warps 49), so the gather gets six warps; with 16 warps in
-// all, a thread keeps up to 128 registers.
-constexpr int kGatherWarps = 6;
+// 6 warps 36, 8 warps 49), so the gather gets eight warps (two keys each per
+// tile); five warpgroups in all, with registers moved from the gather and
+// MMA warpgroups to the softmax ones.
+constexpr int kGatherWarps = 8;
 constexpr int kGatherThreads = kGatherWarps * 32;
 constexpr int kGatherKeys = kGatherThreads / 8;                   // keys one gather step covers
 constexpr int kGatherSteps = (kKeys + kGatherKeys - 1) / kGatherKeys;  // steps per tile
-constexpr int kMmaWarp = kGatherWarps;  // MMA1 and query loads
-constexpr int kSoftWarp0 = kMmaWarp + 1;
+constexpr int kSoftWarp0 = kGatherWarps;            // warpgroups 2 and 3
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kMma2Warp = kSoftWarp0 + kSoftWarps;  // MMA2
-constexpr int kThreads = (kMma2Warp + 1) * 32;       // 512
+constexpr int kMmaWarp = kSoftWarp0 + kSoftWarps;   // MMA1 and query loads (warpgroup 4)
+constexpr int kMma2Warp = kMmaWarp + 1;             // MMA2
+constexpr int kThreads = (kMmaWarp + 4) * 32;       // 640: five warpgroups (the last two warps idle)
+// Register split: launched at kLaunchRegs per thread; the softmax warpgroups
+// raise theirs to kSoftRegs, the others lower theirs to kLeanRegs
+// (3 x 128 x kLeanRegs + 2 x 128 x kSoftRegs <= 640 x kLaunchRegs).
+constexpr int kLaunchRegs = 96, kLeanRegs = 56, kSoftRegs = 152;
+static_assert(3 * 128 * kLeanRegs + 2 * 128 * kSoftRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr uint32_t kChunkBytes = kKeys * 128;   // 64 keys x 64 bf16
 constexpr uint32_t kQChunkBytes = kHG * 128;    // 64 heads x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
@@ -232,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const dsa::Waiter wt = dsa::make_waiter(abort_flag, p.status);
 
   if (warp < kGatherWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLeanRegs));
     // ------------------------------------------------------------ gather
     // Thread g covers piece (g & 7) (16 bytes) of key (g >> 3) + kGatherKeys*kg
     // (keys below 64 only), for every step kg and every 64-dim chunk: one warp
@@ -298,7 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsa::mbar_arrive(&kv_full[b]);
       }
     }
-  } else if (warp == kMmaWarp || warp == kMma2Warp) {
+  } else if (warp >= kMmaWarp) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLeanRegs));
+    if (warp != kMmaWarp && warp != kMma2Warp) goto done;  // the warpgroup's two spare warps
     // ------------------------------------------------------------ MMA issue
     // Two issuing warps, one per product, so that neither waits behind the
     // other's instructions: warp kMmaWarp issues MMA1 (and loads the query),
@@ -433,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ------------------------------------------------------------ softmax + epilogue
     const int sw = warp - kSoftWarp0;           // 0..7
     const int st = threadIdx.x - kSoftWarp0 * 32;  // 0..255
@@ -717,6 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+done:
   __syncthreads();
   if (warp == kMmaWarp) {
     dsa::tc_fence_after();
@@ -792,6 +804,14 @@ extern "C" int dsa_sparse_attn_fwd_ex(const void* q, const void* kv, const void*
   if (rc != DSA_OK) return rc;
   const Layout L = make_layout(p.n_qk, p.n_chunks, p.p_alias);
   const size_t smem = L.total + 1024;
+  {
+    // the register split assumes the launch count it was sized for: with
+    // fewer registers at launch the softmax warps' increase could not be met
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, sparse_attn_kernel) != cudaSuccess || fa.numRegs != kLaunchRegs)
+      return dsa::set_error(DSA_ERR_CUDA, "sparse_attn_kernel: compiled with %d registers per thread, expected %d",
+                            fa.numRegs, kLaunchRegs);
+  }
   if (cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return dsa::launch_error("sparse_attn_kernel smem attribute");
