@@ -409,10 +409,10 @@ int dsa_sparse_attn_fwd(const void* q, const void* kv, const void* v, const int3
  * Duplicate ids are separate slots; invalid ids and slots past topk_length
  * are absent.  P and scale * dS are rounded to bf16 for the tensor-core
  * products (as P is in the forward); every sum is fp32.  The result is
- * bitwise reproducible: dkv is accumulated in 128 fp32 copies, each written
+ * bitwise reproducible: dkv is accumulated in 152 fp32 copies, each written
  * by one CTA in a fixed order, and summed in a fixed order; d_sink likewise.
  *   workspace: dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K) bytes,
- *   256-byte aligned (it holds P and dS of every slot and the 128 copies).
+ *   256-byte aligned (it holds P and dS of every slot and the 152 copies).
  * Shapes: Dqk = 576, Dv = 512, 1 <= H <= 128, K >= 1, scale finite > 0;
  * q, kv, out, dout, dkv 16-byte aligned.
  * Errors: DSA_ERR_VALUE, DSA_ERR_WORKSPACE. */

@@ -20,8 +20,8 @@
 //     accumulates dq^T = K^T . dS^T in TMEM (four M = 128 blocks and one
 //     M = 64 block for dims 512..575).  The kv tile buffer is single: the
 //     query and dout rows take the room of the forward's second buffer.
-//  3. bwd_dkv_kernel: 128 lanes; lane c owns one fp32 copy ("shard") of dkv
-//     and takes tokens c, c + 128, ... in order.  Per 64-slot tile one MMA
+//  3. bwd_dkv_kernel: 152 lanes (one per SM); lane c owns one fp32 copy
+//     ("shard") of dkv and takes tokens c, c + 152, ... in order.  Per 64-slot tile one MMA
 //     sequence forms the tile's key rows [scale dS | P] . [q ; dout]
 //     (M = 64 keys, K = 128, N = 128 dims at a time) and the lane adds them
 //     into its shard, one thread per dim walking the keys in slot order, so
@@ -53,7 +53,7 @@ constexpr int kThreads = (kMma2Warp + 1) * 32;      // 512
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSCol = 0;     // S^T at columns 0..63, dP^T at 64..127
 constexpr int kQCol = 128;   // dq^T blocks at 128 + 64*m (m = 0..3), the M = 64 block at 384
-constexpr int kLanes = 128;  // dkv shards
+constexpr int kLanes = 152;  // dkv shards: one CTA per SM of a GB300 in the dkv pass
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ shared

@@ -179,7 +179,7 @@ def test_long_64k_mxfp8_inputs():
 def test_long_64k_backward_key_shared_by_every_row():
     """dkv of keys referenced by many rows, at the 64K-token shapes.  Key 0
     sits in every row (at slot t % k), key 1 in every other row: dkv[0] sums
-    65534 x 64 contributions through the 128 fp32 copies and their
+    65534 x 64 contributions through the per-SM fp32 copies and their
     fixed-order reduction, dkv[1] half as many.  The backward's inputs out,
     dout and lse_kv are drawn (any finite values are valid inputs of its
     formula; none comes from the CUDA path), so one key's dkv depends only on
