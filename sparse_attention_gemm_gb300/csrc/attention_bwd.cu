@@ -779,25 +779,33 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
           if (f != dt) *dupflag = 1;
         }
         named_bar(1, kDrainThreads);  // first[] of the tile complete
-        for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
-          const int db = blk_ctr & 1;
-          const int nd = nb < 4 ? 128 : 64;
-          // the shard values this thread will update, read while the block's
-          // products finish: thread (key group kg, 4-dim column c4) owns rows
-          // kg + 4k; unique ids never alias, and earlier updates of the same
-          // values are ordered before this by the barrier that ended the
-          // previous block
-          const int kg = dt >> 5, c4 = dt & 31;
-          const bool col_on = 4 * c4 < nd;
-          float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
-          float4 acc[kKeys / 4];
+        // The shard values this thread updates: thread (key group kg, 4-dim
+        // column c4) owns rows kg + 4k of each block of dims; unique ids never
+        // alias.  A block's values are read one block ahead, while the
+        // previous block's products finish and its values are written (the
+        // blocks of a tile cover disjoint dims); earlier updates of the same
+        // values, by any thread, were ordered before the read by the barrier
+        // that ended the previous tile.
+        const int kg = dt >> 5, c4 = dt & 31;
+        float4 acc[kKeys / 4], acc_next[kKeys / 4];
+        auto load_block = [&](int nb, float4 (&a)[kKeys / 4]) {
+          const bool on = 4 * c4 < (nb < 4 ? 128 : 64);
+          const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * c4);
 #pragma unroll
           for (int k = 0; k < kKeys / 4; ++k) {
             const int r = kg + 4 * k;
             const int id = tids[r];
-            acc[k] = (col_on && id >= 0 && first[r] == r) ? base[static_cast<int64_t>(id) * (kDqk / 4)]
-                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            a[k] = (on && id >= 0 && first[r] == r) ? src[static_cast<int64_t>(id) * (kDqk / 4)]
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
           }
+        };
+        load_block(0, acc);
+        for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
+          const int db = blk_ctr & 1;
+          const int nd = nb < 4 ? 128 : 64;
+          const bool col_on = 4 * c4 < nd;
+          float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
+          if (nb + 1 < 5) load_block(nb + 1, acc_next);
           if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
           dsa::tc_fence_after();
           if (!failed) {
@@ -841,6 +849,8 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
               }
             }
           }
+#pragma unroll
+          for (int k = 0; k < kKeys / 4; ++k) acc[k] = acc_next[k];
           // stage is read before the next block overwrites it; the group
           // leaves together if any warp's wait gave up
           if (dsa::named_bar_any(1, kDrainThreads, failed)) {
