@@ -42,7 +42,7 @@ L2_BYTES = 129 * 1024 * 1024
 TRAFFIC = {
     "indexer_kernel": (2950713600, ("indexer.cu", "common.cuh", "topk_select.cuh", "block_sort.cuh"),
                        "e18285ad8d98df92"),
-    "sparse_attn_kernel": (11289313536, ("attention.cu", "common.cuh"), "82ba7a0dc26dc5c5"),
+    "sparse_attn_kernel": (11276293888, ("attention.cu", "common.cuh"), "ba76fd34e903197b"),
 }
 
 
