@@ -17,6 +17,10 @@
  *    a caller contract: the kernels clamp or skip what is out of range but do
  *    not report it.  Bounded device waits that give up, and candidate buffers
  *    that overflow, set bits in the device status word (dsa_device_status).
+ *  - The library looks up device addresses of its own (the status word, the
+ *    scratch array of dsa_indexer_topk_noalloc) once per device and keeps
+ *    them for the life of the process: a process that calls cudaDeviceReset
+ *    must not use the library on that device afterwards.
  *  - Layout names follow the pages: T = total (packed THD) query tokens,
  *    H = attention heads, Hi = indexer heads, d = indexer head dim,
  *    K = top-k / sparse width, Dqk = query/key dim, Dv = value dim.
