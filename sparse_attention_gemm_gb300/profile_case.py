@@ -22,6 +22,8 @@ Cases (kernel to select with -k in parentheses):
   gqa             dsa_sparse_attn_fwd, block-routed GQA, B = 8 x S = T / 8 packed
                   tokens, Hq = 12, D = 256, routes as the GQA workload draws them
                                                                 (sparse_attn_kernel)
+  backward        dsa_sparse_attn_bwd on the fused top-k ids, dout ~ N(0, 1) * 0.1
+                  (bwd_prep_kernel, bwd_dq_kernel, bwd_dkv_kernel, bwd_reduce_*)
 """
 from __future__ import annotations
 
@@ -32,7 +34,7 @@ import sys
 import numpy as np
 import torch
 
-CASES = ("indexer_dense", "indexer_fused", "indexer_mxfp8", "select", "topk", "attention", "gqa")
+CASES = ("indexer_dense", "indexer_fused", "indexer_mxfp8", "select", "topk", "attention", "gqa", "backward")
 
 
 def _bf16(shape, sigma, g, dev):
@@ -109,13 +111,21 @@ def main(argv=None) -> int:
     elif args.case == "select":
         ops.indexer_candidates(qi, ki, w, cu, K, T, workspace=ws)
         twice(lambda: ops.select_candidates(cu, T, Hi, d, K, T, ws))
-    else:  # attention
+    else:  # attention, backward
         idx, tl = ops.indexer_topk(qi, ki, w, cu, K, T, workspace=ws)
         del ws, qi, ki, w
         q = _bf16((T, H, 576), 0.1, g, dev)
         kv = _bf16((T, 576), 0.1, g, dev)
         sink = torch.randn(H, generator=g, device=dev, dtype=torch.float32)
-        twice(lambda: ops.sparse_attn_fwd(q, kv, idx, 1.0 / math.sqrt(576.0), topk_length=tl, sink=sink))
+        scale = 1.0 / math.sqrt(576.0)
+        if args.case == "attention":
+            twice(lambda: ops.sparse_attn_fwd(q, kv, idx, scale, topk_length=tl, sink=sink))
+        else:
+            fwd = ops.sparse_attn_fwd(q, kv, idx, scale, topk_length=tl, sink=sink, want_lse_kv=True)
+            dout = _bf16((T, H, 512), 0.1, g, dev)
+            bws = torch.empty(ops.sparse_attn_bwd_workspace_size(T, T, H, K), dtype=torch.uint8, device=dev)
+            twice(lambda: ops.sparse_attn_bwd(q, kv, fwd["out"], dout, fwd["lse_kv"], idx, scale, topk_length=tl,
+                                              sink=sink, workspace=bws))
     status = ops.device_status(clear=True)
     print(f"{args.case}: T={T} k={K} status={status:#x}")
     return 1 if status else 0
