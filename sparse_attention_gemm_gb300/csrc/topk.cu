@@ -5,14 +5,16 @@
 // Two kernels:
 //
 // topk_stream_kernel (rows of at most 65536 columns, 16-byte aligned rows):
-// one 256-thread CTA per row, four CTAs resident per SM, rows taken longest
-// first.  A row is read from HBM once:
+// one 256-thread CTA per row, five CTAs resident per SM (the candidates keep
+// 16-bit columns and the tie bitmap shares the histogram's space, so that
+// five fit and the L1 cache keeps room for the loads in flight), rows taken
+// longest first.  A row is read from HBM once:
 //   1. a sample of 4096 keys (512 runs of 8 adjacent columns, so that every
 //      sampled 32-byte sector is one the main pass reads next) places a
 //      threshold tau0 a few standard deviations below the expected k-th key;
 //      rows of at most 4096 columns are sampled whole, which makes tau0 a
 //      lower bound of the k-th key by construction;
-//   2. one streaming pass (eight 16-byte loads per thread in flight, no block
+//   2. one streaming pass (six 16-byte loads per thread in flight, no block
 //      barrier) appends every (key, column) with key >= tau0 to a shared
 //      candidate buffer, one atomic per warp; when it starts, the row's next
 //      two rounds are requested into L2, and when it ends, the sampled runs
@@ -38,8 +40,9 @@ namespace {
 namespace st {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kU = 8;                      // 16-byte loads per thread per round
-constexpr int kRound = kThreads * 4 * kU;  // 8192 columns per round
+constexpr int kCtasPerSm = 5;              // resident CTAs per SM (shared memory and registers)
+constexpr int kU = 6;                      // 16-byte loads per thread per round
+constexpr int kRound = kThreads * 4 * kU;  // 6144 columns per round
 constexpr int kCap = 3584;                 // candidate buffer (k <= 2048)
 constexpr int kBins = 2048;
 constexpr int kMaxLen = 65536;
@@ -49,10 +52,16 @@ constexpr int kRuns = 512;                    // sampled runs of 8 columns
 constexpr int kSample = kRuns * 8;            // 4096 keys
 
 struct Shared {
-  uint32_t hist[kBins];
+  // The histogram is all zero after every selection pass (find_bin clears
+  // the bins it reads), so once the k-th key is known its space holds the
+  // bitmap of the columns tied with it.
+  union {
+    uint32_t hist[kBins];
+    uint32_t tie[kWords];
+  };
   uint32_t bits[kWords];
-  uint32_t tie[kWords];
-  uint32_t cbuf[2 * kCap];  // sampled keys; then candidate keys | columns; then the staged ids
+  // sampled keys; then candidate keys | 16-bit columns; then the staged ids
+  uint32_t cbuf[kCap + kCap / 2];
   int wsum[2][kWarps];
   uint32_t wlo[kWarps], whi[kWarps];
   uint32_t lkey[32];
@@ -60,6 +69,24 @@ struct Shared {
   int bin, above, cnt;
   uint32_t tau;
   int need, n_eq;
+};
+
+// Candidates in shared memory: keys and 16-bit columns (rows have at most
+// 65536 columns).  Keeping the buffer small leaves room for the L1 cache,
+// which holds the streaming pass's loads in flight.
+static_assert(kMaxLen <= 65536, "columns are stored in 16 bits");
+struct CandSrc {
+  const uint32_t* key;
+  const uint16_t* col;
+  int n;
+  template <class F>
+  __device__ __forceinline__ void for_each(F&& f) const {
+    for (int base = 0; base < n; base += blockDim.x) {
+      const int i = base + threadIdx.x;
+      const bool a = i < n;
+      f(a ? key[i] : 0u, a ? static_cast<int32_t>(col[i]) : 0, a);
+    }
+  }
 };
 
 // Exclusive block prefix of v (one barrier).  Two consecutive calls must use
@@ -210,7 +237,7 @@ __device__ __forceinline__ void mark(Shared& S, const Src& src) {
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     topk_stream_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ len,
                        const int32_t* __restrict__ row_start, int T, int k, int32_t* __restrict__ idx,
                        int32_t* __restrict__ topk_length, float* __restrict__ vals, int ahead,
@@ -238,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 4)
   // ---- 1. sample -> tau0
   const int m = n < kSample ? n : kSample;
   uint32_t* const ckey = S.cbuf;
-  int32_t* const ccol = reinterpret_cast<int32_t*>(S.cbuf + kCap);
+  uint16_t* const ccol = reinterpret_cast<uint16_t*>(S.cbuf + kCap);
   uint32_t* const samp = S.cbuf;  // [16][256]: key i of thread t at samp[256 * i + t]
-  static_assert(2 * kCap >= kSample, "sample does not fit the candidate buffer");
+  static_assert(kCap + kCap / 2 >= kSample, "sample does not fit the candidate buffer");
   uint32_t lo = 0xFFFFFFFFu, hi = 0u;
   {
     float4 v[4];
@@ -278,10 +305,7 @@ __global__ void __launch_bounds__(kThreads, 4)
   lo = __reduce_min_sync(0xffffffffu, lo);
   hi = __reduce_max_sync(0xffffffffu, hi);
   for (int i = threadIdx.x; i < kBins; i += kThreads) S.hist[i] = 0u;
-  for (int i = threadIdx.x; i < kWords; i += kThreads) {
-    S.bits[i] = 0u;
-    S.tie[i] = 0u;
-  }
+  for (int i = threadIdx.x; i < kWords; i += kThreads) S.bits[i] = 0u;
   if (lane == 0) {
     S.wlo[warp] = lo;
     S.whi[warp] = hi;
@@ -393,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 4)
           for (int e = 0; e < 4; ++e)
             if (pass & (1u << (4 * u + e))) {
               ckey[slot] = dsa::f32_key(x[e]);
-              ccol[slot] = j + e;
+              ccol[slot] = static_cast<uint16_t>(j + e);
               ++slot;
             }
         }
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 
   // ---- 3. exact k-th key
   if (!S.fail && nc >= k) {
-    const dsa::PairSrc cand{ckey, ccol, nc};
+    const CandSrc cand{ckey, ccol, nc};
     uint32_t mx = 0u;
     for (int i = threadIdx.x; i < nc; i += kThreads) mx = max(mx, ckey[i]);
     mx = block_max(mx, S);
@@ -484,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       const int bit = __ffs(b) - 1;
       b &= b - 1;
       // checked build: at most k ids, staged inside the candidate buffer
-      if (dsa::check(pos < k && pos < 2 * kCap, status)) staged[pos] = base + ((w0 + i) << 5) + bit;
+      if (dsa::check(pos < k && pos < kCap + kCap / 2, status)) staged[pos] = base + ((w0 + i) << 5) + bit;
       ++pos;
     }
   }
@@ -560,9 +584,9 @@ int launch_topk_stream(const float* scores, int64_t ld, const int32_t* len, cons
   if (cudaFuncSetAttribute(st::topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return dsa::launch_error("topk_stream_kernel smem attribute");
-  // four CTAs are resident per SM: the block one wave later is 4 * SMs ahead
+  // kCtasPerSm CTAs are resident per SM: the block one wave later is that many SMs' worth ahead
   st::topk_stream_kernel<<<T, st::kThreads, smem, stream>>>(scores, ld, len, row_start, T, k, idx, topk_length, vals,
-                                                            4 * sm_count, dsa::device_status_ptr());
+                                                            st::kCtasPerSm * sm_count, dsa::device_status_ptr());
   return dsa::launch_error("topk_stream_kernel");
 }
 
