@@ -647,7 +647,21 @@ def main():
                "tflops": b_flops / (b_ms / 1e3) / 1e12,
                "frac_peak": b_flops / (b_ms / 1e3) / 1e12 / pk["bf16_tflops"],
                "workspace_gb": b_ws.numel() / 1e9}
-        del fwd, dout_t, b_ws
+        del b_ws
+        torch.cuda.empty_cache()
+        # the pages' default variant: dkv through fp32 atomics (not bitwise reproducible)
+        a_ws = torch.empty(ops.sparse_attn_bwd_workspace_size(T, T, H, K, deterministic=False), dtype=torch.uint8,
+                           device=dev)
+        a_run = lambda: ops.sparse_attn_bwd(d["q"], d["kv"], fwd["out"], dout_t, fwd["lse_kv"], idx, wl.scale,
+                                            topk_length=tl, sink=d["sink"], workspace=a_ws, deterministic=False)
+        a_run()
+        torch.cuda.synchronize()
+        a_ms = timed(a_run)
+        bwd["atomic"] = {"call": "dsa_sparse_attn_bwd_ex (deterministic = 0: dkv by fp32 atomics)", "ms": a_ms,
+                         "tflops": b_flops / (a_ms / 1e3) / 1e12,
+                         "frac_peak": b_flops / (a_ms / 1e3) / 1e12 / pk["bf16_tflops"],
+                         "workspace_gb": a_ws.numel() / 1e9}
+        del fwd, dout_t, a_ws
         torch.cuda.empty_cache()
         ops.device_status(clear=True)
 

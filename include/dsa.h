@@ -427,6 +427,26 @@ int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* out, const vo
                         float scale, void* dq, float* dkv, float* d_sink, void* workspace,
                         size_t ws_bytes, cudaStream_t stream);
 
+/* dsa_sparse_attn_bwd with the choice between the pages' two variants
+ * ([cuDNN-DSA] 2 Sparse Attention Backward, "deterministic", whose default
+ * is False: dKV accumulated with fp32 atomics, not bitwise reproducible):
+ *   deterministic != 0: exactly dsa_sparse_attn_bwd.
+ *   deterministic == 0: every valid slot adds its dkv row into dkv with fp32
+ *       atomic adds (16-byte vector reductions, served by L2); no per-SM
+ *       copies, so the workspace is
+ *       dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, 0) bytes (P and
+ *       dS of every slot).  dq and d_sink are computed as in the
+ *       deterministic variant (bitwise equal to it); dkv equals it up to the
+ *       order of its fp32 additions, which varies from run to run.
+ * dkv is overwritten (zeroed, then accumulated) in both variants.  Other
+ * arguments, results and errors as dsa_sparse_attn_bwd. */
+size_t dsa_sparse_attn_bwd_workspace_size_ex(int T, int Tkv, int H, int K, int deterministic);
+int dsa_sparse_attn_bwd_ex(const void* q, const void* kv, const void* out, const void* dout,
+                           const float* lse_kv, const float* sink, const int32_t* idx,
+                           const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K,
+                           float scale, void* dq, float* dkv, float* d_sink, int deterministic,
+                           void* workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* dsa_sparse_attn_fwd plus the indexer-prefix statistic ([cuDNN-DSA] 1,
  * outputs "lse_indexer" and compile-time "indexer_topk"):
  *   lse_indexer fp32 [T, H] (out): log sum exp(s_j) over the valid slots j <

@@ -28,6 +28,10 @@
 //     repeated ids in a row add up in a fixed order with no race.
 //  4. bwd_reduce_kernel: dkv = the shards summed in lane order; d_sink = the
 //     row terms summed in row order.
+// The non-deterministic variant (the pages' default) runs the same launches
+// except that bwd_dkv_kernel<true> adds each slot's dkv row straight into
+// dkv with fp32 vector atomics (red.global.add on 16 bytes), so there are no
+// shards to read, write or reduce and the updates are served by L2.
 #include <climits>
 
 #include "common.cuh"
@@ -579,7 +583,7 @@ __host__ __device__ inline DkvLayout dkv_layout() {
 struct DkvParams {
   const int32_t* idx;
   const int32_t* topk_length;
-  float* shards;  // [kLanes][Tkv][kDqk]
+  float* shards;  // [kLanes][Tkv][kDqk]; the atomic variant: dkv [Tkv][kDqk]
   uint32_t* status;
   int T, Tkv, H, G, K, Hp;
 };
@@ -596,7 +600,9 @@ __device__ __forceinline__ int dkv_len(const DkvParams& p, int t) {
 // Lane blockIdx.x (of kLanes) takes units (t, g) with t = lane, lane + kLanes,
 // ...; per 64-slot tile and per block of 128 dims (64 for dims 512..575)
 // D[key, dim] = sum_h scale dS[key, h] q[h, dim] + sum_h P[key, h] dout[h, dim]
-// (M = 64 keys, K = 64 + 64 heads, B MN-major), added into the lane's shard.
+// (M = 64 keys, K = 64 + 64 heads, B MN-major), added into the lane's shard
+// (ATOMIC: into dkv, one fp32 vector atomic per 4 dims of each valid slot).
+template <bool ATOMIC>
 __global__ void __launch_bounds__(kDkvThreads, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CUtensorMap map_p,
@@ -744,7 +750,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     const int quarter = warp & 3;          // TMEM lane quarter (warps 2..5)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int kA = quarter * 16 + (lane >> 2), kB = kA + 8;
-    float* shard = p.shards + static_cast<int64_t>(lane_id) * p.Tkv * kDqk;
+    float* shard = ATOMIC ? p.shards : p.shards + static_cast<int64_t>(lane_id) * p.Tkv * kDqk;
     uint32_t blk_ctr = 0;
     bool ok = true;
     // a wait of this warp gave up (warp-uniform): it skips its TMEM reads and
@@ -767,9 +773,10 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
         if (dt == 0) *dupflag = 0;
         named_bar(1, kDrainThreads);
         if (dt < kKeys) {
+          // (atomic updates need no folding: every slot adds its own row)
           const int id = tids[dt];
           int f = dt;
-          if (id >= 0)
+          if (!ATOMIC && id >= 0)
             for (int r = 0; r < dt; ++r)
               if (tids[r] == id) {
                 f = r;
@@ -799,13 +806,13 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
           }
         };
-        load_block(0, acc);
+        if (!ATOMIC) load_block(0, acc);
         for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
           const int db = blk_ctr & 1;
           const int nd = nb < 4 ? 128 : 64;
           const bool col_on = 4 * c4 < nd;
           float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
-          if (nb + 1 < 5) load_block(nb + 1, acc_next);
+          if (!ATOMIC && nb + 1 < 5) load_block(nb + 1, acc_next);
           if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
           dsa::tc_fence_after();
           if (!failed) {
@@ -844,13 +851,18 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
               const int id = tids[r];
               if (id >= 0 && first[r] == r) {
                 const float4 s = *reinterpret_cast<const float4*>(stage + r * kStageLd + 4 * c4);
-                base[static_cast<int64_t>(id) * (kDqk / 4)] =
-                    make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
+                if (ATOMIC)
+                  atomicAdd(base + static_cast<int64_t>(id) * (kDqk / 4), s);
+                else
+                  base[static_cast<int64_t>(id) * (kDqk / 4)] =
+                      make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
               }
             }
           }
+          if (!ATOMIC) {
 #pragma unroll
-          for (int k = 0; k < kKeys / 4; ++k) acc[k] = acc_next[k];
+            for (int k = 0; k < kKeys / 4; ++k) acc[k] = acc_next[k];
+          }
           // stage is read before the next block overwrites it; the group
           // leaves together if any warp's wait gave up
           if (dsa::named_bar_any(1, kDrainThreads, failed)) {
@@ -915,7 +927,7 @@ struct BwdWorkspace {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-BwdWorkspace bwd_workspace(void* base, int T, int Tkv, int H, int K) {
+BwdWorkspace bwd_workspace(void* base, int T, int Tkv, int H, int K, bool deterministic) {
   BwdWorkspace w{};
   const size_t th = static_cast<size_t>(T) * H;
   const size_t hp = static_cast<size_t>((H + kHG - 1) / kHG) * kHG;
@@ -930,25 +942,29 @@ BwdWorkspace bwd_workspace(void* base, int T, int Tkv, int H, int K) {
   o += align256(tkh * 2);
   w.p_g = reinterpret_cast<__nv_bfloat16*>(b + o);
   o += align256(tkh * 2);
-  w.shards = reinterpret_cast<float*>(b + o);
-  o += align256(static_cast<size_t>(kLanes) * Tkv * kDqk * sizeof(float));
+  w.shards = deterministic ? reinterpret_cast<float*>(b + o) : nullptr;
+  if (deterministic) o += align256(static_cast<size_t>(kLanes) * Tkv * kDqk * sizeof(float));
   w.total = o;
   return w;
 }
 
 }  // namespace
 
-extern "C" size_t dsa_sparse_attn_bwd_workspace_size(int T, int Tkv, int H, int K) {
+extern "C" size_t dsa_sparse_attn_bwd_workspace_size_ex(int T, int Tkv, int H, int K, int deterministic) {
   if (T < 0 || Tkv < 1 || H < 1 || H > 128 || K < 1) return 0;
-  return bwd_workspace(nullptr, T, Tkv, H, K).total;
+  return bwd_workspace(nullptr, T, Tkv, H, K, deterministic != 0).total;
 }
 
-extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* out, const void* dout,
-                                   const float* lse_kv, const float* sink, const int32_t* idx,
-                                   const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K,
-                                   float scale, void* dq, float* dkv, float* d_sink, void* workspace,
-                                   size_t ws_bytes, cudaStream_t stream) {
-  dsa::clear_error();
+extern "C" size_t dsa_sparse_attn_bwd_workspace_size(int T, int Tkv, int H, int K) {
+  return dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, 1);
+}
+
+namespace {
+
+int run_bwd(const void* q, const void* kv, const void* out, const void* dout, const float* lse_kv, const float* sink,
+            const int32_t* idx, const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K, float scale,
+            void* dq, float* dkv, float* d_sink, bool deterministic, void* workspace, size_t ws_bytes,
+            cudaStream_t stream) {
   if (Dqk != kDqk || Dv != kDv)
     return dsa::set_error(DSA_ERR_VALUE, "dsa_sparse_attn_bwd: (Dqk, Dv) must be (576, 512): the latent K = V layout");
   if (T < 0 || Tkv < 1 || H < 1 || H > 128 || K < 1)
@@ -960,7 +976,7 @@ extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* ou
   if (!dsa::aligned(q, 16) || !dsa::aligned(kv, 16) || !dsa::aligned(out, 16) || !dsa::aligned(dout, 16) ||
       !dsa::aligned(dkv, 16))
     return dsa::set_error(DSA_ERR_VALUE, "dsa_sparse_attn_bwd: q, kv, out, dout and dkv must be 16-byte aligned");
-  const size_t need = dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K);
+  const size_t need = dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, deterministic ? 1 : 0);
   if (!workspace || ws_bytes < need || !dsa::aligned(workspace, 256))
     return dsa::set_error(DSA_ERR_WORKSPACE, "dsa_sparse_attn_bwd: workspace must be 256-byte aligned and >= %zu bytes",
                           need);
@@ -974,7 +990,7 @@ extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* ou
       return dsa::launch_error("dsa_sparse_attn_bwd: memset");
     return DSA_OK;
   }
-  const BwdWorkspace w = bwd_workspace(workspace, T, Tkv, H, K);
+  const BwdWorkspace w = bwd_workspace(workspace, T, Tkv, H, K, deterministic);
   const int G = (H + kHG - 1) / kHG;
   const int Hp = G * kHG;
   uint32_t* status = dsa::device_status_ptr();
@@ -1020,9 +1036,10 @@ extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* ou
   bwd_dq_kernel<<<units < sms ? units : sms, kThreads, smem_dq, stream>>>(mq, mdo, p);
   if ((rc = dsa::launch_error("bwd_dq_kernel")) != DSA_OK) return rc;
 
-  // 3. dkv into the lanes' shards
-  const size_t shard_bytes = static_cast<size_t>(kLanes) * Tkv * kDqk * sizeof(float);
-  if (cudaMemsetAsync(w.shards, 0, shard_bytes, stream) != cudaSuccess)
+  // 3. dkv into the lanes' shards (the atomic variant: into dkv itself)
+  const size_t shard_bytes = deterministic ? static_cast<size_t>(kLanes) * Tkv * kDqk * sizeof(float) : dkv_bytes;
+  if (cudaMemsetAsync(deterministic ? static_cast<void*>(w.shards) : static_cast<void*>(dkv), 0, shard_bytes,
+                      stream) != cudaSuccess)
     return dsa::launch_error("dsa_sparse_attn_bwd: shard memset");
   CUtensorMap mds, mp;
   const uint64_t tk = static_cast<uint64_t>(T) * K;
@@ -1035,7 +1052,7 @@ extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* ou
   DkvParams dp{};
   dp.idx = idx;
   dp.topk_length = topk_length;
-  dp.shards = w.shards;
+  dp.shards = deterministic ? w.shards : dkv;
   dp.status = status;
   dp.T = T;
   dp.Tkv = Tkv;
@@ -1044,20 +1061,45 @@ extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* ou
   dp.K = K;
   dp.Hp = Hp;
   const size_t smem_dkv = dkv_layout().total + 1024;
-  if (cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_dkv)) !=
+  auto dkv_kernel = deterministic ? bwd_dkv_kernel<false> : bwd_dkv_kernel<true>;
+  if (cudaFuncSetAttribute(dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_dkv)) !=
       cudaSuccess)
     return dsa::launch_error("bwd_dkv_kernel smem attribute");
-  bwd_dkv_kernel<<<kLanes, kDkvThreads, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
+  dkv_kernel<<<kLanes, kDkvThreads, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
   if ((rc = dsa::launch_error("bwd_dkv_kernel")) != DSA_OK) return rc;
 
-  // 4. fixed-order reductions
-  const int64_t n4 = static_cast<int64_t>(Tkv) * kDqk / 4;
-  bwd_reduce_dkv_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(w.shards), n4, reinterpret_cast<float4*>(dkv));
-  if ((rc = dsa::launch_error("bwd_reduce_dkv_kernel")) != DSA_OK) return rc;
+  // 4. fixed-order reductions (the atomic variant has no shards to reduce)
+  if (deterministic) {
+    const int64_t n4 = static_cast<int64_t>(Tkv) * kDqk / 4;
+    bwd_reduce_dkv_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(w.shards), n4, reinterpret_cast<float4*>(dkv));
+    if ((rc = dsa::launch_error("bwd_reduce_dkv_kernel")) != DSA_OK) return rc;
+  }
   if (d_sink) {
     bwd_reduce_sink_kernel<<<H, 256, 0, stream>>>(w.dsink_part, T, H, d_sink);
     if ((rc = dsa::launch_error("bwd_reduce_sink_kernel")) != DSA_OK) return rc;
   }
   return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" int dsa_sparse_attn_bwd(const void* q, const void* kv, const void* out, const void* dout,
+                                   const float* lse_kv, const float* sink, const int32_t* idx,
+                                   const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K,
+                                   float scale, void* dq, float* dkv, float* d_sink, void* workspace,
+                                   size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  return run_bwd(q, kv, out, dout, lse_kv, sink, idx, topk_length, T, Tkv, H, Dqk, Dv, K, scale, dq, dkv, d_sink, true,
+                 workspace, ws_bytes, stream);
+}
+
+extern "C" int dsa_sparse_attn_bwd_ex(const void* q, const void* kv, const void* out, const void* dout,
+                                      const float* lse_kv, const float* sink, const int32_t* idx,
+                                      const int32_t* topk_length, int T, int Tkv, int H, int Dqk, int Dv, int K,
+                                      float scale, void* dq, float* dkv, float* d_sink, int deterministic,
+                                      void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  dsa::clear_error();
+  return run_bwd(q, kv, out, dout, lse_kv, sink, idx, topk_length, T, Tkv, H, Dqk, Dv, K, scale, dq, dkv, d_sink,
+                 deterministic != 0, workspace, ws_bytes, stream);
 }

@@ -70,6 +70,8 @@ _SIGNATURES = {
     "dsa_indexer_topk_mxfp8": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P], I),
     "dsa_sparse_attn_bwd_workspace_size": ([I, I, I, I], SZ),
     "dsa_sparse_attn_bwd": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P], I),
+    "dsa_sparse_attn_bwd_workspace_size_ex": ([I, I, I, I, I], SZ),
+    "dsa_sparse_attn_bwd_ex": ([P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, P, I, P, SZ, P], I),
 }
 
 
@@ -564,13 +566,15 @@ def pack_routes(routes):
     return out
 
 
-def sparse_attn_bwd_workspace_size(T: int, Tkv: int, H: int, K: int) -> int:
-    return int(lib().dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K))
+def sparse_attn_bwd_workspace_size(T: int, Tkv: int, H: int, K: int, deterministic: bool = True) -> int:
+    return int(lib().dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, 1 if deterministic else 0))
 
 
-def sparse_attn_bwd(q, kv, out, dout, lse_kv, idx, scale: float, topk_length=None, sink=None, workspace=None):
+def sparse_attn_bwd(q, kv, out, dout, lse_kv, idx, scale: float, topk_length=None, sink=None, workspace=None,
+                    deterministic: bool = True):
     """Sparse attention backward (latent K = V): dict(dq bf16 [T, H, 576],
-    dkv fp32 [Tkv, 576], d_sink fp32 [H] or None)."""
+    dkv fp32 [Tkv, 576], d_sink fp32 [H] or None).  deterministic=False
+    accumulates dkv with fp32 atomics (not bitwise reproducible)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(kv, "kv", torch.bfloat16, 2)
     _need(out, "out", torch.bfloat16, 3)
@@ -587,12 +591,14 @@ def sparse_attn_bwd(q, kv, out, dout, lse_kv, idx, scale: float, topk_length=Non
     K = idx.shape[1]
     dev = q.device
     if workspace is None:
-        workspace = torch.empty(sparse_attn_bwd_workspace_size(T, Tkv, H, K), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(sparse_attn_bwd_workspace_size(T, Tkv, H, K, deterministic), dtype=torch.uint8,
+                                device=dev)
     dq = torch.empty((T, H, Dqk), dtype=torch.bfloat16, device=dev)
     dkv = torch.empty((Tkv, Dqk), dtype=torch.float32, device=dev)
     d_sink = torch.empty(H, dtype=torch.float32, device=dev) if sink is not None else None
-    _check("dsa_sparse_attn_bwd",
-           lib().dsa_sparse_attn_bwd(_p(q), _p(kv), _p(out), _p(dout), _p(lse_kv), _p(sink), _p(idx), _p(topk_length),
-                                     T, Tkv, H, Dqk, Dv, K, float(scale), _p(dq), _p(dkv), _p(d_sink), _p(workspace),
-                                     workspace.numel() * workspace.element_size(), _stream()))
+    _check("dsa_sparse_attn_bwd_ex",
+           lib().dsa_sparse_attn_bwd_ex(_p(q), _p(kv), _p(out), _p(dout), _p(lse_kv), _p(sink), _p(idx),
+                                        _p(topk_length), T, Tkv, H, Dqk, Dv, K, float(scale), _p(dq), _p(dkv),
+                                        _p(d_sink), 1 if deterministic else 0, _p(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream()))
     return {"dq": dq, "dkv": dkv, "d_sink": d_sink}

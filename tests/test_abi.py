@@ -98,6 +98,10 @@ FAKE = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
                                     FAKE, NULL, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_sparse_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.1, NULL,
                                     FAKE, NULL, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 512, 512, 8, 0.1,
+                                       FAKE, FAKE, NULL, 0, FAKE, 1 << 30, NULL),
+    lambda L: L.dsa_sparse_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.1,
+                                       FAKE, NULL, NULL, 0, FAKE, 1 << 30, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, FAKE, NULL, 1, 10, 0, FAKE, FAKE, NULL),
     lambda L: L.dsa_thd_metadata_ratio(FAKE, NULL, NULL, 1, 10, 4, FAKE, FAKE, NULL),
     lambda L: L.dsa_indexer_scores_ratio(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, 1, 128, 32, 64, 128, 0, 32, FAKE, 32, NULL),
@@ -141,6 +145,34 @@ def test_stage_calls_check_the_workspace(lib):
     assert rc == ops.DSA_ERR_WORKSPACE
     rc = lib.dsa_select_candidates(FAKE, 1, 4096, 64, 128, 2048, 4096, ctypes.c_void_p(4096 + 16), need, FAKE, NULL,
                                    NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("T,Tkv,H,K", [(100, 300, 64, 256), (7, 5, 128, 64), (65536, 65536, 64, 2048)])
+def test_bwd_workspace_layout(lib, T, Tkv, H, K):
+    """The backward's workspace: per (token, head) two fp32 statistics and the
+    d_sink row term, then scale * dS and P of every slot (bf16, heads padded
+    to groups of 64), then, in the deterministic variant only, the 152 fp32
+    dkv copies.  Every part starts on a 256-byte boundary."""
+    def a256(x):
+        return (x + 255) // 256 * 256
+
+    hp = (H + 63) // 64 * 64
+    atomic = a256(T * H * 8) + a256(T * H * 4) + 2 * a256(T * K * hp * 2)
+    assert lib.dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, 0) == atomic
+    det = atomic + a256(152 * Tkv * 576 * 4)
+    assert lib.dsa_sparse_attn_bwd_workspace_size_ex(T, Tkv, H, K, 1) == det
+    assert lib.dsa_sparse_attn_bwd_workspace_size(T, Tkv, H, K) == det
+
+
+def test_bwd_variants_check_their_workspace(lib):
+    atomic = lib.dsa_sparse_attn_bwd_workspace_size_ex(4, 8, 64, 8, 0)
+    # enough for the atomic variant, too small for the deterministic one
+    rc = lib.dsa_sparse_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.1, FAKE,
+                                    FAKE, NULL, 1, FAKE, atomic, NULL)
+    assert rc == ops.DSA_ERR_WORKSPACE
+    rc = lib.dsa_sparse_attn_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, NULL, FAKE, NULL, 4, 8, 64, 576, 512, 8, 0.1, FAKE,
+                                    FAKE, NULL, 0, FAKE, atomic - 1, NULL)
     assert rc == ops.DSA_ERR_WORKSPACE
 
 

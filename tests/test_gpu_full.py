@@ -180,7 +180,8 @@ def test_long_64k_backward_key_shared_by_every_row():
     """dkv of keys referenced by many rows, at the 64K-token shapes.  Key 0
     sits in every row (at slot t % k), key 1 in every other row: dkv[0] sums
     65534 x 64 contributions through the per-SM fp32 copies and their
-    fixed-order reduction, dkv[1] half as many.  The backward's inputs out,
+    fixed-order reduction (or, in the atomic variant, through 65534 fp32
+    atomic adds to one row), dkv[1] half as many.  The backward's inputs out,
     dout and lse_kv are drawn (any finite values are valid inputs of its
     formula; none comes from the CUDA path), so one key's dkv depends only on
     that key's slot of each row: the oracle computes it from one-slot id
@@ -206,10 +207,13 @@ def test_long_64k_backward_key_shared_by_every_row():
     out = W.f32_to_bf16_bits(rng.standard_normal((T, H, wl.Dv), dtype=np.float32) * np.float32(0.1))
     dout = W.f32_to_bf16_bits(rng.standard_normal((T, H, wl.Dv), dtype=np.float32) * np.float32(0.1))
     lse_kv = np.full((T, H), np.log(np.float32(K)), np.float32)
-    res = ops.sparse_attn_bwd(dev_bf16(q), dev_bf16(kv), dev_bf16(out), dev_bf16(dout), dev(lse_kv), dev(idx),
-                              wl.scale, topk_length=dev(tl), sink=dev(sk))
-    got = res["dkv"][:2].cpu().numpy().astype(np.float64)
-    del res
+    a = (dev_bf16(q), dev_bf16(kv), dev_bf16(out), dev_bf16(dout), dev(lse_kv), dev(idx), wl.scale)
+    got = {}
+    for det in (True, False):  # the per-SM copies, and the fp32 atomics of the other variant
+        res = ops.sparse_attn_bwd(*a, topk_length=dev(tl), sink=dev(sk), deterministic=det)
+        got[det] = res["dkv"][:2].cpu().numpy().astype(np.float64)
+        del res
+    del a
     kv2 = f64(kv[:2])
     for key, krows in ((0, rows), (1, odd)):
         ref = np.zeros(kv.shape[1], np.float64)
@@ -220,7 +224,8 @@ def test_long_64k_backward_key_shared_by_every_row():
                                                lse_kv[r].astype(np.float64), topk_length=np.ones(r.size, np.int32),
                                                sink=sk)
             ref += dkv[key]
-        assert_bwd_close(got[key], ref, f"dkv[{key}] ({krows.size} referencing rows)")
+        for det in (True, False):
+            assert_bwd_close(got[det][key], ref, f"dkv[{key}] ({krows.size} referencing rows, deterministic={det})")
 
 
 def test_compressed_thd_8k_workload():

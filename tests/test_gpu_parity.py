@@ -850,12 +850,14 @@ def _bwd_inputs(T, Tkv, H, K, seed, sink=True, lengths="mixed"):
     return q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv
 
 
+@pytest.mark.parametrize("deterministic", [True, False])
 @pytest.mark.parametrize("T,Tkv,H,K,sink", [(40, 300, 64, 256, True), (9, 100, 12, 100, True),
                                             (6, 500, 128, 130, False), (3, 64, 64, 64, True)])
-def test_attention_bwd_against_oracle(T, Tkv, H, K, sink):
+def test_attention_bwd_against_oracle(T, Tkv, H, K, sink, deterministic):
     q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv = _bwd_inputs(T, Tkv, H, K, T * 7 + H, sink)
     res = ops.sparse_attn_bwd(dev_bf16(q), dev_bf16(kv), dev_bf16(out_bits), dev_bf16(dout), dev(lse_kv), dev(idx),
-                              scale, topk_length=dev(tl), sink=None if sk is None else dev(sk))
+                              scale, topk_length=dev(tl), sink=None if sk is None else dev(sk),
+                              deterministic=deterministic)
     dq, dkv, ds = oracle.sparse_attn_bwd(f64(q), f64(kv), idx, scale, f64(out_bits), f64(dout),
                                          lse_kv.astype(np.float64), topk_length=tl, sink=sk)
     assert_bwd_close(res["dq"], dq, "dq")
@@ -873,6 +875,22 @@ def test_attention_bwd_is_deterministic():
     for key in ("dq", "dkv", "d_sink"):
         assert torch.equal(r1[key].view(torch.int32) if r1[key].dtype == torch.float32 else r1[key].view(torch.int16),
                            r2[key].view(torch.int32) if r2[key].dtype == torch.float32 else r2[key].view(torch.int16)), key
+
+
+def test_attention_bwd_atomic_variant_matches_the_deterministic_one():
+    """The atomic variant differs from the deterministic one only in the
+    order of dkv's fp32 additions: dq and d_sink are bitwise equal, and dkv
+    (including the slots with repeated ids) agrees with it to the tolerance
+    both are held to against the oracle, while differing in its last bits."""
+    q, kv, dout, idx, tl, sk, scale, out_bits, lse_kv = _bwd_inputs(64, 200, 64, 192, 9, True, lengths="full")
+    a = (dev_bf16(q), dev_bf16(kv), dev_bf16(out_bits), dev_bf16(dout), dev(lse_kv), dev(idx), scale)
+    r1 = ops.sparse_attn_bwd(*a, topk_length=dev(tl), sink=dev(sk))
+    r2 = ops.sparse_attn_bwd(*a, topk_length=dev(tl), sink=dev(sk), deterministic=False)
+    assert torch.equal(r1["dq"].view(torch.int16), r2["dq"].view(torch.int16))
+    assert torch.equal(r1["d_sink"].view(torch.int32), r2["d_sink"].view(torch.int32))
+    d1 = r1["dkv"].cpu().numpy().astype(np.float64)
+    assert np.count_nonzero(d1) > 0
+    assert_bwd_close(r2["dkv"], d1, "dkv (atomic against deterministic)")
 
 
 def test_attention_bwd_all_rows_empty():
