@@ -750,124 +750,185 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     const int quarter = warp & 3;          // TMEM lane quarter (warps 2..5)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int kA = quarter * 16 + (lane >> 2), kB = kA + 8;
-    float* shard = ATOMIC ? p.shards : p.shards + static_cast<int64_t>(lane_id) * p.Tkv * kDqk;
+    float* shard = ATOMIC ? p.shards : p.shards + static_cast<int64_t>(lane_id) * p.Tkv * kDqk;  // ATOMIC: dkv
     uint32_t blk_ctr = 0;
     bool ok = true;
     // a wait of this warp gave up (warp-uniform): it skips its TMEM reads and
     // shard writes, and the four warps leave together at the block's last
     // barrier, which carries the flag
     bool failed = false;
-    for (int u = lane_id; u < n_units && ok; u += kLanes) {
-      const int len = dkv_len(p, u / p.G);
-      const int nt = (len + kKeys - 1) / kKeys;
-      const int t = u / p.G;
-      for (int i = 0; i < nt && ok; ++i) {
-        // ids of the tile (-1: absent) and, per slot, the first slot of the
-        // tile with the same id
-        named_bar(1, kDrainThreads);  // previous tile's readers of tids / first / stage are done
-        if (dt < kKeys) {
-          const int j = i * kKeys + dt;
-          int id = j < len ? __ldg(p.idx + static_cast<int64_t>(t) * p.K + j) : -1;
-          tids[dt] = (id >= 0 && id < p.Tkv) ? id : -1;
-        }
-        if (dt == 0) *dupflag = 0;
-        named_bar(1, kDrainThreads);
-        if (dt < kKeys) {
-          // (atomic updates need no folding: every slot adds its own row)
-          const int id = tids[dt];
-          int f = dt;
-          if (!ATOMIC && id >= 0)
-            for (int r = 0; r < dt; ++r)
-              if (tids[r] == id) {
-                f = r;
-                break;
-              }
-          first[dt] = f;
-          if (f != dt) *dupflag = 1;
-        }
-        named_bar(1, kDrainThreads);  // first[] of the tile complete
-        // The shard values this thread updates: thread (key group kg, 4-dim
-        // column c4) owns rows kg + 4k of each block of dims; unique ids never
-        // alias.  A block's values are read one block ahead, while the
-        // previous block's products finish and its values are written (the
-        // blocks of a tile cover disjoint dims); earlier updates of the same
-        // values, by any thread, were ordered before the read by the barrier
-        // that ended the previous tile.
-        const int kg = dt >> 5, c4 = dt & 31;
-        float4 acc[kKeys / 4], acc_next[kKeys / 4];
-        auto load_block = [&](int nb, float4 (&a)[kKeys / 4]) {
-          const bool on = 4 * c4 < (nb < 4 ? 128 : 64);
-          const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * c4);
-#pragma unroll
-          for (int k = 0; k < kKeys / 4; ++k) {
-            const int r = kg + 4 * k;
-            const int id = tids[r];
-            a[k] = (on && id >= 0 && first[r] == r) ? src[static_cast<int64_t>(id) * (kDqk / 4)]
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (ATOMIC) {
+      // Each warp drains its own TMEM lane quarter (keys 16*quarter .. +15 of
+      // the tile) through its own rows of the staging tile and adds them into
+      // dkv, one row (512 contiguous bytes) per warp instruction: no barrier
+      // across the four warps per block, and each tile's ids are read once.
+      const int r0 = quarter * 16;
+      for (int u = lane_id; u < n_units && ok; u += kLanes) {
+        const int len = dkv_len(p, u / p.G);
+        const int nt = (len + kKeys - 1) / kKeys;
+        const int t = u / p.G;
+        for (int i = 0; i < nt && ok; ++i) {
+          int my = -1;  // lane k < 16: id of key r0 + k of the tile (-1: absent)
+          if (lane < 16) {
+            const int j = i * kKeys + r0 + lane;
+            const int id = j < len ? __ldg(p.idx + static_cast<int64_t>(t) * p.K + j) : -1;
+            my = (id >= 0 && id < p.Tkv) ? id : -1;
           }
-        };
-        if (!ATOMIC) load_block(0, acc);
-        for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
-          const int db = blk_ctr & 1;
-          const int nd = nb < 4 ? 128 : 64;
-          const bool col_on = 4 * c4 < nd;
-          float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
-          if (!ATOMIC && nb + 1 < 5) load_block(nb + 1, acc_next);
-          if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
-          dsa::tc_fence_after();
-          if (!failed) {
-            uint32_t v[4][16];
+          int ids[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
-            dsa::tmem_wait_ld();
+          for (int k = 0; k < 16; ++k) ids[k] = __shfl_sync(0xffffffffu, my, k);
+          for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
+            const int db = blk_ctr & 1;
+            const int nd = nb < 4 ? 128 : 64;
+            if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
+            dsa::tc_fence_after();
+            if (!failed) {
+              uint32_t v[4][16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              if (32 * q4 >= nd) continue;
+              for (int q4 = 0; q4 < 4; ++q4)
+                if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
+              dsa::tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
-                *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
-                    make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
-                *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
-                    make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+              for (int q4 = 0; q4 < 4; ++q4) {
+                if (32 * q4 >= nd) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
+                  *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                      make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
+                  *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                      make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+                }
               }
             }
+            dsa::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) dsa::mbar_arrive(&d_empty[db]);  // this warp's TMEM reads are done
+            if (!failed && 4 * lane < nd) {
+              float* base = shard + nb * 128 + 4 * lane;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                if (ids[k] < 0) continue;
+                const float4 sv = *reinterpret_cast<const float4*>(stage + (r0 + k) * kStageLd + 4 * lane);
+                atomicAdd(reinterpret_cast<float4*>(base + static_cast<int64_t>(ids[k]) * kDqk), sv);
+              }
+            }
+            __syncwarp();  // this warp's staging rows are read before the next block rewrites them
           }
-          dsa::tc_fence_before();
-          named_bar(1, kDrainThreads);  // stage and first[] complete
-          if (lane == 0) dsa::mbar_arrive(&d_empty[db]);
-          if (*dupflag) {
-            // repeated ids: later slots fold into the first one, in slot order
-            if (dt < nd)
-              for (int r = 1; r < kKeys; ++r)
-                if (first[r] != r) stage[first[r] * kStageLd + dt] += stage[r * kStageLd + dt];
-            named_bar(1, kDrainThreads);
+          // the four warps leave together, at a tile's end, if any wait gave up
+          if (dsa::named_bar_any(1, kDrainThreads, failed)) {
+            ok = false;
+            break;
           }
-          if (col_on && !failed) {
+        }
+      }
+    } else {
+      for (int u = lane_id; u < n_units && ok; u += kLanes) {
+        const int len = dkv_len(p, u / p.G);
+        const int nt = (len + kKeys - 1) / kKeys;
+        const int t = u / p.G;
+        for (int i = 0; i < nt && ok; ++i) {
+          // ids of the tile (-1: absent) and, per slot, the first slot of the
+          // tile with the same id
+          named_bar(1, kDrainThreads);  // previous tile's readers of tids / first / stage are done
+          if (dt < kKeys) {
+            const int j = i * kKeys + dt;
+            int id = j < len ? __ldg(p.idx + static_cast<int64_t>(t) * p.K + j) : -1;
+            tids[dt] = (id >= 0 && id < p.Tkv) ? id : -1;
+          }
+          if (dt == 0) *dupflag = 0;
+          named_bar(1, kDrainThreads);
+          if (dt < kKeys) {
+            const int id = tids[dt];
+            int f = dt;
+            if (id >= 0)
+              for (int r = 0; r < dt; ++r)
+                if (tids[r] == id) {
+                  f = r;
+                  break;
+                }
+            first[dt] = f;
+            if (f != dt) *dupflag = 1;
+          }
+          named_bar(1, kDrainThreads);  // first[] of the tile complete
+          // The shard values this thread updates: thread (key group kg, 4-dim
+          // column c4) owns rows kg + 4k of each block of dims; unique ids never
+          // alias.  A block's values are read one block ahead, while the
+          // previous block's products finish and its values are written (the
+          // blocks of a tile cover disjoint dims); earlier updates of the same
+          // values, by any thread, were ordered before the read by the barrier
+          // that ended the previous tile.
+          const int kg = dt >> 5, c4 = dt & 31;
+          float4 acc[kKeys / 4], acc_next[kKeys / 4];
+          auto load_block = [&](int nb, float4 (&a)[kKeys / 4]) {
+            const bool on = 4 * c4 < (nb < 4 ? 128 : 64);
+            const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * c4);
 #pragma unroll
             for (int k = 0; k < kKeys / 4; ++k) {
               const int r = kg + 4 * k;
               const int id = tids[r];
-              if (id >= 0 && first[r] == r) {
-                const float4 s = *reinterpret_cast<const float4*>(stage + r * kStageLd + 4 * c4);
-                if (ATOMIC)
-                  atomicAdd(base + static_cast<int64_t>(id) * (kDqk / 4), s);
-                else
-                  base[static_cast<int64_t>(id) * (kDqk / 4)] =
-                      make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
+              a[k] = (on && id >= 0 && first[r] == r) ? src[static_cast<int64_t>(id) * (kDqk / 4)]
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          };
+          load_block(0, acc);
+          for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
+            const int db = blk_ctr & 1;
+            const int nd = nb < 4 ? 128 : 64;
+            const bool col_on = 4 * c4 < nd;
+            float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
+            if (nb + 1 < 5) load_block(nb + 1, acc_next);
+            if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
+            dsa::tc_fence_after();
+            if (!failed) {
+              uint32_t v[4][16];
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
+              dsa::tmem_wait_ld();
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                if (32 * q4 >= nd) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
+                  *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                      make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
+                  *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                      make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+                }
               }
             }
-          }
-          if (!ATOMIC) {
+            dsa::tc_fence_before();
+            named_bar(1, kDrainThreads);  // stage and first[] complete
+            if (lane == 0) dsa::mbar_arrive(&d_empty[db]);
+            if (*dupflag) {
+              // repeated ids: later slots fold into the first one, in slot order
+              if (dt < nd)
+                for (int r = 1; r < kKeys; ++r)
+                  if (first[r] != r) stage[first[r] * kStageLd + dt] += stage[r * kStageLd + dt];
+              named_bar(1, kDrainThreads);
+            }
+            if (col_on && !failed) {
+#pragma unroll
+              for (int k = 0; k < kKeys / 4; ++k) {
+                const int r = kg + 4 * k;
+                const int id = tids[r];
+                if (id >= 0 && first[r] == r) {
+                  const float4 s = *reinterpret_cast<const float4*>(stage + r * kStageLd + 4 * c4);
+                  base[static_cast<int64_t>(id) * (kDqk / 4)] =
+                      make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
+                }
+              }
+            }
 #pragma unroll
             for (int k = 0; k < kKeys / 4; ++k) acc[k] = acc_next[k];
-          }
-          // stage is read before the next block overwrites it; the group
-          // leaves together if any warp's wait gave up
-          if (dsa::named_bar_any(1, kDrainThreads, failed)) {
-            ok = false;
-            break;
+            // stage is read before the next block overwrites it; the group
+            // leaves together if any warp's wait gave up
+            if (dsa::named_bar_any(1, kDrainThreads, failed)) {
+              ok = false;
+              break;
+            }
           }
         }
       }

@@ -23,7 +23,8 @@ Cases (kernel to select with -k in parentheses):
                   tokens, Hq = 12, D = 256, routes as the GQA workload draws them
                                                                 (sparse_attn_kernel)
   backward        dsa_sparse_attn_bwd on the fused top-k ids, dout ~ N(0, 1) * 0.1
-                  (bwd_prep_kernel, bwd_dq_kernel, bwd_dkv_kernel, bwd_reduce_*)
+                  (bwd_prep_kernel, bwd_dq_kernel, bwd_dkv_kernel, bwd_reduce_*);
+                  with --atomic the variant whose dkv goes through fp32 atomics
 """
 from __future__ import annotations
 
@@ -46,6 +47,7 @@ def main(argv=None) -> int:
     ap.add_argument("case", choices=CASES)
     ap.add_argument("--T", type=int, default=16384)
     ap.add_argument("--k", type=int, default=2048)
+    ap.add_argument("--atomic", action="store_true", help="backward: dkv by fp32 atomics")
     args = ap.parse_args(argv)
 
     import os
@@ -123,9 +125,10 @@ def main(argv=None) -> int:
         else:
             fwd = ops.sparse_attn_fwd(q, kv, idx, scale, topk_length=tl, sink=sink, want_lse_kv=True)
             dout = _bf16((T, H, 512), 0.1, g, dev)
-            bws = torch.empty(ops.sparse_attn_bwd_workspace_size(T, T, H, K), dtype=torch.uint8, device=dev)
+            det = not args.atomic
+            bws = torch.empty(ops.sparse_attn_bwd_workspace_size(T, T, H, K, det), dtype=torch.uint8, device=dev)
             twice(lambda: ops.sparse_attn_bwd(q, kv, fwd["out"], dout, fwd["lse_kv"], idx, scale, topk_length=tl,
-                                              sink=sink, workspace=bws))
+                                              sink=sink, workspace=bws, deterministic=det))
     status = ops.device_status(clear=True)
     print(f"{args.case}: T={T} k={K} status={status:#x}")
     return 1 if status else 0
