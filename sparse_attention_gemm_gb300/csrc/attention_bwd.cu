@@ -851,15 +851,88 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             if (f != dt) *dupflag = 1;
           }
           named_bar(1, kDrainThreads);  // first[] of the tile complete
-          // The shard values this thread updates: thread (key group kg, 4-dim
-          // column c4) owns rows kg + 4k of each block of dims; unique ids never
-          // alias.  A block's values are read one block ahead, while the
-          // previous block's products finish and its values are written (the
-          // blocks of a tile cover disjoint dims); earlier updates of the same
-          // values, by any thread, were ordered before the read by the barrier
-          // that ended the previous tile.
+          if (!*dupflag) {
+            // No id repeats in this tile (the usual case): each warp updates
+            // the rows of its own TMEM lane quarter (keys 16*quarter .. +15),
+            // one 512-byte row per warp instruction, with no barrier across
+            // the drain warps per block.  Each row has one writer per block,
+            // which adds the same fp32 value to it as the path below, so the
+            // result is the same bits; the barrier at the tile's end orders
+            // these writes before a later tile's reads of the same rows.
+            const int r0 = quarter * 16;
+            const int* ids = tids + r0;  // the warp's 16 ids (-1: absent), read from shared memory
+            float4 pa[16], pn[16];
+            auto load_rows = [&](int nb, float4 (&a)[16]) {
+              const bool on = 4 * lane < (nb < 4 ? 128 : 64);
+              const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * lane);
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const int id = ids[k];
+                a[k] = (on && id >= 0) ? src[static_cast<int64_t>(id) * (kDqk / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            };
+            load_rows(0, pa);
+            for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
+              const int db = blk_ctr & 1;
+              const int nd = nb < 4 ? 128 : 64;
+              if (nb + 1 < 5) load_rows(nb + 1, pn);
+              if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
+              dsa::tc_fence_after();
+              if (!failed) {
+                // two 64-column halves, to leave registers for the rows in flight
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  if (64 * h2 >= nd) break;
+                  uint32_t v[2][16];
+#pragma unroll
+                  for (int q2 = 0; q2 < 2; ++q2)
+                    dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 64 * h2 + 32 * q2, v[q2]);
+                  dsa::tmem_wait_ld();
+#pragma unroll
+                  for (int q2 = 0; q2 < 2; ++q2) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      const int col = 64 * h2 + 32 * q2 + 8 * j + 2 * (lane & 3);
+                      *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                          make_float2(__uint_as_float(v[q2][4 * j]), __uint_as_float(v[q2][4 * j + 1]));
+                      *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                          make_float2(__uint_as_float(v[q2][4 * j + 2]), __uint_as_float(v[q2][4 * j + 3]));
+                    }
+                  }
+                }
+              }
+              dsa::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) dsa::mbar_arrive(&d_empty[db]);  // this warp's TMEM reads are done
+              if (!failed && 4 * lane < nd) {
+                float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * lane);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const int id = ids[k];
+                  if (id < 0) continue;
+                  const float4 sv = *reinterpret_cast<const float4*>(stage + (r0 + k) * kStageLd + 4 * lane);
+                  base[static_cast<int64_t>(id) * (kDqk / 4)] =
+                      make_float4(pa[k].x + sv.x, pa[k].y + sv.y, pa[k].z + sv.z, pa[k].w + sv.w);
+                }
+              }
+              __syncwarp();  // this warp's staging rows are read before the next block rewrites them
+#pragma unroll
+              for (int k = 0; k < 16; ++k) pa[k] = pn[k];
+            }
+            // the four warps leave together, at the tile's end, if any wait gave up
+            if (dsa::named_bar_any(1, kDrainThreads, failed)) {
+              ok = false;
+              break;
+            }
+            continue;
+          }
+          // A tile with repeated ids.  The shard values this thread updates:
+          // thread (key group kg, 4-dim column c4) owns rows kg + 4k of each
+          // block of dims; a repeated id is updated once, through its first
+          // slot, so no two threads write one value.  Earlier updates of the
+          // same values, by any thread, were ordered before the reads by the
+          // barrier that ended the previous tile (or block).
           const int kg = dt >> 5, c4 = dt & 31;
-          float4 acc[kKeys / 4], acc_next[kKeys / 4];
+          float4 acc[kKeys / 4];
           auto load_block = [&](int nb, float4 (&a)[kKeys / 4]) {
             const bool on = 4 * c4 < (nb < 4 ? 128 : 64);
             const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * c4);
@@ -871,13 +944,12 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
             }
           };
-          load_block(0, acc);
           for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
             const int db = blk_ctr & 1;
             const int nd = nb < 4 ? 128 : 64;
             const bool col_on = 4 * c4 < nd;
             float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
-            if (nb + 1 < 5) load_block(nb + 1, acc_next);
+            load_block(nb, acc);
             if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
             dsa::tc_fence_after();
             if (!failed) {
@@ -921,8 +993,6 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
                 }
               }
             }
-#pragma unroll
-            for (int k = 0; k < kKeys / 4; ++k) acc[k] = acc_next[k];
             // stage is read before the next block overwrites it; the group
             // leaves together if any warp's wait gave up
             if (dsa::named_bar_any(1, kDrainThreads, failed)) {
