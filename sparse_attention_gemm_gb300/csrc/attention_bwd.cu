@@ -554,6 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -------------------------------------------------------------- 3. dkv
 constexpr int kDkvThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 drain + shard update
 constexpr int kDrainThreads = 128;
+// The atomic variant drains with eight warps, two per TMEM lane quarter (one
+// per 64-column half of a block): it needs far fewer registers per thread.
+constexpr int kDkvThreadsAtomic = 320;
+constexpr int kDrainThreadsAtomic = kDkvThreadsAtomic - 64;
 // staging row stride (floats): 4 floats of padding put the eight keys a warp
 // writes at once in different banks (unpadded rows 512 bytes apart collide)
 constexpr int kStageLd = 132;
@@ -603,7 +607,7 @@ __device__ __forceinline__ int dkv_len(const DkvParams& p, int t) {
 // (M = 64 keys, K = 64 + 64 heads, B MN-major), added into the lane's shard
 // (ATOMIC: into dkv, one fp32 vector atomic per 4 dims of each valid slot).
 template <bool ATOMIC>
-__global__ void __launch_bounds__(kDkvThreads, 1)
+__global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CUtensorMap map_p,
                    const DkvParams p) {
@@ -638,7 +642,7 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
       dsa::mbar_init(&a_full[b], 1);
       dsa::mbar_init(&a_empty[b], 1);
       dsa::mbar_init(&d_full[b], 1);
-      dsa::mbar_init(&d_empty[b], 4);
+      dsa::mbar_init(&d_empty[b], ATOMIC ? 8 : 4);  // one arrive per drain warp
     }
     dsa::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -758,11 +762,14 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
     // barrier, which carries the flag
     bool failed = false;
     if constexpr (ATOMIC) {
-      // Each warp drains its own TMEM lane quarter (keys 16*quarter .. +15 of
-      // the tile) through its own rows of the staging tile and adds them into
-      // dkv, one row (512 contiguous bytes) per warp instruction: no barrier
-      // across the four warps per block, and each tile's ids are read once.
+      // Each warp drains one 64-column half of its own TMEM lane quarter (keys
+      // 16*quarter .. +15 of the tile) through its own part of the staging
+      // tile and adds it into dkv, two rows (256 contiguous bytes each) per
+      // warp instruction: no barrier across the eight warps per block, and
+      // each tile's ids are read once.
       const int r0 = quarter * 16;
+      const int half = (warp - 2) >> 2;
+      const int c0 = 64 * half;  // this warp's columns of a block: [c0, c0 + 64)
       for (int u = lane_id; u < n_units && ok; u += kLanes) {
         const int len = dkv_len(p, u / p.G);
         const int nt = (len + kKeys - 1) / kKeys;
@@ -774,49 +781,50 @@ __global__ void __launch_bounds__(kDkvThreads, 1)
             const int id = j < len ? __ldg(p.idx + static_cast<int64_t>(t) * p.K + j) : -1;
             my = (id >= 0 && id < p.Tkv) ? id : -1;
           }
-          int ids[16];
+          int ids[8];  // id of row 2k + lane / 16 of the warp's 16
 #pragma unroll
-          for (int k = 0; k < 16; ++k) ids[k] = __shfl_sync(0xffffffffu, my, k);
+          for (int k = 0; k < 8; ++k) ids[k] = __shfl_sync(0xffffffffu, my, 2 * k + (lane >> 4));
           for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
             const int db = blk_ctr & 1;
-            const int nd = nb < 4 ? 128 : 64;
+            const bool active = c0 < (nb < 4 ? 128 : 64);
             if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
             dsa::tc_fence_after();
-            if (!failed) {
-              uint32_t v[4][16];
+            if (!failed && active) {
+              uint32_t v[2][16];
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
+              for (int q2 = 0; q2 < 2; ++q2)
+                dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + c0 + 32 * q2, v[q2]);
               dsa::tmem_wait_ld();
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                if (32 * q4 >= nd) continue;
+              for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                  const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
+                  const int col = c0 + 32 * q2 + 8 * j + 2 * (lane & 3);
                   *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
-                      make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
+                      make_float2(__uint_as_float(v[q2][4 * j]), __uint_as_float(v[q2][4 * j + 1]));
                   *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
-                      make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+                      make_float2(__uint_as_float(v[q2][4 * j + 2]), __uint_as_float(v[q2][4 * j + 3]));
                 }
               }
             }
             dsa::tc_fence_before();
             __syncwarp();
             if (lane == 0) dsa::mbar_arrive(&d_empty[db]);  // this warp's TMEM reads are done
-            if (!failed && 4 * lane < nd) {
-              float* base = shard + nb * 128 + 4 * lane;
+            if (!failed && active) {
+              const int cl = c0 + 4 * (lane & 15);
+              float* base = shard + nb * 128 + cl;
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
+              for (int k = 0; k < 8; ++k) {
                 if (ids[k] < 0) continue;
-                const float4 sv = *reinterpret_cast<const float4*>(stage + (r0 + k) * kStageLd + 4 * lane);
+                const int r = r0 + 2 * k + (lane >> 4);
+                const float4 sv = *reinterpret_cast<const float4*>(stage + r * kStageLd + cl);
                 atomicAdd(reinterpret_cast<float4*>(base + static_cast<int64_t>(ids[k]) * kDqk), sv);
               }
             }
-            __syncwarp();  // this warp's staging rows are read before the next block rewrites them
+            __syncwarp();  // this warp's staging columns are read before the next block rewrites them
           }
-          // the four warps leave together, at a tile's end, if any wait gave up
-          if (dsa::named_bar_any(1, kDrainThreads, failed)) {
+          // the eight warps leave together, at a tile's end, if any wait gave up
+          if (dsa::named_bar_any(1, kDrainThreadsAtomic, failed)) {
             ok = false;
             break;
           }
@@ -1196,7 +1204,7 @@ int run_bwd(const void* q, const void* kv, const void* out, const void* dout, co
   if (cudaFuncSetAttribute(dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_dkv)) !=
       cudaSuccess)
     return dsa::launch_error("bwd_dkv_kernel smem attribute");
-  dkv_kernel<<<kLanes, kDkvThreads, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
+  dkv_kernel<<<kLanes, deterministic ? kDkvThreads : kDkvThreadsAtomic, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
   if ((rc = dsa::launch_error("bwd_dkv_kernel")) != DSA_OK) return rc;
 
   // 4. fixed-order reductions (the atomic variant has no shards to reduce)
