@@ -8,7 +8,7 @@
 //   dkv[id_j] += scale * dS_j q  (+ P_j dout on the value dims),
 //   d_sink = -sum over rows of exp(sink - L) * (dout . out).
 //
-// Four launches, all deterministic (no floating-point atomics):
+// Four launches, all deterministic in this variant (no floating-point atomics):
 //  1. bwd_prep_kernel: per (token, head) the log2-domain normaliser L and
 //     delta = dout . out, and the row's d_sink term.
 //  2. bwd_dq_kernel: per unit (token, 64-head group), in 64-key tiles: the
@@ -21,13 +21,15 @@
 //     M = 64 block for dims 512..575).  The kv tile buffer is single: the
 //     query and dout rows take the room of the forward's second buffer.
 //  3. bwd_dkv_kernel: 152 lanes (one per SM); lane c owns one fp32 copy
-//     ("shard") of dkv and takes tokens c, c + 152, ... in order.  Per 64-slot tile one MMA
-//     sequence forms the tile's key rows [scale dS | P] . [q ; dout]
-//     (M = 64 keys, K = 128, N = 128 dims at a time) and the lane adds them
-//     into its shard, one thread per dim walking the keys in slot order, so
-//     repeated ids in a row add up in a fixed order with no race.
-//  4. bwd_reduce_kernel: dkv = the shards summed in lane order; d_sink = the
-//     row terms summed in row order.
+//     ("shard") of dkv and takes tokens c, c + 152, ... in order.  Per
+//     64-slot tile one MMA sequence forms the tile's key rows
+//     [scale dS | P] . [q ; dout] (M = 64 keys, K = 128, N = 128 dims at a
+//     time) in TMEM, and the drain warps add them into the lane's shard:
+//     each row has one writer per block and the tiles go in slot order, so
+//     every shard value receives its terms in a fixed order with no race
+//     (repeated ids within a tile are first folded in slot order).
+//  4. bwd_reduce_*_kernel: dkv = the shards summed in lane order; d_sink =
+//     the row terms summed in row order.
 // The non-deterministic variant (the pages' default) runs the same launches
 // except that bwd_dkv_kernel<true> adds each slot's dkv row straight into
 // dkv with fp32 vector atomics (red.global.add on 16 bytes), so there are no
