@@ -554,12 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------- 3. dkv
-constexpr int kDkvThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 drain + shard update
-constexpr int kDrainThreads = 128;
-// The atomic variant drains with eight warps, two per TMEM lane quarter (one
-// per 64-column half of a block): it needs far fewer registers per thread.
-constexpr int kDkvThreadsAtomic = 320;
-constexpr int kDrainThreadsAtomic = kDkvThreadsAtomic - 64;
+// warp 0 TMA, warp 1 MMA, warps 2..9 drain + shard update: two per TMEM lane
+// quarter, one per 64-column half of a block
+constexpr int kDkvThreads = 320;
+constexpr int kDrainThreads = kDkvThreads - 64;
+constexpr int kDkvThreadsAtomic = kDkvThreads;
+constexpr int kDrainThreadsAtomic = kDrainThreads;
 // staging row stride (floats): 4 floats of padding put the eight keys a warp
 // writes at once in different banks (unpadded rows 512 bytes apart collide)
 constexpr int kStageLd = 132;
@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
       dsa::mbar_init(&a_full[b], 1);
       dsa::mbar_init(&a_empty[b], 1);
       dsa::mbar_init(&d_full[b], 1);
-      dsa::mbar_init(&d_empty[b], ATOMIC ? 8 : 4);  // one arrive per drain warp
+      dsa::mbar_init(&d_empty[b], 8);  // one arrive per drain warp
     }
     dsa::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------- drain + shard update
-    const int dt = threadIdx.x - 64;       // 0..127
+    const int dt = threadIdx.x - 64;       // 0..255
     const int quarter = warp & 3;          // TMEM lane quarter (warps 2..5)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int kA = quarter * 16 + (lane >> 2), kB = kA + 8;
@@ -870,65 +870,64 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
             // result is the same bits; the barrier at the tile's end orders
             // these writes before a later tile's reads of the same rows.
             const int r0 = quarter * 16;
-            const int* ids = tids + r0;  // the warp's 16 ids (-1: absent), read from shared memory
-            float4 pa[16], pn[16];
-            auto load_rows = [&](int nb, float4 (&a)[16]) {
-              const bool on = 4 * lane < (nb < 4 ? 128 : 64);
-              const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * lane);
+            const int c0 = 64 * ((warp - 2) >> 2);  // this warp's columns of a block: [c0, c0 + 64)
+            const int cl = c0 + 4 * (lane & 15);
+            const int* ids = tids + r0 + (lane >> 4);  // row 2k + lane / 16 of the warp's 16: ids[2k]
+            float4 pa[8], pn[8];
+            auto load_rows = [&](int nb, float4 (&a)[8]) {
+              const bool on = c0 < (nb < 4 ? 128 : 64);
+              const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + cl);
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int id = ids[k];
+              for (int k = 0; k < 8; ++k) {
+                const int id = ids[2 * k];
                 a[k] = (on && id >= 0) ? src[static_cast<int64_t>(id) * (kDqk / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
               }
             };
             load_rows(0, pa);
             for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
               const int db = blk_ctr & 1;
-              const int nd = nb < 4 ? 128 : 64;
+              const bool active = c0 < (nb < 4 ? 128 : 64);
               if (nb + 1 < 5) load_rows(nb + 1, pn);
               if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
               dsa::tc_fence_after();
-              if (!failed) {
-                // two 64-column halves, to leave registers for the rows in flight
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  if (64 * h2 >= nd) break;
-                  uint32_t v[2][16];
+              if (!failed && active) {
+                uint32_t v[2][16];
 #pragma unroll
-                  for (int q2 = 0; q2 < 2; ++q2)
-                    dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 64 * h2 + 32 * q2, v[q2]);
-                  dsa::tmem_wait_ld();
+                for (int q2 = 0; q2 < 2; ++q2)
+                  dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + c0 + 32 * q2, v[q2]);
+                dsa::tmem_wait_ld();
 #pragma unroll
-                  for (int q2 = 0; q2 < 2; ++q2) {
+                for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                      const int col = 64 * h2 + 32 * q2 + 8 * j + 2 * (lane & 3);
-                      *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
-                          make_float2(__uint_as_float(v[q2][4 * j]), __uint_as_float(v[q2][4 * j + 1]));
-                      *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
-                          make_float2(__uint_as_float(v[q2][4 * j + 2]), __uint_as_float(v[q2][4 * j + 3]));
-                    }
+                  for (int j = 0; j < 4; ++j) {
+                    const int col = c0 + 32 * q2 + 8 * j + 2 * (lane & 3);
+                    *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                        make_float2(__uint_as_float(v[q2][4 * j]), __uint_as_float(v[q2][4 * j + 1]));
+                    *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                        make_float2(__uint_as_float(v[q2][4 * j + 2]), __uint_as_float(v[q2][4 * j + 3]));
                   }
                 }
               }
               dsa::tc_fence_before();
               __syncwarp();
               if (lane == 0) dsa::mbar_arrive(&d_empty[db]);  // this warp's TMEM reads are done
-              if (!failed && 4 * lane < nd) {
-                float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * lane);
+              if (!failed && active) {
+                float4* base = reinterpret_cast<float4*>(shard + nb * 128 + cl);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const int id = ids[k];
+                for (int k = 0; k < 8; ++k) {
+                  const int id = ids[2 * k];
                   if (id < 0) continue;
-                  const float4 sv = *reinterpret_cast<const float4*>(stage + (r0 + k) * kStageLd + 4 * lane);
+                  const int r = r0 + 2 * k + (lane >> 4);
+                  const float4 sv = *reinterpret_cast<const float4*>(stage + r * kStageLd + cl);
                   base[static_cast<int64_t>(id) * (kDqk / 4)] =
                       make_float4(pa[k].x + sv.x, pa[k].y + sv.y, pa[k].z + sv.z, pa[k].w + sv.w);
                 }
               }
-              __syncwarp();  // this warp's staging rows are read before the next block rewrites them
+              __syncwarp();  // this warp's staging columns are read before the next block rewrites them
 #pragma unroll
-              for (int k = 0; k < 16; ++k) pa[k] = pn[k];
+              for (int k = 0; k < 8; ++k) pa[k] = pn[k];
             }
-            // the four warps leave together, at the tile's end, if any wait gave up
+            // the eight warps leave together, at the tile's end, if any wait gave up
             if (dsa::named_bar_any(1, kDrainThreads, failed)) {
               ok = false;
               break;
@@ -940,44 +939,36 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
           // block of dims; a repeated id is updated once, through its first
           // slot, so no two threads write one value.  Earlier updates of the
           // same values, by any thread, were ordered before the reads by the
-          // barrier that ended the previous tile (or block).
+          // barrier that ended the previous tile (or block).  The first four
+          // drain warps (one per TMEM lane quarter) do the work; the other
+          // four only take part in the barriers.
+          const bool worker = dt < 128;
           const int kg = dt >> 5, c4 = dt & 31;
-          float4 acc[kKeys / 4];
-          auto load_block = [&](int nb, float4 (&a)[kKeys / 4]) {
-            const bool on = 4 * c4 < (nb < 4 ? 128 : 64);
-            const float4* src = reinterpret_cast<const float4*>(shard + nb * 128 + 4 * c4);
-#pragma unroll
-            for (int k = 0; k < kKeys / 4; ++k) {
-              const int r = kg + 4 * k;
-              const int id = tids[r];
-              a[k] = (on && id >= 0 && first[r] == r) ? src[static_cast<int64_t>(id) * (kDqk / 4)]
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-          };
           for (int nb = 0; nb < 5; ++nb, ++blk_ctr) {
             const int db = blk_ctr & 1;
             const int nd = nb < 4 ? 128 : 64;
             const bool col_on = 4 * c4 < nd;
             float4* base = reinterpret_cast<float4*>(shard + nb * 128 + 4 * c4);
-            load_block(nb, acc);
             if (!failed) failed = !dsa::mbar_wait_warp(&d_full[db], (blk_ctr >> 1) & 1, wt);
             dsa::tc_fence_after();
-            if (!failed) {
-              uint32_t v[4][16];
+            if (!failed && worker) {
+              for (int h2 = 0; h2 < 2; ++h2) {  // two 64-column halves
+                if (64 * h2 >= nd) break;
+                uint32_t v[2][16];
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                if (32 * q4 < nd) dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 32 * q4, v[q4]);
-              dsa::tmem_wait_ld();
+                for (int q2 = 0; q2 < 2; ++q2)
+                  dsa::tmem_ld16x256b_x4(tmem_base + lane_off + db * 128 + 64 * h2 + 32 * q2, v[q2]);
+                dsa::tmem_wait_ld();
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                if (32 * q4 >= nd) continue;
+                for (int q2 = 0; q2 < 2; ++q2) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const int col = 32 * q4 + 8 * j + 2 * (lane & 3);
-                  *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
-                      make_float2(__uint_as_float(v[q4][4 * j]), __uint_as_float(v[q4][4 * j + 1]));
-                  *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
-                      make_float2(__uint_as_float(v[q4][4 * j + 2]), __uint_as_float(v[q4][4 * j + 3]));
+                  for (int j = 0; j < 4; ++j) {
+                    const int col = 64 * h2 + 32 * q2 + 8 * j + 2 * (lane & 3);
+                    *reinterpret_cast<float2*>(stage + kA * kStageLd + col) =
+                        make_float2(__uint_as_float(v[q2][4 * j]), __uint_as_float(v[q2][4 * j + 1]));
+                    *reinterpret_cast<float2*>(stage + kB * kStageLd + col) =
+                        make_float2(__uint_as_float(v[q2][4 * j + 2]), __uint_as_float(v[q2][4 * j + 3]));
+                  }
                 }
               }
             }
@@ -991,15 +982,15 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
                   if (first[r] != r) stage[first[r] * kStageLd + dt] += stage[r * kStageLd + dt];
               named_bar(1, kDrainThreads);
             }
-            if (col_on && !failed) {
+            if (col_on && !failed && worker) {
 #pragma unroll
               for (int k = 0; k < kKeys / 4; ++k) {
                 const int r = kg + 4 * k;
                 const int id = tids[r];
                 if (id >= 0 && first[r] == r) {
                   const float4 s = *reinterpret_cast<const float4*>(stage + r * kStageLd + 4 * c4);
-                  base[static_cast<int64_t>(id) * (kDqk / 4)] =
-                      make_float4(acc[k].x + s.x, acc[k].y + s.y, acc[k].z + s.z, acc[k].w + s.w);
+                  const float4 a = base[static_cast<int64_t>(id) * (kDqk / 4)];
+                  base[static_cast<int64_t>(id) * (kDqk / 4)] = make_float4(a.x + s.x, a.y + s.y, a.z + s.z, a.w + s.w);
                 }
               }
             }
