@@ -558,8 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // quarter, one per 64-column half of a block
 constexpr int kDkvThreads = 320;
 constexpr int kDrainThreads = kDkvThreads - 64;
-constexpr int kDkvThreadsAtomic = kDkvThreads;
-constexpr int kDrainThreadsAtomic = kDrainThreads;
 // staging row stride (floats): 4 floats of padding put the eight keys a warp
 // writes at once in different banks (unpadded rows 512 bytes apart collide)
 constexpr int kStageLd = 132;
@@ -609,7 +607,7 @@ __device__ __forceinline__ int dkv_len(const DkvParams& p, int t) {
 // (M = 64 keys, K = 64 + 64 heads, B MN-major), added into the lane's shard
 // (ATOMIC: into dkv, one fp32 vector atomic per 4 dims of each valid slot).
 template <bool ATOMIC>
-__global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
+__global__ void __launch_bounds__(kDkvThreads, 1)
     bwd_dkv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
                    const __grid_constant__ CUtensorMap map_ds, const __grid_constant__ CUtensorMap map_p,
                    const DkvParams p) {
@@ -826,7 +824,7 @@ __global__ void __launch_bounds__(ATOMIC ? kDkvThreadsAtomic : kDkvThreads, 1)
             __syncwarp();  // this warp's staging columns are read before the next block rewrites them
           }
           // the eight warps leave together, at a tile's end, if any wait gave up
-          if (dsa::named_bar_any(1, kDrainThreadsAtomic, failed)) {
+          if (dsa::named_bar_any(1, kDrainThreads, failed)) {
             ok = false;
             break;
           }
@@ -1197,7 +1195,7 @@ int run_bwd(const void* q, const void* kv, const void* out, const void* dout, co
   if (cudaFuncSetAttribute(dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_dkv)) !=
       cudaSuccess)
     return dsa::launch_error("bwd_dkv_kernel smem attribute");
-  dkv_kernel<<<kLanes, deterministic ? kDkvThreads : kDkvThreadsAtomic, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
+  dkv_kernel<<<kLanes, kDkvThreads, smem_dkv, stream>>>(mq, mdo, mds, mp, dp);
   if ((rc = dsa::launch_error("bwd_dkv_kernel")) != DSA_OK) return rc;
 
   // 4. fixed-order reductions (the atomic variant has no shards to reduce)
