@@ -71,10 +71,11 @@ def _calls(x):
         r = ops.sparse_attn_fwd(x["q"], x["kv"], idx, x["scale"], topk_length=tl, sink=x["sink"], want_lse_kv=True)
         return [r["out"], r["lse"], r["lse_kv"]]
 
-    def backward(idx, tl, fwd):
-        ws = torch.zeros(ops.sparse_attn_bwd_workspace_size(T, T, x["H"], K), dtype=torch.uint8, device=DEV)
+    def backward(idx, tl, fwd, deterministic=True):
+        ws = torch.zeros(ops.sparse_attn_bwd_workspace_size(T, T, x["H"], K, deterministic), dtype=torch.uint8,
+                         device=DEV)
         r = ops.sparse_attn_bwd(x["q"], x["kv"], fwd[0], x["dout"], fwd[2], idx, x["scale"], topk_length=tl,
-                                sink=x["sink"], workspace=ws)
+                                sink=x["sink"], workspace=ws, deterministic=deterministic)
         return [r["dq"], r["dkv"], r["d_sink"]]
 
     return dense, fused, attn_inputs, attention, backward
@@ -103,7 +104,8 @@ def test_forced_wait_timeout_aborts_every_kernel_cleanly():
     try:
         for name, fn in (("dense indexer", dense), ("fused indexer + top-k", fused),
                          ("sparse attention", lambda: attention(idx, tl)),
-                         ("attention backward", lambda: backward(idx, tl, ref_attn))):
+                         ("attention backward", lambda: backward(idx, tl, ref_attn)),
+                         ("attention backward, atomic dkv", lambda: backward(idx, tl, ref_attn, False))):
             fn()
             torch.cuda.synchronize()  # the kernels returned: the context is usable
             st = ops.device_status(clear=True)
@@ -121,6 +123,9 @@ def test_forced_wait_timeout_aborts_every_kernel_cleanly():
     again = attention(idx, tl)
     assert _same(again, ref_attn)
     assert _same(backward(idx, tl, ref_attn), ref_bwd)
+    # the atomic variant: dq and d_sink are the deterministic variant's bits
+    at = backward(idx, tl, ref_attn, False)
+    assert _same([at[0], at[2]], [ref_bwd[0], ref_bwd[2]])
     torch.cuda.synchronize()
     assert ops.device_status(clear=True) == 0
 
