@@ -23,7 +23,8 @@ def test_header_declares_the_hot_path():
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_ex", "dsa_forward_host",
                  "dsa_pack_routes", "dsa_thd_metadata_ratio", "dsa_indexer_scores_ratio", "dsa_indexer_topk_ratio",
                  "dsa_indexer_scores_fp8", "dsa_indexer_topk_fp8", "dsa_sparse_attn_bwd",
-                 "dsa_sparse_attn_bwd_workspace_size",
+                 "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd_ex",
+                 "dsa_sparse_attn_bwd_workspace_size_ex",
                  "dsa_last_error", "dsa_device_status"]:
         assert must in names
 
